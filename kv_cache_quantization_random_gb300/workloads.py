@@ -118,8 +118,8 @@ def kv_params(w: Workload, layer: int = 0):
     """Per-(kv-head, channel) key scale and value scale, [Hkv, d] float64.
 
     llama: sigma_c = exp(N(0,1)); n_outliers channels (without replacement)
-    x outlier_gain; the head is then rescaled so that the root-mean-square key
-    norm equals key_norm.  gauss_outlier: unit sigma with outliers, applied to
+    x outlier_gain; the head is then rescaled so that the mean key norm is
+    key_norm.  gauss_outlier: unit sigma with outliers, applied to
     keys and values alike.
     """
     rng = np.random.default_rng([w.data_seed, layer, 7])
@@ -131,7 +131,11 @@ def kv_params(w: Workload, layer: int = 0):
         if w.dist == "llama":
             sig = np.exp(rng.standard_normal(d))
             sig[out] *= w.outlier_gain
-            sig *= w.key_norm / math.sqrt(np.sum(sig * sig))
+            # rescale so that the mean key norm is key_norm: the norm of
+            # sigma * z has no closed-form mean, so measure it on a fixed
+            # seeded sample of 4096 vectors
+            probe = np.random.default_rng([w.data_seed, layer, h, 11]).standard_normal((4096, d))
+            sig *= w.key_norm / np.mean(np.linalg.norm(probe * sig, axis=1))
             ks[h] = sig
             vs[h] = w.value_sigma
         elif w.dist == "gauss_outlier":
