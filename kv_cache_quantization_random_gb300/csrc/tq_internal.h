@@ -1,0 +1,139 @@
+// Private declarations shared by the host code (tq_host.cpp) and the CUDA
+// translation units of the TurboQuant library.  Not part of the C ABI.
+#pragma once
+
+#include <stdint.h>
+#include <stddef.h>
+
+#include "../../include/tq.h"
+
+namespace tq {
+
+constexpr int kHeadDim = 128;          // the head_dim the kernels implement
+constexpr int kQjlM = 128;             // the QJL projection count the kernels implement
+constexpr int kTargetCtas = 4 * 152;   // decode grid target: 4 CTAs per GB300 SM
+constexpr int kDecodeWarps = 4;        // warps per decode CTA
+constexpr int kChunk = 32;             // tokens per warp round in decode
+
+// ---- device tables (built on the host by tq_build_tables) -------------------
+// [0, 256)                 header, int32 words (see kTbl*)
+// [256, 256 + 8*2048)      codebook slot for bits 1..8: 256 centroids then
+//                          256 boundaries (fp32; unused tail = +inf)
+// signs                    (2*layer + kind) * d fp32 (+1 / -1)
+// qjl                      one m*d bf16 matrix per QJL layer, in layer order
+constexpr size_t kTblHeader = 256;
+constexpr size_t kTblCodebook = 256;
+constexpr size_t kTblCodebookSlot = 2048;
+constexpr uint32_t kTblMagic = 0x42545154u;  // "TQTB"
+
+struct TableOffsets {
+  size_t signs;     // byte offset of the sign vectors
+  size_t qjl;       // byte offset of the QJL matrices
+  size_t total;     // total bytes
+};
+
+// ---- kernel argument blocks ----------------------------------------------------
+struct QuantArgs {
+  // source rows
+  const void* src;      // new rows (dtype src_f32 ? fp32 : bf16)
+  int src_f32;
+  int64_t sb, sh, st;   // element strides of src (batch, head, token)
+  int B, H, n;          // n rows per (b, h)
+  const int32_t* dst_pos;        // plain mode: first plane row per sequence (or null)
+  // append mode (rows come from the window ring or the new input)
+  int append;
+  const int32_t* seq_before;     // T0 per sequence
+  int W;
+  const uint16_t* win;           // bf16 ring [B][H][W][d]
+  // destination planes
+  uint8_t* codes;
+  float* norms;
+  uint8_t* qjl_signs;
+  float* qjl_rnorm;
+  int64_t cap;
+  // codec
+  int bits;
+  const float* centroids;        // [256]
+  const float* boundaries;       // [256]
+  const float* rot_signs;        // [d]
+  int qjl;                       // 0 | 1
+  const uint16_t* S;             // bf16 [m][d]
+  int m;
+  unsigned* err;                 // device error word
+  uint32_t wait_limit;
+  uint32_t extra_tx;             // test hook (tq_set_fault_injection), normally 0
+};
+
+struct WindowScatterArgs {
+  const void* src;
+  int src_f32;
+  int64_t sb, sh, st;
+  int B, H, n;
+  const int32_t* seq_before;
+  int W;
+  uint16_t* win;
+};
+
+struct DequantArgs {
+  const uint8_t* codes;
+  const float* norms;
+  const uint8_t* qjl_signs;
+  const float* qjl_rnorm;
+  int64_t cap;
+  int B, H, n;
+  int bits;
+  const float* centroids;
+  const float* rot_signs;
+  int qjl;
+  const uint16_t* S;
+  int m;
+  float* dst;
+};
+
+struct DecodeArgs {
+  const void* q;
+  int q_f32;
+  float qscale;                  // softmax_scale * log2(e)
+  int B, Hq, Hkv, G;
+  // planes
+  const uint8_t* kc; const float* kn; const uint8_t* ks; const float* kr; int64_t kcap;
+  const uint8_t* vc; const float* vn; int64_t vcap;
+  int kb, vb, qjl, m;
+  const uint16_t* kwin; const uint16_t* vwin; int W;
+  const int32_t* seq_lens;
+  int n_qsplits;                 // splits over the quantized tokens
+  int n_splits;                  // n_qsplits + (W > 0)
+  int split_tokens;              // tokens per quantized split (multiple of 32)
+  // codec
+  const float* ck; const float* cv;
+  const float* sk; const float* sv;
+  const uint16_t* S;
+  // outputs / workspace
+  float* out;
+  float* partials;               // [B][Hkv][n_splits][G][2 + d]
+  unsigned* counters;            // [B][Hkv]
+  unsigned* err;
+  int pk, pv;                    // smem row pitches of K / V code rows
+};
+
+// ---- launchers (defined in the .cu files) -------------------------------------
+int launch_quantize(const QuantArgs& a, void* stream);
+int launch_window_scatter(const WindowScatterArgs& a, void* stream);
+int launch_dequantize(const DequantArgs& a, void* stream);
+int launch_decode(const DecodeArgs& a, void* stream);
+size_t decode_smem_bytes(int G, int kb, int vb, int qjl, int pk, int pv);
+
+// device error words: each .cu owns one; these read-and-clear them
+int quant_read_error(unsigned* out);
+int decode_read_error(unsigned* out);
+unsigned* quant_error_ptr();
+unsigned* decode_error_ptr();
+
+extern uint32_t g_wait_limit;
+extern uint32_t g_fault_injection;
+
+// error bits written by the kernels
+constexpr unsigned kErrTimeout = 1u;
+constexpr unsigned kErrBounds = 2u;
+
+}  // namespace tq

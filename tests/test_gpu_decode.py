@@ -1,0 +1,217 @@
+"""GPU parity of decode attention against the oracle (through the C ABI).
+
+Most tests upload the oracle's own packed codes into the planes, so the
+comparison isolates decode attention from quantize; the end-to-end tests run
+the CUDA quantize too.  The bar is 2e-3 relative L2 per (sequence, query head).
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle as O
+from gpu_helpers import (binding, compare_codes, oracle_qjl, oracle_quantize, rel_l2_per_head,
+                         to64, upload_oracle_planes)
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def B():
+    return binding()
+
+
+def _decode_case(B, *, batch, hq, hkv, seq, kb, vb, W=0, qjl=False, layer=0, n_layers=1,
+                 protect=(0, 0), q_f32=False, seed=0, dist="llama", extra_cap=0, data_seed=5):
+    """Build a cache from seeded inputs, quantize it with the oracle, upload the
+    oracle's planes, run the CUDA decode, run the oracle decode, return both."""
+    import torch
+    from kv_cache_quantization_random_gb300 import workloads as W_
+    seq = np.asarray(seq, dtype=np.int64)
+    Tmax = int(seq.max()) if len(seq) else 0
+    cap = max(Tmax - W, 0) + extra_cap + 1
+    w = W_.scaled(W_.get("llama8b_32k"), batch=batch, n_q_heads=hq, n_kv_heads=hkv,
+                  context=max(Tmax, 1), dist=dist, data_seed=data_seed)
+    K, V = W_.make_kv(w)
+    q = W_.make_q(w)
+    if q_f32:
+        q = q.float()
+    cfg = B.Config(k_bits=kb, v_bits=vb, residual_window=W, seed=seed, n_layers=n_layers,
+                   n_protect_first=protect[0], n_protect_last=protect[1],
+                   k_mode=B.TQ_MODE_MSE_QJL if qjl else B.TQ_MODE_MSE)
+    kb_l, vb_l, mode = B.tq_layer_spec_get(cfg, layer)
+    tables = B.device_tables(cfg)
+    K64, V64 = to64(K), to64(V)
+    nq = max(Tmax - W, 0)
+    oqk = oracle_quantize(K64[:, :, :nq], kb_l, seed, layer, 0)
+    oqv = oracle_quantize(V64[:, :, :nq], vb_l, seed, layer, 1)
+    kp = B.Planes(cfg, layer, 0, batch, hkv, cap)
+    vp = B.Planes(cfg, layer, 1, batch, hkv, cap)
+    qj = None
+    if nq:
+        upload_oracle_planes(B, kp, oqk)
+        upload_oracle_planes(B, vp, oqv)
+        if mode == B.TQ_MODE_MSE_QJL:
+            qj = oracle_qjl(oqk, seed, layer)
+            kp.signs_view()[:, :, :nq].copy_(torch.from_numpy(qj["packed"]))
+            kp.rnorm_view()[:, :, :nq].copy_(torch.from_numpy(qj["gamma"]))
+    # window ring per sequence: token t in slot t mod W, for t in [T_b - W, T_b)
+    kw = vw = None
+    kw64 = vw64 = None
+    if W:
+        kw = torch.zeros(batch, hkv, W, 128, dtype=torch.bfloat16)
+        vw = torch.zeros_like(kw)
+        for b in range(batch):
+            for t in range(max(int(seq[b]) - W, 0), int(seq[b])):
+                kw[b, :, t % W] = K[b, :, t]
+                vw[b, :, t % W] = V[b, :, t]
+        kw64, vw64 = to64(kw), to64(vw)
+        kw, vw = kw.cuda(), vw.cuda()
+    # the oracle reads quantized tokens t < T_b - W; rows beyond are never used
+    kcodes = np.zeros((batch, hkv, cap, 128), dtype=np.int64)
+    vcodes = np.zeros_like(kcodes)
+    kn = np.zeros((batch, hkv, cap), np.float32)
+    vn = np.zeros_like(kn)
+    if nq:
+        kcodes[:, :, :nq], vcodes[:, :, :nq] = oqk["codes"], oqv["codes"]
+        kn[:, :, :nq], vn[:, :, :nq] = oqk["norms"], oqv["norms"]
+    qjl_arg = None
+    if qj is not None:
+        bits = np.zeros((batch, hkv, cap, 128), np.int64)
+        gam = np.zeros((batch, hkv, cap), np.float32)
+        bits[:, :, :nq], gam[:, :, :nq] = qj["bits"], qj["gamma"]
+        qjl_arg = dict(bits=bits, gamma=gam, S=qj["S"])
+    ck, _ = O.codebook_fp32(kb_l, 128)
+    cv, _ = O.codebook_fp32(vb_l, 128)
+    ref = O.decode_attention(to64(q), kcodes, kn, vcodes, vn, ck, cv,
+                             O.rotation_signs(seed, layer, 0, 128),
+                             O.rotation_signs(seed, layer, 1, 128), seq, w.softmax_scale,
+                             window=W, k_win=kw64, v_win=vw64, qjl=qjl_arg)
+    out = torch.full((batch, hq, 128), float("nan"), device="cuda")
+    ws = B.new_workspace(cfg, batch, hq, hkv, Tmax)
+    seq_t = torch.tensor(seq, dtype=torch.int32, device="cuda")
+    B.tq_decode_attention(cfg, tables, layer, q.cuda(), w.softmax_scale, kp, vp, seq_t, Tmax, out,
+                          ws, k_win=kw, v_win=vw)
+    torch.cuda.synchronize()
+    assert B.tq_get_device_error() == B.TQ_OK
+    return to64(out), ref, dict(cfg=cfg, tables=tables, kp=kp, vp=vp, q=q, seq_t=seq_t, Tmax=Tmax,
+                                ws=ws, kw=kw, vw=vw, scale=w.softmax_scale)
+
+
+@pytest.mark.parametrize("kb,vb", [(4, 2), (3, 3), (2, 2), (8, 8), (2, 4), (4, 8)])
+def test_decode_bits(B, kb, vb):
+    out, ref, _ = _decode_case(B, batch=2, hq=8, hkv=2, seq=[700, 333], kb=kb, vb=vb)
+    assert rel_l2_per_head(out, ref).max() < TOL
+
+
+@pytest.mark.parametrize("g", [1, 2, 4, 8])
+def test_decode_group_sizes(B, g):
+    out, ref, _ = _decode_case(B, batch=1, hq=2 * g, hkv=2, seq=[1500], kb=3, vb=3)
+    assert rel_l2_per_head(out, ref).max() < TOL
+
+
+def test_decode_single_head_1k_config(B):
+    """The single-head 1024-token config: fp32 K/V with outliers, K3/V3, W=0,
+    query prescaled by 1/sqrt(d) with softmax scale 1."""
+    import torch
+    from kv_cache_quantization_random_gb300 import workloads as W_
+    w = W_.get("single_head_1k")
+    K, V = W_.make_kv(w)
+    q = W_.make_q(w)
+    cfg = B.Config(k_bits=3, v_bits=3, seed=w.codec_seed)
+    tables = B.device_tables(cfg)
+    kp = B.Planes(cfg, 0, 0, 1, 1, 1024)
+    vp = B.Planes(cfg, 0, 1, 1, 1, 1024)
+    B.tq_quantize_kv(cfg, tables, 0, 0, K.cuda(), kp)
+    B.tq_quantize_kv(cfg, tables, 0, 1, V.cuda(), vp)
+    out = torch.empty(1, 1, 128, device="cuda")
+    ws = B.new_workspace(cfg, 1, 1, 1, 1024)
+    seq = torch.tensor([1024], dtype=torch.int32, device="cuda")
+    B.tq_decode_attention(cfg, tables, 0, q.cuda(), 1.0, kp, vp, seq, 1024, out, ws)
+    torch.cuda.synchronize()
+    oqk = oracle_quantize(to64(K), 3, 0, 0, 0)
+    oqv = oracle_quantize(to64(V), 3, 0, 0, 1)
+    compare_codes(kp.codes_view().cpu().numpy(), oqk, 3)
+    compare_codes(vp.codes_view().cpu().numpy(), oqv, 3)
+    ref = O.decode_attention(to64(q), oqk["codes"], oqk["norms"], oqv["codes"], oqv["norms"],
+                             oqk["c32"], oqv["c32"], oqk["signs"], oqv["signs"], [1024], 1.0)
+    assert rel_l2_per_head(to64(out), ref).max() < TOL
+
+
+def test_decode_ragged_edges_with_window(B):
+    W = 16
+    seq = [0, 1, W - 1, W, W + 1, 2 * W + 3, 300, 1027]
+    out, ref, _ = _decode_case(B, batch=len(seq), hq=4, hkv=1, seq=seq, kb=4, vb=2, W=W)
+    assert np.all(out[0] == 0.0)
+    assert rel_l2_per_head(out[1:], ref[1:]).max() < TOL
+
+
+def test_decode_ragged_no_window_and_empty(B):
+    seq = [0, 1, 2, 31, 32, 33, 255, 256, 257, 2000]
+    out, ref, _ = _decode_case(B, batch=len(seq), hq=8, hkv=2, seq=seq, kb=3, vb=2)
+    assert np.all(out[0] == 0.0)
+    assert rel_l2_per_head(out[1:], ref[1:]).max() < TOL
+
+
+def test_decode_qjl_keys(B):
+    out, ref, _ = _decode_case(B, batch=3, hq=8, hkv=2, seq=[900, 64, 1], kb=2, vb=3, qjl=True)
+    assert rel_l2_per_head(out, ref).max() < TOL
+
+
+def test_decode_protected_layers(B):
+    for layer in (0, 5, 11):
+        out, ref, _ = _decode_case(B, batch=2, hq=8, hkv=2, seq=[600, 1200], kb=4, vb=2,
+                                   n_layers=12, protect=(4, 4), layer=layer)
+        assert rel_l2_per_head(out, ref).max() < TOL
+
+
+def test_decode_fp32_query_and_repeat_calls_reuse_workspace(B):
+    import torch
+    out, ref, ctx = _decode_case(B, batch=2, hq=4, hkv=2, seq=[513, 2049], kb=4, vb=4, q_f32=True)
+    assert rel_l2_per_head(out, ref).max() < TOL
+    out2 = torch.empty(2, 4, 128, device="cuda")
+    for _ in range(3):     # the split counters reset themselves
+        B.tq_decode_attention(ctx["cfg"], ctx["tables"], 0, ctx["q"].cuda(), ctx["scale"], ctx["kp"],
+                              ctx["vp"], ctx["seq_t"], ctx["Tmax"], out2, ctx["ws"])
+    torch.cuda.synchronize()
+    assert np.array_equal(to64(out2), out)
+
+
+def test_decode_end_to_end_gpu_quantize(B):
+    """CUDA quantize + CUDA decode against oracle quantize + oracle decode."""
+    import torch
+    from kv_cache_quantization_random_gb300 import workloads as W_
+    w = W_.scaled(W_.get("llama8b_32k"), context=3000)
+    K, V = W_.make_kv(w)
+    q = W_.make_q(w)
+    Wn = w.window
+    T = w.context
+    nq = T - Wn
+    cfg = B.Config(k_bits=4, v_bits=2, residual_window=Wn, seed=w.codec_seed)
+    tables = B.device_tables(cfg)
+    kp = B.Planes(cfg, 0, 0, 1, 8, nq)
+    vp = B.Planes(cfg, 0, 1, 1, 8, nq)
+    B.tq_quantize_kv(cfg, tables, 0, 0, K[:, :, :nq].cuda(), kp)
+    B.tq_quantize_kv(cfg, tables, 0, 1, V[:, :, :nq].cuda(), vp)
+    kw = torch.empty(1, 8, Wn, 128, dtype=torch.bfloat16)
+    vw = torch.empty_like(kw)
+    for t in range(nq, T):
+        kw[:, :, t % Wn] = K[:, :, t]
+        vw[:, :, t % Wn] = V[:, :, t]
+    out = torch.empty(1, 32, 128, device="cuda")
+    ws = B.new_workspace(cfg, 1, 32, 8, T)
+    seq = torch.tensor([T], dtype=torch.int32, device="cuda")
+    B.tq_decode_attention(cfg, tables, 0, q.cuda(), w.softmax_scale, kp, vp, seq, T, out, ws,
+                          k_win=kw.cuda(), v_win=vw.cuda())
+    torch.cuda.synchronize()
+    assert B.tq_get_device_error() == B.TQ_OK
+    oqk = oracle_quantize(to64(K[:, :, :nq]), 4, 0, 0, 0)
+    oqv = oracle_quantize(to64(V[:, :, :nq]), 2, 0, 0, 1)
+    compare_codes(kp.codes_view().cpu().numpy(), oqk, 4)
+    compare_codes(vp.codes_view().cpu().numpy(), oqv, 2)
+    ref = O.decode_attention(to64(q), oqk["codes"], oqk["norms"], oqv["codes"], oqv["norms"],
+                             oqk["c32"], oqv["c32"], oqk["signs"], oqv["signs"], [T],
+                             w.softmax_scale, window=Wn, k_win=to64(kw), v_win=to64(vw))
+    assert rel_l2_per_head(to64(out), ref).max() < TOL
