@@ -1,0 +1,604 @@
+#!/usr/bin/env python3
+"""Benchmark of the TurboQuant hot path on one GB300 (or N replicas).
+
+A step is one decode step of a serving loop over the workload's cache:
+  append   one new token per (sequence, kv-head): the token leaving the
+           residual window is quantized into the planes and the new token is
+           written into the window ring (norm, rotation, code search, packing,
+           window bookkeeping);
+  decode   attention of every query head over the whole compressed context
+           (query rotation, compressed-domain scoring, softmax, rotated V sum,
+           split merge and inverse rotation).
+The headline value is context tokens attended per second.  Bulk quantize of
+the whole context (K and V) is measured separately and reported in GB/s.
+
+Inputs are seeded synthetic tensors shaped like the workload (see
+kv_cache_quantization_random_gb300/workloads.py).  Timed steps cycle through R
+copies of the compressed cache whose total is more than 4x the L2 cache, so
+every step streams its cache from HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...     (the CPU oracle as the reference arm)
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn compressed KV tokens/s and HBM GB/s (% of peak); quantize GB/s"
+
+
+# ----------------------------------------------------------------- helpers
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def largest_divisor_at_most(n: int, cap: int) -> int:
+    for s in range(min(n, cap), 0, -1):
+        if n % s == 0:
+            return s
+    return 1
+
+
+# --------------------------------------------------------------- workload
+def packed_bytes(w):
+    """Bytes of one packed key and one packed value vector (codes + norms [+ QJL])."""
+    d = w.head_dim
+    kbytes = d * w.k_bits // 8 + 4 + ((w.qjl_m // 8 + 4) if w.k_qjl else 0)
+    vbytes = d * w.v_bits // 8 + 4
+    return kbytes, vbytes
+
+
+def algorithmic_bytes(w, seq, W):
+    """Bytes decode attention must move: packed K and V of quantized tokens,
+    bf16 window K and V, bf16 query in, fp32 output."""
+    d = w.head_dim
+    kbytes, vbytes = packed_bytes(w)
+    total = 0
+    for T in seq:
+        nq = max(int(T) - W, 0)
+        nw = int(T) - nq
+        total += w.n_kv_heads * (nq * (kbytes + vbytes) + nw * d * 2 * 2)
+    total += len(seq) * w.n_q_heads * d * (2 + 4)
+    return total
+
+
+def build_state(B, w, device, layer=0):
+    """Inputs, planes and window ring of the workload's context (not yet quantized)."""
+    import torch
+    from kv_cache_quantization_random_gb300 import workloads as WL
+    T, Wn = w.context, w.window
+    nq = T - Wn
+    cfg = B.Config(k_bits=w.k_bits, v_bits=w.v_bits, residual_window=Wn, seed=w.codec_seed,
+                   k_mode=B.TQ_MODE_MSE_QJL if w.k_qjl else B.TQ_MODE_MSE, qjl_m=w.qjl_m)
+    tables = B.device_tables(cfg, device)
+    K, V = WL.make_kv(w, layer=layer, device=device)
+    kp = B.Planes(cfg, layer, 0, w.batch, w.n_kv_heads, nq, device)
+    vp = B.Planes(cfg, layer, 1, w.batch, w.n_kv_heads, nq, device)
+    kw = vw = None
+    if Wn:
+        kw = torch.empty(w.batch, w.n_kv_heads, Wn, w.head_dim, dtype=torch.bfloat16, device=device)
+        vw = torch.empty_like(kw)
+    st = dict(cfg=cfg, tables=tables, K=K, V=V, kp=kp, vp=vp, kw=kw, vw=vw, nq=nq)
+    reset_window(st, w)
+    return st
+
+
+def reset_window(st, w):
+    """Window ring: token t in [T - W, T) in slot t mod W."""
+    import torch
+    T, Wn, nq = w.context, w.window, st["nq"]
+    if Wn:
+        idx = torch.arange(nq, T, device=st["K"].device)
+        st["kw"][:, :, idx % Wn] = st["K"][:, :, nq:T]
+        st["vw"][:, :, idx % Wn] = st["V"][:, :, nq:T]
+
+
+def run_ours(args, w, rank, world, local):
+    import numpy as np
+    import torch
+
+    from kv_cache_quantization_random_gb300 import binding as B
+    from kv_cache_quantization_random_gb300 import workloads as WL
+
+    B.load(build_if_missing=True)
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    peaks, peak_kind = measured_peaks()
+    hbm_peak = float(peaks["hbm_gbs"])
+
+    st = build_state(B, w, device)
+    cfg, tables, kp, vp = st["cfg"], st["tables"], st["kp"], st["vp"]
+    K, V, nq, Wn, T = st["K"], st["V"], st["nq"], w.window, w.context
+
+    # ---- bulk quantize of the whole context (K and V), timed separately
+    def quantize_all():
+        B.tq_quantize_kv(cfg, tables, 0, 0, K[:, :, :nq], kp)
+        B.tq_quantize_kv(cfg, tables, 0, 1, V[:, :, :nq], vp)
+
+    for _ in range(3):
+        quantize_all()
+    torch.cuda.synchronize()
+    qiters = 10
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(qiters):
+        quantize_all()
+    e1.record()
+    torch.cuda.synchronize()
+    q_ms = e0.elapsed_time(e1) / qiters
+    n_vec = w.batch * w.n_kv_heads * nq
+    in_b = w.head_dim * (4 if w.in_dtype == "fp32" else 2)
+    kbts, vbts = packed_bytes(w)
+    q_bytes = n_vec * (2 * in_b + kbts + vbts)
+    q_gbs = q_bytes / (q_ms * 1e-3) / 1e9
+    if B.tq_get_device_error() != B.TQ_OK:
+        raise RuntimeError("device error after quantize")
+
+    # ---- replicas of the compressed cache (more than 4x L2 in total)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    seq = WL.seq_lens(w)
+    dec_bytes = algorithmic_bytes(w, seq, Wn)
+    cache_bytes = sum(t.numel() for t in (kp.codes, kp.norms, vp.codes, vp.norms)) + \
+        (2 * st["kw"].numel() * 2 if Wn else 0)
+    R = max(2, min(64, math.ceil(4 * l2 / max(cache_bytes, 1)) + 1))
+    reps = []
+    for r in range(R):
+        if r == 0:
+            reps.append((kp, vp, st["kw"], st["vw"]))
+            continue
+        kr = B.Planes(cfg, 0, 0, w.batch, w.n_kv_heads, nq, device)
+        vr = B.Planes(cfg, 0, 1, w.batch, w.n_kv_heads, nq, device)
+        for src, dst in ((kp, kr), (vp, vr)):
+            dst.codes.copy_(src.codes)
+            dst.norms.copy_(src.norms)
+            if src.qjl_signs is not None:
+                dst.qjl_signs.copy_(src.qjl_signs)
+                dst.qjl_rnorm.copy_(src.qjl_rnorm)
+        kwr = st["kw"].clone() if Wn else None
+        vwr = st["vw"].clone() if Wn else None
+        reps.append((kr, vr, kwr, vwr))
+
+    # ---- step inputs: one new token per (sequence, kv-head), one query per head
+    q = WL.make_q(w, device=device)
+    knew = K[:, :, T - 1:T].contiguous()
+    vnew = V[:, :, T - 1:T].contiguous()
+    seq_before = torch.tensor(seq - 1, dtype=torch.int32, device=device)
+    seq_t = torch.tensor(seq, dtype=torch.int32, device=device)
+    Tmax = int(seq.max())
+    out = torch.empty(w.batch, w.n_q_heads, w.head_dim, device=device)
+    ws = B.new_workspace(cfg, w.batch, w.n_q_heads, w.n_kv_heads, Tmax, device)
+
+    def append(r):
+        kr, vr, kwr, vwr = reps[r]
+        B.tq_append_kv(cfg, tables, 0, knew, vnew, seq_before, kwr, vwr, kr, vr)
+
+    def decode(r):
+        kr, vr, kwr, vwr = reps[r]
+        B.tq_decode_attention(cfg, tables, 0, q, w.softmax_scale, kr, vr, seq_t, Tmax, out, ws,
+                              k_win=kwr, v_win=vwr)
+
+    def step(i):
+        append(i % R)
+        decode(i % R)
+
+    launches_per_step = (2 + (2 if Wn else 0)) + 1
+
+    # ---- warmup (direct launches), then capture graphs of S steps
+    warm = max(args.warmup, 3)
+    for i in range(warm):
+        step(i)
+    torch.cuda.synchronize()
+    if B.tq_get_device_error() != B.TQ_OK:
+        raise RuntimeError("device error during warmup")
+    K_steps = args.steps
+    S = largest_divisor_at_most(K_steps, 128)
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                for i in range(S):
+                    fn(i)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        return g
+
+    g_step = capture(step)
+    g_dec = capture(lambda i: decode(i % R))
+    g_app = capture(lambda i: append(i % R))
+    for g in (g_step, g_dec, g_app):
+        g.replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region: exactly K steps
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(K_steps // S):
+            g_step.replay()
+        t1.record()
+        torch.cuda.synchronize()
+    step_ms_total = t0.elapsed_time(t1)
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([step_ms_total], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        dist.barrier()
+        step_ms_total = float(tt.item())
+    ms_per_step = step_ms_total / K_steps
+    tokens_per_step = int(seq.sum())
+    value = world * tokens_per_step / (ms_per_step * 1e-3)
+
+    # ---- per-kernel durations (decode-only and append-only graphs, same stream)
+    def time_graph(g, reps_):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps_):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / (reps_ * S)
+
+    reps_t = max(1, min(K_steps // S, 200))
+    dec_ms = time_graph(g_dec, reps_t)
+    app_ms = time_graph(g_app, reps_t)
+    if B.tq_get_device_error() != B.TQ_OK:
+        raise RuntimeError("device error during timed steps")
+    dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
+
+    # ---- end to end through the public API with host buffers
+    qh = q.cpu().pin_memory()
+    kh = knew.cpu().pin_memory()
+    vh = vnew.cpu().pin_memory()
+    outh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    qd, kd, vd = torch.empty_like(q), torch.empty_like(knew), torch.empty_like(vnew)
+    n_e2e = max(3, min(K_steps, 2000))
+
+    def e2e_step(i):
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        kr, vr, kwr, vwr = reps[i % R]
+        B.tq_append_kv(cfg, tables, 0, kd, vd, seq_before, kwr, vwr, kr, vr)
+        B.tq_decode_attention(cfg, tables, 0, qd, w.softmax_scale, kr, vr, seq_t, Tmax, out, ws,
+                              k_win=kwr, v_win=vwr)
+        outh.copy_(out, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for i in range(n_e2e):
+        e2e_step(i)
+    b.record()
+    torch.cuda.synchronize()
+    e2e_ms = a.elapsed_time(b) / n_e2e
+    h2d = qh.numel() * qh.element_size() + 2 * kh.numel() * kh.element_size()
+    d2h = outh.numel() * outh.element_size()
+
+    # ---- sampled parity at full size, in the launch configuration timed above
+    parity = None
+    if not args.no_parity and rank == 0:
+        # the timed steps rewrote one row and one window slot of every replica:
+        # restore replica 0 from the inputs before checking it
+        quantize_all()
+        reset_window(st, w)
+        parity = sampled_parity(B, w, st, q, out, reps[0], seq, decode)
+
+    res = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": K_steps, "warmup": warm, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp32", "data": "synthetic",
+        "config": {
+            "workload": w.name, "batch": w.batch, "q_heads": w.n_q_heads,
+            "kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "context": int(seq.max()),
+            "k_bits": w.k_bits, "v_bits": w.v_bits, "k_qjl": w.k_qjl, "window": Wn,
+            "new_tokens_per_step": 1, "parallelism": f"replicas x{world}",
+            "l2": f"{R} cache replicas cycled ({R * cache_bytes / 1e6:.0f} MB > 4 x L2 {l2 / 1e6:.0f} MB)",
+            "graph_steps": S,
+        },
+        "roofline": {
+            "kernel": "tq::decode_kernel", "bound": "hbm", "achieved": dec_gbs,
+            "peak": hbm_peak, "unit": "GB/s", "frac": dec_gbs / hbm_peak,
+            "peak_source": f"{peak_kind} hbm_gbs", "traffic": args.decode_traffic,
+            "bytes_per_launch": dec_bytes, "launch_ms": dec_ms,
+        },
+        "decode": {"ms": dec_ms, "gbs": dec_gbs, "frac_of_peak": dec_gbs / hbm_peak,
+                   "tokens_per_s": tokens_per_step / (dec_ms * 1e-3), "bytes": dec_bytes},
+        "append": {"ms": app_ms, "launches": launches_per_step - 1},
+        "quantize": {"ms": q_ms, "gbs": q_gbs, "frac_of_peak": q_gbs / hbm_peak,
+                     "vectors": 2 * n_vec, "bytes": q_bytes, "what": "bulk quantize of the "
+                     "context's K and V (bf16 in, packed planes out)"},
+        "e2e": {"value": world * tokens_per_step / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": n_e2e},
+        "gpu_launches": K_steps * launches_per_step,
+        "clocks": clocks.summary(),
+        "parity": parity,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(w, st, q, seq, budget_s=args.cpu_seconds)
+    return res
+
+
+def _oracle_inputs(w, st, q, heads):
+    """fp64 copies of the inputs of kv-heads `heads` (sequence 0)."""
+    import numpy as np
+    f64 = lambda t: t.float().cpu().numpy().astype(np.float64)
+    K = f64(st["K"][:1, heads])
+    V = f64(st["V"][:1, heads])
+    g = w.group
+    qh = [h * g + j for h in heads for j in range(g)]
+    return K, V, f64(q[:1, qh])
+
+
+def _oracle_cache(w, K, V, T):
+    """The oracle's own compressed cache of K, V (sequence 0), plus window ring."""
+    import numpy as np
+    import oracle as O
+    Wn = w.window
+    nq = T - Wn
+    ck, bk = O.codebook_fp32(w.k_bits, w.head_dim)
+    cv, bv = O.codebook_fp32(w.v_bits, w.head_dim)
+    sk = O.rotation_signs(w.codec_seed, 0, 0, w.head_dim)
+    sv = O.rotation_signs(w.codec_seed, 0, 1, w.head_dim)
+    qk = O.quantize_vectors(K[:, :, :nq], ck, bk, sk)
+    qv = O.quantize_vectors(V[:, :, :nq], cv, bv, sv)
+    qjl = None
+    if w.k_qjl:
+        S = O.qjl_matrix(w.codec_seed, 0, w.qjl_m, w.head_dim)
+        r = O.qjl_residual(qk["y"], qk["codes"], qk["norm64"], ck)
+        bits, gamma, _ = O.qjl_sketch(r, S)
+        qjl = dict(bits=bits, gamma=gamma, S=S)
+    kw = vw = None
+    if Wn:
+        kw = np.zeros((1, K.shape[1], Wn, w.head_dim))
+        vw = np.zeros_like(kw)
+        for t in range(nq, T):
+            kw[:, :, t % Wn] = K[:, :, t]
+            vw[:, :, t % Wn] = V[:, :, t]
+    return dict(ck=ck, bk=bk, cv=cv, bv=bv, sk=sk, sv=sv, qk=qk, qv=qv, qjl=qjl, kw=kw, vw=vw)
+
+
+def _oracle_decode(w, c, qs, T):
+    import oracle as O
+    return O.decode_attention(qs, c["qk"]["codes"], c["qk"]["norms"], c["qv"]["codes"],
+                              c["qv"]["norms"], c["ck"], c["cv"], c["sk"], c["sv"], [T],
+                              w.softmax_scale, window=w.window, k_win=c["kw"], v_win=c["vw"],
+                              qjl=c["qjl"])
+
+
+def sampled_parity(B, w, st, q, out, rep0, seq, decode):
+    """Oracle decode of a sample of kv-heads of sequence 0 at full context,
+    against the CUDA output of the timed launch configuration."""
+    import numpy as np
+    import torch
+    import oracle as O
+    decode(0)
+    torch.cuda.synchronize()
+    got = out.float().cpu().numpy().astype(np.float64)
+    heads = [0, w.n_kv_heads - 1] if w.n_kv_heads > 1 else [0]
+    K, V, qs = _oracle_inputs(w, st, q, heads)
+    T = int(seq[0])
+    c = _oracle_cache(w, K, V, T)
+    gk = O.unpack_codes(rep0[0].codes_view()[:1, heads].cpu().numpy(), w.k_bits, w.head_dim)
+    band = O.near_boundary(c["qk"]["y"], c["bk"], w.head_dim)
+    code_diff = int((gk != c["qk"]["codes"]).sum())
+    outside = int(((gk != c["qk"]["codes"]) & ~band).sum())
+    ref = _oracle_decode(w, c, qs, T)
+    g = w.group
+    qh = [h * g + j for h in heads for j in range(g)]
+    mine = got[:1, qh]
+    rel = np.linalg.norm(mine - ref, axis=-1) / np.linalg.norm(ref, axis=-1)
+    return {"max_rel_l2": float(rel.max()), "tolerance": 2e-3, "pass": bool(rel.max() < 2e-3),
+            "kv_heads_checked": heads, "query_heads_checked": len(qh),
+            "key_code_mismatches_in_boundary_band": code_diff - outside,
+            "key_code_mismatches_outside_band": outside}
+
+
+def cpu_baseline(w, st, q, seq, budget_s=15.0):
+    """The oracle, as it stands, timed on this host's cores on a bounded sample:
+    decode attention of one kv-head group of sequence 0 (the step's append of
+    one token is negligible next to it), scaled to the workload."""
+    import numpy as np
+    cores = len(os.sched_getaffinity(0))
+    T = int(seq[0])
+    K, V, qs = _oracle_inputs(w, st, q, [0])
+    c = _oracle_cache(w, K, V, T)
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        _oracle_decode(w, c, qs, T)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or n >= 1000:
+            break
+    per_group = el / n
+    groups = w.batch * w.n_kv_heads
+    step_s = per_group * groups * (float(np.mean(seq)) / T)
+    tokens = float(np.sum(seq))
+    return {"value": tokens / step_s, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} oracle decode(s) of one kv-head group ({w.group} query heads) "
+                      f"over {T} tokens of sequence 0, {el:.1f} s, scaled x{groups} groups"}
+
+
+# ------------------------------------------------------------ reference arm
+def run_reference(args, w, rank, world):
+    """The CPU oracle timed as the reference implementation, on the same
+    workload, metric and unit; each step is a bounded sample (one kv-head group)."""
+    import numpy as np
+    import oracle as O
+    from kv_cache_quantization_random_gb300 import workloads as WL
+    if rank != 0:
+        return None
+    cores = len(os.sched_getaffinity(0))
+    seq = WL.seq_lens(w)
+    T, Wn = int(seq[0]), w.window
+    nq = T - Wn
+    f64 = lambda t: t.float().numpy().astype(np.float64)
+    K, V = WL.make_kv(w, batch=1)
+    K, V = f64(K[:, :1]), f64(V[:, :1])
+    qs = f64(WL.make_q(w)[:1, :w.group])
+    c = _oracle_cache(w, K, V, T)
+
+    def step():
+        # append: quantize the token leaving the window (one vector per kind)
+        O.quantize_vectors(K[:, :, nq - 1:nq], c["ck"], c["bk"], c["sk"])
+        O.quantize_vectors(V[:, :, nq - 1:nq], c["cv"], c["bv"], c["sv"])
+        _oracle_decode(w, c, qs, T)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    steps = min(args.steps, args.reference_max_steps)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    el = time.perf_counter() - t0
+    groups = w.batch * w.n_kv_heads
+    ms_per_step = el / steps * groups * 1e3 * (float(np.mean(seq)) / T)
+    value = float(np.sum(seq)) / (ms_per_step * 1e-3)
+    sample = (f"each step: oracle append of 1 token + decode of one kv-head group "
+              f"({w.group} query heads) over {T} tokens, scaled x{groups} groups")
+    return {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": w.name, "batch": w.batch, "q_heads": w.n_q_heads,
+                       "kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "context": T,
+                       "k_bits": w.k_bits, "v_bits": w.v_bits, "window": Wn,
+                       "parallelism": "host cores"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__,
+                                 formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama8b_32k")
+    ap.add_argument("--no-parity", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--reference-max-steps", type=int, default=200)
+    ap.add_argument("--decode-traffic", type=float, default=None,
+                    help="dram bytes per decode launch from an ncu capture of the current kernel")
+    args = ap.parse_args()
+
+    from kv_cache_quantization_random_gb300 import workloads as WL
+    w = WL.get(args.workload)
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, w, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    res = run_ours(args, w, rank, world, local)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
