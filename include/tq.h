@@ -254,6 +254,35 @@ void tq_set_wait_limit(uint32_t iterations);
  * mode 0 (default) turns it off. */
 void tq_set_fault_injection(int mode);
 
+/* Allocation-free variant of tq_decode_attention.  The pages have no
+ * counterpart: this is an integration convenience for callers that cannot
+ * give the library a workspace -- for example a plugin inside a serving engine
+ * that owns all device memory and hands over only tensor pointers, or a
+ * latency-bound decode loop that must not call the CUDA allocator (cudaMalloc
+ * may synchronize the whole device).
+ *
+ * Same arguments and results as tq_decode_attention, minus the workspace: the
+ * split partials and counters live in a fixed device array of 8 MiB
+ * (8388608 bytes) that the library reserves on every GPU that loads it and
+ * holds until the process exits.
+ * Nothing is allocated by the call.
+ *   - A problem whose tq_workspace_bytes() exceeds that size is rejected with
+ *     TQ_ERR_BUFFER_TOO_SMALL before anything is launched.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     outside any stream capture.
+ *   - Each call clears the part of the array it uses (an async memset on
+ *     `stream`) before the decode launch.
+ *   - Every call on a device shares the one array: calls whose work can
+ *     overlap on the GPU (different streams, no ordering between them) race
+ *     and give wrong results.  Order them on one stream or by events. */
+tq_status tq_decode_attention_noalloc(const tq_config* cfg, const void* tables, int layer,
+                                      const void* q, int q_dtype, float softmax_scale, int batch,
+                                      int n_q_heads, int n_kv_heads, tq_planes k, tq_planes v,
+                                      const uint16_t* k_win, const uint16_t* v_win,
+                                      const int32_t* seq_lens, int max_seq_len, float* out,
+                                      void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -35,7 +35,7 @@ EXPORTED = [
     "tq_make_qjl_matrix", "tq_tables_bytes", "tq_build_tables", "tq_plane_bytes",
     "tq_workspace_bytes", "tq_workspace_init", "tq_quantize_kv", "tq_append_kv",
     "tq_dequantize", "tq_decode_attention", "tq_get_device_error", "tq_set_wait_limit",
-    "tq_set_fault_injection",
+    "tq_set_fault_injection", "tq_decode_attention_noalloc",
 ]
 
 
@@ -104,6 +104,8 @@ def load(build_if_missing: bool = False):
         "tq_get_device_error": (I, [P]),
         "tq_set_wait_limit": (None, [C.c_uint32]),
         "tq_set_fault_injection": (None, [I]),
+        "tq_decode_attention_noalloc": (I, [cfgp, P, I, P, I, F, I, I, I, tq_planes, tq_planes,
+                                            P, P, P, I, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -320,6 +322,22 @@ def tq_decode_attention(cfg: Config, tables, layer: int, q, softmax_scale: float
         seq_lens.data_ptr(), max_seq_len, out.data_ptr(), workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _stream_ptr(stream))
     _check(st, "tq_decode_attention")
+
+
+def tq_decode_attention_noalloc(cfg: Config, tables, layer: int, q, softmax_scale: float,
+                                k: Planes, v: Planes, seq_lens, max_seq_len: int, out,
+                                k_win=None, v_win=None, stream=None):
+    """tq_decode_attention without a caller workspace (the library's fixed
+    device array is used instead; see include/tq.h)."""
+    B, Hq, _ = q.shape
+    st = load().tq_decode_attention_noalloc(
+        C.byref(cfg.c()), tables.data_ptr(), layer, q.data_ptr(), _dtype_code(q),
+        float(softmax_scale), B, Hq, k.n_kv_heads, k.c(), v.c(), _ptr(k_win), _ptr(v_win),
+        seq_lens.data_ptr(), max_seq_len, out.data_ptr(), _stream_ptr(stream))
+    _check(st, "tq_decode_attention_noalloc")
+
+
+NOALLOC_MAX_BYTES = 8 << 20   # size of the library's fixed decode array (include/tq.h)
 
 
 def tq_get_device_error(stream=None) -> int:
