@@ -1,0 +1,925 @@
+// Decode attention over a TurboQuant-compressed KV cache (sm_103a): the kernel
+// template, instantiated per (query heads per kv-head G, key bits, value bits,
+// QJL) in tq_decode_g{1,2,4,8}.cu so that each launch runs code for exactly
+// one storage format.
+//
+// "TurboQuant KV 캐시 압축 for llama.cpp": v1.7.0 decision 4 (the decode kernel
+// applies the encoders' WHT to Q, so q_rot . k_rot = q . k by Parseval);
+// v1.5.2 changes 1-2 (accumulate in fp32, never half) and 4 (V is summed in
+// the rotated domain and needs one inverse rotation at the output); v1.4.2
+// items 1 and 2 (dequantized codes fed to tensor-core MMA; the QJL term is a
+// correction from the sign bits and the stored residual scale).
+//
+// One CTA = (split, kv-head, sequence), 4 warps.  Prologue: the G query heads
+// of the kv-head are scaled by softmax_scale*log2(e), rotated with the K sign
+// vector and split into fp16 hi + lo MMA operands held in registers; QJL keys
+// also get S q_rot as hi + lo operands.  Main loop, per warp and 32-token
+// chunk (bulk copies into a two-slot ring, bounded mbarrier waits), all on
+// mma.sync m16n8k16 with fp32 accumulators:
+//   scores   S[tokens x heads] = K_c[tokens x coords] Q[coords x heads]: the
+//            packed codes are decoded in registers through tables of fp16
+//            centroid hi/lo parts; hi*hi + lo*hi + hi*lo carry ~22 bits, so the
+//            scores match fp32 arithmetic; times ||k|| (fp32), plus for QJL
+//            keys gamma * sqrt(pi/2)/m * (+-1 signs)[tokens x m] (S q_rot);
+//   softmax  online, per head, in the log2 domain, on the accumulator layout;
+//   V sum    D[coords x heads] += V_c^T W with fp16 centroid pairs and fp16
+//            weights scaled per chunk into range (error <= ~5e-4 relative).
+// The split owning the residual window scores the bf16 window tokens in the
+// original domain on CUDA cores.  Epilogue: warps merge by log-sum-exp, the
+// CTA writes (m, l, o) for its split; the last CTA of the (sequence, kv-head)
+// merges the splits, one warp per head, inverse-rotates with the V sign vector
+// by an in-register butterfly and writes the output.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tq_device.cuh"
+
+namespace tq {
+
+constexpr int kDWarps = 4;
+constexpr int kDT = kDWarps * 32;
+constexpr int kD2 = 128;
+constexpr float kNegBig = -1.0e30f;
+constexpr float kCScale = 64.f;   // centroids are scaled by 64 in the K tables
+
+// Byte layout of the dynamic shared memory of a decode CTA.
+struct DecodeSmem {
+  int qr, qo, sv, qjlb, warps, warp_stride;
+  int kbuf, vbuf, kn, vn, sbuf, rn, ws, bar;   // offsets inside one warp's region
+  int comb, total;
+  __host__ __device__ DecodeSmem(int G, int qjl, int kb, int vb) {
+    int off = 0;
+    qr = off; off += kD2 * G * 4;                 // [128][G] rotated, scaled queries
+    qo = off; off += kD2 * G * 4;                 // [128][G] original-domain queries
+    sv = off; off += kD2 * 4;
+    qjlb = off; off += qjl ? 32 * 8 * 16 : 0;     // per lane, per k-tile: S q hi/lo operands
+    warps = off;
+    int w = 0;
+    kbuf = w; w += 2 * 32 * 16 * kb;
+    vbuf = w; w += 2 * 32 * 16 * vb;
+    kn = w; w += 2 * 128;
+    vn = w; w += 2 * 128;
+    sbuf = w; w += qjl ? 2 * 32 * 16 : 0;
+    rn = w; w += qjl ? 2 * 128 : 0;
+    ws = w; w += 8 * 32 * 2;                      // [8 heads][32 tokens] fp16 weights
+    bar = w; w += 16;
+    warp_stride = w;
+    int region = kDWarps * w;
+    const int comb_need = kDWarps * G * (2 + kD2) * 4;   // cm, cl, co
+    const int scratch_need = 2 * G * kD2 * 4;
+    if (region < comb_need) region = comb_need;
+    if (region < scratch_need) region = scratch_need;
+    comb = warps;
+    off += region;
+    total = off + 16;                             // + is-last flag
+  }
+};
+
+__device__ __forceinline__ uint32_t byte_of(uint32_t x, int b) {
+  return __byte_perm(x, 0u, 0x4440u | (uint32_t)b);
+}
+__device__ __forceinline__ uint32_t half_of(uint32_t x, int h) {
+  return __byte_perm(x, 0u, h ? 0x4432u : 0x4410u);
+}
+__device__ __forceinline__ uint32_t h16(float x) {
+  return (uint32_t)__half_as_ushort(__float2half_rn(x));
+}
+// fp16 hi and lo parts of x (x ~= hi + lo to ~22 bits), packed hi | lo << 16
+__device__ __forceinline__ uint32_t hilo(float x) {
+  const __half h = __float2half_rn(x);
+  return (uint32_t)__half_as_ushort(h) | (h16(x - __half2float(h)) << 16);
+}
+// pack two (hi | lo << 16) entries into the hi pair and the lo pair
+__device__ __forceinline__ void pack_hilo(uint32_t e0, uint32_t e1, uint32_t& hi, uint32_t& lo) {
+  hi = __byte_perm(e0, e1, 0x5410);
+  lo = __byte_perm(e0, e1, 0x7632);
+}
+// ---- V sum on the tensor cores ------------------------------------------------
+// D[coords x heads] += V^T[coords x tokens] W[tokens x heads] with
+// mma.sync m16n8k16 (fp16 operands, fp32 accumulate).  The m index is a free
+// permutation of the coordinates: thread (g = lane/4, tig = lane%4) owns rows
+// g and g+8 of every m-tile k, mapped to coordinates 16g+2k and 16g+2k+1, so
+// its 16 coordinates are contiguous in a packed row.  Columns 2tig, 2tig+1
+// (and +8, +9) of a k-tile are tokens; B holds the fp16 softmax weights.
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t lut_u32(const uint32_t* lut, uint32_t byte_off) {
+  return *(const uint32_t*)((const char*)lut + byte_off);
+}
+
+// A operands of k-tile kt for the 8 m-tiles, then the 8 MMAs.  lutp: for 2-
+// and 3-bit values, half2 (c[i0], c[i1]) indexed by the pair (i0 | i1 << VB)
+// of the codes of the two tokens of an operand register; for 4- and 8-bit
+// values, fp16 c[i] in the low half (pairs are packed with a byte permute).
+template <int VB>
+__device__ __forceinline__ void vmma_ktile(const uint8_t* vbuf, const uint32_t* lutp, int kt,
+                                           int g, int tig, uint32_t b0, uint32_t b1,
+                                           float (&d)[8][4]) {
+  constexpr int VROW = 16 * VB;
+  const int t0 = 16 * kt + 2 * tig;
+  const uint8_t* r0 = vbuf + t0 * VROW;
+  const uint8_t* r1 = r0 + VROW;
+  const uint8_t* r2 = r0 + 8 * VROW;
+  const uint8_t* r3 = r2 + VROW;
+  if constexpr (VB == 2) {
+    const uint32_t x0 = *(const uint32_t*)(r0 + 4 * g), x1 = *(const uint32_t*)(r1 + 4 * g);
+    const uint32_t x2 = *(const uint32_t*)(r2 + 4 * g), x3 = *(const uint32_t*)(r3 + 4 * g);
+    // nibble k of zA: codes of coordinate 16g+2k for tokens t0 (bits 0-1) and t0+1 (bits 2-3);
+    // zA2 the same for coordinate 16g+2k+1
+    const uint32_t zA = (x0 & 0x33333333u) | ((x1 & 0x33333333u) << 2);
+    const uint32_t zA2 = ((x0 >> 2) & 0x33333333u) | (x1 & 0xCCCCCCCCu);
+    const uint32_t zB = (x2 & 0x33333333u) | ((x3 & 0x33333333u) << 2);
+    const uint32_t zB2 = ((x2 >> 2) & 0x33333333u) | (x3 & 0xCCCCCCCCu);
+    const uint32_t eA = (zA << 2) & 0x3C3C3C3Cu, oA = (zA >> 2) & 0x3C3C3C3Cu;
+    const uint32_t eA2 = (zA2 << 2) & 0x3C3C3C3Cu, oA2 = (zA2 >> 2) & 0x3C3C3C3Cu;
+    const uint32_t eB = (zB << 2) & 0x3C3C3C3Cu, oB = (zB >> 2) & 0x3C3C3C3Cu;
+    const uint32_t eB2 = (zB2 << 2) & 0x3C3C3C3Cu, oB2 = (zB2 >> 2) & 0x3C3C3C3Cu;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int by = k >> 1;
+      const uint32_t a0 = lut_u32(lutp, byte_of((k & 1) ? oA : eA, by));
+      const uint32_t a1 = lut_u32(lutp, byte_of((k & 1) ? oA2 : eA2, by));
+      const uint32_t a2 = lut_u32(lutp, byte_of((k & 1) ? oB : eB, by));
+      const uint32_t a3 = lut_u32(lutp, byte_of((k & 1) ? oB2 : eB2, by));
+      mma16816(d[k], a0, a1, a2, a3, b0, b1);
+    }
+  } else if constexpr (VB == 3) {
+    // 48 bits of coordinates 16g..16g+15 start at byte 6g of a 48-byte row
+    const int bo = 6 * g;
+    const int sh = 8 * (bo & 3);
+    auto bits48 = [&](const uint8_t* r) {
+      const uint32_t* w = (const uint32_t*)(r + (bo & ~3));
+      return (((uint64_t)w[1] << 32) | w[0]) >> sh;
+    };
+    const uint64_t v0 = bits48(r0), v1 = bits48(r1), v2 = bits48(r2), v3 = bits48(r3);
+    auto pair_off = [](uint64_t va, uint64_t vb, int i) {
+      const uint32_t x = (uint32_t)(va >> (3 * i)), y = (uint32_t)(vb >> (3 * i));
+      return ((x << 2) & 0x1Cu) | ((y << 5) & 0xE0u);
+    };
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t a0 = lut_u32(lutp, pair_off(v0, v1, 2 * k));
+      const uint32_t a1 = lut_u32(lutp, pair_off(v0, v1, 2 * k + 1));
+      const uint32_t a2 = lut_u32(lutp, pair_off(v2, v3, 2 * k));
+      const uint32_t a3 = lut_u32(lutp, pair_off(v2, v3, 2 * k + 1));
+      mma16816(d[k], a0, a1, a2, a3, b0, b1);
+    }
+  } else if constexpr (VB == 4) {
+    const uint2 x0 = *(const uint2*)(r0 + 8 * g), x1 = *(const uint2*)(r1 + 8 * g);
+    const uint2 x2 = *(const uint2*)(r2 + 8 * g), x3 = *(const uint2*)(r3 + 8 * g);
+    const uint32_t w0[2] = {x0.x, x0.y}, w1[2] = {x1.x, x1.y}, w2[2] = {x2.x, x2.y},
+                   w3[2] = {x3.x, x3.y};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int wi = k >> 2, by = k & 3;
+      // low nibble of byte k%4 of word k/4: coordinate 16g+2k; high nibble: 16g+2k+1
+      auto lo = [&](uint32_t w) { return lut_u32(lutp, byte_of((w << 2) & 0x3C3C3C3Cu, by)); };
+      auto hi = [&](uint32_t w) { return lut_u32(lutp, byte_of((w >> 2) & 0x3C3C3C3Cu, by)); };
+      const uint32_t a0 = __byte_perm(lo(w0[wi]), lo(w1[wi]), 0x5410);
+      const uint32_t a1 = __byte_perm(hi(w0[wi]), hi(w1[wi]), 0x5410);
+      const uint32_t a2 = __byte_perm(lo(w2[wi]), lo(w3[wi]), 0x5410);
+      const uint32_t a3 = __byte_perm(hi(w2[wi]), hi(w3[wi]), 0x5410);
+      mma16816(d[k], a0, a1, a2, a3, b0, b1);
+    }
+  } else {   // VB == 8: one byte per coordinate, 16 bytes at byte 16g
+    const uint4 x0 = *(const uint4*)(r0 + 16 * g), x1 = *(const uint4*)(r1 + 16 * g);
+    const uint4 x2 = *(const uint4*)(r2 + 16 * g), x3 = *(const uint4*)(r3 + 16 * g);
+    const uint32_t w0[4] = {x0.x, x0.y, x0.z, x0.w}, w1[4] = {x1.x, x1.y, x1.z, x1.w},
+                   w2[4] = {x2.x, x2.y, x2.z, x2.w}, w3[4] = {x3.x, x3.y, x3.z, x3.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int wi = k >> 1, hh = k & 1;
+      // bytes 2(k%2) and 2(k%2)+1 of word k/2: coordinates 16g+2k, 16g+2k+1
+      auto ev = [&](uint32_t w) { return lut_u32(lutp, half_of((w << 2) & 0x03FC03FCu, hh)); };
+      auto od = [&](uint32_t w) { return lut_u32(lutp, half_of((w >> 6) & 0x03FC03FCu, hh)); };
+      const uint32_t a0 = __byte_perm(ev(w0[wi]), ev(w1[wi]), 0x5410);
+      const uint32_t a1 = __byte_perm(od(w0[wi]), od(w1[wi]), 0x5410);
+      const uint32_t a2 = __byte_perm(ev(w2[wi]), ev(w3[wi]), 0x5410);
+      const uint32_t a3 = __byte_perm(od(w2[wi]), od(w3[wi]), 0x5410);
+      mma16816(d[k], a0, a1, a2, a3, b0, b1);
+    }
+  }
+}
+
+// ---- scores on the tensor cores ---------------------------------------------
+// S[tokens x heads] = K_c[tokens x coords] Q[coords x heads].  The k index is a
+// free permutation of the coordinates: thread (g, tig) supplies columns 2tig,
+// 2tig+1 (and 2tig+8, 2tig+9) of k-tile kt, mapped to coordinates 32tig+4kt,
+// +1 (and +2, +3), so its 32 coordinates are contiguous in a packed row.
+// Key tables (centroids x kCScale): 2 and 3 bits: uint2 (hi pair, lo pair)
+// indexed by the code pair (c_i | c_{i+1} << KB); 4 and 8 bits: u32
+// hi | lo << 16 per code.
+template <int KB>
+struct KCodes {  // one token's 32 codes for this thread, as table offsets
+  uint32_t w[KB];
+};
+
+template <int KB>
+__device__ __forceinline__ void load_kcodes(const uint8_t* row, int tig, KCodes<KB>& c) {
+  if constexpr (KB == 2) {
+    const uint2 x = *(const uint2*)(row + 8 * tig);
+    c.w[0] = x.x;
+    c.w[1] = x.y;
+  } else if constexpr (KB == 3) {
+    const uint32_t* p = (const uint32_t*)(row + 12 * tig);
+    c.w[0] = p[0];
+    c.w[1] = p[1];
+    c.w[2] = p[2];
+  } else if constexpr (KB == 4) {
+    const uint4 x = *(const uint4*)(row + 16 * tig);
+    c.w[0] = x.x; c.w[1] = x.y; c.w[2] = x.z; c.w[3] = x.w;
+  } else {
+    const uint4 x = *(const uint4*)(row + 32 * tig);
+    const uint4 y = *(const uint4*)(row + 32 * tig + 16);
+    c.w[0] = x.x; c.w[1] = x.y; c.w[2] = x.z; c.w[3] = x.w;
+    c.w[4] = y.x; c.w[5] = y.y; c.w[6] = y.z; c.w[7] = y.w;
+  }
+}
+
+// (hi pair, lo pair) operand of coordinates 32tig + i, i+1 (i even, compile time)
+template <int KB, int I>
+__device__ __forceinline__ void kpair(const KCodes<KB>& c, const uint32_t* lut, uint32_t& hi,
+                                      uint32_t& lo) {
+  if constexpr (KB == 2) {
+    // nibble I/2 of the 64 code bits: byte (I/4) % 4 of word I/16, low or high nibble
+    const uint32_t w = c.w[I / 16];
+    const uint32_t off = (I / 2) % 2 == 0 ? byte_of((w << 3) & 0x78787878u, (I / 4) % 4)
+                                          : byte_of((w >> 1) & 0x78787878u, (I / 4) % 4);
+    const uint2 e = *(const uint2*)((const char*)lut + off);
+    hi = e.x;
+    lo = e.y;
+  } else if constexpr (KB == 3) {
+    constexpr int o = 3 * I;                     // bit offset of the pair (6 bits)
+    uint32_t v;
+    if constexpr (o + 6 <= 32) {
+      v = c.w[0] >> o;
+    } else if constexpr (o < 32) {
+      v = (c.w[0] >> o) | (c.w[1] << (32 - o));
+    } else if constexpr (o + 6 <= 64) {
+      v = c.w[1] >> (o - 32);
+    } else if constexpr (o < 64) {
+      v = (c.w[1] >> (o - 32)) | (c.w[2] << (64 - o));
+    } else {
+      v = c.w[2] >> (o - 64);
+    }
+    const uint2 e = *(const uint2*)((const char*)lut + ((v << 3) & 0x1F8u));
+    hi = e.x;
+    lo = e.y;
+  } else if constexpr (KB == 4) {
+    // byte I/2 of the 128 code bits: word I/8, byte (I/2)%4; low nibble = c_I
+    const uint32_t w = c.w[I / 8];
+    const uint32_t e0 = *(const uint32_t*)((const char*)lut + byte_of((w << 2) & 0x3C3C3C3Cu, (I / 2) % 4));
+    const uint32_t e1 = *(const uint32_t*)((const char*)lut + byte_of((w >> 2) & 0x3C3C3C3Cu, (I / 2) % 4));
+    pack_hilo(e0, e1, hi, lo);
+  } else {
+    // bytes I, I+1 of the 256 code bits: word I/4, half (I/2)%2
+    const uint32_t w = c.w[I / 4];
+    const uint32_t e0 = *(const uint32_t*)((const char*)lut + half_of((w << 2) & 0x03FC03FCu, (I / 2) % 2));
+    const uint32_t e1 = *(const uint32_t*)((const char*)lut + half_of((w >> 6) & 0x03FC03FCu, (I / 2) % 2));
+    pack_hilo(e0, e1, hi, lo);
+  }
+}
+
+// Scores of tokens ta (rows g) and ta+8 (rows g+8) for heads 2tig, 2tig+1.
+template <int KB, int KT>
+__device__ __forceinline__ void score_ktile(const KCodes<KB>& ca, const KCodes<KB>& cb,
+                                            const uint32_t* lut, const uint32_t (&bh)[8][2],
+                                            const uint32_t (&bl)[8][2], float (&d)[4]) {
+  uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
+  kpair<KB, 4 * KT>(ca, lut, h0, l0);
+  kpair<KB, 4 * KT>(cb, lut, h1, l1);
+  kpair<KB, 4 * KT + 2>(ca, lut, h2, l2);
+  kpair<KB, 4 * KT + 2>(cb, lut, h3, l3);
+  mma16816(d, h0, h1, h2, h3, bh[KT][0], bh[KT][1]);
+  mma16816(d, l0, l1, l2, l3, bh[KT][0], bh[KT][1]);
+  mma16816(d, h0, h1, h2, h3, bl[KT][0], bl[KT][1]);
+}
+
+template <int KB, int KT>
+__device__ __forceinline__ void score_all(const KCodes<KB>& ca, const KCodes<KB>& cb,
+                                          const uint32_t* lut, const uint32_t (&bh)[8][2],
+                                          const uint32_t (&bl)[8][2], float (&d)[4]) {
+  if constexpr (KT < 8) {
+    score_ktile<KB, KT>(ca, cb, lut, bh, bl, d);
+    score_all<KB, KT + 1>(ca, cb, lut, bh, bl, d);
+  }
+}
+
+// QJL: sum_j (2 bit_j - 1) (S q)_j for tokens ta, ta+8: A = exact +-1 signs,
+// B = S q hi and lo (per lane, per k-tile, from shared memory).
+__device__ __forceinline__ void qjl_scores(uint32_t sa, uint32_t sb, const uint32_t* slut,
+                                           const uint4* qb, float (&d)[4]) {
+#pragma unroll
+  for (int kt = 0; kt < 8; ++kt) {
+    // sign bits 4kt, 4kt+1 (pair 0) and 4kt+2, 4kt+3 (pair 1) of this lane's 32
+    const uint32_t a0 = slut[(sa >> (4 * kt)) & 3u], a1 = slut[(sb >> (4 * kt)) & 3u];
+    const uint32_t a2 = slut[(sa >> (4 * kt + 2)) & 3u], a3 = slut[(sb >> (4 * kt + 2)) & 3u];
+    const uint4 b = qb[kt];
+    mma16816(d, a0, a1, a2, a3, b.x, b.y);
+    mma16816(d, a0, a1, a2, a3, b.z, b.w);
+  }
+}
+
+template <int G, int KB, int VB, bool QJL>
+__global__ void __launch_bounds__(kDT, 3) decode_kernel(const DecodeArgs a) {
+  constexpr int KROW = 16 * KB, VROW = 16 * VB;
+  __shared__ __align__(16) uint32_t lutk[256];   // K centroid tables (see kpair)
+  __shared__ __align__(16) uint32_t lutv[256];   // V fp16 centroids (pairs for 2/3 bits)
+  __shared__ uint32_t slut[4];                   // (+-1, +-1) fp16 pairs of two sign bits
+  extern __shared__ __align__(128) uint8_t smem[];
+  const DecodeSmem L(G, QJL ? 1 : 0, KB, VB);
+  float* qr = (float*)(smem + L.qr);
+  float* qo = (float*)(smem + L.qo);
+  float* svs = (float*)(smem + L.sv);
+  int* is_last = (int*)(smem + L.total - 16);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int Hkv = a.Hkv;
+  const uint32_t limit = a.wait_limit ? a.wait_limit : kDefaultWaitLimit;
+  const int mg = lane >> 2, tig = lane & 3;   // MMA group / thread-in-group
+
+  // ------------------------------------------------------------- prologue
+  for (int i = tid; i < 256; i += kDT) {
+    if constexpr (KB == 2 || KB == 3) {
+      if (i < (1 << (2 * KB))) {
+        const int msk = (1 << KB) - 1;
+        const uint32_t e0 = hilo(a.ck[i & msk] * kCScale), e1 = hilo(a.ck[(i >> KB) & msk] * kCScale);
+        uint32_t hp, lp;
+        pack_hilo(e0, e1, hp, lp);
+        lutk[2 * i] = hp;
+        lutk[2 * i + 1] = lp;
+      }
+    } else {
+      lutk[i] = hilo(a.ck[i] * kCScale);
+    }
+    uint32_t e;
+    if constexpr (VB == 2 || VB == 3) {
+      const int msk = (1 << VB) - 1;
+      e = (h16(a.cv[(i >> VB) & msk]) << 16) | h16(a.cv[i & msk]);
+    } else {
+      e = h16(a.cv[i]);
+    }
+    lutv[i] = e;
+  }
+  if (tid < 4) slut[tid] = ((tid & 2) ? 0x3C000000u : 0xBC000000u) | ((tid & 1) ? 0x3C00u : 0xBC00u);
+  svs[tid] = a.sv[tid];
+  uint8_t* wreg = smem + L.warps + warp * L.warp_stride;
+  uint64_t* bar = (uint64_t*)(wreg + L.bar);
+  float* scratch = (float*)(smem + L.warps);        // [G][128], aliases warp buffers
+  {
+    const long long qbase = ((long long)b * a.Hq + (long long)kvh * G) * kD2;
+    for (int e = tid; e < G * kD2; e += kDT) {
+      const int g = e / kD2, i = e % kD2;
+      float v = a.q_f32 ? ((const float*)a.q)[qbase + e]
+                        : __uint_as_float((uint32_t)((const uint16_t*)a.q)[qbase + e] << 16);
+      v *= a.qscale;
+      qo[i * G + g] = v;
+      scratch[g * kD2 + i] = v * a.sk[i];
+    }
+  }
+  __syncthreads();
+  for (int h = 1; h < kD2; h <<= 1) {               // butterfly, Sylvester order
+    for (int e = tid; e < G * (kD2 / 2); e += kDT) {
+      const int g = e / (kD2 / 2), r = e % (kD2 / 2);
+      const int i = (r / h) * 2 * h + (r % h);
+      float* x = scratch + g * kD2;
+      const float u = x[i], v = x[i + h];
+      x[i] = u + v;
+      x[i + h] = u - v;
+    }
+    __syncthreads();
+  }
+  float qmax = 0.f;
+  for (int e = tid; e < G * kD2; e += kDT) {
+    const int g = e / kD2, i = e % kD2;
+    const float v = scratch[e] * 0.08838834764831845f;   // 1/sqrt(128)
+    qr[i * G + g] = v;
+    qmax = fmaxf(qmax, fabsf(v));
+  }
+  // power-of-two scale bringing max |q_rot| below 1 for the fp16 operands
+  __shared__ float red[kDWarps];
+  qmax = warp_max(qmax);
+  if (lane == 0) red[warp] = qmax;
+  __syncthreads();
+  qmax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  int qe = 0;
+  (void)frexpf(qmax, &qe);
+  const float qsp = qmax > 0.f ? ldexpf(1.f, -qe) : 1.f;
+  // B operands (q hi/lo) of this lane: head mg, coordinates 32tig + 4kt + {0,1} / {2,3}
+  uint32_t bh[8][2], bl[8][2];
+#pragma unroll
+  for (int kt = 0; kt < 8; ++kt) {
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      uint32_t hp = 0u, lp = 0u;
+      if (mg < G) {
+        const int c = 32 * tig + 4 * kt + 2 * p;
+        pack_hilo(hilo(qr[c * G + mg] * qsp), hilo(qr[(c + 1) * G + mg] * qsp), hp, lp);
+      }
+      bh[kt][p] = hp;
+      bl[kt][p] = lp;
+    }
+  }
+  float qsq = 1.f;                                   // scale of the S q operands
+  if constexpr (QJL) {
+    __syncthreads();                                 // scratch is reused below
+    float* sq = scratch;                             // [G][m]
+    float smax = 0.f;
+    for (int j = tid; j < kQjlM; j += kDT) {
+      float acc[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) acc[g] = 0.f;
+      const uint16_t* Sj = a.S + (size_t)j * kD2;
+      for (int k = 0; k < kD2; ++k) {
+        const float sv = __uint_as_float((uint32_t)Sj[k] << 16);
+#pragma unroll
+        for (int g = 0; g < G; ++g) acc[g] = fmaf(sv, qr[k * G + g], acc[g]);
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        sq[g * kQjlM + j] = acc[g];
+        smax = fmaxf(smax, fabsf(acc[g]));
+      }
+    }
+    smax = warp_max(smax);
+    __syncthreads();
+    if (lane == 0) red[warp] = smax;
+    __syncthreads();
+    smax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    int se = 0;
+    (void)frexpf(smax, &se);
+    qsq = smax > 0.f ? ldexpf(1.f, -se) : 1.f;
+    // per lane, per k-tile: (b0 hi, b1 hi, b0 lo, b1 lo) of head lane/4, sketch
+    // indices 32(lane%4) + 4kt + {0,1} / {2,3}
+    uint4* qjlb = (uint4*)(smem + L.qjlb);
+    for (int e = tid; e < 32 * 8; e += kDT) {
+      const int ln = e / 8, kt = e % 8, g = ln >> 2, tg = ln & 3;
+      uint4 o = make_uint4(0u, 0u, 0u, 0u);
+      if (g < G) {
+        const int c = 32 * tg + 4 * kt;
+        pack_hilo(hilo(sq[g * kQjlM + c] * qsq), hilo(sq[g * kQjlM + c + 1] * qsq), o.x, o.z);
+        pack_hilo(hilo(sq[g * kQjlM + c + 2] * qsq), hilo(sq[g * kQjlM + c + 3] * qsq), o.y, o.w);
+      }
+      qjlb[e] = o;
+    }
+  }
+  __syncthreads();
+  if (lane == 0) {
+    mbar_init(bar + 0, 1);
+    mbar_init(bar + 1, 1);
+    fence_mbarrier_init();
+  }
+  __syncwarp();
+
+  // ------------------------------------------------------------- main loop
+  const int T = a.seq_lens[b];
+  const int W = a.W;
+  const int nq = T - W > 0 ? T - W : 0;
+  const bool window_split = split >= a.n_qsplits;
+  float* cm = (float*)(smem + L.comb);   // [warps][G]      (merge area, after the loop)
+  float* cl = cm + kDWarps * G;          // [warps][G]
+  float* co = cl + kDWarps * G;          // [warps][G][128]
+
+  if (!window_split) {
+    // online-softmax state of heads 2tig, 2tig+1 (accumulator columns)
+    float m0 = kNegBig, m1 = kNegBig, l0 = 0.f, l1 = 0.f;
+    float d[8][4];           // fp32 V-sum accumulators (MMA layout)
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) d[k][j] = 0.f;
+    const bool h0ok = 2 * tig < G, h1ok = 2 * tig + 1 < G;
+    const int t_begin = split * a.split_tokens;
+    int t_end = t_begin + a.split_tokens;
+    if (t_end > nq) t_end = nq;
+    const long long row0 = ((long long)b * Hkv + kvh);
+    const uint8_t* kc = a.kc + row0 * a.kcap * KROW;
+    const uint8_t* vc = a.vc + row0 * a.vcap * VROW;
+    const float* knp = a.kn + row0 * a.kcap;
+    const float* vnp = a.vn + row0 * a.vcap;
+    const uint8_t* ksp = QJL ? a.ks + row0 * a.kcap * 16 : nullptr;
+    const float* krp = QJL ? a.kr + row0 * a.kcap : nullptr;
+    uint16_t* ws16 = (uint16_t*)(wreg + L.ws);   // [8 heads][32 tokens] fp16 weights
+    const float kscale = 1.f / (kCScale * qsp);
+    const float qjl_scale = 1.2533141373155003f / (float)kQjlM / qsq;   // sqrt(pi/2)/m
+    const uint4* qjlb = QJL ? (const uint4*)(smem + L.qjlb) + lane * 8 : nullptr;
+
+    // chunk c0 -> ring slot: codes by bulk copy; norms by bulk copy when the
+    // 16-byte-rounded range stays inside the plane, else by plain loads
+    auto issue = [&](int c0, int slot) {
+      const int nv = t_end - c0 < 32 ? t_end - c0 : 32;
+      const int n4 = (nv + 3) & ~3;
+      // bulk copies need 16-byte aligned sources: the norm rows of a (sequence,
+      // head) start at row0 * capacity floats, aligned only if capacity % 4 == 0
+      const bool aligned = (((uintptr_t)(knp + c0) | (uintptr_t)(vnp + c0) |
+                             (QJL ? (uintptr_t)(krp + c0) : (uintptr_t)0)) & 15u) == 0;
+      const bool bulk_norms =
+          aligned && (long long)c0 + n4 <= a.kcap && (long long)c0 + n4 <= a.vcap;
+      uint8_t* kb_ = wreg + L.kbuf + slot * 32 * KROW;
+      uint8_t* vb_ = wreg + L.vbuf + slot * 32 * VROW;
+      float* kn_ = (float*)(wreg + L.kn + slot * 128);
+      float* vn_ = (float*)(wreg + L.vn + slot * 128);
+      if (!bulk_norms && lane < nv) {
+        kn_[lane] = knp[c0 + lane];
+        vn_[lane] = vnp[c0 + lane];
+        if constexpr (QJL) ((float*)(wreg + L.rn + slot * 128))[lane] = krp[c0 + lane];
+      }
+      __syncwarp();
+      if (lane == 0) {
+        uint32_t bytes = nv * (KROW + VROW) + (bulk_norms ? 2 * n4 * 4 : 0);
+        if constexpr (QJL) bytes += nv * 16 + (bulk_norms ? n4 * 4 : 0);
+        mbar_arrive_expect_tx(bar + slot, bytes);
+        bulk_g2s(kb_, kc + (long long)c0 * KROW, nv * KROW, bar + slot);
+        bulk_g2s(vb_, vc + (long long)c0 * VROW, nv * VROW, bar + slot);
+        if (bulk_norms) {
+          bulk_g2s(kn_, knp + c0, n4 * 4, bar + slot);
+          bulk_g2s(vn_, vnp + c0, n4 * 4, bar + slot);
+        }
+        if constexpr (QJL) {
+          bulk_g2s(wreg + L.sbuf + slot * 512, ksp + (long long)c0 * 16, nv * 16, bar + slot);
+          if (bulk_norms) bulk_g2s(wreg + L.rn + slot * 128, krp + c0, n4 * 4, bar + slot);
+        }
+      }
+    };
+
+    int c0 = t_begin + 32 * warp;
+    if (c0 < t_end) issue(c0, 0);
+    bool ok = true;
+    int kq = 0;
+    for (; c0 < t_end; c0 += 32 * kDWarps, ++kq) {
+      const int slot = kq & 1;
+      const int c1 = c0 + 32 * kDWarps;
+      if (c1 < t_end) issue(c1, slot ^ 1);
+      ok = __all_sync(0xffffffffu, mbar_wait(bar + slot, (kq >> 1) & 1, limit, a.err));
+      if (!ok) break;
+      const int nv = t_end - c0 < 32 ? t_end - c0 : 32;
+      const uint8_t* kb_ = wreg + L.kbuf + slot * 32 * KROW;
+      const float* kn_ = (const float*)(wreg + L.kn + slot * 128);
+      const float* vn_ = (const float*)(wreg + L.vn + slot * 128);
+      // ---- scores on the tensor cores: sc[mt][0,1] token 16mt+mg, sc[mt][2,3] token +8;
+      //      columns 0 / 1 are heads 2tig / 2tig+1
+      float sc[2][4];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        const int ta = 16 * mt + mg, tb = ta + 8;
+        KCodes<KB> ca, cb;
+        load_kcodes<KB>(kb_ + ta * KROW, tig, ca);
+        load_kcodes<KB>(kb_ + tb * KROW, tig, cb);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        score_all<KB, 0>(ca, cb, lutk, bh, bl, acc);
+        const float na = kn_[ta] * kscale, nb = kn_[tb] * kscale;
+        sc[mt][0] = acc[0] * na;
+        sc[mt][1] = acc[1] * na;
+        sc[mt][2] = acc[2] * nb;
+        sc[mt][3] = acc[3] * nb;
+        if constexpr (QJL) {
+          const uint8_t* sb_ = wreg + L.sbuf + slot * 512;
+          const float* rn_ = (const float*)(wreg + L.rn + slot * 128);
+          const uint32_t sa = *(const uint32_t*)(sb_ + ta * 16 + 4 * tig);
+          const uint32_t sbits = *(const uint32_t*)(sb_ + tb * 16 + 4 * tig);
+          float qa[4] = {0.f, 0.f, 0.f, 0.f};
+          qjl_scores(sa, sbits, slut, qjlb, qa);
+          const float ga = rn_[ta] * qjl_scale, gb = rn_[tb] * qjl_scale;
+          sc[mt][0] = fmaf(qa[0], ga, sc[mt][0]);
+          sc[mt][1] = fmaf(qa[1], ga, sc[mt][1]);
+          sc[mt][2] = fmaf(qa[2], gb, sc[mt][2]);
+          sc[mt][3] = fmaf(qa[3], gb, sc[mt][3]);
+        }
+        if (ta >= nv || !h0ok) sc[mt][0] = kNegBig;
+        if (ta >= nv || !h1ok) sc[mt][1] = kNegBig;
+        if (tb >= nv || !h0ok) sc[mt][2] = kNegBig;
+        if (tb >= nv || !h1ok) sc[mt][3] = kNegBig;
+      }
+      // ---- online softmax (log2 domain) per head column; reduce over mg
+      float x0 = fmaxf(fmaxf(sc[0][0], sc[0][2]), fmaxf(sc[1][0], sc[1][2]));
+      float x1 = fmaxf(fmaxf(sc[0][1], sc[0][3]), fmaxf(sc[1][1], sc[1][3]));
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, o));
+        x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, o));
+      }
+      const float mn0 = fmaxf(m0, x0), mn1 = fmaxf(m1, x1);
+      const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+      m0 = mn0;
+      m1 = mn1;
+      float w[2][4];
+      float wloc = 0.f, ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        const int ta = 16 * mt + mg, tb = ta + 8;
+        const float va = ta < nv ? vn_[ta] : 0.f, vb = tb < nv ? vn_[tb] : 0.f;
+        const float p0 = exp2f(sc[mt][0] - mn0), p1 = exp2f(sc[mt][1] - mn1);
+        const float p2 = exp2f(sc[mt][2] - mn0), p3 = exp2f(sc[mt][3] - mn1);
+        ps0 += p0 + p2;
+        ps1 += p1 + p3;
+        w[mt][0] = p0 * va;
+        w[mt][1] = p1 * va;
+        w[mt][2] = p2 * vb;
+        w[mt][3] = p3 * vb;
+        wloc = fmaxf(wloc, fmaxf(fmaxf(w[mt][0], w[mt][1]), fmaxf(w[mt][2], w[mt][3])));
+      }
+      l0 = fmaf(l0, al0, ps0);
+      l1 = fmaf(l1, al1, ps1);
+      const float wmax = warp_max(wloc);
+      const float scl = wmax > 0.f ? 16384.f / wmax : 1.f;
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        const int ta = 16 * mt + mg, tb = ta + 8;
+        if (h0ok) {
+          ws16[(2 * tig) * 32 + ta] = (uint16_t)h16(w[mt][0] * scl);
+          ws16[(2 * tig) * 32 + tb] = (uint16_t)h16(w[mt][2] * scl);
+        }
+        if (h1ok) {
+          ws16[(2 * tig + 1) * 32 + ta] = (uint16_t)h16(w[mt][1] * scl);
+          ws16[(2 * tig + 1) * 32 + tb] = (uint16_t)h16(w[mt][3] * scl);
+        }
+      }
+      __syncwarp();
+      // ---- rotated-domain V sum on the tensor cores: d = (alpha d) + V^T W
+      const float2 pre = make_float2(al0 * scl, al1 * scl);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float2 lo = __fmul2_rn(make_float2(d[k][0], d[k][1]), pre);
+        const float2 hi = __fmul2_rn(make_float2(d[k][2], d[k][3]), pre);
+        d[k][0] = lo.x; d[k][1] = lo.y; d[k][2] = hi.x; d[k][3] = hi.y;
+      }
+      const uint8_t* vb_ = wreg + L.vbuf + slot * 32 * VROW;
+#pragma unroll
+      for (int kt = 0; kt < 2; ++kt) {
+        const uint32_t b0 = mg < G ? *(const uint32_t*)(ws16 + mg * 32 + 16 * kt + 2 * tig) : 0u;
+        const uint32_t b1 = mg < G ? *(const uint32_t*)(ws16 + mg * 32 + 16 * kt + 2 * tig + 8) : 0u;
+        vmma_ktile<VB>(vb_, lutv, kt, mg, tig, b0, b1, d);
+      }
+      const float inv = 1.f / scl;
+      const float2 post = make_float2(inv, inv);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float2 lo = __fmul2_rn(make_float2(d[k][0], d[k][1]), post);
+        const float2 hi = __fmul2_rn(make_float2(d[k][2], d[k][3]), post);
+        d[k][0] = lo.x; d[k][1] = lo.y; d[k][2] = hi.x; d[k][3] = hi.y;
+      }
+      __syncwarp();
+    }
+    if (!ok) {
+      // a staging wait ran out (error word set): give the copies still in
+      // flight (at most one chunk per ring slot) a bounded wait, then stop
+      for (int dd = 0; dd < 2; ++dd) {
+        const int kk = kq + dd;
+        if (t_begin + 32 * warp + kk * 32 * kDWarps >= t_end) break;
+        for (uint32_t i = 0; i < limit && !mbar_try_wait(bar + (kk & 1), (kk >> 1) & 1); ++i) {
+        }
+      }
+    }
+    // per-head l: sum over the 8 lanes of each column group
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+    }
+    __syncthreads();                     // every warp is done with its ring buffers
+    if (mg == 0) {
+      if (h0ok) {
+        cm[warp * G + 2 * tig] = m0;
+        cl[warp * G + 2 * tig] = l0;
+      }
+      if (h1ok) {
+        cm[warp * G + 2 * tig + 1] = m1;
+        cl[warp * G + 2 * tig + 1] = l1;
+      }
+    }
+    // thread (mg, tig): m-tile k rows -> coordinates 16mg+2k (+1); columns -> heads 2tig (+1)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int c = 16 * mg + 2 * k;
+      if (h0ok) {
+        float* dst = co + (warp * G + 2 * tig) * kD2 + c;
+        dst[0] = d[k][0];
+        dst[1] = d[k][2];
+      }
+      if (h1ok) {
+        float* dst = co + (warp * G + 2 * tig + 1) * kD2 + c;
+        dst[0] = d[k][1];
+        dst[1] = d[k][3];
+      }
+    }
+  } else {
+    // residual window: tokens [T - nw, T) in slots t mod W, original domain
+    float m[G], l[G], ow[G][4];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      m[g] = kNegBig;
+      l[g] = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) ow[g][j] = 0.f;
+    }
+    const int nw = T < W ? T : W;
+    const int tw0 = T - nw;
+    const long long base = ((long long)b * Hkv + kvh) * W;
+    // warp w takes window tokens w, w+4, ...; 8 tokens' rows are loaded before
+    // any is used, so the loads overlap instead of paying one latency each
+    for (int k0 = warp; k0 < nw; k0 += 8 * kDWarps) {
+      uint2 kw[8], vw[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int k = k0 + u * kDWarps;
+        if (k < nw) {
+          const long long slotrow = (base + (tw0 + k) % W) * kD2;
+          kw[u] = *(const uint2*)(a.kwin + slotrow + 4 * lane);
+          vw[u] = *(const uint2*)(a.vwin + slotrow + 4 * lane);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (k0 + u * kDWarps >= nw) break;
+        const float kx[4] = {bf16lo(kw[u].x), bf16hi(kw[u].x), bf16lo(kw[u].y), bf16hi(kw[u].y)};
+        const float vx[4] = {bf16lo(vw[u].x), bf16hi(vw[u].x), bf16lo(vw[u].y), bf16hi(vw[u].y)};
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float part = 0.f;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) part = fmaf(qo[(4 * lane + j) * G + g], kx[j], part);
+          const float s = warp_sum(part);
+          const float mnew = fmaxf(m[g], s);
+          const float al = exp2f(m[g] - mnew);
+          const float p = exp2f(s - mnew);
+          l[g] = fmaf(l[g], al, p);
+          m[g] = mnew;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) ow[g][j] = fmaf(p, vx[j], ow[g][j] * al);
+        }
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      if (lane == 0) {
+        cm[warp * G + g] = m[g];
+        cl[warp * G + g] = l[g];
+      }
+      *(float4*)(co + (warp * G + g) * kD2 + 4 * lane) =
+          make_float4(ow[g][0], ow[g][1], ow[g][2], ow[g][3]);
+    }
+  }
+
+  // ------------------------------------------------------------- epilogue
+  __syncthreads();
+  const long long unit = (long long)b * Hkv + kvh;
+  const int stride = kPartialStride;
+  float* part = a.partials + (unit * a.n_splits + split) * G * stride;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float M = kNegBig;
+#pragma unroll
+    for (int w = 0; w < kDWarps; ++w) M = fmaxf(M, cm[w * G + g]);
+    float O = 0.f, Lsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kDWarps; ++w) {
+      const float f = exp2f(cm[w * G + g] - M);
+      O = fmaf(co[(w * G + g) * kD2 + tid], f, O);
+      Lsum = fmaf(cl[w * G + g], f, Lsum);
+    }
+    part[g * stride + 4 + tid] = O;
+    if (tid == 0) {
+      part[g * stride] = M;
+      part[g * stride + 1] = Lsum;
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned prev = atomicAdd(&a.counters[unit], 1u);
+    *is_last = prev == (unsigned)(a.n_splits - 1);
+  }
+  __syncthreads();
+  if (!*is_last) return;
+  __threadfence();
+
+  // last CTA of this (sequence, kv-head): one warp per head merges the splits,
+  // inverse-rotates (R^T = D_s H / sqrt(d)) in registers and writes the output
+  const float* base = a.partials + unit * a.n_splits * G * stride;
+  float* fsc = (float*)(smem + L.comb);  // [warps][32] per-split factors (merge area is free now)
+  for (int g = warp; g < G; g += kDWarps) {
+    // pass 1, lanes over splits: M = max m_s, L = sum l_s 2^(m_s - M)
+    float M = kNegBig;
+    for (int s2 = lane; s2 < a.n_splits; s2 += 32) M = fmaxf(M, __ldcg(base + (s2 * G + g) * stride));
+    M = warp_max(M);
+    float Lsum = 0.f;
+    for (int s2 = lane; s2 < a.n_splits; s2 += 32) {
+      const float* ps = base + (s2 * G + g) * stride;
+      Lsum = fmaf(__ldcg(ps + 1), exp2f(__ldcg(ps) - M), Lsum);
+    }
+    Lsum = warp_sum(Lsum);
+    // pass 2, lanes over coordinates: 8 split rows in flight at a time
+    float4 rot = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < a.n_qsplits; s0 += 32) {
+      const int ns = a.n_qsplits - s0 < 32 ? a.n_qsplits - s0 : 32;
+      if (lane < ns) fsc[warp * 32 + lane] = exp2f(__ldcg(base + ((s0 + lane) * G + g) * stride) - M);
+      __syncwarp();
+      int j = 0;
+      for (; j + 8 <= ns; j += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = __ldcg((const float4*)(base + ((s0 + j + u) * G + g) * stride + 4) + lane);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float f = fsc[warp * 32 + j + u];
+          rot.x = fmaf(v[u].x, f, rot.x);
+          rot.y = fmaf(v[u].y, f, rot.y);
+          rot.z = fmaf(v[u].z, f, rot.z);
+          rot.w = fmaf(v[u].w, f, rot.w);
+        }
+      }
+      for (; j < ns; ++j) {
+        const float4 v = __ldcg((const float4*)(base + ((s0 + j) * G + g) * stride + 4) + lane);
+        const float f = fsc[warp * 32 + j];
+        rot.x = fmaf(v.x, f, rot.x);
+        rot.y = fmaf(v.y, f, rot.y);
+        rot.z = fmaf(v.z, f, rot.z);
+        rot.w = fmaf(v.w, f, rot.w);
+      }
+      __syncwarp();
+    }
+    float4 win = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (a.n_splits > a.n_qsplits) {
+      const float* ps = base + (a.n_qsplits * G + g) * stride;
+      const float f = exp2f(__ldcg(ps) - M);
+      const float4 v = __ldcg((const float4*)(ps + 4) + lane);
+      win = make_float4(v.x * f, v.y * f, v.z * f, v.w * f);
+    }
+    // butterfly over 128 values, 4 per lane (coordinates 4*lane .. 4*lane+3)
+    float x[4] = {rot.x, rot.y, rot.z, rot.w};
+    {
+      float u0 = x[0] + x[1], u1 = x[0] - x[1], u2 = x[2] + x[3], u3 = x[2] - x[3];
+      x[0] = u0 + u2; x[2] = u0 - u2; x[1] = u1 + u3; x[3] = u1 - u3;
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const bool upper = (lane & o) != 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float other = __shfl_xor_sync(0xffffffffu, x[j], o);
+        x[j] = upper ? other - x[j] : x[j] + other;
+      }
+    }
+    const float4 sv4 = *(const float4*)(svs + 4 * lane);
+    const float r = 0.08838834764831845f;
+    const float inv = Lsum > 0.f ? 1.0f / Lsum : 0.f;
+    const float4 res = make_float4((x[0] * r * sv4.x + win.x) * inv, (x[1] * r * sv4.y + win.y) * inv,
+                                   (x[2] * r * sv4.z + win.z) * inv, (x[3] * r * sv4.w + win.w) * inv);
+    *(float4*)(a.out + ((long long)b * a.Hq + (long long)kvh * G + g) * kD2 + 4 * lane) = res;
+  }
+  if (tid == 0) a.counters[unit] = 0u;   // leave the counter ready for the next call
+}
+
+
+template <int G, int KB, int VB, bool QJL>
+int launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
+  auto k = decode_kernel<G, KB, VB, QJL>;
+  const size_t smem = (size_t)DecodeSmem(G, QJL ? 1 : 0, KB, VB).total;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return 1;
+  dim3 grid((unsigned)a.n_splits, (unsigned)a.Hkv, (unsigned)a.B);
+  k<<<grid, kDT, smem, s>>>(a);
+  return cudaGetLastError() != cudaSuccess;
+}
+
+// Dispatch over (KB, VB, QJL) for one G; defined once per G translation unit.
+template <int G>
+int launch_decode_g(const DecodeArgs& a, cudaStream_t s) {
+#define TQ_VB_CASES(KB_, QJL_)                                               \
+  switch (a.vb) {                                                          \
+    case 2: return launch_decode_t<G, KB_, 2, QJL_>(a, s);                 \
+    case 3: return launch_decode_t<G, KB_, 3, QJL_>(a, s);                 \
+    case 4: return launch_decode_t<G, KB_, 4, QJL_>(a, s);                 \
+    case 8: return launch_decode_t<G, KB_, 8, QJL_>(a, s);                 \
+  }                                                                        \
+  return 1;
+  if (a.qjl) {
+    switch (a.kb) {
+      case 2: { TQ_VB_CASES(2, true) }
+      case 3: { TQ_VB_CASES(3, true) }
+      case 4: { TQ_VB_CASES(4, true) }
+    }
+    return 1;
+  }
+  switch (a.kb) {
+    case 2: { TQ_VB_CASES(2, false) }
+    case 3: { TQ_VB_CASES(3, false) }
+    case 4: { TQ_VB_CASES(4, false) }
+    case 8: { TQ_VB_CASES(8, false) }
+  }
+#undef TQ_VB_CASES
+  return 1;
+}
+
+}  // namespace tq

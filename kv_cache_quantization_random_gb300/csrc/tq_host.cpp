@@ -346,7 +346,7 @@ static DecodePlan decode_plan(const tq_config* cfg, int batch, int n_q_heads, in
   p.n_qsplits = (int)((max_nq + st - 1) / st);
   p.n_splits = p.n_qsplits + (W > 0 ? 1 : 0);
   p.G = n_kv_heads > 0 ? n_q_heads / n_kv_heads : 0;
-  p.partial_floats = (size_t)units * p.n_splits * p.G * (2 + cfg->head_dim);
+  p.partial_floats = (size_t)units * p.n_splits * p.G * kPartialStride;
   p.counters_off = align256(p.partial_floats * sizeof(float));
   p.total = p.counters_off + align256((size_t)units * sizeof(unsigned));
   return p;
@@ -623,12 +623,7 @@ extern "C" tq_status tq_decode_attention(const tq_config* cfg, const void* table
   a.partials = (float*)workspace;
   a.counters = (unsigned*)((uint8_t*)workspace + p.counters_off);
   a.err = decode_error_ptr();
-  auto pitch = [](int bits) {
-    int bytes = 16 * bits;               // code bytes of a d = 128 row
-    return (bytes / 16) % 2 == 0 ? bytes + 16 : bytes;
-  };
-  a.pk = pitch(a.kb);
-  a.pv = pitch(a.vb);
+  a.wait_limit = g_wait_limit;
   if (p.n_splits == 0) {
     // every sequence is empty: the output is zero
     if (cudaMemsetAsync(out, 0, (size_t)batch * n_q_heads * kHeadDim * sizeof(float),

@@ -11,9 +11,8 @@ namespace tq {
 
 constexpr int kHeadDim = 128;          // the head_dim the kernels implement
 constexpr int kQjlM = 128;             // the QJL projection count the kernels implement
-constexpr int kTargetCtas = 4 * 152;   // decode grid target: 4 CTAs per GB300 SM
-constexpr int kDecodeWarps = 4;        // warps per decode CTA
-constexpr int kChunk = 32;             // tokens per warp round in decode
+constexpr int kTargetCtas = 3 * 152;   // decode grid target: 3 resident CTAs per GB300 SM
+constexpr int kPartialStride = 4 + kHeadDim;   // floats per (split, head): m, l, pad, pad, o[d]
 
 // ---- device tables (built on the host by tq_build_tables) -------------------
 // [0, 256)                 header, int32 words (see kTbl*)
@@ -110,10 +109,10 @@ struct DecodeArgs {
   const uint16_t* S;
   // outputs / workspace
   float* out;
-  float* partials;               // [B][Hkv][n_splits][G][2 + d]
+  float* partials;               // [B][Hkv][n_splits][G][4 + d]
   unsigned* counters;            // [B][Hkv]
   unsigned* err;
-  int pk, pv;                    // smem row pitches of K / V code rows
+  uint32_t wait_limit;           // polls per bounded wait (0 = default)
 };
 
 // ---- launchers (defined in the .cu files) -------------------------------------
@@ -121,7 +120,6 @@ int launch_quantize(const QuantArgs& a, void* stream);
 int launch_window_scatter(const WindowScatterArgs& a, void* stream);
 int launch_dequantize(const DequantArgs& a, void* stream);
 int launch_decode(const DecodeArgs& a, void* stream);
-size_t decode_smem_bytes(int G, int kb, int vb, int qjl, int pk, int pv);
 
 // device error words: each .cu owns one; these read-and-clear them
 int quant_read_error(unsigned* out);
