@@ -115,6 +115,36 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def sources_digest() -> str:
+    """sha256 of the concatenated CUDA/C++ sources (sorted by name)."""
+    import hashlib
+    d = os.path.join(ROOT, "kv_cache_quantization_random_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(d)):
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def captured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel sources changed since that capture."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    digest = sources_digest()
+    for ln in lines:
+        parts = ln.split()
+        if len(parts) != 4 or ln.startswith("#") or parts[:2] != [kernel, workload]:
+            continue
+        kv = dict(p.split("=", 1) for p in parts[2:])
+        if kv.get("sources") == digest:
+            return int(kv["dram_bytes_per_launch"])
+    return None
+
+
 def largest_divisor_at_most(n: int, cap: int) -> int:
     for s in range(min(n, cap), 0, -1):
         if n % s == 0:
@@ -390,7 +420,9 @@ def run_ours(args, w, rank, world, local):
         "roofline": {
             "kernel": "tq::decode_kernel", "bound": "hbm", "achieved": dec_gbs,
             "peak": hbm_peak, "unit": "GB/s", "frac": dec_gbs / hbm_peak,
-            "peak_source": f"{peak_kind} hbm_gbs", "traffic": args.decode_traffic,
+            "peak_source": f"{peak_kind} hbm_gbs",
+            "traffic": (args.decode_traffic if args.decode_traffic is not None
+                        else captured_traffic("decode_kernel", w.name)),
             "bytes_per_launch": dec_bytes, "launch_ms": dec_ms,
         },
         "decode": {"ms": dec_ms, "gbs": dec_gbs, "frac_of_peak": dec_gbs / hbm_peak,
