@@ -294,7 +294,8 @@ def run_ours(args, w, rank, world, local):
         append(i % R)
         decode(i % R)
 
-    launches_per_step = (2 + (2 if Wn else 0)) + 1
+    # one fused append launch (one new token per sequence) + one decode launch
+    launches_per_step = 2
 
     # ---- warmup (direct launches), then capture graphs of S steps
     warm = max(args.warmup, 3)

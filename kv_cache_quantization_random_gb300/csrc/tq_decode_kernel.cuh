@@ -826,12 +826,12 @@ __global__ void __launch_bounds__(kDT, 3) decode_kernel(const DecodeArgs a) {
       if (lane < ns) fsc[warp * 32 + lane] = exp2f(__ldcg(base + ((s0 + lane) * G + g) * stride) - M);
       __syncwarp();
       int j = 0;
-      for (; j + 8 <= ns; j += 8) {
-        float4 v[8];
+      for (; j + 16 <= ns; j += 16) {
+        float4 v[16];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = __ldcg((const float4*)(base + ((s0 + j + u) * G + g) * stride + 4) + lane);
+        for (int u = 0; u < 16; ++u) v[u] = __ldcg((const float4*)(base + ((s0 + j + u) * G + g) * stride + 4) + lane);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < 16; ++u) {
           const float f = fsc[warp * 32 + j + u];
           rot.x = fmaf(v[u].x, f, rot.x);
           rot.y = fmaf(v[u].y, f, rot.y);

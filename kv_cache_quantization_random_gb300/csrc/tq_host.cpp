@@ -7,9 +7,11 @@
 // "[GitHub 탐방] TurboQuant 3-bit KV 캐시 압축 — 단일 GPU 재현 기록", "GPU 세대가
 // 바뀌면" item (1): 2^bits Lloyd-Max centroids per rotated coordinate.
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include <cuda_runtime.h>
@@ -339,8 +341,12 @@ static DecodePlan decode_plan(const tq_config* cfg, int batch, int n_q_heads, in
   long long max_nq = (long long)max_seq_len - W;
   if (max_nq < 0) max_nq = 0;
   long long units = (long long)batch * n_kv_heads;
-  long long per = units > 0 ? (units * max_nq + kTargetCtas - 1) / kTargetCtas : 0;
-  long long st = (per + 127) / 128 * 128;
+  // one wave of about kTargetCtas CTAs: split the quantized tokens evenly over
+  // what is left after the window splits, in multiples of 32 tokens
+  long long slots = kTargetCtas - (W > 0 ? units : 0);
+  if (slots < units) slots = units;
+  long long per = units > 0 ? (units * max_nq + slots - 1) / slots : 0;
+  long long st = (per + 31) / 32 * 32;
   if (st < 256) st = 256;
   p.split_tokens = (int)st;
   p.n_qsplits = (int)((max_nq + st - 1) / st);
@@ -403,6 +409,36 @@ static tq_status check_planes(const tq_config* cfg, int layer, int kind, const t
   if (qjl && (!aligned16(p.qjl_signs) || !aligned16(p.qjl_rnorm))) return TQ_ERR_ALIGNMENT;
   return TQ_OK;
 }
+// Search grid of a codebook (see SearchGrid), from the same fp32 boundaries
+// the device tables hold; cached per (bits, density, head_dim).
+static SearchGrid search_grid(const tq_config* cfg, int bits) {
+  static std::mutex mu;
+  static std::vector<std::pair<uint64_t, SearchGrid>> cache;
+  const uint64_t key = ((uint64_t)bits << 40) | ((uint64_t)cfg->density << 32) | (uint32_t)cfg->head_dim;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (auto& e : cache)
+      if (e.first == key) return e.second;
+  }
+  std::vector<float> c(256), b(256);
+  SearchGrid g{0.f, 0.f, 0.f, 0};
+  if (tq_make_codebook(bits, cfg->head_dim, cfg->density, c.data(), b.data()) != TQ_OK) return g;
+  const int L = 1 << bits;
+  double gap = 1.0, maxb = 0.0;
+  for (int j = 0; j + 1 < L - 1; ++j) gap = std::min(gap, (double)b[j + 1] - (double)b[j]);
+  for (int j = 0; j + 1 < L; ++j) maxb = std::max(maxb, std::fabs((double)b[j]));
+  g.scale = (float)(4.0 / gap);
+  // 2..4 bits: the grid spans |y| <= 1.01 (a unit vector's coordinates); 8
+  // bits: only the span of the boundaries, with |y| clamped onto it
+  const double span = bits <= 4 ? 1.01 : maxb + 3.0 / g.scale;
+  g.clamp = bits <= 4 ? 0.f : (float)(maxb + 2.0 / g.scale);
+  g.cells = 2 * (int)std::ceil(span * g.scale) + 4;
+  g.magic = 12582912.0f + (float)(g.cells / 2);
+  std::lock_guard<std::mutex> lock(mu);
+  cache.push_back({key, g});
+  return g;
+}
+
 static void fill_quant_codec(QuantArgs& a, const tq_config* cfg, const void* tables, int layer,
                              int kind) {
   tq_layer_spec s = spec_of(cfg, layer);
@@ -417,6 +453,14 @@ static void fill_quant_codec(QuantArgs& a, const tq_config* cfg, const void* tab
   a.err = quant_error_ptr();
   a.wait_limit = g_wait_limit;
   a.extra_tx = g_fault_injection == 1 ? 16u : 0u;
+  const SearchGrid g = search_grid(cfg, a.bits);
+  a.grid_scale = g.scale;
+  a.grid_magic = g.magic;
+  a.grid_clamp = g.clamp;
+  a.grid_cells = g.cells;
+  float sg[kHeadDim];
+  tq_make_signs(cfg->seed, layer, kind, kHeadDim, sg);
+  for (int i = 0; i < kHeadDim; ++i) a.smask[i] = sg[i] < 0.f ? 0x80000000u : 0u;
 }
 }  // namespace tq
 
@@ -438,6 +482,7 @@ extern "C" tq_status tq_quantize_kv(const tq_config* cfg, const void* tables, in
   for (int i = 0; i < 3; ++i)
     if (src_strides[i] < 0 || (src_strides[i] * esz) % 16 != 0) return TQ_ERR_ALIGNMENT;
   if (!dst_pos && n_tokens > dst.capacity) return TQ_ERR_INVALID_ARG;
+  if ((long long)batch * n_kv_heads * n_tokens >= (1ll << 31)) return TQ_ERR_UNSUPPORTED;
   QuantArgs a{};
   a.src = src;
   a.src_f32 = src_dtype == TQ_F32;
@@ -454,6 +499,7 @@ extern "C" tq_status tq_quantize_kv(const tq_config* cfg, const void* tables, in
   a.qjl_rnorm = dst.qjl_rnorm;
   a.cap = dst.capacity;
   fill_quant_codec(a, cfg, tables, layer, kind);
+  if (a.grid_cells <= 0 || a.grid_cells > kMaxGridCells) return TQ_ERR_UNSUPPORTED;
   return launch_quantize(a, stream) == 0 ? TQ_OK : TQ_ERR_CUDA;
 }
 
@@ -480,6 +526,43 @@ extern "C" tq_status tq_append_kv(const tq_config* cfg, const void* tables, int 
     st = check_planes(cfg, layer, kind, kind == 0 ? k : v);
     if (st != TQ_OK) return st;
   }
+  if (n_new <= kAppendFusedMaxNew) {
+    AppendArgs a{};
+    a.src[0] = k_new;
+    a.src[1] = v_new;
+    a.src_f32 = src_dtype == TQ_F32;
+    a.sb = src_strides[0];
+    a.sh = src_strides[1];
+    a.st = src_strides[2];
+    a.B = batch;
+    a.H = n_kv_heads;
+    a.n = n_new;
+    a.seq_before = seq_lens_before;
+    a.W = W;
+    a.win[0] = k_win;
+    a.win[1] = v_win;
+    for (int kind = 0; kind < 2; ++kind) {
+      const tq_planes& p = kind == 0 ? k : v;
+      QuantArgs q{};
+      fill_quant_codec(q, cfg, tables, layer, kind);
+      a.codes[kind] = p.codes;
+      a.norms[kind] = p.norms;
+      a.cap[kind] = p.capacity;
+      a.bits[kind] = q.bits;
+      a.centroids[kind] = q.centroids;
+      a.boundaries[kind] = q.boundaries;
+      a.rot_signs[kind] = q.rot_signs;
+      if (kind == 0) {
+        a.qjl = q.qjl;
+        a.S = q.S;
+        a.qjl_signs = p.qjl_signs;
+        a.qjl_rnorm = p.qjl_rnorm;
+        a.err = q.err;
+      }
+    }
+    return launch_append(a, stream) != 0 ? TQ_ERR_CUDA : TQ_OK;
+  }
+  if ((long long)batch * n_kv_heads * n_new >= (1ll << 31)) return TQ_ERR_UNSUPPORTED;
   for (int kind = 0; kind < 2; ++kind) {
     const tq_planes& p = kind == 0 ? k : v;
     QuantArgs a{};
@@ -501,6 +584,7 @@ extern "C" tq_status tq_append_kv(const tq_config* cfg, const void* tables, int 
     a.qjl_rnorm = p.qjl_rnorm;
     a.cap = p.capacity;
     fill_quant_codec(a, cfg, tables, layer, kind);
+    if (a.grid_cells <= 0 || a.grid_cells > kMaxGridCells) return TQ_ERR_UNSUPPORTED;
     if (launch_quantize(a, stream) != 0) return TQ_ERR_CUDA;
   }
   if (W > 0) {

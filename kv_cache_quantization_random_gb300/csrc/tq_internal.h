@@ -61,7 +61,25 @@ struct QuantArgs {
   unsigned* err;                 // device error word
   uint32_t wait_limit;
   uint32_t extra_tx;             // test hook (tq_set_fault_injection), normally 0
+  // code search grid (see SearchGrid) and the rotation signs as fp32 sign-bit
+  // masks, kept in the parameter block so the kernel reads them as operands
+  float grid_scale;              // cells per unit of y
+  float grid_magic;              // 1.5 * 2^23 + grid_cells / 2
+  float grid_clamp;              // |y| clamp before the cell index (0: none)
+  int grid_cells;
+  uint32_t smask[kHeadDim];
 };
+
+// Code search by a uniform grid over y: cell k = round(y * scale) + cells / 2.
+// The cell width is a quarter of the smallest gap between two boundaries, so
+// any three neighbouring cells hold at most one boundary, and the entry of
+// cell k (the number of boundaries below the lower edge of cells k-1..k+1 and
+// the first boundary above it) gives the code with one comparison.
+struct SearchGrid {
+  float scale, magic, clamp;
+  int cells;
+};
+constexpr int kMaxGridCells = 2560;
 
 struct WindowScatterArgs {
   const void* src;
@@ -72,6 +90,31 @@ struct WindowScatterArgs {
   int W;
   uint16_t* win;
 };
+
+// tq_append_kv for a few new tokens per sequence: one launch does the K and
+// V quantize of the tokens leaving the window and the window ring update.
+struct AppendArgs {
+  const void* src[2];            // k_new, v_new
+  int src_f32;
+  int64_t sb, sh, st;            // element strides of both sources
+  int B, H, n;
+  const int32_t* seq_before;
+  int W;
+  uint16_t* win[2];              // bf16 rings (W > 0)
+  uint8_t* codes[2];
+  float* norms[2];
+  int64_t cap[2];
+  uint8_t* qjl_signs;            // K only
+  float* qjl_rnorm;
+  int bits[2];
+  const float* centroids[2];
+  const float* boundaries[2];
+  const float* rot_signs[2];
+  int qjl;                       // K in MSE+QJL mode
+  const uint16_t* S;             // bf16 [m][d]
+  unsigned* err;
+};
+constexpr int kAppendFusedMaxNew = 8;   // larger appends take the bulk quantize kernel
 
 struct DequantArgs {
   const uint8_t* codes;
@@ -118,6 +161,7 @@ struct DecodeArgs {
 // ---- launchers (defined in the .cu files) -------------------------------------
 int launch_quantize(const QuantArgs& a, void* stream);
 int launch_window_scatter(const WindowScatterArgs& a, void* stream);
+int launch_append(const AppendArgs& a, void* stream);
 int launch_dequantize(const DequantArgs& a, void* stream);
 int launch_decode(const DecodeArgs& a, void* stream);
 

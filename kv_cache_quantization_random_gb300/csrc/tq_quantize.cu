@@ -29,26 +29,31 @@ struct RowCfg {
   static constexpr int kPitch = kRowBytes + 16;   // odd multiple of 16 B: conflict-free rows
 };
 
-__host__ __device__ constexpr size_t quant_smem_bytes(bool f32, bool qjl) {
-  return (size_t)kQRows * (f32 ? RowCfg<true>::kPitch : RowCfg<false>::kPitch)  // rows
-         + 256 * 4 + 256 * 4 + kD * 4                                              // tables
-         + 16                                                                      // mbarrier
-         + (qjl ? (size_t)kQjlM * kD * 4 : 0);                                     // S (fp32)
+// dynamic shared memory: two row buffers, the search grid, boundaries,
+// centroids, two mbarriers and (QJL) the fp32 projection matrix
+__host__ __device__ constexpr size_t quant_rows_bytes(bool f32) {
+  return (size_t)kQRows * (f32 ? RowCfg<true>::kPitch : RowCfg<false>::kPitch);
+}
+__host__ __device__ constexpr size_t quant_smem_bytes(bool f32, bool qjl, int cells) {
+  return 2 * quant_rows_bytes(f32) + (size_t)cells * 8 + 256 * 4 + (qjl ? 256 * 4 : 0) + 16 +
+         (qjl ? (size_t)kQjlM * kD * 4 : 0);
 }
 
-// Resolve row r of the tile: its source address and destination plane row.
-__device__ __forceinline__ bool resolve_row(const QuantArgs& a, long long v, const void** src,
+// Resolve vector v of the launch: its plane row and, for the stager, its
+// source address.  All index arithmetic is 32-bit (a launch covers fewer than
+// 2^31 vectors, checked on the host).
+__device__ __forceinline__ bool resolve_row(const QuantArgs& a, uint32_t v, const void** src,
                                             long long* dst_row) {
-  const int n = a.n;
-  const int j = (int)(v % n);
-  const long long bh = v / n;
-  const int h = (int)(bh % a.H);
-  const int b = (int)(bh / a.H);
+  const uint32_t n = (uint32_t)a.n;
+  const uint32_t bh = v / n;
+  const uint32_t j = v - bh * n;
+  const uint32_t b = bh / (uint32_t)a.H;
+  const uint32_t h = bh - b * (uint32_t)a.H;
   const int esz = a.src_f32 ? 4 : 2;
   long long pos;
   if (!a.append) {
     pos = (a.dst_pos ? (long long)a.dst_pos[b] : 0) + j;
-    *src = (const uint8_t*)a.src + (b * a.sb + h * a.sh + (long long)j * a.st) * esz;
+    *src = (const uint8_t*)a.src + ((long long)b * a.sb + (long long)h * a.sh + (long long)j * a.st) * esz;
   } else {
     const long long T0 = a.seq_before[b];
     const long long q0 = T0 - a.W > 0 ? T0 - a.W : 0;
@@ -60,140 +65,218 @@ __device__ __forceinline__ bool resolve_row(const QuantArgs& a, long long v, con
       const long long slot = pos % a.W;
       *src = (const uint8_t*)a.win + (((long long)b * a.H + h) * a.W + slot) * kD * 2;
     } else {
-      *src = (const uint8_t*)a.src + (b * a.sb + h * a.sh + (pos - T0) * a.st) * esz;
+      *src = (const uint8_t*)a.src + ((long long)b * a.sb + (long long)h * a.sh + (pos - T0) * a.st) * esz;
     }
   }
   if (pos < 0 || pos >= a.cap) {
     atomicOr(a.err, kErrBounds);
     return false;
   }
-  *dst_row = ((long long)b * a.H + h) * a.cap + pos;
+  *dst_row = ((long long)bh) * a.cap + pos;
   return true;
 }
 
-template <int BITS, bool QJL, bool F32>
-__global__ void __launch_bounds__(kQRows) quantize_kernel(const QuantArgs a) {
-  constexpr int L = 1 << BITS;
-  constexpr int NW = 4 * BITS;         // 32-bit code words per vector (128 * BITS / 32)
+__device__ __forceinline__ float2 lds64f(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+  return v;
+}
+
+// Warp 0 stages the rows of one tile into a row buffer with bulk copies that
+// complete on `bar`; rows that resolve to nothing are skipped.
+template <bool F32>
+__device__ __forceinline__ void stage_tile(const QuantArgs& a, uint32_t v0, uint32_t total,
+                                           uint8_t* rows, uint64_t* bar, int lane) {
   constexpr int kRowBytes = RowCfg<F32>::kRowBytes;
   constexpr int kPitch = RowCfg<F32>::kPitch;
+  const void* srcs[kQRows / 32];
+  uint32_t mine = 0;
+#pragma unroll
+  for (int k = 0; k < kQRows / 32; ++k) {
+    const uint32_t v = v0 + lane + 32 * k;
+    long long dummy;
+    const bool ok = v < total && resolve_row(a, v, &srcs[k], &dummy);
+    mine |= (ok ? 1u : 0u) << k;
+  }
+  const uint32_t count = __reduce_add_sync(0xffffffffu, (uint32_t)__popc(mine));
+  // a.extra_tx is a test hook: bytes that never arrive, so the wait on this
+  // tile can only end by running out of polls
+  if (lane == 0) mbar_arrive_expect_tx(bar, count * kRowBytes + a.extra_tx);
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < kQRows / 32; ++k)
+    if (mine & (1u << k)) bulk_g2s(rows + (lane + 32 * k) * kPitch, srcs[k], kRowBytes, bar);
+}
+
+// Rotated coordinates of one vector, held as pairs (y_j, y_{j+64}), j < 64,
+// so that six of the seven butterfly stages run on packed fp32 pairs.
+template <bool F32>
+__device__ __forceinline__ float load_rotate(const QuantArgs& a, const uint8_t* row,
+                                             float2 (&p)[64]) {
+  if constexpr (F32) {
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const uint4 lo = lds128(row + 16 * c);            // coordinates 4c .. 4c+3
+      const uint4 hi = lds128(row + 256 + 16 * c);      // coordinates 64+4c ..
+      p[4 * c + 0] = make_float2(__uint_as_float(lo.x ^ a.smask[4 * c + 0]), __uint_as_float(hi.x ^ a.smask[64 + 4 * c + 0]));
+      p[4 * c + 1] = make_float2(__uint_as_float(lo.y ^ a.smask[4 * c + 1]), __uint_as_float(hi.y ^ a.smask[64 + 4 * c + 1]));
+      p[4 * c + 2] = make_float2(__uint_as_float(lo.z ^ a.smask[4 * c + 2]), __uint_as_float(hi.z ^ a.smask[64 + 4 * c + 2]));
+      p[4 * c + 3] = make_float2(__uint_as_float(lo.w ^ a.smask[4 * c + 3]), __uint_as_float(hi.w ^ a.smask[64 + 4 * c + 3]));
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 lo = lds128(row + 16 * c);            // coordinates 8c .. 8c+7
+      const uint4 hi = lds128(row + 128 + 16 * c);      // coordinates 64+8c ..
+      const uint32_t l[4] = {lo.x, lo.y, lo.z, lo.w};
+      const uint32_t h[4] = {hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = 8 * c + 2 * u;
+        // bf16 -> fp32 with the sign flip: adding 0x80000000 flips the sign bit
+        p[i] = make_float2(__uint_as_float(l[u] * 65536u + a.smask[i]),
+                           __uint_as_float(h[u] * 65536u + a.smask[64 + i]));
+        p[i + 1] = make_float2(__uint_as_float((l[u] & 0xFFFF0000u) ^ a.smask[i + 1]),
+                               __uint_as_float((h[u] & 0xFFFF0000u) ^ a.smask[64 + i + 1]));
+      }
+    }
+  }
+  float2 s0 = make_float2(0.f, 0.f), s1 = s0;
+#pragma unroll
+  for (int j = 0; j < 64; j += 2) {
+    s0 = __ffma2_rn(p[j], p[j], s0);
+    s1 = __ffma2_rn(p[j + 1], p[j + 1], s1);
+  }
+  const float2 s = __fadd2_rn(s0, s1);
+  // butterflies between pairs: stages 1, 2, 4, ..., 32 of the index j
+  const float2 neg1 = make_float2(-1.f, -1.f);
+#pragma unroll
+  for (int hs = 1; hs < 64; hs <<= 1) {
+#pragma unroll
+    for (int j = 0; j < 64; ++j) {
+      if ((j & hs) == 0) {
+        const float2 u = p[j], w = p[j + hs];
+        p[j] = __fadd2_rn(u, w);
+        p[j + hs] = __ffma2_rn(w, neg1, u);
+      }
+    }
+  }
+  // stage 64: inside each pair
+#pragma unroll
+  for (int j = 0; j < 64; ++j) p[j] = make_float2(p[j].x + p[j].y, p[j].x - p[j].y);
+  return sqrtf(s.x + s.y);
+}
+
+template <int BITS, bool QJL, bool F32, bool CLAMP>
+__global__ void __launch_bounds__(kQRows, (QJL ? 1 : 3)) quantize_kernel(const QuantArgs a) {
+  constexpr int NW = 4 * BITS;         // 32-bit code words per vector (128 * BITS / 32)
+  constexpr int kPitch = RowCfg<F32>::kPitch;
   extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* rows = smem;
-  float* bnd = (float*)(smem + kQRows * kPitch);
-  float* cen = bnd + 256;
-  uint32_t* smask = (uint32_t*)(cen + 256);
-  uint64_t* bar = (uint64_t*)(smask + kD);
+  uint8_t* rows0 = smem;
+  uint8_t* rows1 = smem + quant_rows_bytes(F32);
+  float2* grid = (float2*)(smem + 2 * quant_rows_bytes(F32));
+  float* bnd = (float*)(grid + a.grid_cells);
+  float* cen = bnd + 256;                               // QJL only
+  uint64_t* bar = (uint64_t*)(cen + (QJL ? 256 : 0));
   float* Sf = (float*)(bar + 2);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int i = tid; i < 256; i += kQRows) {
     bnd[i] = a.boundaries[i];
-    cen[i] = a.centroids[i];
+    if constexpr (QJL) cen[i] = a.centroids[i];
   }
-  smask[tid] = a.rot_signs[tid] < 0.f ? 0x80000000u : 0u;
   if constexpr (QJL) {
     for (int e = tid; e < kQjlM * kD; e += kQRows) Sf[e] = __uint_as_float((uint32_t)a.S[e] << 16);
   }
   if (tid == 0) {
-    mbar_init(bar, 1);
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
     fence_mbarrier_init();
   }
   __syncthreads();
+  // search grid: entry k = (first boundary at or above the lower edge of
+  // cells k-1..k+1, number of boundaries below that edge)
+  const int off = a.grid_cells / 2;
+  for (int k = tid; k < a.grid_cells; k += kQRows) {
+    const float lo = ((float)(k - off) - 1.5f) / a.grid_scale;
+    uint32_t idx = 0;
+#pragma unroll
+    for (int step = (1 << BITS) / 2; step >= 1; step >>= 1)
+      if (bnd[idx + step - 1] < lo) idx += step;
+    grid[k] = make_float2(bnd[idx], __uint_as_float(idx));
+  }
+  __syncthreads();
+  const uint32_t grid_base = smem_u32(grid);
+  const uint32_t kmax = (uint32_t)a.grid_cells - 1u;
 
-  const long long total = (long long)a.B * a.H * a.n;
-  const long long ntiles = (total + kQRows - 1) / kQRows;
+  const uint32_t total = (uint32_t)a.B * (uint32_t)a.H * (uint32_t)a.n;
+  const uint32_t ntiles = (total + kQRows - 1) / kQRows;
   const uint32_t limit = a.wait_limit ? a.wait_limit : kDefaultWaitLimit;
-  uint32_t parity = 0;
-  for (long long tile = blockIdx.x; tile < ntiles; tile += gridDim.x, parity ^= 1u) {
-    const long long v0 = tile * kQRows;
-    // ---- stage the tile's rows (warp 0 issues one bulk copy per row)
-    if (warp == 0) {
-      const void* srcs[kQRows / 32];
-      long long dummy;
-      uint32_t mine = 0, count = 0;
-#pragma unroll
-      for (int k = 0; k < kQRows / 32; ++k) {
-        const long long v = v0 + lane + 32 * k;
-        bool ok = v < total && resolve_row(a, v, &srcs[k], &dummy);
-        mine |= (ok ? 1u : 0u) << k;
-      }
-      count = __reduce_add_sync(0xffffffffu, (uint32_t)__popc(mine));
-      // a.extra_tx is a test hook: bytes that never arrive, so the wait below
-      // can only end by running out of polls
-      if (lane == 0) mbar_arrive_expect_tx(bar, count * kRowBytes + a.extra_tx);
-      __syncwarp();
-#pragma unroll
-      for (int k = 0; k < kQRows / 32; ++k)
-        if (mine & (1u << k)) bulk_g2s(rows + (lane + 32 * k) * kPitch, srcs[k], kRowBytes, bar);
-    }
-    const bool staged = __syncthreads_and(mbar_wait(bar, parity, limit, a.err));
+  uint32_t phase0 = 0, phase1 = 0;
+  int buf = 0;
+  uint32_t tile = blockIdx.x;
+  if (warp == 0 && tile < ntiles) stage_tile<F32>(a, tile * kQRows, total, rows0, &bar[0], lane);
+  for (; tile < ntiles; tile += gridDim.x) {
+    const uint32_t next = tile + gridDim.x;
+    if (warp == 0 && next < ntiles)          // the other buffer was released by the last barrier
+      stage_tile<F32>(a, next * kQRows, total, buf ? rows0 : rows1, buf ? &bar[0] : &bar[1], lane);
+    const uint32_t ph = buf ? phase1 : phase0;
+    const bool staged = __syncthreads_and(mbar_wait(&bar[buf], ph, limit, a.err));
     if (!staged) {
-      // the staging wait ran out (error word already set): give copies still in
-      // flight one more bounded wait, then leave without touching the planes
-      for (uint32_t i = 0; i < limit && !mbar_try_wait(bar, parity); ++i) {
+      // a staging wait ran out (error word already set): give the copies still
+      // in flight one more bounded wait each, then leave the planes untouched
+      for (uint32_t i = 0; i < limit && !mbar_try_wait(&bar[buf], ph); ++i) {
+      }
+      if (next < ntiles) {
+        const uint32_t ph2 = buf ? phase0 : phase1;
+        for (uint32_t i = 0; i < limit && !mbar_try_wait(&bar[buf ^ 1], ph2); ++i) {
+        }
       }
       return;
     }
-    const long long v = v0 + tid;
+    if (buf) phase1 ^= 1u; else phase0 ^= 1u;
+    const uint8_t* rows = buf ? rows1 : rows0;
+
+    const uint32_t v = tile * kQRows + tid;
     const void* srcp;
     long long drow;
     if (v < total && resolve_row(a, v, &srcp, &drow)) {
-      // ---- widen, flip signs, accumulate ||x||^2
-      float x[kD];
-      const uint8_t* row = rows + tid * kPitch;
-      if constexpr (F32) {
-#pragma unroll
-        for (int c = 0; c < kD / 4; ++c) {
-          uint4 w = lds128(row + 16 * c);
-          uint4 m = lds128(smask + 4 * c);
-          x[4 * c + 0] = __uint_as_float(w.x ^ m.x);
-          x[4 * c + 1] = __uint_as_float(w.y ^ m.y);
-          x[4 * c + 2] = __uint_as_float(w.z ^ m.z);
-          x[4 * c + 3] = __uint_as_float(w.w ^ m.w);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < kD / 8; ++c) {
-          uint4 w = lds128(row + 16 * c);
-          uint4 m0 = lds128(smask + 8 * c);
-          uint4 m1 = lds128(smask + 8 * c + 4);
-          x[8 * c + 0] = __uint_as_float((w.x << 16) ^ m0.x);
-          x[8 * c + 1] = __uint_as_float((w.x & 0xFFFF0000u) ^ m0.y);
-          x[8 * c + 2] = __uint_as_float((w.y << 16) ^ m0.z);
-          x[8 * c + 3] = __uint_as_float((w.y & 0xFFFF0000u) ^ m0.w);
-          x[8 * c + 4] = __uint_as_float((w.z << 16) ^ m1.x);
-          x[8 * c + 5] = __uint_as_float((w.z & 0xFFFF0000u) ^ m1.y);
-          x[8 * c + 6] = __uint_as_float((w.w << 16) ^ m1.z);
-          x[8 * c + 7] = __uint_as_float((w.w & 0xFFFF0000u) ^ m1.w);
-        }
-      }
-      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-      for (int i = 0; i < kD; i += 4) {
-        s0 = fmaf(x[i], x[i], s0);
-        s1 = fmaf(x[i + 1], x[i + 1], s1);
-        s2 = fmaf(x[i + 2], x[i + 2], s2);
-        s3 = fmaf(x[i + 3], x[i + 3], s3);
-      }
-      const float nrm = sqrtf((s0 + s1) + (s2 + s3));
-      // ---- rotate: y = H (s * x) / (||x|| sqrt d)
-      fwht_regs<kD>(x);
+      float2 p[64];
+      const float nrm = load_rotate<F32>(a, rows + tid * kPitch, p);
       const float inv = nrm > 0.f ? 1.0f / (nrm * 11.313708498984761f) : 0.f;
-      // ---- code search and packing
+      const float2 inv2 = make_float2(inv, inv);
+      const float2 gs2 = make_float2(a.grid_scale, a.grid_scale);
+      const float2 gm2 = make_float2(a.grid_magic, a.grid_magic);
       uint32_t words[NW];
 #pragma unroll
       for (int k = 0; k < NW; ++k) words[k] = 0u;
 #pragma unroll
-      for (int i = 0; i < kD; ++i) {
-        const float y = x[i] * inv;
-        uint32_t idx = 0;
+      for (int j = 0; j < 64; ++j) {
+        const float2 y = __fmul2_rn(p[j], inv2);
+        float2 yc = y;
+        if constexpr (CLAMP) {
+          yc.x = fminf(fmaxf(y.x, -a.grid_clamp), a.grid_clamp);
+          yc.y = fminf(fmaxf(y.y, -a.grid_clamp), a.grid_clamp);
+        }
+        const float2 t = __ffma2_rn(yc, gs2, gm2);
+        const uint32_t k0 = min(__float_as_uint(t.x) - 0x4B400000u, kmax);
+        const uint32_t k1 = min(__float_as_uint(t.y) - 0x4B400000u, kmax);
+        const float2 e0 = lds64f(grid_base + k0 * 8u);
+        const float2 e1 = lds64f(grid_base + k1 * 8u);
+        const uint32_t c0 = __float_as_uint(e0.y) + (e0.x < y.x ? 1u : 0u);
+        const uint32_t c1 = __float_as_uint(e1.y) + (e1.x < y.y ? 1u : 0u);
 #pragma unroll
-        for (int step = L / 2; step >= 1; step >>= 1)
-          if (bnd[idx + step - 1] < y) idx += step;
-        const int p = i * BITS;
-        words[p >> 5] |= idx << (p & 31);
-        if ((p & 31) + BITS > 32) words[(p >> 5) + 1] |= idx >> (32 - (p & 31));
-        if constexpr (QJL) x[i] = nrm * (y - cen[idx]);   // rotated-domain residual
+        for (int half = 0; half < 2; ++half) {
+          const int i = j + 64 * half;                   // coordinate
+          const uint32_t code = half ? c1 : c0;
+          const int pb = i * BITS;
+          words[pb >> 5] |= code << (pb & 31);
+          if ((pb & 31) + BITS > 32) words[(pb >> 5) + 1] |= code >> (32 - (pb & 31));
+        }
+        if constexpr (QJL) {
+          // rotated-domain residual r = n (y - c[idx])
+          p[j] = make_float2(nrm * (y.x - cen[c0]), nrm * (y.y - cen[c1]));
+        }
       }
       uint4* dc = (uint4*)(a.codes + drow * (16 * BITS));
 #pragma unroll
@@ -201,35 +284,34 @@ __global__ void __launch_bounds__(kQRows) quantize_kernel(const QuantArgs a) {
         dc[k] = make_uint4(words[4 * k], words[4 * k + 1], words[4 * k + 2], words[4 * k + 3]);
       a.norms[drow] = nrm;
       if constexpr (QJL) {
-        float g0 = 0.f, g1 = 0.f;
+        float2 g2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < kD; i += 2) {
-          g0 = fmaf(x[i], x[i], g0);
-          g1 = fmaf(x[i + 1], x[i + 1], g1);
-        }
-        const float gamma = sqrtf(g0 + g1);
+        for (int j = 0; j < 64; ++j) g2 = __ffma2_rn(p[j], p[j], g2);
+        const float gamma = sqrtf(g2.x + g2.y);
         uint32_t sb[kQjlM / 32];
 #pragma unroll
         for (int k = 0; k < kQjlM / 32; ++k) sb[k] = 0u;
-        for (int j = 0; j < kQjlM; ++j) {
-          const float* Sj = Sf + j * kD;
-          float z0 = 0.f, z1 = 0.f, z2 = 0.f, z3 = 0.f;
+        for (int jm = 0; jm < kQjlM; ++jm) {
+          const float* Sj = Sf + jm * kD;
+          float2 z0 = make_float2(0.f, 0.f), z1 = z0;
 #pragma unroll
-          for (int k = 0; k < kD; k += 4) {
-            float4 s = *(const float4*)(Sj + k);
-            z0 = fmaf(s.x, x[k], z0);
-            z1 = fmaf(s.y, x[k + 1], z1);
-            z2 = fmaf(s.z, x[k + 2], z2);
-            z3 = fmaf(s.w, x[k + 3], z3);
+          for (int k = 0; k < 64; k += 4) {
+            const float4 lo = *(const float4*)(Sj + k);       // S[jm][k .. k+3]
+            const float4 hi = *(const float4*)(Sj + 64 + k);  // S[jm][64+k ..]
+            z0 = __ffma2_rn(make_float2(lo.x, hi.x), p[k], z0);
+            z1 = __ffma2_rn(make_float2(lo.y, hi.y), p[k + 1], z1);
+            z0 = __ffma2_rn(make_float2(lo.z, hi.z), p[k + 2], z0);
+            z1 = __ffma2_rn(make_float2(lo.w, hi.w), p[k + 3], z1);
           }
-          const float z = (z0 + z1) + (z2 + z3);
-          sb[j >> 5] |= (z >= 0.f ? 1u : 0u) << (j & 31);
+          const float z = (z0.x + z0.y) + (z1.x + z1.y);
+          sb[jm >> 5] |= (z >= 0.f ? 1u : 0u) << (jm & 31);
         }
         *(uint4*)(a.qjl_signs + drow * (kQjlM / 8)) = make_uint4(sb[0], sb[1], sb[2], sb[3]);
         a.qjl_rnorm[drow] = gamma;
       }
     }
-    __syncthreads();   // every thread is done with the tile's rows before they are refilled
+    __syncthreads();   // every thread is done with this buffer before it is refilled
+    buf ^= 1;
   }
 }
 
@@ -251,6 +333,157 @@ __global__ void window_scatter_kernel(const WindowScatterArgs a) {
   const uint4* s = (const uint4*)((const uint8_t*)a.src + (b * a.sb + h * a.sh + (long long)j * a.st) * 2);
   uint4* d = (uint4*)(a.win + (((long long)b * a.H + h) * a.W + t % a.W) * kD);
   d[part] = s[part];
+}
+
+// ---- tq_append_kv with a few new tokens: one CTA per (sequence, kv-head).
+// Warp 0 quantizes the keys and warp 1 the values that leave the window (or
+// go straight to the planes); lane l owns coordinates 4l..4l+3, so the
+// Walsh-Hadamard butterfly takes two in-register stages and five shuffle
+// stages.  After a CTA barrier (every ring slot that is about to be
+// overwritten has been read) all threads write the new tokens into the ring.
+__device__ __forceinline__ void append_quantize_row(const AppendArgs& a, int kind, const void* src,
+                                                    int f32, long long drow, const float* bnd,
+                                                    const float* cen, float4 sg, uint32_t* words,
+                                                    float* rbuf, int lane) {
+  constexpr int kDim = 128;
+  const int bits = a.bits[kind];
+  float x[4];
+  if (f32) {
+    const float4 v = ((const float4*)src)[lane];
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+  } else {
+    const uint2 v = ((const uint2*)src)[lane];
+    x[0] = bf16lo(v.x); x[1] = bf16hi(v.x); x[2] = bf16lo(v.y); x[3] = bf16hi(v.y);
+  }
+  x[0] *= sg.x; x[1] *= sg.y; x[2] *= sg.z; x[3] *= sg.w;
+  float ss = x[0] * x[0];
+  ss = fmaf(x[1], x[1], ss);
+  ss = fmaf(x[2], x[2], ss);
+  ss = fmaf(x[3], x[3], ss);
+  const float nrm = sqrtf(warp_sum(ss));
+  // butterfly: stages 1 and 2 inside the lane, 4..64 across lanes
+  float t0 = x[0] + x[1], t1 = x[0] - x[1], t2 = x[2] + x[3], t3 = x[2] - x[3];
+  x[0] = t0 + t2; x[2] = t0 - t2; x[1] = t1 + t3; x[3] = t1 - t3;
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const bool hi = (lane & m) != 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const float p = __shfl_xor_sync(0xffffffffu, x[c], m);
+      x[c] = hi ? p - x[c] : x[c] + p;
+    }
+  }
+  const float inv = nrm > 0.f ? 1.0f / (nrm * 11.313708498984761f) : 0.f;
+  uint32_t packed = 0;
+  float r[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const float y = x[c] * inv;
+    uint32_t idx = 0;
+    for (int step = 1 << (bits - 1); step >= 1; step >>= 1)
+      if (bnd[idx + step - 1] < y) idx += step;
+    packed |= idx << (c * bits);
+    r[c] = nrm * (y - cen[idx]);
+  }
+  // dense LSB-first stream: lane l's 4*bits bits start at bit 4*bits*l
+  const int pos = 4 * bits * lane;
+  const int wi = pos >> 5, sh = pos & 31;
+  atomicOr(&words[wi], packed << sh);
+  if (sh + 4 * bits > 32) atomicOr(&words[wi + 1], packed >> (32 - sh));
+  __syncwarp();
+  if (lane < bits) {
+    uint4* dc = (uint4*)(a.codes[kind] + drow * (16 * bits));
+    dc[lane] = make_uint4(words[4 * lane], words[4 * lane + 1], words[4 * lane + 2],
+                          words[4 * lane + 3]);
+  }
+  if (lane == 0) a.norms[kind][drow] = nrm;
+  if (kind == 0 && a.qjl) {
+    float g = r[0] * r[0];
+    g = fmaf(r[1], r[1], g);
+    g = fmaf(r[2], r[2], g);
+    g = fmaf(r[3], r[3], g);
+    const float gamma = sqrtf(warp_sum(g));
+    *(float4*)(rbuf + 4 * lane) = make_float4(r[0], r[1], r[2], r[3]);
+    __syncwarp();
+    uint32_t sb[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4* Sj = (const uint4*)(a.S + (size_t)(32 * k + lane) * kDim);
+      float z0 = 0.f, z1 = 0.f;
+#pragma unroll 4
+      for (int e = 0; e < kDim / 8; ++e) {
+        const uint4 s8 = __ldg(Sj + e);
+        const float4 ra = *(const float4*)(rbuf + 8 * e);
+        const float4 rb = *(const float4*)(rbuf + 8 * e + 4);
+        z0 = fmaf(bf16lo(s8.x), ra.x, z0);
+        z1 = fmaf(bf16hi(s8.x), ra.y, z1);
+        z0 = fmaf(bf16lo(s8.y), ra.z, z0);
+        z1 = fmaf(bf16hi(s8.y), ra.w, z1);
+        z0 = fmaf(bf16lo(s8.z), rb.x, z0);
+        z1 = fmaf(bf16hi(s8.z), rb.y, z1);
+        z0 = fmaf(bf16lo(s8.w), rb.z, z0);
+        z1 = fmaf(bf16hi(s8.w), rb.w, z1);
+      }
+      sb[k] = __ballot_sync(0xffffffffu, z0 + z1 >= 0.f);
+    }
+    if (lane == 0) {
+      *(uint4*)(a.qjl_signs + drow * (kQjlM / 8)) = make_uint4(sb[0], sb[1], sb[2], sb[3]);
+      a.qjl_rnorm[drow] = gamma;
+    }
+  }
+  __syncwarp();
+  if (lane < 4 * bits) words[lane] = 0u;
+  __syncwarp();
+}
+
+__global__ void __launch_bounds__(64) append_kernel(const AppendArgs a) {
+  __shared__ float bnd[2][256];
+  __shared__ float cen[2][256];
+  __shared__ uint32_t words[2][32];
+  __shared__ __align__(16) float rbuf[kD];
+  const int tid = threadIdx.x, lane = tid & 31, kind = tid >> 5;
+  const int h = blockIdx.x % a.H, b = blockIdx.x / a.H;
+  for (int i = lane; i < 256; i += 32) {
+    bnd[kind][i] = a.boundaries[kind][i];
+    cen[kind][i] = a.centroids[kind][i];
+  }
+  words[kind][lane] = 0u;
+  const float4 sg = ((const float4*)a.rot_signs[kind])[lane];
+  __syncwarp();
+  const long long T0 = a.seq_before[b];
+  const long long T1 = T0 + a.n;
+  const long long q0 = T0 - a.W > 0 ? T0 - a.W : 0;
+  const long long q1 = T1 - a.W > 0 ? T1 - a.W : 0;
+  const int esz = a.src_f32 ? 4 : 2;
+  for (long long pos = q0; pos < q1; ++pos) {
+    const void* src;
+    int f32 = a.src_f32;
+    if (pos < T0) {                                   // leaves the window ring
+      src = a.win[kind] + (((long long)b * a.H + h) * a.W + pos % a.W) * kD;
+      f32 = 0;
+    } else {
+      src = (const uint8_t*)a.src[kind] + (b * a.sb + h * a.sh + (pos - T0) * a.st) * esz;
+    }
+    if (pos < 0 || pos >= a.cap[kind]) {
+      if (lane == 0) atomicOr(a.err, kErrBounds);
+      continue;
+    }
+    const long long drow = ((long long)b * a.H + h) * a.cap[kind] + pos;
+    append_quantize_row(a, kind, src, f32, drow, bnd[kind], cen[kind], sg, words[kind], rbuf, lane);
+  }
+  if (a.W == 0) return;
+  __syncthreads();                                    // ring slots read before they are rewritten
+  const long long first = T1 - a.W > T0 ? T1 - a.W : T0;   // first new token kept in the ring
+  const int n_ring = (int)(T1 - first);
+  for (int e = tid; e < 2 * n_ring * 16; e += 64) {
+    const int part = e & 15, row = e >> 4;
+    const int k2 = row / n_ring;
+    const long long t = first + row % n_ring;
+    const uint4* s4 = (const uint4*)((const uint8_t*)a.src[k2] +
+                                     (b * a.sb + h * a.sh + (t - T0) * a.st) * 2);
+    uint4* d4 = (uint4*)(a.win[k2] + (((long long)b * a.H + h) * a.W + t % a.W) * kD);
+    d4[part] = s4[part];
+  }
 }
 
 template <int BITS, bool QJL>
@@ -321,8 +554,8 @@ static int sm_count() {
 
 template <int BITS, bool QJL, bool F32>
 static int launch_q(const QuantArgs& a, cudaStream_t s) {
-  auto k = quantize_kernel<BITS, QJL, F32>;
-  const size_t smem = quant_smem_bytes(F32, QJL);
+  auto k = quantize_kernel<BITS, QJL, F32, (BITS > 4)>;
+  const size_t smem = quant_smem_bytes(F32, QJL, a.grid_cells);
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return 1;
   int per_sm = 0;
@@ -358,6 +591,13 @@ int launch_window_scatter(const WindowScatterArgs& a, void* stream) {
   const long long threads = (long long)a.B * a.H * a.n * 16;
   const int block = 256;
   window_scatter_kernel<<<(unsigned)((threads + block - 1) / block), block, 0, (cudaStream_t)stream>>>(a);
+  return cudaGetLastError() != cudaSuccess;
+}
+
+int launch_append(const AppendArgs& a, void* stream) {
+  const long long units = (long long)a.B * a.H;
+  if (units <= 0) return 0;
+  append_kernel<<<(unsigned)units, 64, 0, (cudaStream_t)stream>>>(a);
   return cudaGetLastError() != cudaSuccess;
 }
 

@@ -184,6 +184,60 @@ def test_streaming_append_with_window(B, W_):
             assert torch.equal(vw[:, :, t % W_].cpu(), V[:, :, t])
 
 
+@pytest.mark.parametrize("kb,vb,qjl,W_", [(3, 3, False, 8), (8, 8, False, 0), (2, 3, True, 0),
+                                        (4, 2, True, 32)])
+def test_append_one_launch_and_bulk_paths(B, kb, vb, qjl, W_):
+    """Appends of at most 8 tokens per sequence run as one fused launch (warp
+    per vector); larger ones take the bulk quantize kernel.  Both must give the
+    oracle's codes, norms and (QJL keys) sign sketches."""
+    import torch
+    from kv_cache_quantization_random_gb300 import workloads as W
+    Bsz, H, cap = 3, 2, 80
+    cfg = B.Config(k_bits=kb, v_bits=vb, residual_window=W_, seed=11,
+                   k_mode=B.TQ_MODE_MSE_QJL if qjl else B.TQ_MODE_MSE)
+    tables = B.device_tables(cfg)
+    kp = B.Planes(cfg, 0, 0, Bsz, H, cap)
+    vp = B.Planes(cfg, 0, 1, Bsz, H, cap)
+    kw = torch.zeros(Bsz, H, max(W_, 1), 128, dtype=torch.bfloat16, device="cuda")
+    vw = torch.zeros_like(kw)
+    w = W.scaled(W.get("llama8b_32k"), batch=Bsz, n_kv_heads=H, context=cap, data_seed=5)
+    K, V = W.make_kv(w)
+    lens = np.zeros(Bsz, dtype=np.int64)
+    for n_new in (1, 8, 9, 3, 1, 30):
+        if lens[0] + n_new > cap:
+            break
+        kn = K[:, :, int(lens[0]):int(lens[0]) + n_new].contiguous()
+        vn = V[:, :, int(lens[0]):int(lens[0]) + n_new].contiguous()
+        before = torch.tensor(lens, dtype=torch.int32, device="cuda")
+        B.tq_append_kv(cfg, tables, 0, kn.cuda(), vn.cuda(), before, kw if W_ else None,
+                       vw if W_ else None, kp, vp)
+        torch.cuda.synchronize()
+        assert B.tq_get_device_error() == B.TQ_OK
+        lens += n_new
+    T = int(lens[0])
+    nq = max(T - W_, 0)
+    for kind, X, P, bits in ((0, K, kp, kb), (1, V, vp, vb)):
+        oq = oracle_quantize(to64(X[:, :, :nq]), bits, 11, 0, kind)
+        compare_codes(P.codes_view()[:, :, :nq].cpu().numpy(), oq, bits)
+        compare_norms(P.norms_view()[:, :, :nq].cpu().numpy(), oq["norms"])
+        if kind == 0 and qjl:
+            # sketch of the oracle's residual of the GPU's own codes (codes may
+            # differ inside the boundary band); a sign may differ only where
+            # |z_j| <= 1e-5 ||S_j|| gamma
+            gcodes = O.unpack_codes(P.codes_view()[:, :, :nq].cpu().numpy(), bits, 128)
+            S = O.qjl_matrix(11, 0, 128, 128)
+            r = O.qjl_residual(oq["y"], gcodes, oq["norm64"], oq["c32"])
+            sb, gamma, z = O.qjl_sketch(r, S)
+            gbits = O.unpack_bits(P.signs_view()[:, :, :nq].cpu().numpy(), 128)
+            compare_norms(P.rnorm_view()[:, :, :nq].cpu().numpy(), gamma, rel=2e-6)
+            band = np.abs(z) <= 1e-5 * np.linalg.norm(S, axis=1) * gamma[..., None]
+            assert not ((gbits != sb) & ~band).any()
+    if W_:
+        for t in range(nq, T):
+            assert torch.equal(kw[:, :, t % W_].cpu(), K[:, :, t])
+            assert torch.equal(vw[:, :, t % W_].cpu(), V[:, :, t])
+
+
 def test_fault_injection_times_out_and_context_stays_usable(B):
     import torch
     cfg = B.Config(k_bits=3, v_bits=3)
