@@ -247,10 +247,12 @@ tq_status tq_get_device_error(void* stream);
  * hanging anything. */
 void tq_set_wait_limit(uint32_t iterations);
 
-/* Test hook for failure detection without a GPU fault.  mode 1: the staging
- * barrier of the quantize kernels is told to expect 16 bytes more than any
- * copy delivers, so its bounded wait can only end by running out; the kernel
- * then flags TQ_ERR_DEVICE_TIMEOUT, leaves the planes untouched and exits.
+/* Test hook for failure detection without a GPU fault.  mode 1: every
+ * staging barrier of the decode kernel is told to expect 16 bytes more than
+ * its copies deliver, so each bounded wait can only end by running out; the
+ * kernel then flags TQ_ERR_DEVICE_TIMEOUT, gives its copies in flight one more
+ * bounded wait, and finishes the call with an undefined output (the split
+ * counters still return to zero, so the workspace stays usable).
  * mode 0 (default) turns it off. */
 void tq_set_fault_injection(int mode);
 

@@ -47,7 +47,7 @@ constexpr float kCScale = 64.f;   // centroids are scaled by 64 in the K tables
 
 // Byte layout of the dynamic shared memory of a decode CTA.
 struct DecodeSmem {
-  int qr, qo, sv, qjlb, warps, warp_stride;
+  int qr, qo, sv, qjlb, sq, warps, warp_stride;
   int kbuf, vbuf, kn, vn, sbuf, rn, ws, bar;   // offsets inside one warp's region
   int comb, total;
   __host__ __device__ DecodeSmem(int G, int qjl, int kb, int vb) {
@@ -56,6 +56,7 @@ struct DecodeSmem {
     qo = off; off += kD2 * G * 4;                 // [128][G] original-domain queries
     sv = off; off += kD2 * 4;
     qjlb = off; off += qjl ? 32 * 8 * 16 : 0;     // per lane, per k-tile: S q hi/lo operands
+    sq = off; off += qjl ? G * kQjlM * 4 : 0;     // [G][m] S q_rot (QJL)
     warps = off;
     int w = 0;
     kbuf = w; w += 2 * 32 * 16 * kb;
@@ -69,9 +70,7 @@ struct DecodeSmem {
     warp_stride = w;
     int region = kDWarps * w;
     const int comb_need = kDWarps * G * (2 + kD2) * 4;   // cm, cl, co
-    const int scratch_need = 2 * G * kD2 * 4;
     if (region < comb_need) region = comb_need;
-    if (region < scratch_need) region = scratch_need;
     comb = warps;
     off += region;
     total = off + 16;                             // + is-last flag
@@ -349,62 +348,162 @@ __global__ void __launch_bounds__(kDT, 3) decode_kernel(const DecodeArgs a) {
   const int mg = lane >> 2, tig = lane & 3;   // MMA group / thread-in-group
 
   // ------------------------------------------------------------- prologue
+  // Every global load of the prologue is issued before any result is used,
+  // and each warp starts the bulk copies of its first chunk before the query
+  // is rotated, so the prologue costs about one memory round trip.
+  __shared__ float cks[256], cvs[256];
+  const int T = a.seq_lens[b];
+  const int W = a.W;
+  const int nq = T - W > 0 ? T - W : 0;
+  const bool window_split = split >= a.n_qsplits;
+  constexpr int GW = (G + kDWarps - 1) / kDWarps;   // query heads rotated per warp
+  float ck0 = 0.f, ck1 = 0.f, cv0 = 0.f, cv1 = 0.f;
+  if (tid < (1 << KB)) ck0 = __ldg(a.ck + tid);
+  if (tid + kDT < (1 << KB)) ck1 = __ldg(a.ck + tid + kDT);
+  if (tid < (1 << VB)) cv0 = __ldg(a.cv + tid);
+  if (tid + kDT < (1 << VB)) cv1 = __ldg(a.cv + tid + kDT);
+  const float svv = __ldg(a.sv + tid);
+  const float4 sk4 = __ldg((const float4*)a.sk + lane);
+  const long long qbase = ((long long)b * a.Hq + (long long)kvh * G) * kD2;
+  float qv[GW][4];
+#pragma unroll
+  for (int j = 0; j < GW; ++j) {
+    const int g = warp + kDWarps * j;
+    qv[j][0] = qv[j][1] = qv[j][2] = qv[j][3] = 0.f;
+    if (g < G) {
+      if (a.q_f32) {
+        const float4 v = __ldg((const float4*)((const float*)a.q + qbase + g * kD2) + lane);
+        qv[j][0] = v.x; qv[j][1] = v.y; qv[j][2] = v.z; qv[j][3] = v.w;
+      } else {
+        const uint2 v = __ldg((const uint2*)((const uint16_t*)a.q + qbase + g * kD2) + lane);
+        qv[j][0] = bf16lo(v.x); qv[j][1] = bf16hi(v.x); qv[j][2] = bf16lo(v.y); qv[j][3] = bf16hi(v.y);
+      }
+    }
+  }
+  cks[tid] = ck0;
+  cks[tid + kDT] = ck1;
+  cvs[tid] = cv0;
+  cvs[tid + kDT] = cv1;
+  svs[tid] = svv;
+  uint8_t* wreg = smem + L.warps + warp * L.warp_stride;
+  uint64_t* bar = (uint64_t*)(wreg + L.bar);
+  if (lane == 0) {
+    mbar_init(bar + 0, 1);
+    mbar_init(bar + 1, 1);
+    fence_mbarrier_init();
+  }
+  __syncwarp();
+
+  // this split's token range and plane rows (quantized splits)
+  const int t_begin = split * a.split_tokens;
+  int t_end = t_begin + a.split_tokens;
+  if (t_end > nq) t_end = nq;
+  const long long row0 = ((long long)b * Hkv + kvh);
+  const uint8_t* kc = a.kc + row0 * a.kcap * KROW;
+  const uint8_t* vc = a.vc + row0 * a.vcap * VROW;
+  const float* knp = a.kn + row0 * a.kcap;
+  const float* vnp = a.vn + row0 * a.vcap;
+  const uint8_t* ksp = QJL ? a.ks + row0 * a.kcap * 16 : nullptr;
+  const float* krp = QJL ? a.kr + row0 * a.kcap : nullptr;
+
+  // chunk c0 -> ring slot: codes by bulk copy; norms by bulk copy when the
+  // 16-byte-rounded range stays inside the plane, else by plain loads
+  auto issue = [&](int c0, int slot) {
+    const int nv = t_end - c0 < 32 ? t_end - c0 : 32;
+    const int n4 = (nv + 3) & ~3;
+    // bulk copies need 16-byte aligned sources: the norm rows of a (sequence,
+    // head) start at row0 * capacity floats, aligned only if capacity % 4 == 0
+    const bool aligned = (((uintptr_t)(knp + c0) | (uintptr_t)(vnp + c0) |
+                           (QJL ? (uintptr_t)(krp + c0) : (uintptr_t)0)) & 15u) == 0;
+    const bool bulk_norms =
+        aligned && (long long)c0 + n4 <= a.kcap && (long long)c0 + n4 <= a.vcap;
+    uint8_t* kb_ = wreg + L.kbuf + slot * 32 * KROW;
+    uint8_t* vb_ = wreg + L.vbuf + slot * 32 * VROW;
+    float* kn_ = (float*)(wreg + L.kn + slot * 128);
+    float* vn_ = (float*)(wreg + L.vn + slot * 128);
+    if (!bulk_norms && lane < nv) {
+      kn_[lane] = knp[c0 + lane];
+      vn_[lane] = vnp[c0 + lane];
+      if constexpr (QJL) ((float*)(wreg + L.rn + slot * 128))[lane] = krp[c0 + lane];
+    }
+    __syncwarp();
+    if (lane == 0) {
+      uint32_t bytes = nv * (KROW + VROW) + (bulk_norms ? 2 * n4 * 4 : 0);
+      if constexpr (QJL) bytes += nv * 16 + (bulk_norms ? n4 * 4 : 0);
+      // a.extra_tx is a test hook: bytes that never arrive, so the wait on
+      // this chunk can only end by running out of polls
+      mbar_arrive_expect_tx(bar + slot, bytes + a.extra_tx);
+      bulk_g2s(kb_, kc + (long long)c0 * KROW, nv * KROW, bar + slot);
+      bulk_g2s(vb_, vc + (long long)c0 * VROW, nv * VROW, bar + slot);
+      if (bulk_norms) {
+        bulk_g2s(kn_, knp + c0, n4 * 4, bar + slot);
+        bulk_g2s(vn_, vnp + c0, n4 * 4, bar + slot);
+      }
+      if constexpr (QJL) {
+        bulk_g2s(wreg + L.sbuf + slot * 512, ksp + (long long)c0 * 16, nv * 16, bar + slot);
+        if (bulk_norms) bulk_g2s(wreg + L.rn + slot * 128, krp + c0, n4 * 4, bar + slot);
+      }
+    }
+  };
+  if (!window_split && t_begin + 32 * warp < t_end) issue(t_begin + 32 * warp, 0);
+
+  __syncthreads();                                   // cks, cvs, svs
   for (int i = tid; i < 256; i += kDT) {
     if constexpr (KB == 2 || KB == 3) {
       if (i < (1 << (2 * KB))) {
         const int msk = (1 << KB) - 1;
-        const uint32_t e0 = hilo(a.ck[i & msk] * kCScale), e1 = hilo(a.ck[(i >> KB) & msk] * kCScale);
+        const uint32_t e0 = hilo(cks[i & msk] * kCScale), e1 = hilo(cks[(i >> KB) & msk] * kCScale);
         uint32_t hp, lp;
         pack_hilo(e0, e1, hp, lp);
         lutk[2 * i] = hp;
         lutk[2 * i + 1] = lp;
       }
     } else {
-      lutk[i] = hilo(a.ck[i] * kCScale);
+      lutk[i] = hilo(cks[i] * kCScale);
     }
     uint32_t e;
     if constexpr (VB == 2 || VB == 3) {
       const int msk = (1 << VB) - 1;
-      e = (h16(a.cv[(i >> VB) & msk]) << 16) | h16(a.cv[i & msk]);
+      e = (h16(cvs[(i >> VB) & msk]) << 16) | h16(cvs[i & msk]);
     } else {
-      e = h16(a.cv[i]);
+      e = h16(cvs[i]);
     }
     lutv[i] = e;
   }
   if (tid < 4) slut[tid] = ((tid & 2) ? 0x3C000000u : 0xBC000000u) | ((tid & 1) ? 0x3C00u : 0xBC00u);
-  svs[tid] = a.sv[tid];
-  uint8_t* wreg = smem + L.warps + warp * L.warp_stride;
-  uint64_t* bar = (uint64_t*)(wreg + L.bar);
-  float* scratch = (float*)(smem + L.warps);        // [G][128], aliases warp buffers
-  {
-    const long long qbase = ((long long)b * a.Hq + (long long)kvh * G) * kD2;
-    for (int e = tid; e < G * kD2; e += kDT) {
-      const int g = e / kD2, i = e % kD2;
-      float v = a.q_f32 ? ((const float*)a.q)[qbase + e]
-                        : __uint_as_float((uint32_t)((const uint16_t*)a.q)[qbase + e] << 16);
-      v *= a.qscale;
-      qo[i * G + g] = v;
-      scratch[g * kD2 + i] = v * a.sk[i];
-    }
-  }
-  __syncthreads();
-  for (int h = 1; h < kD2; h <<= 1) {               // butterfly, Sylvester order
-    for (int e = tid; e < G * (kD2 / 2); e += kDT) {
-      const int g = e / (kD2 / 2), r = e % (kD2 / 2);
-      const int i = (r / h) * 2 * h + (r % h);
-      float* x = scratch + g * kD2;
-      const float u = x[i], v = x[i + h];
-      x[i] = u + v;
-      x[i + h] = u - v;
-    }
-    __syncthreads();
-  }
+  // query rotation in registers: warp w rotates heads w (and w + 4), lane l
+  // holds coordinates 4l .. 4l+3; two butterfly stages in the lane, five by shuffles
   float qmax = 0.f;
-  for (int e = tid; e < G * kD2; e += kDT) {
-    const int g = e / kD2, i = e % kD2;
-    const float v = scratch[e] * 0.08838834764831845f;   // 1/sqrt(128)
-    qr[i * G + g] = v;
-    qmax = fmaxf(qmax, fabsf(v));
+#pragma unroll
+  for (int j = 0; j < GW; ++j) {
+    const int g = warp + kDWarps * j;
+    if (g < G) {
+      float x[4];
+      const float sgs[4] = {sk4.x, sk4.y, sk4.z, sk4.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float v = qv[j][c] * a.qscale;
+        qo[(4 * lane + c) * G + g] = v;
+        x[c] = v * sgs[c];
+      }
+      const float u0 = x[0] + x[1], u1 = x[0] - x[1], u2 = x[2] + x[3], u3 = x[2] - x[3];
+      x[0] = u0 + u2; x[2] = u0 - u2; x[1] = u1 + u3; x[3] = u1 - u3;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float other = __shfl_xor_sync(0xffffffffu, x[c], o);
+          x[c] = upper ? other - x[c] : x[c] + other;
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float v = x[c] * 0.08838834764831845f;   // 1/sqrt(128)
+        qr[(4 * lane + c) * G + g] = v;
+        qmax = fmaxf(qmax, fabsf(v));
+      }
+    }
   }
   // power-of-two scale bringing max |q_rot| below 1 for the fp16 operands
   __shared__ float red[kDWarps];
@@ -432,8 +531,7 @@ __global__ void __launch_bounds__(kDT, 3) decode_kernel(const DecodeArgs a) {
   }
   float qsq = 1.f;                                   // scale of the S q operands
   if constexpr (QJL) {
-    __syncthreads();                                 // scratch is reused below
-    float* sq = scratch;                             // [G][m]
+    float* sq = (float*)(smem + L.sq);               // [G][m]
     float smax = 0.f;
     for (int j = tid; j < kQjlM; j += kDT) {
       float acc[G];
@@ -474,18 +572,8 @@ __global__ void __launch_bounds__(kDT, 3) decode_kernel(const DecodeArgs a) {
     }
   }
   __syncthreads();
-  if (lane == 0) {
-    mbar_init(bar + 0, 1);
-    mbar_init(bar + 1, 1);
-    fence_mbarrier_init();
-  }
-  __syncwarp();
 
   // ------------------------------------------------------------- main loop
-  const int T = a.seq_lens[b];
-  const int W = a.W;
-  const int nq = T - W > 0 ? T - W : 0;
-  const bool window_split = split >= a.n_qsplits;
   float* cm = (float*)(smem + L.comb);   // [warps][G]      (merge area, after the loop)
   float* cl = cm + kDWarps * G;          // [warps][G]
   float* co = cl + kDWarps * G;          // [warps][G][128]
@@ -499,61 +587,12 @@ __global__ void __launch_bounds__(kDT, 3) decode_kernel(const DecodeArgs a) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) d[k][j] = 0.f;
     const bool h0ok = 2 * tig < G, h1ok = 2 * tig + 1 < G;
-    const int t_begin = split * a.split_tokens;
-    int t_end = t_begin + a.split_tokens;
-    if (t_end > nq) t_end = nq;
-    const long long row0 = ((long long)b * Hkv + kvh);
-    const uint8_t* kc = a.kc + row0 * a.kcap * KROW;
-    const uint8_t* vc = a.vc + row0 * a.vcap * VROW;
-    const float* knp = a.kn + row0 * a.kcap;
-    const float* vnp = a.vn + row0 * a.vcap;
-    const uint8_t* ksp = QJL ? a.ks + row0 * a.kcap * 16 : nullptr;
-    const float* krp = QJL ? a.kr + row0 * a.kcap : nullptr;
     uint16_t* ws16 = (uint16_t*)(wreg + L.ws);   // [8 heads][32 tokens] fp16 weights
     const float kscale = 1.f / (kCScale * qsp);
     const float qjl_scale = 1.2533141373155003f / (float)kQjlM / qsq;   // sqrt(pi/2)/m
     const uint4* qjlb = QJL ? (const uint4*)(smem + L.qjlb) + lane * 8 : nullptr;
 
-    // chunk c0 -> ring slot: codes by bulk copy; norms by bulk copy when the
-    // 16-byte-rounded range stays inside the plane, else by plain loads
-    auto issue = [&](int c0, int slot) {
-      const int nv = t_end - c0 < 32 ? t_end - c0 : 32;
-      const int n4 = (nv + 3) & ~3;
-      // bulk copies need 16-byte aligned sources: the norm rows of a (sequence,
-      // head) start at row0 * capacity floats, aligned only if capacity % 4 == 0
-      const bool aligned = (((uintptr_t)(knp + c0) | (uintptr_t)(vnp + c0) |
-                             (QJL ? (uintptr_t)(krp + c0) : (uintptr_t)0)) & 15u) == 0;
-      const bool bulk_norms =
-          aligned && (long long)c0 + n4 <= a.kcap && (long long)c0 + n4 <= a.vcap;
-      uint8_t* kb_ = wreg + L.kbuf + slot * 32 * KROW;
-      uint8_t* vb_ = wreg + L.vbuf + slot * 32 * VROW;
-      float* kn_ = (float*)(wreg + L.kn + slot * 128);
-      float* vn_ = (float*)(wreg + L.vn + slot * 128);
-      if (!bulk_norms && lane < nv) {
-        kn_[lane] = knp[c0 + lane];
-        vn_[lane] = vnp[c0 + lane];
-        if constexpr (QJL) ((float*)(wreg + L.rn + slot * 128))[lane] = krp[c0 + lane];
-      }
-      __syncwarp();
-      if (lane == 0) {
-        uint32_t bytes = nv * (KROW + VROW) + (bulk_norms ? 2 * n4 * 4 : 0);
-        if constexpr (QJL) bytes += nv * 16 + (bulk_norms ? n4 * 4 : 0);
-        mbar_arrive_expect_tx(bar + slot, bytes);
-        bulk_g2s(kb_, kc + (long long)c0 * KROW, nv * KROW, bar + slot);
-        bulk_g2s(vb_, vc + (long long)c0 * VROW, nv * VROW, bar + slot);
-        if (bulk_norms) {
-          bulk_g2s(kn_, knp + c0, n4 * 4, bar + slot);
-          bulk_g2s(vn_, vnp + c0, n4 * 4, bar + slot);
-        }
-        if constexpr (QJL) {
-          bulk_g2s(wreg + L.sbuf + slot * 512, ksp + (long long)c0 * 16, nv * 16, bar + slot);
-          if (bulk_norms) bulk_g2s(wreg + L.rn + slot * 128, krp + c0, n4 * 4, bar + slot);
-        }
-      }
-    };
-
-    int c0 = t_begin + 32 * warp;
-    if (c0 < t_end) issue(c0, 0);
+    int c0 = t_begin + 32 * warp;           // its copies were started in the prologue
     bool ok = true;
     int kq = 0;
     for (; c0 < t_end; c0 += 32 * kDWarps, ++kq) {
@@ -722,12 +761,14 @@ __global__ void __launch_bounds__(kDT, 3) decode_kernel(const DecodeArgs a) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) ow[g][j] = 0.f;
     }
-    const int nw = T < W ? T : W;
+    const int nw = T < W ? T : W;                     // window tokens of this sequence
     const int tw0 = T - nw;
+    const int kw0 = 32 * (split - a.n_qsplits);       // this split's 32 of them
+    const int kw1 = kw0 + 32 < nw ? kw0 + 32 : nw;
     const long long base = ((long long)b * Hkv + kvh) * W;
     // warp w takes window tokens w, w+4, ...; 8 tokens' rows are loaded before
     // any is used, so the loads overlap instead of paying one latency each
-    for (int k0 = warp; k0 < nw; k0 += 8 * kDWarps) {
+    for (int k0 = kw0 + warp; k0 < kw1; k0 += 8 * kDWarps) {
       uint2 kw[8], vw[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -807,54 +848,45 @@ __global__ void __launch_bounds__(kDT, 3) decode_kernel(const DecodeArgs a) {
   // last CTA of this (sequence, kv-head): one warp per head merges the splits,
   // inverse-rotates (R^T = D_s H / sqrt(d)) in registers and writes the output
   const float* base = a.partials + unit * a.n_splits * G * stride;
-  float* fsc = (float*)(smem + L.comb);  // [warps][32] per-split factors (merge area is free now)
   for (int g = warp; g < G; g += kDWarps) {
-    // pass 1, lanes over splits: M = max m_s, L = sum l_s 2^(m_s - M)
-    float M = kNegBig;
-    for (int s2 = lane; s2 < a.n_splits; s2 += 32) M = fmaxf(M, __ldcg(base + (s2 * G + g) * stride));
-    M = warp_max(M);
-    float Lsum = 0.f;
-    for (int s2 = lane; s2 < a.n_splits; s2 += 32) {
-      const float* ps = base + (s2 * G + g) * stride;
-      Lsum = fmaf(__ldcg(ps + 1), exp2f(__ldcg(ps) - M), Lsum);
-    }
-    Lsum = warp_sum(Lsum);
-    // pass 2, lanes over coordinates: 8 split rows in flight at a time
-    float4 rot = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < a.n_qsplits; s0 += 32) {
-      const int ns = a.n_qsplits - s0 < 32 ? a.n_qsplits - s0 : 32;
-      if (lane < ns) fsc[warp * 32 + lane] = exp2f(__ldcg(base + ((s0 + lane) * G + g) * stride) - M);
-      __syncwarp();
-      int j = 0;
-      for (; j + 16 <= ns; j += 16) {
-        float4 v[16];
+    // one pass over the splits, 32 split rows in flight per batch, with online
+    // rescaling: lane s holds (m, l) of split s0 + s, every lane its 4
+    // coordinates of all 32 rows.  Rows of quantized splits are rotated-domain
+    // sums, rows of window splits original-domain sums: two accumulators.
+    float M = kNegBig, Lsum = 0.f;
+    float4 rot = make_float4(0.f, 0.f, 0.f, 0.f), win = rot;
+    for (int s0 = 0; s0 < a.n_splits; s0 += 32) {
+      const int sl = s0 + lane;
+      const float* pl = base + (sl * G + g) * stride;
+      const float ml = sl < a.n_splits ? __ldcg(pl) : kNegBig;
+      const float ll = sl < a.n_splits ? __ldcg(pl + 1) : 0.f;
+      float4 v[32];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) v[u] = __ldcg((const float4*)(base + ((s0 + j + u) * G + g) * stride + 4) + lane);
+      for (int u = 0; u < 32; ++u)
+        v[u] = s0 + u < a.n_splits
+                   ? __ldcg((const float4*)(base + ((s0 + u) * G + g) * stride + 4) + lane)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float Mn = fmaxf(M, warp_max(ml));
+      const float r = exp2f(M - Mn);
+      const float fl = exp2f(ml - Mn);
+      Lsum = fmaf(Lsum, r, warp_sum(ll * fl));
+      rot = make_float4(rot.x * r, rot.y * r, rot.z * r, rot.w * r);
+      win = make_float4(win.x * r, win.y * r, win.z * r, win.w * r);
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const float f = fsc[warp * 32 + j + u];
-          rot.x = fmaf(v[u].x, f, rot.x);
-          rot.y = fmaf(v[u].y, f, rot.y);
-          rot.z = fmaf(v[u].z, f, rot.z);
-          rot.w = fmaf(v[u].w, f, rot.w);
-        }
+      for (int u = 0; u < 32; ++u) {
+        const float f = __shfl_sync(0xffffffffu, fl, u);
+        const bool q = s0 + u < a.n_qsplits;
+        const float fq = q ? f : 0.f, fw = q ? 0.f : f;
+        rot.x = fmaf(v[u].x, fq, rot.x);
+        rot.y = fmaf(v[u].y, fq, rot.y);
+        rot.z = fmaf(v[u].z, fq, rot.z);
+        rot.w = fmaf(v[u].w, fq, rot.w);
+        win.x = fmaf(v[u].x, fw, win.x);
+        win.y = fmaf(v[u].y, fw, win.y);
+        win.z = fmaf(v[u].z, fw, win.z);
+        win.w = fmaf(v[u].w, fw, win.w);
       }
-      for (; j < ns; ++j) {
-        const float4 v = __ldcg((const float4*)(base + ((s0 + j) * G + g) * stride + 4) + lane);
-        const float f = fsc[warp * 32 + j];
-        rot.x = fmaf(v.x, f, rot.x);
-        rot.y = fmaf(v.y, f, rot.y);
-        rot.z = fmaf(v.z, f, rot.z);
-        rot.w = fmaf(v.w, f, rot.w);
-      }
-      __syncwarp();
-    }
-    float4 win = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (a.n_splits > a.n_qsplits) {
-      const float* ps = base + (a.n_qsplits * G + g) * stride;
-      const float f = exp2f(__ldcg(ps) - M);
-      const float4 v = __ldcg((const float4*)(ps + 4) + lane);
-      win = make_float4(v.x * f, v.y * f, v.z * f, v.w * f);
+      M = Mn;
     }
     // butterfly over 128 values, 4 per lane (coordinates 4*lane .. 4*lane+3)
     float x[4] = {rot.x, rot.y, rot.z, rot.w};

@@ -341,16 +341,17 @@ static DecodePlan decode_plan(const tq_config* cfg, int batch, int n_q_heads, in
   long long max_nq = (long long)max_seq_len - W;
   if (max_nq < 0) max_nq = 0;
   long long units = (long long)batch * n_kv_heads;
-  // one wave of about kTargetCtas CTAs: split the quantized tokens evenly over
-  // what is left after the window splits, in multiples of 32 tokens
-  long long slots = kTargetCtas - (W > 0 ? units : 0);
+  // the window: one split per 32 window tokens; the quantized tokens: one wave
+  // of about kTargetCtas CTAs in all, split evenly in multiples of 32 tokens
+  const int n_wsplits = W > 0 ? (W + 31) / 32 : 0;
+  long long slots = kTargetCtas - units * n_wsplits;
   if (slots < units) slots = units;
   long long per = units > 0 ? (units * max_nq + slots - 1) / slots : 0;
   long long st = (per + 31) / 32 * 32;
   if (st < 256) st = 256;
   p.split_tokens = (int)st;
   p.n_qsplits = (int)((max_nq + st - 1) / st);
-  p.n_splits = p.n_qsplits + (W > 0 ? 1 : 0);
+  p.n_splits = p.n_qsplits + n_wsplits;
   p.G = n_kv_heads > 0 ? n_q_heads / n_kv_heads : 0;
   p.partial_floats = (size_t)units * p.n_splits * p.G * kPartialStride;
   p.counters_off = align256(p.partial_floats * sizeof(float));
@@ -451,8 +452,6 @@ static void fill_quant_codec(QuantArgs& a, const tq_config* cfg, const void* tab
   a.S = a.qjl ? tbl_qjl(cfg, tables, layer) : nullptr;
   a.m = cfg->qjl_m;
   a.err = quant_error_ptr();
-  a.wait_limit = g_wait_limit;
-  a.extra_tx = g_fault_injection == 1 ? 16u : 0u;
   const SearchGrid g = search_grid(cfg, a.bits);
   a.grid_scale = g.scale;
   a.grid_magic = g.magic;
@@ -708,6 +707,7 @@ extern "C" tq_status tq_decode_attention(const tq_config* cfg, const void* table
   a.counters = (unsigned*)((uint8_t*)workspace + p.counters_off);
   a.err = decode_error_ptr();
   a.wait_limit = g_wait_limit;
+  a.extra_tx = g_fault_injection == 1 ? 16u : 0u;
   if (p.n_splits == 0) {
     // every sequence is empty: the output is zero
     if (cudaMemsetAsync(out, 0, (size_t)batch * n_q_heads * kHeadDim * sizeof(float),

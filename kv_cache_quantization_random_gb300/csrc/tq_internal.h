@@ -11,7 +11,7 @@ namespace tq {
 
 constexpr int kHeadDim = 128;          // the head_dim the kernels implement
 constexpr int kQjlM = 128;             // the QJL projection count the kernels implement
-constexpr int kTargetCtas = 3 * 152;   // decode grid target: 3 resident CTAs per GB300 SM
+constexpr int kTargetCtas = 2 * 152;   // decode grid target: 2 resident CTAs per GB300 SM
 constexpr int kPartialStride = 4 + kHeadDim;   // floats per (split, head): m, l, pad, pad, o[d]
 
 // ---- device tables (built on the host by tq_build_tables) -------------------
@@ -59,8 +59,6 @@ struct QuantArgs {
   const uint16_t* S;             // bf16 [m][d]
   int m;
   unsigned* err;                 // device error word
-  uint32_t wait_limit;
-  uint32_t extra_tx;             // test hook (tq_set_fault_injection), normally 0
   // code search grid (see SearchGrid) and the rotation signs as fp32 sign-bit
   // masks, kept in the parameter block so the kernel reads them as operands
   float grid_scale;              // cells per unit of y
@@ -144,7 +142,7 @@ struct DecodeArgs {
   const uint16_t* kwin; const uint16_t* vwin; int W;
   const int32_t* seq_lens;
   int n_qsplits;                 // splits over the quantized tokens
-  int n_splits;                  // n_qsplits + (W > 0)
+  int n_splits;                  // n_qsplits + one split per 32 window tokens
   int split_tokens;              // tokens per quantized split (multiple of 32)
   // codec
   const float* ck; const float* cv;
@@ -156,6 +154,7 @@ struct DecodeArgs {
   unsigned* counters;            // [B][Hkv]
   unsigned* err;
   uint32_t wait_limit;           // polls per bounded wait (0 = default)
+  uint32_t extra_tx;             // test hook (tq_set_fault_injection), normally 0
 };
 
 // ---- launchers (defined in the .cu files) -------------------------------------

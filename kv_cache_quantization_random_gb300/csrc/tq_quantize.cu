@@ -29,13 +29,13 @@ struct RowCfg {
   static constexpr int kPitch = kRowBytes + 16;   // odd multiple of 16 B: conflict-free rows
 };
 
-// dynamic shared memory: two row buffers, the search grid, boundaries,
-// centroids, two mbarriers and (QJL) the fp32 projection matrix
+// dynamic shared memory: per warp two buffers of 32 rows, the search grid,
+// boundaries, centroids and (QJL) the fp32 projection matrix
 __host__ __device__ constexpr size_t quant_rows_bytes(bool f32) {
   return (size_t)kQRows * (f32 ? RowCfg<true>::kPitch : RowCfg<false>::kPitch);
 }
 __host__ __device__ constexpr size_t quant_smem_bytes(bool f32, bool qjl, int cells) {
-  return 2 * quant_rows_bytes(f32) + (size_t)cells * 8 + 256 * 4 + (qjl ? 256 * 4 : 0) + 16 +
+  return 2 * quant_rows_bytes(f32) + (size_t)cells * 8 + 256 * 4 + (qjl ? 256 * 4 : 0) +
          (qjl ? (size_t)kQjlM * kD * 4 : 0);
 }
 
@@ -82,30 +82,24 @@ __device__ __forceinline__ float2 lds64f(uint32_t addr) {
   return v;
 }
 
-// Warp 0 stages the rows of one tile into a row buffer with bulk copies that
-// complete on `bar`; rows that resolve to nothing are skipped.
+// A warp stages the 32 rows of its next tile into one of its two row buffers
+// with 16-byte asynchronous copies (cp.async): lane l resolved row l; each
+// pass copies 512 contiguous source bytes (two bf16 rows or one fp32 row),
+// one 16-byte chunk per lane.  Rows that resolve to nothing are not copied.
 template <bool F32>
-__device__ __forceinline__ void stage_tile(const QuantArgs& a, uint32_t v0, uint32_t total,
-                                           uint8_t* rows, uint64_t* bar, int lane) {
+__device__ __forceinline__ void stage_rows(const void* src, bool valid, uint8_t* rows, int lane) {
   constexpr int kRowBytes = RowCfg<F32>::kRowBytes;
   constexpr int kPitch = RowCfg<F32>::kPitch;
-  const void* srcs[kQRows / 32];
-  uint32_t mine = 0;
-#pragma unroll
-  for (int k = 0; k < kQRows / 32; ++k) {
-    const uint32_t v = v0 + lane + 32 * k;
-    long long dummy;
-    const bool ok = v < total && resolve_row(a, v, &srcs[k], &dummy);
-    mine |= (ok ? 1u : 0u) << k;
+  constexpr int kChunks = kRowBytes / 16;            // 16 (bf16) or 32 (fp32)
+  constexpr int kRowsPerPass = 32 / kChunks;
+  const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+  const int c = lane % kChunks;
+#pragma unroll 4
+  for (int pass = 0; pass < 32 / kRowsPerPass; ++pass) {
+    const int r = pass * kRowsPerPass + lane / kChunks;
+    const uint8_t* sp = (const uint8_t*)__shfl_sync(0xffffffffu, (unsigned long long)src, r);
+    if ((vmask >> r) & 1u) cp_async16(rows + r * kPitch + 16 * c, sp + 16 * c);
   }
-  const uint32_t count = __reduce_add_sync(0xffffffffu, (uint32_t)__popc(mine));
-  // a.extra_tx is a test hook: bytes that never arrive, so the wait on this
-  // tile can only end by running out of polls
-  if (lane == 0) mbar_arrive_expect_tx(bar, count * kRowBytes + a.extra_tx);
-  __syncwarp();
-#pragma unroll
-  for (int k = 0; k < kQRows / 32; ++k)
-    if (mine & (1u << k)) bulk_g2s(rows + (lane + 32 * k) * kPitch, srcs[k], kRowBytes, bar);
 }
 
 // Rotated coordinates of one vector, held as pairs (y_j, y_{j+64}), j < 64,
@@ -172,26 +166,20 @@ __global__ void __launch_bounds__(kQRows, (QJL ? 1 : 3)) quantize_kernel(const Q
   constexpr int NW = 4 * BITS;         // 32-bit code words per vector (128 * BITS / 32)
   constexpr int kPitch = RowCfg<F32>::kPitch;
   extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* rows0 = smem;
-  uint8_t* rows1 = smem + quant_rows_bytes(F32);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // this warp's two buffers of 32 rows
+  uint8_t* wrows = smem + (size_t)warp * 2 * 32 * kPitch;
   float2* grid = (float2*)(smem + 2 * quant_rows_bytes(F32));
   float* bnd = (float*)(grid + a.grid_cells);
   float* cen = bnd + 256;                               // QJL only
-  uint64_t* bar = (uint64_t*)(cen + (QJL ? 256 : 0));
-  float* Sf = (float*)(bar + 2);
+  float* Sf = cen + (QJL ? 256 : 0);
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int i = tid; i < 256; i += kQRows) {
     bnd[i] = a.boundaries[i];
     if constexpr (QJL) cen[i] = a.centroids[i];
   }
   if constexpr (QJL) {
     for (int e = tid; e < kQjlM * kD; e += kQRows) Sf[e] = __uint_as_float((uint32_t)a.S[e] << 16);
-  }
-  if (tid == 0) {
-    mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
-    fence_mbarrier_init();
   }
   __syncthreads();
   // search grid: entry k = (first boundary at or above the lower edge of
@@ -209,40 +197,38 @@ __global__ void __launch_bounds__(kQRows, (QJL ? 1 : 3)) quantize_kernel(const Q
   const uint32_t grid_base = smem_u32(grid);
   const uint32_t kmax = (uint32_t)a.grid_cells - 1u;
 
+  // every warp streams its own tiles of 32 vectors: no CTA barrier below
   const uint32_t total = (uint32_t)a.B * (uint32_t)a.H * (uint32_t)a.n;
-  const uint32_t ntiles = (total + kQRows - 1) / kQRows;
-  const uint32_t limit = a.wait_limit ? a.wait_limit : kDefaultWaitLimit;
-  uint32_t phase0 = 0, phase1 = 0;
+  const uint32_t ntiles = (total + 31) / 32;
+  const uint32_t stride = gridDim.x * (kQRows / 32);
+  uint32_t tile = blockIdx.x * (kQRows / 32) + warp;
+  const void* src = nullptr;
+  long long drow = 0;
+  bool valid = false;
+  if (tile < ntiles) {
+    const uint32_t v = tile * 32 + lane;
+    valid = v < total && resolve_row(a, v, &src, &drow);
+    stage_rows<F32>(src, valid, wrows, lane);
+  }
+  cp_async_commit();
   int buf = 0;
-  uint32_t tile = blockIdx.x;
-  if (warp == 0 && tile < ntiles) stage_tile<F32>(a, tile * kQRows, total, rows0, &bar[0], lane);
-  for (; tile < ntiles; tile += gridDim.x) {
-    const uint32_t next = tile + gridDim.x;
-    if (warp == 0 && next < ntiles)          // the other buffer was released by the last barrier
-      stage_tile<F32>(a, next * kQRows, total, buf ? rows0 : rows1, buf ? &bar[0] : &bar[1], lane);
-    const uint32_t ph = buf ? phase1 : phase0;
-    const bool staged = __syncthreads_and(mbar_wait(&bar[buf], ph, limit, a.err));
-    if (!staged) {
-      // a staging wait ran out (error word already set): give the copies still
-      // in flight one more bounded wait each, then leave the planes untouched
-      for (uint32_t i = 0; i < limit && !mbar_try_wait(&bar[buf], ph); ++i) {
-      }
-      if (next < ntiles) {
-        const uint32_t ph2 = buf ? phase0 : phase1;
-        for (uint32_t i = 0; i < limit && !mbar_try_wait(&bar[buf ^ 1], ph2); ++i) {
-        }
-      }
-      return;
+  for (; tile < ntiles; tile += stride) {
+    const uint32_t next = tile + stride;
+    const void* nsrc = nullptr;
+    long long ndrow = 0;
+    bool nvalid = false;
+    if (next < ntiles) {                 // the other buffer was released by the last __syncwarp
+      const uint32_t v = next * 32 + lane;
+      nvalid = v < total && resolve_row(a, v, &nsrc, &ndrow);
+      stage_rows<F32>(nsrc, nvalid, wrows + (buf ^ 1) * 32 * kPitch, lane);
     }
-    if (buf) phase1 ^= 1u; else phase0 ^= 1u;
-    const uint8_t* rows = buf ? rows1 : rows0;
-
-    const uint32_t v = tile * kQRows + tid;
-    const void* srcp;
-    long long drow;
-    if (v < total && resolve_row(a, v, &srcp, &drow)) {
+    cp_async_commit();
+    cp_async_wait<1>();                  // this lane's copies of `tile` have landed
+    __syncwarp();                        // ... and every other lane's
+    const uint8_t* rows = wrows + buf * 32 * kPitch;
+    if (valid) {
       float2 p[64];
-      const float nrm = load_rotate<F32>(a, rows + tid * kPitch, p);
+      const float nrm = load_rotate<F32>(a, rows + lane * kPitch, p);
       const float inv = nrm > 0.f ? 1.0f / (nrm * 11.313708498984761f) : 0.f;
       const float2 inv2 = make_float2(inv, inv);
       const float2 gs2 = make_float2(a.grid_scale, a.grid_scale);
@@ -310,9 +296,13 @@ __global__ void __launch_bounds__(kQRows, (QJL ? 1 : 3)) quantize_kernel(const Q
         a.qjl_rnorm[drow] = gamma;
       }
     }
-    __syncthreads();   // every thread is done with this buffer before it is refilled
+    __syncwarp();      // every lane is done with this buffer before it is refilled
     buf ^= 1;
+    src = nsrc;
+    drow = ndrow;
+    valid = nvalid;
   }
+  cp_async_wait<0>();
 }
 
 // Window ring update of tq_append_kv: new token t >= T1 - W goes to slot t mod W.

@@ -148,6 +148,15 @@ def test_decode_ragged_edges_with_window(B):
     assert rel_l2_per_head(out[1:], ref[1:]).max() < TOL
 
 
+@pytest.mark.parametrize("W", [100, 256])
+def test_decode_window_spread_over_several_splits(B, W):
+    """A window of W tokens is split 32 tokens per CTA; sequences shorter than
+    the window leave some of those splits partly or wholly empty."""
+    seq = [5, 31, 33, 64, W - 1, W, W + 1, W + 64, 900]
+    out, ref, _ = _decode_case(B, batch=len(seq), hq=8, hkv=2, seq=seq, kb=4, vb=2, W=W)
+    assert rel_l2_per_head(out, ref).max() < TOL
+
+
 def test_decode_ragged_no_window_and_empty(B):
     seq = [0, 1, 2, 31, 32, 33, 255, 256, 257, 2000]
     out, ref, _ = _decode_case(B, batch=len(seq), hq=8, hkv=2, seq=seq, kb=3, vb=2)
@@ -214,4 +223,27 @@ def test_decode_end_to_end_gpu_quantize(B):
     ref = O.decode_attention(to64(q), oqk["codes"], oqk["norms"], oqv["codes"], oqv["norms"],
                              oqk["c32"], oqv["c32"], oqk["signs"], oqv["signs"], [T],
                              w.softmax_scale, window=Wn, k_win=to64(kw), v_win=to64(vw))
+    assert rel_l2_per_head(to64(out), ref).max() < TOL
+
+
+def test_fault_injection_times_out_and_context_stays_usable(B):
+    """The decode kernel's staging waits are told to expect bytes that never
+    arrive: each bounded wait runs out, the call reports a device timeout, and
+    the next call on the same workspace is correct again."""
+    import torch
+    got, ref, c = _decode_case(B, batch=2, hq=8, hkv=2, seq=[700, 300], kb=4, vb=2, W=16)
+    assert rel_l2_per_head(got, ref).max() < TOL
+    out = torch.empty(2, 8, 128, device="cuda")
+    B.tq_set_wait_limit(2000)
+    B.tq_set_fault_injection(1)
+    try:
+        B.tq_decode_attention(c["cfg"], c["tables"], 0, c["q"].cuda(), c["scale"], c["kp"], c["vp"],
+                              c["seq_t"], c["Tmax"], out, c["ws"], k_win=c["kw"], v_win=c["vw"])
+        assert B.tq_get_device_error() == 5          # TQ_ERR_DEVICE_TIMEOUT
+    finally:
+        B.tq_set_fault_injection(0)
+        B.tq_set_wait_limit(0)
+    B.tq_decode_attention(c["cfg"], c["tables"], 0, c["q"].cuda(), c["scale"], c["kp"], c["vp"],
+                          c["seq_t"], c["Tmax"], out, c["ws"], k_win=c["kw"], v_win=c["vw"])
+    assert B.tq_get_device_error() == B.TQ_OK
     assert rel_l2_per_head(to64(out), ref).max() < TOL

@@ -238,27 +238,6 @@ def test_append_one_launch_and_bulk_paths(B, kb, vb, qjl, W_):
             assert torch.equal(vw[:, :, t % W_].cpu(), V[:, :, t])
 
 
-def test_fault_injection_times_out_and_context_stays_usable(B):
-    import torch
-    cfg = B.Config(k_bits=3, v_bits=3)
-    tables = B.device_tables(cfg)
-    X = torch.randn(1, 1, 300, 128).to(torch.bfloat16).cuda()
-    planes = B.Planes(cfg, 0, 0, 1, 1, 300)
-    B.tq_set_wait_limit(2000)
-    B.tq_set_fault_injection(1)
-    try:
-        B.tq_quantize_kv(cfg, tables, 0, 0, X, planes)
-        assert B.tq_get_device_error() == 5          # TQ_ERR_DEVICE_TIMEOUT
-        assert torch.count_nonzero(planes.codes).item() == 0
-    finally:
-        B.tq_set_fault_injection(0)
-        B.tq_set_wait_limit(0)
-    B.tq_quantize_kv(cfg, tables, 0, 0, X, planes)
-    assert B.tq_get_device_error() == B.TQ_OK
-    oq = oracle_quantize(to64(X), 3, 0, 0, 0)
-    compare_codes(planes.codes_view().cpu().numpy(), oq, 3)
-
-
 def test_gpu_argument_validation_with_real_buffers(B):
     import torch
     cfg = B.Config(k_bits=3, v_bits=3)
