@@ -14,7 +14,7 @@
 // of the kv-head are scaled by softmax_scale*log2(e), rotated with the K sign
 // vector and split into fp16 hi + lo MMA operands held in registers; QJL keys
 // also get S q_rot as hi + lo operands.  Main loop, per warp and 32-token
-// chunk (bulk copies into a two-slot ring, bounded mbarrier waits), all on
+// chunk (bulk copies into a 3- or 4-slot ring, bounded mbarrier waits), all on
 // mma.sync m16n8k16 with fp32 accumulators:
 //   scores   S[tokens x heads] = K_c[tokens x coords] Q[coords x heads]: the
 //            packed codes are decoded in registers through tables of fp16
@@ -45,9 +45,13 @@ constexpr int kD2 = 128;
 constexpr float kNegBig = -1.0e30f;
 constexpr float kCScale = 64.f;   // centroids are scaled by 64 in the K tables
 
+// Chunks in each warp's ring: enough bytes in flight per SM to cover the HBM
+// latency (3 chunks ahead); formats with wide rows keep a 3-slot ring.
+__host__ __device__ constexpr int ring_slots(int kb, int vb) { return kb + vb <= 8 ? 4 : 3; }
+
 // Byte layout of the dynamic shared memory of a decode CTA.
 struct DecodeSmem {
-  int qr, qo, sv, qjlb, sq, warps, warp_stride;
+  int qr, qo, sv, qjlb, sq, lutk4, warps, warp_stride;
   int kbuf, vbuf, kn, vn, sbuf, rn, ws, bar;   // offsets inside one warp's region
   int comb, total;
   __host__ __device__ DecodeSmem(int G, int qjl, int kb, int vb) {
@@ -57,16 +61,19 @@ struct DecodeSmem {
     sv = off; off += kD2 * 4;
     qjlb = off; off += qjl ? 32 * 8 * 16 : 0;     // per lane, per k-tile: S q hi/lo operands
     sq = off; off += qjl ? G * kQjlM * 4 : 0;     // [G][m] S q_rot (QJL)
+    lutk4 = off; off += kb == 4 ? 256 * 16 * 8 : 0;   // 4-bit key pair table, 16 replicas
     warps = off;
+    const int ns = ring_slots(kb, vb);
     int w = 0;
-    kbuf = w; w += 2 * 32 * 16 * kb;
-    vbuf = w; w += 2 * 32 * 16 * vb;
-    kn = w; w += 2 * 128;
-    vn = w; w += 2 * 128;
-    sbuf = w; w += qjl ? 2 * 32 * 16 : 0;
-    rn = w; w += qjl ? 2 * 128 : 0;
+    kbuf = w; w += ns * 32 * 16 * kb;
+    vbuf = w; w += ns * 32 * 16 * vb;
+    kn = w; w += ns * 128;
+    vn = w; w += ns * 128;
+    sbuf = w; w += qjl ? ns * 32 * 16 : 0;
+    rn = w; w += qjl ? ns * 128 : 0;
     ws = w; w += 8 * 32 * 2;                      // [8 heads][32 tokens] fp16 weights
-    bar = w; w += 16;
+    bar = w; w += 8 * ns;
+    w = (w + 15) & ~15;
     warp_stride = w;
     int region = kDWarps * w;
     const int comb_need = kDWarps * G * (2 + kD2) * 4;   // cm, cl, co
@@ -105,7 +112,7 @@ __device__ __forceinline__ void pack_hilo(uint32_t e0, uint32_t e1, uint32_t& hi
 // (and +8, +9) of a k-tile are tokens; B holds the fp16 softmax weights.
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -214,9 +221,11 @@ __device__ __forceinline__ void vmma_ktile(const uint8_t* vbuf, const uint32_t* 
 // free permutation of the coordinates: thread (g, tig) supplies columns 2tig,
 // 2tig+1 (and 2tig+8, 2tig+9) of k-tile kt, mapped to coordinates 32tig+4kt,
 // +1 (and +2, +3), so its 32 coordinates are contiguous in a packed row.
-// Key tables (centroids x kCScale): 2 and 3 bits: uint2 (hi pair, lo pair)
-// indexed by the code pair (c_i | c_{i+1} << KB); 4 and 8 bits: u32
-// hi | lo << 16 per code.
+// Key tables (centroids x kCScale): 2, 3 and 4 bits: uint2 (hi pair, lo pair)
+// indexed by the code pair (c_i | c_{i+1} << KB); the 4-bit table (256 pairs)
+// is kept in 16 replicas interleaved 8 bytes apart, lane l reading replica
+// l % 16, so the 16 lanes of a half-warp always hit 16 different bank pairs;
+// 8 bits: u32 hi | lo << 16 per code.
 template <int KB>
 struct KCodes {  // one token's 32 codes for this thread, as table offsets
   uint32_t w[KB];
@@ -274,11 +283,12 @@ __device__ __forceinline__ void kpair(const KCodes<KB>& c, const uint32_t* lut, 
     hi = e.x;
     lo = e.y;
   } else if constexpr (KB == 4) {
-    // byte I/2 of the 128 code bits: word I/8, byte (I/2)%4; low nibble = c_I
-    const uint32_t w = c.w[I / 8];
-    const uint32_t e0 = *(const uint32_t*)((const char*)lut + byte_of((w << 2) & 0x3C3C3C3Cu, (I / 2) % 4));
-    const uint32_t e1 = *(const uint32_t*)((const char*)lut + byte_of((w >> 2) & 0x3C3C3C3Cu, (I / 2) % 4));
-    pack_hilo(e0, e1, hi, lo);
+    // byte I/2 of the 128 code bits (word I/8, byte (I/2)%4) is the pair index
+    // c_I | c_{I+1} << 4; lut points at this lane's replica, entries 128 B apart
+    const uint32_t p = __byte_perm(c.w[I / 8], 0u, 0x4440u | ((I / 2) % 4));
+    const uint2 e = *(const uint2*)((const char*)lut + p * 128u);
+    hi = e.x;
+    lo = e.y;
   } else {
     // bytes I, I+1 of the 256 code bits: word I/4, half (I/2)%2
     const uint32_t w = c.w[I / 4];
@@ -288,35 +298,41 @@ __device__ __forceinline__ void kpair(const KCodes<KB>& c, const uint32_t* lut, 
   }
 }
 
-// Scores of tokens ta (rows g) and ta+8 (rows g+8) for heads 2tig, 2tig+1.
+// Scores of the chunk's 32 tokens for heads 2tig, 2tig+1: codes c[0..3] are
+// tokens g, g+8 (m-tile 0) and 16+g, 24+g (m-tile 1).  The hi*hi, lo*hi and
+// hi*lo products of each m-tile accumulate in separate chains, so six
+// independent MMA chains of eight run side by side instead of two of 24.
 template <int KB, int KT>
-__device__ __forceinline__ void score_ktile(const KCodes<KB>& ca, const KCodes<KB>& cb,
-                                            const uint32_t* lut, const uint32_t (&bh)[8][2],
-                                            const uint32_t (&bl)[8][2], float (&d)[4]) {
-  uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
-  kpair<KB, 4 * KT>(ca, lut, h0, l0);
-  kpair<KB, 4 * KT>(cb, lut, h1, l1);
-  kpair<KB, 4 * KT + 2>(ca, lut, h2, l2);
-  kpair<KB, 4 * KT + 2>(cb, lut, h3, l3);
-  mma16816(d, h0, h1, h2, h3, bh[KT][0], bh[KT][1]);
-  mma16816(d, l0, l1, l2, l3, bh[KT][0], bh[KT][1]);
-  mma16816(d, h0, h1, h2, h3, bl[KT][0], bl[KT][1]);
+__device__ __forceinline__ void score_ktile(const KCodes<KB> (&c)[4], const uint32_t* lut,
+                                            const uint32_t (&bh)[8][2], const uint32_t (&bl)[8][2],
+                                            float (&hh)[2][4], float (&lh)[2][4], float (&hl)[2][4]) {
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt) {
+    uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
+    kpair<KB, 4 * KT>(c[2 * mt], lut, h0, l0);
+    kpair<KB, 4 * KT>(c[2 * mt + 1], lut, h1, l1);
+    kpair<KB, 4 * KT + 2>(c[2 * mt], lut, h2, l2);
+    kpair<KB, 4 * KT + 2>(c[2 * mt + 1], lut, h3, l3);
+    mma16816(hh[mt], h0, h1, h2, h3, bh[KT][0], bh[KT][1]);
+    mma16816(lh[mt], l0, l1, l2, l3, bh[KT][0], bh[KT][1]);
+    mma16816(hl[mt], h0, h1, h2, h3, bl[KT][0], bl[KT][1]);
+  }
 }
 
 template <int KB, int KT>
-__device__ __forceinline__ void score_all(const KCodes<KB>& ca, const KCodes<KB>& cb,
-                                          const uint32_t* lut, const uint32_t (&bh)[8][2],
-                                          const uint32_t (&bl)[8][2], float (&d)[4]) {
+__device__ __forceinline__ void score_all(const KCodes<KB> (&c)[4], const uint32_t* lut,
+                                          const uint32_t (&bh)[8][2], const uint32_t (&bl)[8][2],
+                                          float (&hh)[2][4], float (&lh)[2][4], float (&hl)[2][4]) {
   if constexpr (KT < 8) {
-    score_ktile<KB, KT>(ca, cb, lut, bh, bl, d);
-    score_all<KB, KT + 1>(ca, cb, lut, bh, bl, d);
+    score_ktile<KB, KT>(c, lut, bh, bl, hh, lh, hl);
+    score_all<KB, KT + 1>(c, lut, bh, bl, hh, lh, hl);
   }
 }
 
 // QJL: sum_j (2 bit_j - 1) (S q)_j for tokens ta, ta+8: A = exact +-1 signs,
 // B = S q hi and lo (per lane, per k-tile, from shared memory).
 __device__ __forceinline__ void qjl_scores(uint32_t sa, uint32_t sb, const uint32_t* slut,
-                                           const uint4* qb, float (&d)[4]) {
+                                           const uint4* qb, float (&d)[4], float (&dl)[4]) {
 #pragma unroll
   for (int kt = 0; kt < 8; ++kt) {
     // sign bits 4kt, 4kt+1 (pair 0) and 4kt+2, 4kt+3 (pair 1) of this lane's 32
@@ -324,12 +340,12 @@ __device__ __forceinline__ void qjl_scores(uint32_t sa, uint32_t sb, const uint3
     const uint32_t a2 = slut[(sa >> (4 * kt + 2)) & 3u], a3 = slut[(sb >> (4 * kt + 2)) & 3u];
     const uint4 b = qb[kt];
     mma16816(d, a0, a1, a2, a3, b.x, b.y);
-    mma16816(d, a0, a1, a2, a3, b.z, b.w);
+    mma16816(dl, a0, a1, a2, a3, b.z, b.w);
   }
 }
 
 template <int G, int KB, int VB, bool QJL>
-__global__ void __launch_bounds__(kDT, 3) decode_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
   constexpr int KROW = 16 * KB, VROW = 16 * VB;
   __shared__ __align__(16) uint32_t lutk[256];   // K centroid tables (see kpair)
   __shared__ __align__(16) uint32_t lutv[256];   // V fp16 centroids (pairs for 2/3 bits)
@@ -387,9 +403,10 @@ __global__ void __launch_bounds__(kDT, 3) decode_kernel(const DecodeArgs a) {
   svs[tid] = svv;
   uint8_t* wreg = smem + L.warps + warp * L.warp_stride;
   uint64_t* bar = (uint64_t*)(wreg + L.bar);
+  constexpr int NS = ring_slots(KB, VB);
   if (lane == 0) {
-    mbar_init(bar + 0, 1);
-    mbar_init(bar + 1, 1);
+#pragma unroll
+    for (int i = 0; i < NS; ++i) mbar_init(bar + i, 1);
     fence_mbarrier_init();
   }
   __syncwarp();
@@ -445,7 +462,17 @@ __global__ void __launch_bounds__(kDT, 3) decode_kernel(const DecodeArgs a) {
       }
     }
   };
-  if (!window_split && t_begin + 32 * warp < t_end) issue(t_begin + 32 * warp, 0);
+  // everything below may read what the previous kernel on the stream wrote
+  // (planes, window ring, workspace): wait for it to finish
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the warp's first NS - 1 chunks (c = t_begin + 32 warp + 128 j) go in flight now
+  if (!window_split) {
+#pragma unroll
+    for (int j = 0; j < NS - 1; ++j) {
+      const int c = t_begin + 32 * warp + 32 * kDWarps * j;
+      if (c < t_end) issue(c, j);
+    }
+  }
 
   __syncthreads();                                   // cks, cvs, svs
   for (int i = tid; i < 256; i += kDT) {
@@ -458,6 +485,14 @@ __global__ void __launch_bounds__(kDT, 3) decode_kernel(const DecodeArgs a) {
         lutk[2 * i] = hp;
         lutk[2 * i + 1] = lp;
       }
+    } else if constexpr (KB == 4) {
+      // pair i = c_lo | c_hi << 4 into all 16 replicas; at step j lane l
+      // writes replica (l + j) % 16, so a half-warp's stores never collide
+      uint32_t hp, lp;
+      pack_hilo(hilo(cks[i & 15] * kCScale), hilo(cks[i >> 4] * kCScale), hp, lp);
+      uint2* row = (uint2*)(smem + L.lutk4) + i * 16;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) row[(lane + j) & 15] = make_uint2(hp, lp);
     } else {
       lutk[i] = hilo(cks[i] * kCScale);
     }
@@ -581,12 +616,14 @@ __global__ void __launch_bounds__(kDT, 3) decode_kernel(const DecodeArgs a) {
   if (!window_split) {
     // online-softmax state of heads 2tig, 2tig+1 (accumulator columns)
     float m0 = kNegBig, m1 = kNegBig, l0 = 0.f, l1 = 0.f;
+    float dscale = 1.f;      // d holds the V sum times dscale
     float d[8][4];           // fp32 V-sum accumulators (MMA layout)
 #pragma unroll
     for (int k = 0; k < 8; ++k)
 #pragma unroll
       for (int j = 0; j < 4; ++j) d[k][j] = 0.f;
     const bool h0ok = 2 * tig < G, h1ok = 2 * tig + 1 < G;
+    const uint32_t* klut = KB == 4 ? (const uint32_t*)(smem + L.lutk4 + 8 * (lane & 15)) : lutk;
     uint16_t* ws16 = (uint16_t*)(wreg + L.ws);   // [8 heads][32 tokens] fp16 weights
     const float kscale = 1.f / (kCScale * qsp);
     const float qjl_scale = 1.2533141373155003f / (float)kQjlM / qsq;   // sqrt(pi/2)/m
@@ -596,10 +633,12 @@ __global__ void __launch_bounds__(kDT, 3) decode_kernel(const DecodeArgs a) {
     bool ok = true;
     int kq = 0;
     for (; c0 < t_end; c0 += 32 * kDWarps, ++kq) {
-      const int slot = kq & 1;
-      const int c1 = c0 + 32 * kDWarps;
-      if (c1 < t_end) issue(c1, slot ^ 1);
-      ok = __all_sync(0xffffffffu, mbar_wait(bar + slot, (kq >> 1) & 1, limit, a.err));
+      const int slot = kq % NS;
+      // the chunk NS - 1 ahead goes into the slot released at the end of the
+      // previous iteration
+      const int c1 = c0 + 32 * kDWarps * (NS - 1);
+      if (c1 < t_end) issue(c1, (kq + NS - 1) % NS);
+      ok = __all_sync(0xffffffffu, mbar_wait(bar + slot, (kq / NS) & 1, limit, a.err));
       if (!ok) break;
       const int nv = t_end - c0 < 32 ? t_end - c0 : 32;
       const uint8_t* kb_ = wreg + L.kbuf + slot * 32 * KROW;
@@ -608,36 +647,42 @@ __global__ void __launch_bounds__(kDT, 3) decode_kernel(const DecodeArgs a) {
       // ---- scores on the tensor cores: sc[mt][0,1] token 16mt+mg, sc[mt][2,3] token +8;
       //      columns 0 / 1 are heads 2tig / 2tig+1
       float sc[2][4];
+      {
+        KCodes<KB> c[4];
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
-        const int ta = 16 * mt + mg, tb = ta + 8;
-        KCodes<KB> ca, cb;
-        load_kcodes<KB>(kb_ + ta * KROW, tig, ca);
-        load_kcodes<KB>(kb_ + tb * KROW, tig, cb);
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        score_all<KB, 0>(ca, cb, lutk, bh, bl, acc);
-        const float na = kn_[ta] * kscale, nb = kn_[tb] * kscale;
-        sc[mt][0] = acc[0] * na;
-        sc[mt][1] = acc[1] * na;
-        sc[mt][2] = acc[2] * nb;
-        sc[mt][3] = acc[3] * nb;
-        if constexpr (QJL) {
-          const uint8_t* sb_ = wreg + L.sbuf + slot * 512;
-          const float* rn_ = (const float*)(wreg + L.rn + slot * 128);
-          const uint32_t sa = *(const uint32_t*)(sb_ + ta * 16 + 4 * tig);
-          const uint32_t sbits = *(const uint32_t*)(sb_ + tb * 16 + 4 * tig);
-          float qa[4] = {0.f, 0.f, 0.f, 0.f};
-          qjl_scores(sa, sbits, slut, qjlb, qa);
-          const float ga = rn_[ta] * qjl_scale, gb = rn_[tb] * qjl_scale;
-          sc[mt][0] = fmaf(qa[0], ga, sc[mt][0]);
-          sc[mt][1] = fmaf(qa[1], ga, sc[mt][1]);
-          sc[mt][2] = fmaf(qa[2], gb, sc[mt][2]);
-          sc[mt][3] = fmaf(qa[3], gb, sc[mt][3]);
+        for (int r = 0; r < 4; ++r) load_kcodes<KB>(kb_ + (8 * r + mg) * KROW, tig, c[r]);
+        float hh[2][4], lh[2][4], hl[2][4];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) hh[mt][j] = lh[mt][j] = hl[mt][j] = 0.f;
+        score_all<KB, 0>(c, klut, bh, bl, hh, lh, hl);
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          const int ta = 16 * mt + mg, tb = ta + 8;
+          const float na = kn_[ta] * kscale, nb = kn_[tb] * kscale;
+          sc[mt][0] = (hh[mt][0] + (lh[mt][0] + hl[mt][0])) * na;
+          sc[mt][1] = (hh[mt][1] + (lh[mt][1] + hl[mt][1])) * na;
+          sc[mt][2] = (hh[mt][2] + (lh[mt][2] + hl[mt][2])) * nb;
+          sc[mt][3] = (hh[mt][3] + (lh[mt][3] + hl[mt][3])) * nb;
+          if constexpr (QJL) {
+            const uint8_t* sb_ = wreg + L.sbuf + slot * 512;
+            const float* rn_ = (const float*)(wreg + L.rn + slot * 128);
+            const uint32_t sa = *(const uint32_t*)(sb_ + ta * 16 + 4 * tig);
+            const uint32_t sbits = *(const uint32_t*)(sb_ + tb * 16 + 4 * tig);
+            float qa[4] = {0.f, 0.f, 0.f, 0.f}, ql[4] = {0.f, 0.f, 0.f, 0.f};
+            qjl_scores(sa, sbits, slut, qjlb, qa, ql);
+            const float ga = rn_[ta] * qjl_scale, gb = rn_[tb] * qjl_scale;
+            sc[mt][0] = fmaf(qa[0] + ql[0], ga, sc[mt][0]);
+            sc[mt][1] = fmaf(qa[1] + ql[1], ga, sc[mt][1]);
+            sc[mt][2] = fmaf(qa[2] + ql[2], gb, sc[mt][2]);
+            sc[mt][3] = fmaf(qa[3] + ql[3], gb, sc[mt][3]);
+          }
+          if (ta >= nv || !h0ok) sc[mt][0] = kNegBig;
+          if (ta >= nv || !h1ok) sc[mt][1] = kNegBig;
+          if (tb >= nv || !h0ok) sc[mt][2] = kNegBig;
+          if (tb >= nv || !h1ok) sc[mt][3] = kNegBig;
         }
-        if (ta >= nv || !h0ok) sc[mt][0] = kNegBig;
-        if (ta >= nv || !h1ok) sc[mt][1] = kNegBig;
-        if (tb >= nv || !h0ok) sc[mt][2] = kNegBig;
-        if (tb >= nv || !h1ok) sc[mt][3] = kNegBig;
       }
       // ---- online softmax (log2 domain) per head column; reduce over mg
       float x0 = fmaxf(fmaxf(sc[0][0], sc[0][2]), fmaxf(sc[1][0], sc[1][2]));
@@ -670,7 +715,9 @@ __global__ void __launch_bounds__(kDT, 3) decode_kernel(const DecodeArgs a) {
       l0 = fmaf(l0, al0, ps0);
       l1 = fmaf(l1, al1, ps1);
       const float wmax = warp_max(wloc);
-      const float scl = wmax > 0.f ? 16384.f / wmax : 1.f;
+      // fp16 weights scaled into range: the largest is 16384 (capped at 2^64
+      // so that the accumulator, kept in the scale of the latest chunk, stays finite)
+      const float scl = wmax > 0.f ? fminf(16384.f / wmax, 1.8446744073709552e19f) : 1.f;
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
         const int ta = 16 * mt + mg, tb = ta + 8;
@@ -684,8 +731,11 @@ __global__ void __launch_bounds__(kDT, 3) decode_kernel(const DecodeArgs a) {
         }
       }
       __syncwarp();
-      // ---- rotated-domain V sum on the tensor cores: d = (alpha d) + V^T W
-      const float2 pre = make_float2(al0 * scl, al1 * scl);
+      // ---- rotated-domain V sum on the tensor cores: d holds the sum times
+      // the current chunk's weight scale; rescale, then d += V^T W
+      const float rs = scl / dscale;
+      dscale = scl;
+      const float2 pre = make_float2(al0 * rs, al1 * rs);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const float2 lo = __fmul2_rn(make_float2(d[k][0], d[k][1]), pre);
@@ -699,23 +749,22 @@ __global__ void __launch_bounds__(kDT, 3) decode_kernel(const DecodeArgs a) {
         const uint32_t b1 = mg < G ? *(const uint32_t*)(ws16 + mg * 32 + 16 * kt + 2 * tig + 8) : 0u;
         vmma_ktile<VB>(vb_, lutv, kt, mg, tig, b0, b1, d);
       }
-      const float inv = 1.f / scl;
-      const float2 post = make_float2(inv, inv);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float2 lo = __fmul2_rn(make_float2(d[k][0], d[k][1]), post);
-        const float2 hi = __fmul2_rn(make_float2(d[k][2], d[k][3]), post);
-        d[k][0] = lo.x; d[k][1] = lo.y; d[k][2] = hi.x; d[k][3] = hi.y;
-      }
       __syncwarp();
+    }
+    {
+      const float inv = 1.f / dscale;             // back to the unscaled sum
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) d[k][j] *= inv;
     }
     if (!ok) {
       // a staging wait ran out (error word set): give the copies still in
-      // flight (at most one chunk per ring slot) a bounded wait, then stop
-      for (int dd = 0; dd < 2; ++dd) {
+      // flight (chunks kq .. kq + NS - 1, one per ring slot) a bounded wait, then stop
+      for (int dd = 0; dd < NS; ++dd) {
         const int kk = kq + dd;
         if (t_begin + 32 * warp + kk * 32 * kDWarps >= t_end) break;
-        for (uint32_t i = 0; i < limit && !mbar_try_wait(bar + (kk & 1), (kk >> 1) & 1); ++i) {
+        for (uint32_t i = 0; i < limit && !mbar_try_wait(bar + kk % NS, (kk / NS) & 1); ++i) {
         }
       }
     }
@@ -920,8 +969,20 @@ int launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
   const size_t smem = (size_t)DecodeSmem(G, QJL ? 1 : 0, KB, VB).total;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return 1;
-  dim3 grid((unsigned)a.n_splits, (unsigned)a.Hkv, (unsigned)a.B);
-  k<<<grid, kDT, smem, s>>>(a);
+  // programmatic dependent launch: the CTAs may start while the previous
+  // kernel on the stream (the library's append) is still running; they read
+  // only q, seq_lens and the codec tables before griddepcontrol.wait
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a.n_splits, (unsigned)a.Hkv, (unsigned)a.B);
+  cfg.blockDim = dim3(kDT, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, k, a) != cudaSuccess) return 1;
   return cudaGetLastError() != cudaSuccess;
 }
 

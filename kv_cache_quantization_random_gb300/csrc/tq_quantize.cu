@@ -431,6 +431,9 @@ __global__ void __launch_bounds__(64) append_kernel(const AppendArgs a) {
   __shared__ float cen[2][256];
   __shared__ uint32_t words[2][32];
   __shared__ __align__(16) float rbuf[kD];
+  // a decode launched after this kernel may start its prologue now (it reads
+  // nothing this kernel writes before its griddepcontrol.wait)
+  asm volatile("griddepcontrol.launch_dependents;");
   const int tid = threadIdx.x, lane = tid & 31, kind = tid >> 5;
   const int h = blockIdx.x % a.H, b = blockIdx.x / a.H;
   for (int i = lane; i < 256; i += 32) {
