@@ -572,11 +572,18 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
       float acc[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) acc[g] = 0.f;
-      const uint16_t* Sj = a.S + (size_t)j * kD2;
-      for (int k = 0; k < kD2; ++k) {
-        const float sv = __uint_as_float((uint32_t)Sj[k] << 16);
+      const uint4* Sj = (const uint4*)(a.S + (size_t)j * kD2);
+#pragma unroll 2
+      for (int c = 0; c < kD2 / 8; ++c) {
+        const uint4 s8 = __ldg(Sj + c);
+        const uint32_t sw[4] = {s8.x, s8.y, s8.z, s8.w};
 #pragma unroll
-        for (int g = 0; g < G; ++g) acc[g] = fmaf(sv, qr[k * G + g], acc[g]);
+        for (int u = 0; u < 8; ++u) {
+          const float sv = (u & 1) ? bf16hi(sw[u >> 1]) : bf16lo(sw[u >> 1]);
+          const int k = 8 * c + u;
+#pragma unroll
+          for (int g = 0; g < G; ++g) acc[g] = fmaf(sv, qr[k * G + g], acc[g]);
+        }
       }
 #pragma unroll
       for (int g = 0; g < G; ++g) {

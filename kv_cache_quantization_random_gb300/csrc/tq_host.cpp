@@ -452,6 +452,7 @@ static void fill_quant_codec(QuantArgs& a, const tq_config* cfg, const void* tab
   a.S = a.qjl ? tbl_qjl(cfg, tables, layer) : nullptr;
   a.m = cfg->qjl_m;
   a.err = quant_error_ptr();
+  a.wait_limit = g_wait_limit;
   const SearchGrid g = search_grid(cfg, a.bits);
   a.grid_scale = g.scale;
   a.grid_magic = g.magic;

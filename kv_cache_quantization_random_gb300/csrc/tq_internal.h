@@ -5,6 +5,8 @@
 #include <stdint.h>
 #include <stddef.h>
 
+#include <cuda_runtime.h>
+
 #include "../../include/tq.h"
 
 namespace tq {
@@ -59,6 +61,7 @@ struct QuantArgs {
   const uint16_t* S;             // bf16 [m][d]
   int m;
   unsigned* err;                 // device error word
+  uint32_t wait_limit;           // polls per bounded wait (0 = default)
   // code search grid (see SearchGrid) and the rotation signs as fp32 sign-bit
   // masks, kept in the parameter block so the kernel reads them as operands
   float grid_scale;              // cells per unit of y
@@ -159,6 +162,8 @@ struct DecodeArgs {
 
 // ---- launchers (defined in the .cu files) -------------------------------------
 int launch_quantize(const QuantArgs& a, void* stream);
+int launch_quantize_qjl(const QuantArgs& a, cudaStream_t stream);   // keys in MSE+QJL mode
+int sm_count();
 int launch_window_scatter(const WindowScatterArgs& a, void* stream);
 int launch_append(const AppendArgs& a, void* stream);
 int launch_dequantize(const DequantArgs& a, void* stream);

@@ -1,0 +1,269 @@
+// Keys in MSE+QJL mode: codes, norm and the 1-bit QJL sketch of the residual,
+// with the Gaussian projection on the 5th-generation tensor cores (sm_103a).
+//
+// "TurboQuant KV 캐시 압축 for llama.cpp", "QJL 보정 효과" (QJL is
+// TurboQuant_prod: a 1-bit correction of the residual) and v1.4.2 item 2 (the
+// correction is formed from the sign bits and a stored residual scale).  Per
+// key: r = ||x|| (y - c[idx]) in the rotated domain, gamma = ||r||, and
+// bit_j = [(S r)_j >= 0] for the m = 128 rows of the Gaussian matrix S.
+//
+// One CTA = 128 threads = one tile of 128 keys; thread t owns key t.  Each
+// thread quantizes its key in registers (tq_quant_common.cuh) and writes its
+// residual, split into bf16 hi + lo parts (r ~= hi + lo to ~16 bits), as row t
+// of two [128 x 128] K-major operand tiles in shared memory.  One thread then
+// issues Z = R_hi S^T + R_lo S^T as 16 tcgen05.mma (M = N = 128, K = 16, bf16
+// in, fp32 accumulate) into a 128-column TMEM accumulator; S (bf16, exact)
+// stays in shared memory for the whole launch.  TMEM lane t holds z for key
+// t, so after the commit each warp reads its 32 lanes with tcgen05.ld and
+// every thread turns its own 128 projections into 4 words of sign bits.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tq_quant_common.cuh"
+
+namespace tq {
+
+// ---- shared-memory operand layout for tcgen05 (K-major, no swizzle) -----------
+// A [128 rows][128 k] bf16: 8x8 core matrices of 128 contiguous bytes; the 16
+// core matrices of an 8-row group follow each other along K (leading byte
+// offset 128), 8-row groups are 2048 bytes apart (stride byte offset).
+constexpr uint32_t kCoreLbo = 128;
+constexpr uint32_t kCoreSbo = 2048;
+constexpr uint32_t kOpBytes = 128 * 128 * 2;   // one [128 x 128] bf16 operand
+
+__device__ __forceinline__ uint32_t op_offset(int row, int kchunk) {   // 8-element chunk
+  return (uint32_t)(row >> 3) * kCoreSbo + (uint32_t)kchunk * kCoreLbo + (uint32_t)(row & 7) * 16u;
+}
+
+// Shared-memory matrix descriptor: start address, leading and stride byte
+// offsets (all >> 4), descriptor version 1, no swizzle.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((kCoreLbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((kCoreSbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, N = 128, M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) |
+                            ((128u >> 4) << 24);
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__host__ __device__ constexpr size_t qjl_smem_bytes(bool f32, int cells) {
+  return 1024                                    // alignment slack
+         + 3 * (size_t)kOpBytes                  // R hi, R lo, S
+         + quant_rows_bytes(f32)                 // staged rows (one tile)
+         + (size_t)cells * 8 + 2 * 256 * 4       // grid, boundaries, centroids
+         + 16;                                   // mbarrier + TMEM address
+}
+
+template <int BITS, bool F32>
+__global__ void __launch_bounds__(kQRows, 1) quantize_qjl_kernel(const QuantArgs a) {
+  constexpr int kPitch = RowCfg<F32>::kPitch;
+  extern __shared__ uint8_t smem_raw[];
+  // operand tiles on a 1 KB boundary
+  uint8_t* base = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* ahi = base;
+  uint8_t* alo = base + kOpBytes;
+  uint8_t* sop = base + 2 * kOpBytes;
+  uint8_t* rows = base + 3 * kOpBytes;
+  float2* grid = (float2*)(rows + quant_rows_bytes(F32));
+  float* bnd = (float*)(grid + a.grid_cells);
+  float* cen = bnd + 256;
+  uint64_t* bar = (uint64_t*)(cen + 256);
+  uint32_t* tslot = (uint32_t*)(bar + 1);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 128;" ::"r"(
+                     smem_u32(tslot))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  for (int i = tid; i < 256; i += kQRows) {
+    bnd[i] = a.boundaries[i];
+    cen[i] = a.centroids[i];
+  }
+  // S (bf16 [m][d]) as the B operand: row n = tid, 16 chunks of 8 values
+  {
+    const uint4* srow = (const uint4*)(a.S + (size_t)tid * kD);
+#pragma unroll
+    for (int c = 0; c < 16; ++c) *(uint4*)(sop + op_offset(tid, c)) = __ldg(srow + c);
+  }
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  build_grid<BITS>(a, bnd, grid, tid, kQRows);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  const uint32_t grid_base = smem_u32(grid);
+  const uint32_t kmax = (uint32_t)a.grid_cells - 1u;
+  const uint32_t limit = a.wait_limit ? a.wait_limit : kDefaultWaitLimit;
+
+  const uint32_t total = (uint32_t)a.B * (uint32_t)a.H * (uint32_t)a.n;
+  const uint32_t ntiles = (total + kQRows - 1) / kQRows;
+  uint32_t phase = 0;
+  bool failed = false;
+  for (uint32_t tile = blockIdx.x; tile < ntiles && !failed; tile += gridDim.x, phase ^= 1u) {
+    // ---- stage: warp w copies rows 32w .. 32w+31 of the tile
+    const uint32_t v = tile * kQRows + tid;
+    const void* src = nullptr;
+    long long drow = 0;
+    const bool valid = v < total && resolve_row(a, v, &src, &drow);
+    stage_rows<F32>(src, valid, rows + warp * 32 * kPitch, lane);
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncwarp();
+    // ---- codes, norm and residual of this thread's key; residual rows of R
+    float gamma = 0.f;
+    {
+      float2 p[64];
+      if (valid) {
+        const float nrm = quantize_row<BITS, F32, (BITS > 4), true>(
+            a, rows + tid * kPitch, grid_base, kmax, cen, a.codes + drow * (16 * BITS), p);
+        a.norms[drow] = nrm;
+        float2 g2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 64; ++j) g2 = __ffma2_rn(p[j], p[j], g2);
+        gamma = sqrtf(g2.x + g2.y);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 64; ++j) p[j] = make_float2(0.f, 0.f);
+      }
+      // p[j] = (r_j, r_{j+64}); chunk c of the row holds coordinates 8c .. 8c+7
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i0 = 8 * c + 2 * u;                 // coordinates i0, i0 + 1
+          const float r0 = i0 < 64 ? p[i0].x : p[i0 - 64].y;
+          const float r1 = i0 + 1 < 64 ? p[i0 + 1].x : p[i0 + 1 - 64].y;
+          const __nv_bfloat16 h0 = __float2bfloat16_rn(r0), h1 = __float2bfloat16_rn(r1);
+          const __nv_bfloat16 l0 = __float2bfloat16_rn(r0 - __bfloat162float(h0));
+          const __nv_bfloat16 l1 = __float2bfloat16_rn(r1 - __bfloat162float(h1));
+          hw[u] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+          lw[u] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+        }
+        *(uint4*)(ahi + op_offset(tid, c)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *(uint4*)(alo + op_offset(tid, c)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      }
+    }
+    // generic-proxy stores -> visible to the tensor cores' (async proxy) reads
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    // ---- Z = R_hi S^T + R_lo S^T: 8 K-steps of 16 for each part
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t ah = smem_u32(ahi), al = smem_u32(alo), sb = smem_u32(sop);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        umma_bf16(tmem, umma_desc(ah + ks * 2 * kCoreLbo), umma_desc(sb + ks * 2 * kCoreLbo),
+                  ks > 0 ? 1u : 0u);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        umma_bf16(tmem, umma_desc(al + ks * 2 * kCoreLbo), umma_desc(sb + ks * 2 * kCoreLbo), 1u);
+      umma_commit(bar);
+    }
+    __syncwarp();
+    if (!__syncthreads_and(mbar_wait(bar, phase, limit, a.err))) {
+      // the accumulator never completed (error word set): one more bounded
+      // wait for the MMAs in flight, then free the TMEM and stop
+      for (uint32_t i = 0; i < limit && !mbar_try_wait(bar, phase); ++i) {
+      }
+      failed = true;
+      break;
+    }
+    tc_fence_after();
+    // ---- signs: warp w reads TMEM lanes 32w .. 32w+31 (its threads' keys)
+    uint32_t sbits[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t z[32];
+      tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + 32u * q, z);
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      uint32_t w = 0u;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) w |= (__uint_as_float(z[j]) >= 0.f ? 1u : 0u) << j;
+      sbits[q] = w;
+    }
+    if (valid) {
+      *(uint4*)(a.qjl_signs + drow * (kQjlM / 8)) = make_uint4(sbits[0], sbits[1], sbits[2], sbits[3]);
+      a.qjl_rnorm[drow] = gamma;
+    }
+    tc_fence_before();
+    __syncthreads();   // TMEM, R tiles and rows are reused by the next tile
+  }
+  (void)failed;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 128;" ::"r"(tmem) : "memory");
+}
+
+template <int BITS, bool F32>
+static int launch_qjl_t(const QuantArgs& a, cudaStream_t s) {
+  auto k = quantize_qjl_kernel<BITS, F32>;
+  const size_t smem = qjl_smem_bytes(F32, a.grid_cells);
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return 1;
+  const long long total = (long long)a.B * a.H * a.n;
+  const long long ntiles = (total + kQRows - 1) / kQRows;
+  long long grid = sm_count();              // one CTA per SM (shared memory bound)
+  if (grid > ntiles) grid = ntiles;
+  k<<<(unsigned)grid, kQRows, smem, s>>>(a);
+  return cudaGetLastError() != cudaSuccess;
+}
+
+int launch_quantize_qjl(const QuantArgs& a, cudaStream_t s) {
+  switch (a.bits) {
+    case 2: return a.src_f32 ? launch_qjl_t<2, true>(a, s) : launch_qjl_t<2, false>(a, s);
+    case 3: return a.src_f32 ? launch_qjl_t<3, true>(a, s) : launch_qjl_t<3, false>(a, s);
+    case 4: return a.src_f32 ? launch_qjl_t<4, true>(a, s) : launch_qjl_t<4, false>(a, s);
+    case 8: return a.src_f32 ? launch_qjl_t<8, true>(a, s) : launch_qjl_t<8, false>(a, s);
+  }
+  return 1;
+}
+
+}  // namespace tq

@@ -1,0 +1,216 @@
+// Device pieces shared by the quantize kernels (tq_quantize.cu: codes and
+// norms; tq_qjl.cu: codes, norms and the QJL sign sketch on the tensor cores).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tq_device.cuh"
+
+namespace tq {
+
+constexpr int kQRows = 128;           // vectors per tile = threads per CTA
+constexpr int kD = 128;
+
+template <bool F32>
+struct RowCfg {
+  static constexpr int kRowBytes = F32 ? kD * 4 : kD * 2;
+  static constexpr int kPitch = kRowBytes + 16;   // odd multiple of 16 B: conflict-free rows
+};
+
+// 128 padded rows (one tile)
+__host__ __device__ constexpr size_t quant_rows_bytes(bool f32) {
+  return (size_t)kQRows * (f32 ? RowCfg<true>::kPitch : RowCfg<false>::kPitch);
+}
+
+// Resolve vector v of the launch: its plane row and, for the stager, its
+// source address.  All index arithmetic is 32-bit (a launch covers fewer than
+// 2^31 vectors, checked on the host).
+__device__ __forceinline__ bool resolve_row(const QuantArgs& a, uint32_t v, const void** src,
+                                            long long* dst_row) {
+  const uint32_t n = (uint32_t)a.n;
+  const uint32_t bh = v / n;
+  const uint32_t j = v - bh * n;
+  const uint32_t b = bh / (uint32_t)a.H;
+  const uint32_t h = bh - b * (uint32_t)a.H;
+  const int esz = a.src_f32 ? 4 : 2;
+  long long pos;
+  if (!a.append) {
+    pos = (a.dst_pos ? (long long)a.dst_pos[b] : 0) + j;
+    *src = (const uint8_t*)a.src + ((long long)b * a.sb + (long long)h * a.sh + (long long)j * a.st) * esz;
+  } else {
+    const long long T0 = a.seq_before[b];
+    const long long q0 = T0 - a.W > 0 ? T0 - a.W : 0;
+    const long long T1 = T0 + n;
+    const long long q1 = T1 - a.W > 0 ? T1 - a.W : 0;
+    pos = q0 + j;
+    if (pos >= q1) return false;                       // stays in (or enters) the window
+    if (pos < T0) {                                     // leaves the window ring
+      const long long slot = pos % a.W;
+      *src = (const uint8_t*)a.win + (((long long)b * a.H + h) * a.W + slot) * kD * 2;
+    } else {
+      *src = (const uint8_t*)a.src + ((long long)b * a.sb + (long long)h * a.sh + (pos - T0) * a.st) * esz;
+    }
+  }
+  if (pos < 0 || pos >= a.cap) {
+    atomicOr(a.err, kErrBounds);
+    return false;
+  }
+  *dst_row = ((long long)bh) * a.cap + pos;
+  return true;
+}
+
+__device__ __forceinline__ float2 lds64f(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+  return v;
+}
+
+// A warp stages the 32 rows of its next tile into one of its two row buffers
+// with 16-byte asynchronous copies (cp.async): lane l resolved row l; each
+// pass copies 512 contiguous source bytes (two bf16 rows or one fp32 row),
+// one 16-byte chunk per lane.  Rows that resolve to nothing are not copied.
+template <bool F32>
+__device__ __forceinline__ void stage_rows(const void* src, bool valid, uint8_t* rows, int lane) {
+  constexpr int kRowBytes = RowCfg<F32>::kRowBytes;
+  constexpr int kPitch = RowCfg<F32>::kPitch;
+  constexpr int kChunks = kRowBytes / 16;            // 16 (bf16) or 32 (fp32)
+  constexpr int kRowsPerPass = 32 / kChunks;
+  const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+  const int c = lane % kChunks;
+#pragma unroll 4
+  for (int pass = 0; pass < 32 / kRowsPerPass; ++pass) {
+    const int r = pass * kRowsPerPass + lane / kChunks;
+    const uint8_t* sp = (const uint8_t*)__shfl_sync(0xffffffffu, (unsigned long long)src, r);
+    if ((vmask >> r) & 1u) cp_async16(rows + r * kPitch + 16 * c, sp + 16 * c);
+  }
+}
+
+// Rotated coordinates of one vector, held as pairs (y_j, y_{j+64}), j < 64,
+// so that six of the seven butterfly stages run on packed fp32 pairs.
+template <bool F32>
+__device__ __forceinline__ float load_rotate(const QuantArgs& a, const uint8_t* row,
+                                             float2 (&p)[64]) {
+  if constexpr (F32) {
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const uint4 lo = lds128(row + 16 * c);            // coordinates 4c .. 4c+3
+      const uint4 hi = lds128(row + 256 + 16 * c);      // coordinates 64+4c ..
+      p[4 * c + 0] = make_float2(__uint_as_float(lo.x ^ a.smask[4 * c + 0]), __uint_as_float(hi.x ^ a.smask[64 + 4 * c + 0]));
+      p[4 * c + 1] = make_float2(__uint_as_float(lo.y ^ a.smask[4 * c + 1]), __uint_as_float(hi.y ^ a.smask[64 + 4 * c + 1]));
+      p[4 * c + 2] = make_float2(__uint_as_float(lo.z ^ a.smask[4 * c + 2]), __uint_as_float(hi.z ^ a.smask[64 + 4 * c + 2]));
+      p[4 * c + 3] = make_float2(__uint_as_float(lo.w ^ a.smask[4 * c + 3]), __uint_as_float(hi.w ^ a.smask[64 + 4 * c + 3]));
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 lo = lds128(row + 16 * c);            // coordinates 8c .. 8c+7
+      const uint4 hi = lds128(row + 128 + 16 * c);      // coordinates 64+8c ..
+      const uint32_t l[4] = {lo.x, lo.y, lo.z, lo.w};
+      const uint32_t h[4] = {hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = 8 * c + 2 * u;
+        // bf16 -> fp32 with the sign flip: adding 0x80000000 flips the sign bit
+        p[i] = make_float2(__uint_as_float(l[u] * 65536u + a.smask[i]),
+                           __uint_as_float(h[u] * 65536u + a.smask[64 + i]));
+        p[i + 1] = make_float2(__uint_as_float((l[u] & 0xFFFF0000u) ^ a.smask[i + 1]),
+                               __uint_as_float((h[u] & 0xFFFF0000u) ^ a.smask[64 + i + 1]));
+      }
+    }
+  }
+  float2 s0 = make_float2(0.f, 0.f), s1 = s0;
+#pragma unroll
+  for (int j = 0; j < 64; j += 2) {
+    s0 = __ffma2_rn(p[j], p[j], s0);
+    s1 = __ffma2_rn(p[j + 1], p[j + 1], s1);
+  }
+  const float2 s = __fadd2_rn(s0, s1);
+  // butterflies between pairs: stages 1, 2, 4, ..., 32 of the index j
+  const float2 neg1 = make_float2(-1.f, -1.f);
+#pragma unroll
+  for (int hs = 1; hs < 64; hs <<= 1) {
+#pragma unroll
+    for (int j = 0; j < 64; ++j) {
+      if ((j & hs) == 0) {
+        const float2 u = p[j], w = p[j + hs];
+        p[j] = __fadd2_rn(u, w);
+        p[j + hs] = __ffma2_rn(w, neg1, u);
+      }
+    }
+  }
+  // stage 64: inside each pair
+#pragma unroll
+  for (int j = 0; j < 64; ++j) p[j] = make_float2(p[j].x + p[j].y, p[j].x - p[j].y);
+  return sqrtf(s.x + s.y);
+}
+
+// Search-grid table (see SearchGrid in tq_internal.h) from the boundaries in
+// shared memory: entry k = (first boundary at or above the lower edge of cells
+// k-1..k+1, number of boundaries below that edge).  Called by all threads of
+// the CTA; the caller synchronises before using the table.
+template <int BITS>
+__device__ __forceinline__ void build_grid(const QuantArgs& a, const float* bnd, float2* grid,
+                                           int tid, int nthreads) {
+  const int off = a.grid_cells / 2;
+  for (int k = tid; k < a.grid_cells; k += nthreads) {
+    const float lo = ((float)(k - off) - 1.5f) / a.grid_scale;
+    uint32_t idx = 0;
+#pragma unroll
+    for (int step = (1 << BITS) / 2; step >= 1; step >>= 1)
+      if (bnd[idx + step - 1] < lo) idx += step;
+    grid[k] = make_float2(bnd[idx], __uint_as_float(idx));
+  }
+}
+
+// Norm, rotation, code search and packing of the vector in `row` (shared
+// memory); the codes go to codes_dst (16 * BITS bytes).  Returns ||x||.  With
+// RESID, p holds the rotated-domain residual n (y - c[idx]) afterwards (pairs
+// (r_j, r_{j+64})), from the centroids `cen` in shared memory.
+template <int BITS, bool F32, bool CLAMP, bool RESID>
+__device__ __forceinline__ float quantize_row(const QuantArgs& a, const uint8_t* row,
+                                              uint32_t grid_base, uint32_t kmax,
+                                              const float* cen, uint8_t* codes_dst,
+                                              float2 (&p)[64]) {
+  constexpr int NW = 4 * BITS;         // 32-bit code words per vector (128 * BITS / 32)
+  const float nrm = load_rotate<F32>(a, row, p);
+  const float inv = nrm > 0.f ? 1.0f / (nrm * 11.313708498984761f) : 0.f;
+  const float2 inv2 = make_float2(inv, inv);
+  const float2 gs2 = make_float2(a.grid_scale, a.grid_scale);
+  const float2 gm2 = make_float2(a.grid_magic, a.grid_magic);
+  uint32_t words[NW];
+#pragma unroll
+  for (int k = 0; k < NW; ++k) words[k] = 0u;
+#pragma unroll
+  for (int j = 0; j < 64; ++j) {
+    const float2 y = __fmul2_rn(p[j], inv2);
+    float2 yc = y;
+    if constexpr (CLAMP) {
+      yc.x = fminf(fmaxf(y.x, -a.grid_clamp), a.grid_clamp);
+      yc.y = fminf(fmaxf(y.y, -a.grid_clamp), a.grid_clamp);
+    }
+    const float2 t = __ffma2_rn(yc, gs2, gm2);
+    const uint32_t k0 = min(__float_as_uint(t.x) - 0x4B400000u, kmax);
+    const uint32_t k1 = min(__float_as_uint(t.y) - 0x4B400000u, kmax);
+    const float2 e0 = lds64f(grid_base + k0 * 8u);
+    const float2 e1 = lds64f(grid_base + k1 * 8u);
+    const uint32_t c0 = __float_as_uint(e0.y) + (e0.x < y.x ? 1u : 0u);
+    const uint32_t c1 = __float_as_uint(e1.y) + (e1.x < y.y ? 1u : 0u);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int i = j + 64 * half;                   // coordinate
+      const uint32_t code = half ? c1 : c0;
+      const int pb = i * BITS;
+      words[pb >> 5] |= code << (pb & 31);
+      if ((pb & 31) + BITS > 32) words[(pb >> 5) + 1] |= code >> (32 - (pb & 31));
+    }
+    if constexpr (RESID) p[j] = make_float2(nrm * (y.x - cen[c0]), nrm * (y.y - cen[c1]));
+  }
+  uint4* dc = (uint4*)codes_dst;
+#pragma unroll
+  for (int k = 0; k < BITS; ++k)
+    dc[k] = make_uint4(words[4 * k], words[4 * k + 1], words[4 * k + 2], words[4 * k + 3]);
+  return nrm;
+}
+
+}  // namespace tq

@@ -2,168 +2,32 @@
 //
 // Quantize ("윈도우용 터보퀀트(TurboQuant) 구현을 개선하다", recap: rotate, then
 // quantize; "TurboQuant KV 캐시 압축 for llama.cpp", v1.7.0 decision 4: sign
-// flip + butterfly WHT inside the encoder): one thread owns one vector.  A CTA
-// stages 128 rows with bulk (TMA) copies into padded shared memory, then each
-// thread keeps its 128 coordinates in registers: sign flip (folded into the
-// bf16 -> fp32 widening), sum of squares, the 7-stage Walsh-Hadamard butterfly,
-// scaling by 1/(||x|| sqrt d), branch-free binary search over the fp32
-// boundaries, and packing into a dense LSB-first stream ("... 개선하다",
-// finding 3: 3 bits x 128 = 48 B + 4 B norm).  Keys in MSE+QJL mode also form
-// the rotated-domain residual r = n (y - c[idx]), its norm and the sign sketch
-// of S r ("TurboQuant KV 캐시 압축 for llama.cpp", "QJL 보정 효과").
+// flip + butterfly WHT inside the encoder): one thread owns one vector.  Each
+// warp streams its own tiles of 32 rows through two padded shared-memory
+// buffers with cp.async, and each thread keeps its 128 coordinates in
+// registers (see quantize_row in tq_quant_common.cuh): sign flip folded into
+// the bf16 -> fp32 widening, sum of squares, the Walsh-Hadamard butterfly on
+// packed fp32 pairs, code search on a uniform grid with one exact boundary
+// compare, and packing into a dense LSB-first stream ("... 개선하다", finding
+// 3: 3 bits x 128 = 48 B + 4 B norm).  Keys in MSE+QJL mode take the tensor-
+// core kernel in tq_qjl.cu instead.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "tq_device.cuh"
+#include "tq_quant_common.cuh"
 
 namespace tq {
 
 __device__ unsigned g_quant_err;
 
-constexpr int kQRows = 128;           // vectors per tile = threads per CTA
-constexpr int kD = 128;
-
-template <bool F32>
-struct RowCfg {
-  static constexpr int kRowBytes = F32 ? kD * 4 : kD * 2;
-  static constexpr int kPitch = kRowBytes + 16;   // odd multiple of 16 B: conflict-free rows
-};
-
-// dynamic shared memory: per warp two buffers of 32 rows, the search grid,
-// boundaries, centroids and (QJL) the fp32 projection matrix
-__host__ __device__ constexpr size_t quant_rows_bytes(bool f32) {
-  return (size_t)kQRows * (f32 ? RowCfg<true>::kPitch : RowCfg<false>::kPitch);
-}
-__host__ __device__ constexpr size_t quant_smem_bytes(bool f32, bool qjl, int cells) {
-  return 2 * quant_rows_bytes(f32) + (size_t)cells * 8 + 256 * 4 + (qjl ? 256 * 4 : 0) +
-         (qjl ? (size_t)kQjlM * kD * 4 : 0);
+// dynamic shared memory of quantize_kernel: per warp two buffers of 32 rows,
+// the search grid and the boundaries
+__host__ __device__ constexpr size_t quant_smem_bytes(bool f32, int cells) {
+  return 2 * quant_rows_bytes(f32) + (size_t)cells * 8 + 256 * 4;
 }
 
-// Resolve vector v of the launch: its plane row and, for the stager, its
-// source address.  All index arithmetic is 32-bit (a launch covers fewer than
-// 2^31 vectors, checked on the host).
-__device__ __forceinline__ bool resolve_row(const QuantArgs& a, uint32_t v, const void** src,
-                                            long long* dst_row) {
-  const uint32_t n = (uint32_t)a.n;
-  const uint32_t bh = v / n;
-  const uint32_t j = v - bh * n;
-  const uint32_t b = bh / (uint32_t)a.H;
-  const uint32_t h = bh - b * (uint32_t)a.H;
-  const int esz = a.src_f32 ? 4 : 2;
-  long long pos;
-  if (!a.append) {
-    pos = (a.dst_pos ? (long long)a.dst_pos[b] : 0) + j;
-    *src = (const uint8_t*)a.src + ((long long)b * a.sb + (long long)h * a.sh + (long long)j * a.st) * esz;
-  } else {
-    const long long T0 = a.seq_before[b];
-    const long long q0 = T0 - a.W > 0 ? T0 - a.W : 0;
-    const long long T1 = T0 + n;
-    const long long q1 = T1 - a.W > 0 ? T1 - a.W : 0;
-    pos = q0 + j;
-    if (pos >= q1) return false;                       // stays in (or enters) the window
-    if (pos < T0) {                                     // leaves the window ring
-      const long long slot = pos % a.W;
-      *src = (const uint8_t*)a.win + (((long long)b * a.H + h) * a.W + slot) * kD * 2;
-    } else {
-      *src = (const uint8_t*)a.src + ((long long)b * a.sb + (long long)h * a.sh + (pos - T0) * a.st) * esz;
-    }
-  }
-  if (pos < 0 || pos >= a.cap) {
-    atomicOr(a.err, kErrBounds);
-    return false;
-  }
-  *dst_row = ((long long)bh) * a.cap + pos;
-  return true;
-}
-
-__device__ __forceinline__ float2 lds64f(uint32_t addr) {
-  float2 v;
-  asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
-  return v;
-}
-
-// A warp stages the 32 rows of its next tile into one of its two row buffers
-// with 16-byte asynchronous copies (cp.async): lane l resolved row l; each
-// pass copies 512 contiguous source bytes (two bf16 rows or one fp32 row),
-// one 16-byte chunk per lane.  Rows that resolve to nothing are not copied.
-template <bool F32>
-__device__ __forceinline__ void stage_rows(const void* src, bool valid, uint8_t* rows, int lane) {
-  constexpr int kRowBytes = RowCfg<F32>::kRowBytes;
-  constexpr int kPitch = RowCfg<F32>::kPitch;
-  constexpr int kChunks = kRowBytes / 16;            // 16 (bf16) or 32 (fp32)
-  constexpr int kRowsPerPass = 32 / kChunks;
-  const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
-  const int c = lane % kChunks;
-#pragma unroll 4
-  for (int pass = 0; pass < 32 / kRowsPerPass; ++pass) {
-    const int r = pass * kRowsPerPass + lane / kChunks;
-    const uint8_t* sp = (const uint8_t*)__shfl_sync(0xffffffffu, (unsigned long long)src, r);
-    if ((vmask >> r) & 1u) cp_async16(rows + r * kPitch + 16 * c, sp + 16 * c);
-  }
-}
-
-// Rotated coordinates of one vector, held as pairs (y_j, y_{j+64}), j < 64,
-// so that six of the seven butterfly stages run on packed fp32 pairs.
-template <bool F32>
-__device__ __forceinline__ float load_rotate(const QuantArgs& a, const uint8_t* row,
-                                             float2 (&p)[64]) {
-  if constexpr (F32) {
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const uint4 lo = lds128(row + 16 * c);            // coordinates 4c .. 4c+3
-      const uint4 hi = lds128(row + 256 + 16 * c);      // coordinates 64+4c ..
-      p[4 * c + 0] = make_float2(__uint_as_float(lo.x ^ a.smask[4 * c + 0]), __uint_as_float(hi.x ^ a.smask[64 + 4 * c + 0]));
-      p[4 * c + 1] = make_float2(__uint_as_float(lo.y ^ a.smask[4 * c + 1]), __uint_as_float(hi.y ^ a.smask[64 + 4 * c + 1]));
-      p[4 * c + 2] = make_float2(__uint_as_float(lo.z ^ a.smask[4 * c + 2]), __uint_as_float(hi.z ^ a.smask[64 + 4 * c + 2]));
-      p[4 * c + 3] = make_float2(__uint_as_float(lo.w ^ a.smask[4 * c + 3]), __uint_as_float(hi.w ^ a.smask[64 + 4 * c + 3]));
-    }
-  } else {
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint4 lo = lds128(row + 16 * c);            // coordinates 8c .. 8c+7
-      const uint4 hi = lds128(row + 128 + 16 * c);      // coordinates 64+8c ..
-      const uint32_t l[4] = {lo.x, lo.y, lo.z, lo.w};
-      const uint32_t h[4] = {hi.x, hi.y, hi.z, hi.w};
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = 8 * c + 2 * u;
-        // bf16 -> fp32 with the sign flip: adding 0x80000000 flips the sign bit
-        p[i] = make_float2(__uint_as_float(l[u] * 65536u + a.smask[i]),
-                           __uint_as_float(h[u] * 65536u + a.smask[64 + i]));
-        p[i + 1] = make_float2(__uint_as_float((l[u] & 0xFFFF0000u) ^ a.smask[i + 1]),
-                               __uint_as_float((h[u] & 0xFFFF0000u) ^ a.smask[64 + i + 1]));
-      }
-    }
-  }
-  float2 s0 = make_float2(0.f, 0.f), s1 = s0;
-#pragma unroll
-  for (int j = 0; j < 64; j += 2) {
-    s0 = __ffma2_rn(p[j], p[j], s0);
-    s1 = __ffma2_rn(p[j + 1], p[j + 1], s1);
-  }
-  const float2 s = __fadd2_rn(s0, s1);
-  // butterflies between pairs: stages 1, 2, 4, ..., 32 of the index j
-  const float2 neg1 = make_float2(-1.f, -1.f);
-#pragma unroll
-  for (int hs = 1; hs < 64; hs <<= 1) {
-#pragma unroll
-    for (int j = 0; j < 64; ++j) {
-      if ((j & hs) == 0) {
-        const float2 u = p[j], w = p[j + hs];
-        p[j] = __fadd2_rn(u, w);
-        p[j + hs] = __ffma2_rn(w, neg1, u);
-      }
-    }
-  }
-  // stage 64: inside each pair
-#pragma unroll
-  for (int j = 0; j < 64; ++j) p[j] = make_float2(p[j].x + p[j].y, p[j].x - p[j].y);
-  return sqrtf(s.x + s.y);
-}
-
-template <int BITS, bool QJL, bool F32, bool CLAMP>
-__global__ void __launch_bounds__(kQRows, (QJL ? 1 : 3)) quantize_kernel(const QuantArgs a) {
-  constexpr int NW = 4 * BITS;         // 32-bit code words per vector (128 * BITS / 32)
+template <int BITS, bool F32, bool CLAMP>
+__global__ void __launch_bounds__(kQRows, 3) quantize_kernel(const QuantArgs a) {
   constexpr int kPitch = RowCfg<F32>::kPitch;
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -171,28 +35,9 @@ __global__ void __launch_bounds__(kQRows, (QJL ? 1 : 3)) quantize_kernel(const Q
   uint8_t* wrows = smem + (size_t)warp * 2 * 32 * kPitch;
   float2* grid = (float2*)(smem + 2 * quant_rows_bytes(F32));
   float* bnd = (float*)(grid + a.grid_cells);
-  float* cen = bnd + 256;                               // QJL only
-  float* Sf = cen + (QJL ? 256 : 0);
-
-  for (int i = tid; i < 256; i += kQRows) {
-    bnd[i] = a.boundaries[i];
-    if constexpr (QJL) cen[i] = a.centroids[i];
-  }
-  if constexpr (QJL) {
-    for (int e = tid; e < kQjlM * kD; e += kQRows) Sf[e] = __uint_as_float((uint32_t)a.S[e] << 16);
-  }
+  for (int i = tid; i < 256; i += kQRows) bnd[i] = a.boundaries[i];
   __syncthreads();
-  // search grid: entry k = (first boundary at or above the lower edge of
-  // cells k-1..k+1, number of boundaries below that edge)
-  const int off = a.grid_cells / 2;
-  for (int k = tid; k < a.grid_cells; k += kQRows) {
-    const float lo = ((float)(k - off) - 1.5f) / a.grid_scale;
-    uint32_t idx = 0;
-#pragma unroll
-    for (int step = (1 << BITS) / 2; step >= 1; step >>= 1)
-      if (bnd[idx + step - 1] < lo) idx += step;
-    grid[k] = make_float2(bnd[idx], __uint_as_float(idx));
-  }
+  build_grid<BITS>(a, bnd, grid, tid, kQRows);
   __syncthreads();
   const uint32_t grid_base = smem_u32(grid);
   const uint32_t kmax = (uint32_t)a.grid_cells - 1u;
@@ -228,73 +73,9 @@ __global__ void __launch_bounds__(kQRows, (QJL ? 1 : 3)) quantize_kernel(const Q
     const uint8_t* rows = wrows + buf * 32 * kPitch;
     if (valid) {
       float2 p[64];
-      const float nrm = load_rotate<F32>(a, rows + lane * kPitch, p);
-      const float inv = nrm > 0.f ? 1.0f / (nrm * 11.313708498984761f) : 0.f;
-      const float2 inv2 = make_float2(inv, inv);
-      const float2 gs2 = make_float2(a.grid_scale, a.grid_scale);
-      const float2 gm2 = make_float2(a.grid_magic, a.grid_magic);
-      uint32_t words[NW];
-#pragma unroll
-      for (int k = 0; k < NW; ++k) words[k] = 0u;
-#pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        const float2 y = __fmul2_rn(p[j], inv2);
-        float2 yc = y;
-        if constexpr (CLAMP) {
-          yc.x = fminf(fmaxf(y.x, -a.grid_clamp), a.grid_clamp);
-          yc.y = fminf(fmaxf(y.y, -a.grid_clamp), a.grid_clamp);
-        }
-        const float2 t = __ffma2_rn(yc, gs2, gm2);
-        const uint32_t k0 = min(__float_as_uint(t.x) - 0x4B400000u, kmax);
-        const uint32_t k1 = min(__float_as_uint(t.y) - 0x4B400000u, kmax);
-        const float2 e0 = lds64f(grid_base + k0 * 8u);
-        const float2 e1 = lds64f(grid_base + k1 * 8u);
-        const uint32_t c0 = __float_as_uint(e0.y) + (e0.x < y.x ? 1u : 0u);
-        const uint32_t c1 = __float_as_uint(e1.y) + (e1.x < y.y ? 1u : 0u);
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int i = j + 64 * half;                   // coordinate
-          const uint32_t code = half ? c1 : c0;
-          const int pb = i * BITS;
-          words[pb >> 5] |= code << (pb & 31);
-          if ((pb & 31) + BITS > 32) words[(pb >> 5) + 1] |= code >> (32 - (pb & 31));
-        }
-        if constexpr (QJL) {
-          // rotated-domain residual r = n (y - c[idx])
-          p[j] = make_float2(nrm * (y.x - cen[c0]), nrm * (y.y - cen[c1]));
-        }
-      }
-      uint4* dc = (uint4*)(a.codes + drow * (16 * BITS));
-#pragma unroll
-      for (int k = 0; k < BITS; ++k)
-        dc[k] = make_uint4(words[4 * k], words[4 * k + 1], words[4 * k + 2], words[4 * k + 3]);
+      const float nrm = quantize_row<BITS, F32, CLAMP, false>(
+          a, rows + lane * kPitch, grid_base, kmax, nullptr, a.codes + drow * (16 * BITS), p);
       a.norms[drow] = nrm;
-      if constexpr (QJL) {
-        float2 g2 = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int j = 0; j < 64; ++j) g2 = __ffma2_rn(p[j], p[j], g2);
-        const float gamma = sqrtf(g2.x + g2.y);
-        uint32_t sb[kQjlM / 32];
-#pragma unroll
-        for (int k = 0; k < kQjlM / 32; ++k) sb[k] = 0u;
-        for (int jm = 0; jm < kQjlM; ++jm) {
-          const float* Sj = Sf + jm * kD;
-          float2 z0 = make_float2(0.f, 0.f), z1 = z0;
-#pragma unroll
-          for (int k = 0; k < 64; k += 4) {
-            const float4 lo = *(const float4*)(Sj + k);       // S[jm][k .. k+3]
-            const float4 hi = *(const float4*)(Sj + 64 + k);  // S[jm][64+k ..]
-            z0 = __ffma2_rn(make_float2(lo.x, hi.x), p[k], z0);
-            z1 = __ffma2_rn(make_float2(lo.y, hi.y), p[k + 1], z1);
-            z0 = __ffma2_rn(make_float2(lo.z, hi.z), p[k + 2], z0);
-            z1 = __ffma2_rn(make_float2(lo.w, hi.w), p[k + 3], z1);
-          }
-          const float z = (z0.x + z0.y) + (z1.x + z1.y);
-          sb[jm >> 5] |= (z >= 0.f ? 1u : 0u) << (jm & 31);
-        }
-        *(uint4*)(a.qjl_signs + drow * (kQjlM / 8)) = make_uint4(sb[0], sb[1], sb[2], sb[3]);
-        a.qjl_rnorm[drow] = gamma;
-      }
     }
     __syncwarp();      // every lane is done with this buffer before it is refilled
     buf ^= 1;
@@ -534,7 +315,7 @@ __global__ void __launch_bounds__(128) dequantize_kernel(const DequantArgs a) {
 }
 
 // ---------------------------------------------------------------- launchers
-static int sm_count() {
+int sm_count() {
   static int n = 0;
   if (n == 0) {
     int dev = 0;
@@ -545,10 +326,10 @@ static int sm_count() {
   return n;
 }
 
-template <int BITS, bool QJL, bool F32>
+template <int BITS, bool F32>
 static int launch_q(const QuantArgs& a, cudaStream_t s) {
-  auto k = quantize_kernel<BITS, QJL, F32, (BITS > 4)>;
-  const size_t smem = quant_smem_bytes(F32, QJL, a.grid_cells);
+  auto k = quantize_kernel<BITS, F32, (BITS > 4)>;
+  const size_t smem = quant_smem_bytes(F32, a.grid_cells);
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return 1;
   int per_sm = 0;
@@ -565,8 +346,8 @@ static int launch_q(const QuantArgs& a, cudaStream_t s) {
 
 template <int BITS>
 static int launch_q_bits(const QuantArgs& a, cudaStream_t s) {
-  if (a.qjl) return a.src_f32 ? launch_q<BITS, true, true>(a, s) : launch_q<BITS, true, false>(a, s);
-  return a.src_f32 ? launch_q<BITS, false, true>(a, s) : launch_q<BITS, false, false>(a, s);
+  if (a.qjl) return launch_quantize_qjl(a, s);
+  return a.src_f32 ? launch_q<BITS, true>(a, s) : launch_q<BITS, false>(a, s);
 }
 
 int launch_quantize(const QuantArgs& a, void* stream) {
