@@ -145,6 +145,24 @@ def captured_traffic(kernel: str, workload: str):
     return None
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest value of x over the ranks of the default process group (x
+    itself without one); every rank gets the result."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, ms_per_step: float, world: int) -> float:
+    """Units per second of the whole job: every rank processes units_per_rank
+    per step, and a step takes the slowest rank's time."""
+    return world * units_per_rank / (ms_per_step * 1e-3)
+
+
 def largest_divisor_at_most(n: int, cap: int) -> int:
     for s in range(min(n, cap), 0, -1):
         if n % s == 0:
@@ -338,16 +356,13 @@ def run_ours(args, w, rank, world, local):
             g_step.replay()
         t1.record()
         torch.cuda.synchronize()
-    step_ms_total = t0.elapsed_time(t1)
+    step_ms_total = max_over_ranks(t0.elapsed_time(t1), device)
     if world > 1:
         import torch.distributed as dist
-        tt = torch.tensor([step_ms_total], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         dist.barrier()
-        step_ms_total = float(tt.item())
     ms_per_step = step_ms_total / K_steps
     tokens_per_step = int(seq.sum())
-    value = world * tokens_per_step / (ms_per_step * 1e-3)
+    value = whole_job_rate(tokens_per_step, ms_per_step, world)
 
     # ---- per-kernel durations (decode-only and append-only graphs, same stream)
     def time_graph(g, reps_):
@@ -393,7 +408,7 @@ def run_ours(args, w, rank, world, local):
         e2e_step(i)
     b.record()
     torch.cuda.synchronize()
-    e2e_ms = a.elapsed_time(b) / n_e2e
+    e2e_ms = max_over_ranks(a.elapsed_time(b) / n_e2e, device)
     h2d = qh.numel() * qh.element_size() + 2 * kh.numel() * kh.element_size()
     d2h = outh.numel() * outh.element_size()
 
@@ -432,7 +447,7 @@ def run_ours(args, w, rank, world, local):
         "quantize": {"ms": q_ms, "gbs": q_gbs, "frac_of_peak": q_gbs / hbm_peak,
                      "vectors": 2 * n_vec, "bytes": q_bytes, "what": "bulk quantize of the "
                      "context's K and V (bf16 in, packed planes out)"},
-        "e2e": {"value": world * tokens_per_step / (e2e_ms * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": whole_job_rate(tokens_per_step, e2e_ms, world), "unit": "tokens/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": n_e2e},
         "gpu_launches": K_steps * launches_per_step,
