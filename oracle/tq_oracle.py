@@ -46,6 +46,7 @@ __all__ = [
     "rotation_signs", "qjl_matrix", "round_to_bf16", "round_to_fp32",
     "hadamard", "rotation_matrix", "rotate", "inverse_rotate",
     "lloyd_max_gaussian", "codebook_fp32", "gaussian_distortion",
+    "sphere_pdf", "lloyd_max_sphere", "codebook_sphere_fp32", "quantizer_distortion",
     "quantize_vectors", "near_boundary", "pack_codes", "unpack_codes",
     "pack_bits", "unpack_bits", "qjl_residual", "qjl_sketch",
     "qjl_inner_product_estimate", "dequantize", "dequantize_qjl",
@@ -267,6 +268,120 @@ def codebook_fp32(bits: int, d: int):
     c, beta = lloyd_max_gaussian(bits)
     sigma = 1.0 / math.sqrt(d)
     return round_to_fp32(c * sigma), round_to_fp32(beta * sigma)
+
+
+# --------------------------------------------------------------------------
+# Exact rotated-coordinate density (the "sphere" codebook).  A coordinate y of
+# a uniformly random unit vector in R^d has density
+#   f(y) = (1 - y^2)^((d-3)/2) / B(1/2, (d-1)/2),  -1 <= y <= 1,
+# which tends to N(0, 1/d) as d grows.  Lloyd-Max on f is the alternative
+# reading of "Lloyd-Max on the rotated-coordinate density" to N(0, 1/d).
+# --------------------------------------------------------------------------
+
+def _sphere_log_norm(d: int) -> float:
+    from scipy.special import gammaln
+    return gammaln(d / 2.0) - gammaln(0.5) - gammaln((d - 1) / 2.0)
+
+
+def sphere_pdf(y, d: int):
+    """Density of one coordinate of a uniform unit vector in R^d."""
+    y = np.asarray(y, dtype=np.float64)
+    return np.exp(_sphere_log_norm(d)) * np.clip(1.0 - y * y, 0.0, None) ** ((d - 3) / 2.0)
+
+
+def _sphere_mass(lo: float, hi: float, d: int) -> float:
+    """P(lo < Y <= hi) from the regularized incomplete beta function:
+    P(0 < Y <= y) = I_{y^2}(1/2, (d-1)/2) / 2 for y >= 0 (symmetric), taken
+    from the upper tail where that avoids cancellation."""
+    from scipy.special import betainc, betaincc
+    a, b = 0.5, (d - 1) / 2.0
+    if lo >= 0.0:
+        return 0.5 * (betaincc(a, b, lo * lo) - betaincc(a, b, min(hi, 1.0) ** 2))
+    if hi <= 0.0:
+        return _sphere_mass(-hi, -lo, d)
+    return 0.5 * (betainc(a, b, min(hi, 1.0) ** 2) + betainc(a, b, min(-lo, 1.0) ** 2))
+
+
+def _sphere_first_moment(lo: float, hi: float, d: int) -> float:
+    """int_lo^hi y f(y) dy = C_d / (d - 1) [(1 - lo^2)^((d-1)/2) - (1 - hi^2)^((d-1)/2)]
+    (the antiderivative of y (1 - y^2)^k is -(1 - y^2)^(k+1) / (2 (k+1)))."""
+    e = (d - 1) / 2.0
+    g = lambda y: max(1.0 - y * y, 0.0) ** e
+    return math.exp(_sphere_log_norm(d)) / (d - 1) * (g(lo) - g(hi))
+
+
+def lloyd_max_sphere(bits: int, d: int, iters: int = 80):
+    """Lloyd-Max quantizer of the sphere-coordinate density f (above), fp64.
+
+    The same two conditions as lloyd_max_gaussian (midpoints; centroid =
+    conditional mean), with cells [-1, beta_0], ..., [beta_{L-2}, 1], solved
+    by the same Newton iteration.  Returns (centroids[L], boundaries[L-1]) in units of y (not scaled).
+    Starting point: the uniform quantizer of [-1, 1] for d <= 16, else the
+    N(0, 1/d) quantizer."""
+    L = 1 << bits
+    if d <= 16:      # far from Gaussian: start from the uniform quantizer of [-1, 1]
+        c = [-1.0 + (2 * j + 1) / L for j in range(L)]
+    else:
+        c0, _ = lloyd_max_gaussian(bits)
+        c = list(c0 / math.sqrt(d))
+    for _ in range(iters):
+        beta = [0.5 * (c[j] + c[j + 1]) for j in range(L - 1)]
+        lo = [-1.0] + beta
+        hi = beta + [1.0]
+        P = [_sphere_mass(lo[j], hi[j], d) for j in range(L)]
+        m = [_sphere_first_moment(lo[j], hi[j], d) / P[j] for j in range(L)]
+        F = [c[j] - m[j] for j in range(L)]
+        fb = [float(sphere_pdf(x, d)) for x in beta]
+        sub = [0.0] * L
+        diag = [1.0] * L
+        sup = [0.0] * L
+        for j in range(L):
+            if j < L - 1:
+                t = 0.5 * fb[j] * (beta[j] - m[j]) / P[j]
+                diag[j] -= t
+                sup[j] -= t
+            if j > 0:
+                t = 0.5 * fb[j - 1] * (m[j] - beta[j - 1]) / P[j]
+                sub[j] -= t
+                diag[j] -= t
+        cp = [0.0] * L
+        dp = [0.0] * L
+        cp[0] = sup[0] / diag[0]
+        dp[0] = -F[0] / diag[0]
+        for j in range(1, L):
+            den = diag[j] - sub[j] * cp[j - 1]
+            cp[j] = sup[j] / den if j < L - 1 else 0.0
+            dp[j] = (-F[j] - sub[j] * dp[j - 1]) / den
+        dx = [0.0] * L
+        dx[L - 1] = dp[L - 1]
+        for j in range(L - 2, -1, -1):
+            dx[j] = dp[j] - cp[j] * dx[j + 1]
+        c = [c[j] + dx[j] for j in range(L)]
+        c = [0.5 * (c[j] - c[L - 1 - j]) for j in range(L)]
+    c = np.array(c)
+    beta = 0.5 * (c[:-1] + c[1:])
+    if L % 2 == 0:
+        beta[L // 2 - 1] = 0.0
+    return c, beta
+
+
+def codebook_sphere_fp32(bits: int, d: int):
+    """Sphere-density codebook rounded to fp32 (centroids, boundaries)."""
+    c, beta = lloyd_max_sphere(bits, d)
+    return round_to_fp32(c), round_to_fp32(beta)
+
+
+def quantizer_distortion(c, beta, pdf, lo=-np.inf, hi=np.inf) -> float:
+    """E[(Y - Q(Y))^2] under density pdf for the quantizer (c, beta), by
+    adaptive quadrature cell by cell (scipy.integrate.quad)."""
+    from scipy.integrate import quad
+    edges = [lo] + list(np.asarray(beta, dtype=np.float64)) + [hi]
+    total = 0.0
+    for j, cj in enumerate(np.asarray(c, dtype=np.float64)):
+        v, _ = quad(lambda y: (y - cj) ** 2 * pdf(y), edges[j], edges[j + 1], limit=200,
+                    epsabs=1e-15, epsrel=1e-12)
+        total += v
+    return total
 
 
 def gaussian_distortion(bits: int) -> float:

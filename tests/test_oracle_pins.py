@@ -454,3 +454,69 @@ def test_protected_layer_table():
     assert all(t == (8, 8, False) for t in table[:4] + table[32:])
     assert all(t == (4, 2, False) for t in table[4:32])
     assert O.layer_bits(10, 36, 2, 3, True, 4, 4) == (2, 3, True)
+
+
+# ---------------------------------------------------------------- sphere density
+# Lloyd-Max on the exact density of one coordinate of a uniform unit vector,
+# f(y) = (1 - y^2)^((d-3)/2) / B(1/2, (d-1)/2): the pins below come from
+# outside the oracle's own formulas (scipy quadrature, the uniform and
+# Gaussian limits), not from its incomplete-beta or closed-form moments.
+
+@pytest.mark.parametrize("bits", [1, 2, 3, 4, 8])
+def test_sphere_codebook_at_d3_is_the_uniform_quantizer(bits):
+    # d = 3: f = 1/2 on [-1, 1] (Archimedes), whose Lloyd-Max quantizer is the
+    # uniform one: centroids -1 + (2j+1)/L, boundaries -1 + 2(j+1)/L
+    c, beta = O.lloyd_max_sphere(bits, 3)
+    L = 1 << bits
+    j = np.arange(L)
+    # (incomplete-beta and moment round-off: ~1e-12 at 256 levels)
+    assert np.allclose(c, -1 + (2 * j + 1) / L, atol=1e-11, rtol=0)
+    assert np.allclose(beta, -1 + 2 * (j[:-1] + 1) / L, atol=1e-11, rtol=0)
+
+
+@pytest.mark.parametrize("d", [4, 8, 128])
+def test_sphere_pdf_integrates_to_one_and_has_variance_1_over_d(d):
+    from scipy.integrate import quad
+    mass, _ = quad(lambda y: O.sphere_pdf(y, d), -1, 1, epsabs=1e-14, epsrel=1e-13, limit=200)
+    var, _ = quad(lambda y: y * y * O.sphere_pdf(y, d), -1, 1, epsabs=1e-14, epsrel=1e-13,
+                  limit=200)
+    assert abs(mass - 1) < 1e-10
+    assert abs(var - 1.0 / d) < 1e-10 / d        # E[y_i^2] = 1/d by symmetry of the sphere
+
+
+@pytest.mark.parametrize("d,bits", [(8, 2), (8, 4), (128, 2), (128, 4), (64, 3)])
+def test_sphere_codebook_meets_centroid_condition_by_quadrature(d, bits):
+    from scipy.integrate import quad
+    c, beta = O.lloyd_max_sphere(bits, d)
+    edges = [-1.0] + list(beta) + [1.0]
+    for j, cj in enumerate(c):
+        num, _ = quad(lambda y: y * O.sphere_pdf(y, d), edges[j], edges[j + 1], epsabs=1e-16,
+                      epsrel=1e-13, limit=200)
+        den, _ = quad(lambda y: O.sphere_pdf(y, d), edges[j], edges[j + 1], epsabs=1e-16,
+                      epsrel=1e-13, limit=200)
+        assert abs(num / den - cj) < 1e-10 * max(1.0, abs(cj) * d)
+    assert np.allclose(beta, 0.5 * (c[:-1] + c[1:]), atol=1e-15)
+
+
+@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+def test_sphere_codebook_tends_to_the_gaussian_one_for_large_d(bits):
+    d = 1 << 16
+    c, _ = O.lloyd_max_sphere(bits, d)
+    g, _ = O.lloyd_max_gaussian(bits)
+    assert np.allclose(c * math.sqrt(d), g, atol=2e-4 * max(1.0, abs(g).max()), rtol=0)
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_sphere_codebook_has_lower_distortion_under_the_true_density(bits):
+    # Lloyd-Max optimality: under f, the quantizer designed for f has a lower
+    # mean squared error than the N(0, 1/d) one; at d = 128 they are close
+    for d, gap in ((16, None), (128, 0.01)):
+        cs, bs = O.lloyd_max_sphere(bits, d)
+        cg, bg = O.lloyd_max_gaussian(bits)
+        cg, bg = cg / math.sqrt(d), bg / math.sqrt(d)
+        pdf = lambda y: O.sphere_pdf(y, d)
+        ds = O.quantizer_distortion(cs, bs, pdf, -1.0, 1.0)
+        dg = O.quantizer_distortion(cg, bg, pdf, -1.0, 1.0)
+        assert ds < dg
+        if gap is not None:
+            assert (dg - ds) / ds < gap
