@@ -143,9 +143,14 @@ const char* tq_status_string(tq_status s);
 tq_status tq_layer_spec_get(const tq_config* cfg, int layer, tq_layer_spec* out);
 
 /* Lloyd-Max codebook of 2^bits levels for the rotated-coordinate density
- * (host only).  centroids[2^bits] and boundaries[2^bits - 1] (host memory,
- * caller-owned) receive fp32 values, ascending; symmetric about 0.
- * bits in 1..8; head_dim a power of two >= 2. */
+ * ("[GitHub 탐방] TurboQuant 3-bit KV 캐시 압축 — 단일 GPU 재현 기록", "GPU 세대가
+ * 바뀌면" (1): each coordinate maps to one of 2^bits Lloyd-Max centroids)
+ * (host only).  density TQ_DENSITY_GAUSSIAN: N(0, 1/d);
+ * TQ_DENSITY_SPHERE_BETA: the exact density (1 - y^2)^((d-3)/2) / B(1/2,
+ * (d-1)/2) of one coordinate of a uniform unit vector in R^d.
+ * centroids[2^bits] and boundaries[2^bits - 1] (host memory, caller-owned)
+ * receive fp32 values, ascending; symmetric about 0.  bits in {1, 2, 3, 4,
+ * 8}; head_dim a power of two >= 2.  TQ_ERR_INVALID_ARG otherwise. */
 tq_status tq_make_codebook(int bits, int head_dim, int density, float* centroids,
                            float* boundaries);
 

@@ -139,6 +139,128 @@ static void lloyd_max_gaussian(int bits, std::vector<ld>& c, std::vector<ld>& be
   if (L % 2 == 0) beta[L / 2 - 1] = 0;
 }
 
+// ---- Lloyd-Max on the exact rotated-coordinate density ---------------------
+// One coordinate y of a uniformly random unit vector in R^d has density
+// f(y) = C_d (1 - y^2)^((d-3)/2) on [-1, 1], C_d = Gamma(d/2) / (Gamma(1/2)
+// Gamma((d-1)/2)); it tends to N(0, 1/d) as d grows.  With y = sin(t) the
+// mass of a cell is C_d * integral of cos^(d-2)(t) dt, whose integrand is
+// smooth everywhere (also at the ends of the support), so composite
+// Gauss-Legendre quadrature on the angle is accurate to long-double round-off;
+// the first moment has the closed form C_d / (d-1) [(1-lo^2)^((d-1)/2) -
+// (1-hi^2)^((d-1)/2)].  The optimality conditions are solved by the same
+// Newton iteration as the Gaussian case.
+static void gauss_legendre(int n, std::vector<ld>& x, std::vector<ld>& w) {
+  // nodes: roots of P_n by Newton from cos(pi (i - 1/4) / (n + 1/2));
+  // weights 2 / ((1 - x^2) P_n'(x)^2)
+  const ld pi = 3.14159265358979323846264338327950288L;
+  x.assign(n, 0);
+  w.assign(n, 0);
+  for (int i = 0; i < n; ++i) {
+    ld z = std::cos(pi * ((ld)i + 0.75L) / ((ld)n + 0.5L));
+    ld dp = 0;
+    for (int it = 0; it < 100; ++it) {
+      ld p0 = 1, p1 = z;
+      for (int k = 2; k <= n; ++k) {
+        ld p2 = ((2 * k - 1) * z * p1 - (k - 1) * p0) / k;
+        p0 = p1;
+        p1 = p2;
+      }
+      dp = n * (z * p1 - p0) / (z * z - 1);
+      ld dz = p1 / dp;
+      z -= dz;
+      if (std::fabs(dz) < 1e-19L) break;
+    }
+    x[i] = z;
+    w[i] = 2 / ((1 - z * z) * dp * dp);
+  }
+}
+
+static ld sphere_log_norm(int d) {
+  return std::lgamma((ld)d / 2) - std::lgamma(0.5L) - std::lgamma(((ld)d - 1) / 2);
+}
+
+// C_d * integral over [asin lo, asin hi] of cos^(d-2)(t)
+static ld sphere_mass(ld lo, ld hi, int d, const std::vector<ld>& gx, const std::vector<ld>& gw) {
+  const ld t0 = std::asin(std::max(-1.0L, std::min(1.0L, lo)));
+  const ld t1 = std::asin(std::max(-1.0L, std::min(1.0L, hi)));
+  const int panels = 16;
+  const ld h = (t1 - t0) / panels;
+  ld sum = 0;
+  for (int p = 0; p < panels; ++p) {
+    const ld mid = t0 + (p + 0.5L) * h;
+    ld part = 0;
+    for (size_t i = 0; i < gx.size(); ++i) part += gw[i] * std::pow(std::cos(mid + 0.5L * h * gx[i]), (ld)(d - 2));
+    sum += 0.5L * h * part;
+  }
+  return std::exp(sphere_log_norm(d)) * sum;
+}
+
+static ld sphere_first_moment(ld lo, ld hi, int d) {
+  const ld e = ((ld)d - 1) / 2;
+  auto g = [&](ld y) { return std::pow(std::max(0.0L, 1 - y * y), e); };
+  return std::exp(sphere_log_norm(d)) / (d - 1) * (g(lo) - g(hi));
+}
+
+static ld sphere_pdf(ld y, int d) {
+  return std::exp(sphere_log_norm(d)) * std::pow(std::max(0.0L, 1 - y * y), ((ld)d - 3) / 2);
+}
+
+static void lloyd_max_sphere(int bits, int d, std::vector<ld>& c, std::vector<ld>& beta) {
+  const int L = 1 << bits;
+  std::vector<ld> gx, gw;
+  gauss_legendre(24, gx, gw);
+  c.assign(L, 0);
+  if (d <= 16) {
+    for (int j = 0; j < L; ++j) c[j] = -1 + (2 * (ld)j + 1) / L;   // uniform start
+  } else {
+    std::vector<ld> g, gb;
+    lloyd_max_gaussian(bits, g, gb);
+    for (int j = 0; j < L; ++j) c[j] = g[j] / std::sqrt((ld)d);
+  }
+  std::vector<ld> b(L - 1), lo(L), hi(L), P(L), m(L), F(L), sub(L), diag(L), sup(L), cp(L), dp(L),
+      dx(L);
+  for (int it = 0; it < 80; ++it) {
+    for (int j = 0; j + 1 < L; ++j) b[j] = 0.5L * (c[j] + c[j + 1]);
+    for (int j = 0; j < L; ++j) {
+      lo[j] = j == 0 ? -1.0L : b[j - 1];
+      hi[j] = j == L - 1 ? 1.0L : b[j];
+      P[j] = sphere_mass(lo[j], hi[j], d, gx, gw);
+      m[j] = sphere_first_moment(lo[j], hi[j], d) / P[j];
+      F[j] = c[j] - m[j];
+      sub[j] = 0;
+      diag[j] = 1;
+      sup[j] = 0;
+    }
+    for (int j = 0; j < L; ++j) {
+      if (j < L - 1) {
+        ld t = 0.5L * sphere_pdf(b[j], d) * (b[j] - m[j]) / P[j];
+        diag[j] -= t;
+        sup[j] -= t;
+      }
+      if (j > 0) {
+        ld t = 0.5L * sphere_pdf(b[j - 1], d) * (m[j] - b[j - 1]) / P[j];
+        sub[j] -= t;
+        diag[j] -= t;
+      }
+    }
+    cp[0] = sup[0] / diag[0];
+    dp[0] = -F[0] / diag[0];
+    for (int j = 1; j < L; ++j) {
+      ld den = diag[j] - sub[j] * cp[j - 1];
+      cp[j] = j < L - 1 ? sup[j] / den : 0;
+      dp[j] = (-F[j] - sub[j] * dp[j - 1]) / den;
+    }
+    dx[L - 1] = dp[L - 1];
+    for (int j = L - 2; j >= 0; --j) dx[j] = dp[j] - cp[j] * dx[j + 1];
+    for (int j = 0; j < L; ++j) c[j] += dx[j];
+    std::vector<ld> s(c);
+    for (int j = 0; j < L; ++j) c[j] = 0.5L * (s[j] - s[L - 1 - j]);
+  }
+  beta.assign(L - 1, 0);
+  for (int j = 0; j + 1 < L; ++j) beta[j] = 0.5L * (c[j] + c[j + 1]);
+  if (L % 2 == 0) beta[L / 2 - 1] = 0;
+}
+
 static bool valid_bits(int b) { return b == 1 || b == 2 || b == 3 || b == 4 || b == 8; }
 static bool gpu_bits(int b) { return b == 2 || b == 3 || b == 4 || b == 8; }
 static bool pow2(int d) { return d >= 2 && (d & (d - 1)) == 0; }
@@ -231,11 +353,15 @@ extern "C" tq_status tq_layer_spec_get(const tq_config* cfg, int layer, tq_layer
 extern "C" tq_status tq_make_codebook(int bits, int head_dim, int density, float* centroids,
                                       float* boundaries) {
   if (!valid_bits(bits) || !pow2(head_dim) || !centroids || !boundaries) return TQ_ERR_INVALID_ARG;
-  if (density == TQ_DENSITY_SPHERE_BETA) return TQ_ERR_UNSUPPORTED;
-  if (density != TQ_DENSITY_GAUSSIAN) return TQ_ERR_INVALID_ARG;
+  if (density != TQ_DENSITY_GAUSSIAN && density != TQ_DENSITY_SPHERE_BETA) return TQ_ERR_INVALID_ARG;
   std::vector<ld> c, b;
-  lloyd_max_gaussian(bits, c, b);
-  const ld sigma = 1.0L / std::sqrt((ld)head_dim);
+  ld sigma = 1.0L / std::sqrt((ld)head_dim);
+  if (density == TQ_DENSITY_SPHERE_BETA) {
+    lloyd_max_sphere(bits, head_dim, c, b);
+    sigma = 1.0L;                        // already in units of the coordinate
+  } else {
+    lloyd_max_gaussian(bits, c, b);
+  }
   const int L = 1 << bits;
   for (int j = 0; j < L; ++j) centroids[j] = (float)(double)(c[j] * sigma);
   for (int j = 0; j + 1 < L; ++j) boundaries[j] = (float)(double)(b[j] * sigma);
@@ -395,7 +521,6 @@ static tq_status check_gpu_common(const tq_config* cfg, const void* tables, int 
   if (!tables || layer < 0 || layer >= cfg->n_layers) return TQ_ERR_INVALID_ARG;
   if (!aligned16(tables)) return TQ_ERR_ALIGNMENT;
   if (cfg->head_dim != kHeadDim) return TQ_ERR_UNSUPPORTED;
-  if (cfg->density != TQ_DENSITY_GAUSSIAN) return TQ_ERR_UNSUPPORTED;
   tq_layer_spec s = spec_of(cfg, layer);
   if (!gpu_bits(s.k_bits) || !gpu_bits(s.v_bits)) return TQ_ERR_UNSUPPORTED;
   if (s.k_mode == TQ_MODE_MSE_QJL && cfg->qjl_m != kQjlM) return TQ_ERR_UNSUPPORTED;

@@ -23,8 +23,13 @@ def oracle_codec(bits, d=128):
     return O.codebook_fp32(bits, d)
 
 
-def oracle_quantize(X64, bits, seed, layer, kind, d=128):
-    c32, b32 = O.codebook_fp32(bits, d)
+def oracle_codebook(bits, d=128, density=0):
+    """fp32 codebook of the oracle: N(0, 1/d) (density 0) or sphere (1)."""
+    return O.codebook_sphere_fp32(bits, d) if density == 1 else O.codebook_fp32(bits, d)
+
+
+def oracle_quantize(X64, bits, seed, layer, kind, d=128, density=0):
+    c32, b32 = oracle_codebook(bits, d, density)
     s = O.rotation_signs(seed, layer, kind, d)
     q = O.quantize_vectors(X64, c32, b32, s)
     q["packed"] = O.pack_codes(q["codes"], bits)

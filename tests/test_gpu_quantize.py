@@ -56,6 +56,41 @@ def test_quantize_bits_and_ragged_tiles_bf16(B, bits, n):
         compare_norms(planes.norms_view().cpu().numpy(), oq["norms"])
 
 
+@pytest.mark.parametrize("bits", [2, 4])
+def test_quantize_and_decode_with_the_sphere_density_codebook(B, bits):
+    """Codebook from the exact coordinate density (TQ_DENSITY_SPHERE_BETA):
+    the kernels are the same, the codes follow the sphere codebook, and decode
+    attention matches the oracle's."""
+    import torch
+    from kv_cache_quantization_random_gb300 import workloads as W
+    w = W.scaled(W.get("llama8b_32k"), batch=2, n_q_heads=8, n_kv_heads=2, context=700, window=0)
+    K, V = W.make_kv(w)
+    q = W.make_q(w)
+    cfg = B.Config(k_bits=bits, v_bits=bits, seed=9, density=B.TQ_DENSITY_SPHERE_BETA)
+    tables = B.device_tables(cfg)
+    kp = B.Planes(cfg, 0, 0, 2, 2, 700)
+    vp = B.Planes(cfg, 0, 1, 2, 2, 700)
+    B.tq_quantize_kv(cfg, tables, 0, 0, K.cuda(), kp)
+    B.tq_quantize_kv(cfg, tables, 0, 1, V.cuda(), vp)
+    torch.cuda.synchronize()
+    assert B.tq_get_device_error() == B.TQ_OK
+    oqk = oracle_quantize(to64(K), bits, 9, 0, 0, density=1)
+    oqv = oracle_quantize(to64(V), bits, 9, 0, 1, density=1)
+    compare_codes(kp.codes_view().cpu().numpy(), oqk, bits)
+    compare_codes(vp.codes_view().cpu().numpy(), oqv, bits)
+    out = torch.empty(2, 8, 128, device="cuda")
+    ws = B.new_workspace(cfg, 2, 8, 2, 700)
+    seq = torch.tensor([700, 411], dtype=torch.int32, device="cuda")
+    B.tq_decode_attention(cfg, tables, 0, q.cuda(), w.softmax_scale, kp, vp, seq, 700, out, ws)
+    torch.cuda.synchronize()
+    ref = O.decode_attention(to64(q), oqk["codes"], oqk["norms"], oqv["codes"], oqv["norms"],
+                             oqk["c32"], oqv["c32"], oqk["signs"], oqv["signs"], [700, 411],
+                             w.softmax_scale)
+    got = to64(out)
+    rel = np.linalg.norm(got - ref, axis=-1) / np.linalg.norm(ref, axis=-1)
+    assert rel.max() < 2e-3
+
+
 def test_quantize_strided_source_dst_pos_and_zero_rows(B):
     import torch
     g = torch.Generator().manual_seed(3)

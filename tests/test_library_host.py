@@ -56,6 +56,26 @@ def test_codebook_other_dims(B):
         assert np.array_equal(c, oc) and np.array_equal(b, ob)
 
 
+@pytest.mark.parametrize("d", [4, 8, 64, 128])
+@pytest.mark.parametrize("bits", [1, 2, 3, 4, 8])
+def test_sphere_codebook_matches_oracle(B, bits, d):
+    """fp32 values equal the oracle's, except that at 256 levels (where the
+    optimality system is ill-conditioned and the fp64 oracle resolves the
+    fixed point to ~1e-10) a value may round to the neighbouring fp32 number
+    when the oracle's fp64 value lies within 1e-9 (relative) of the rounding tie."""
+    c, b = B.tq_make_codebook(bits, d, density=B.TQ_DENSITY_SPHERE_BETA)
+    oc64, ob64 = O.lloyd_max_sphere(bits, d)
+    for got, ref64 in ((c, oc64), (b, ob64)):
+        ref = ref64.astype(np.float32)
+        diff = np.nonzero(got != ref)[0]
+        assert bits == 8 or diff.size == 0
+        for i in diff:
+            nxt = np.nextafter(ref[i], got[i])
+            assert got[i] == nxt                              # one ulp apart
+            tie = 0.5 * (float(ref[i]) + float(nxt))
+            assert abs(ref64[i] - tie) <= 1e-9 * abs(tie)
+
+
 def test_sign_vectors_match_oracle(B):
     for seed in (0, 1, 123456789123):
         for layer in (0, 5, 35):
