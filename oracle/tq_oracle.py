@@ -49,7 +49,7 @@ __all__ = [
     "sphere_pdf", "lloyd_max_sphere", "codebook_sphere_fp32", "quantizer_distortion",
     "quantize_vectors", "near_boundary", "pack_codes", "unpack_codes",
     "pack_bits", "unpack_bits", "qjl_residual", "qjl_sketch",
-    "qjl_inner_product_estimate", "dequantize", "dequantize_qjl",
+    "qjl_inner_product_estimate", "direct_sign_sketch", "direct_sign_estimate", "dequantize", "dequantize_qjl",
     "layer_bits", "softmax", "decode_attention", "exact_attention",
 ]
 
@@ -514,6 +514,32 @@ def qjl_inner_product_estimate(q_rot: np.ndarray, bits: np.ndarray, gamma, S: np
 
 
 # --------------------------------------------------------------------------
+# Direct Sign residual ([README] v1.1.0 "Direct Sign": at head_dim <= 128 the
+# sign of each rotated residual coordinate is stored directly instead of a
+# projected sketch; no second transform is needed on the query side)
+# --------------------------------------------------------------------------
+
+def direct_sign_sketch(r: np.ndarray):
+    """bit_i = [r_i >= 0] for every rotated residual coordinate, and the scale
+    a = mean_i |r_i| (stored fp32): the least-squares a for r ~= a (2 bit - 1).
+    Returns (bits int64[..., d], scale fp32[...])."""
+    r = np.asarray(r, dtype=np.float64)
+    bits = (r >= 0).astype(np.int64)
+    scale = np.mean(np.abs(r), axis=-1)
+    return bits, round_to_fp32(scale)
+
+
+def direct_sign_estimate(q_rot: np.ndarray, bits: np.ndarray, scale) -> np.ndarray:
+    """Estimate of <q_rot, r> from the direct signs: a * sum_i q_i (2 bit_i - 1).
+    For residual coordinates ~ N(0, s^2) its error variance per coordinate is
+    s^2 (1 - 2/pi), against s^2 pi/2 d/m for the m-row QJL sketch: the ratio
+    (1 - 2/pi) / (pi/2) = 0.23 at m = d."""
+    sgn = 2.0 * np.asarray(bits, dtype=np.float64) - 1.0
+    return np.asarray(scale, dtype=np.float64) * np.sum(np.asarray(q_rot, dtype=np.float64) * sgn,
+                                                        axis=-1)
+
+
+# --------------------------------------------------------------------------
 # Dequantize
 # --------------------------------------------------------------------------
 
@@ -558,7 +584,7 @@ def softmax(s: np.ndarray) -> np.ndarray:
 
 def decode_attention(q, k_codes, k_norms, v_codes, v_norms, ck32, cv32,
                      signs_k, signs_v, seq_lens, scale, window=0,
-                     k_win=None, v_win=None, qjl=None):
+                     k_win=None, v_win=None, qjl=None, dsign=None):
     """One decode step of attention over a compressed cache.
 
     q        [B, Hq, d] query values (fp64 copy of the inputs)
@@ -569,6 +595,8 @@ def decode_attention(q, k_codes, k_norms, v_codes, v_norms, ck32, cv32,
              ([B, Hkv, W, d], slot t mod W) in the original domain;
              tokens t < T-W come from the codes.
     qjl      None, or dict(bits=[B,Hkv,cap,m], gamma=[B,Hkv,cap], S=[m,d])
+    dsign    None, or dict(bits=[B,Hkv,cap,d], scale=[B,Hkv,cap]): Direct Sign
+             keys, s_t += scale * a_t <q_rot, 2 bit_t - 1>
 
     Per query head h (kv-head h // (Hq/Hkv)):
       q_rot = R_K q;
@@ -608,6 +636,10 @@ def decode_attention(q, k_codes, k_norms, v_codes, v_norms, ck32, cv32,
                     sgn = 2.0 * np.asarray(qjl["bits"][b, kh, :nq], dtype=np.float64) - 1.0
                     gam = np.asarray(qjl["gamma"][b, kh, :nq], dtype=np.float64)
                     s_q = s_q + gam * math.sqrt(math.pi / 2.0) / m * (sgn @ (S @ q_rot))
+                if dsign is not None:
+                    sgn = 2.0 * np.asarray(dsign["bits"][b, kh, :nq], dtype=np.float64) - 1.0
+                    a = np.asarray(dsign["scale"][b, kh, :nq], dtype=np.float64)
+                    s_q = s_q + a * (sgn @ q_rot)
                 scores.append(scale * s_q)
             if win_tokens:
                 slots = [t % window for t in win_tokens]

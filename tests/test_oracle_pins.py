@@ -520,3 +520,44 @@ def test_sphere_codebook_has_lower_distortion_under_the_true_density(bits):
         assert ds < dg
         if gap is not None:
             assert (dg - ds) / ds < gap
+
+
+# ------------------------------------------------------------------- Direct Sign
+def test_direct_sign_is_exact_when_all_residual_coordinates_have_equal_magnitude():
+    rng = np.random.default_rng(31)
+    s = np.where(rng.random(128) < 0.5, -1.0, 1.0)
+    r = 0.37 * s
+    q = rng.standard_normal(128)
+    bits, a = O.direct_sign_sketch(r)
+    assert np.array_equal(bits, (s > 0).astype(np.int64))
+    assert O.direct_sign_estimate(q, bits, a) == pytest.approx(q @ r, rel=1e-6)
+
+
+def test_direct_sign_scale_is_the_least_squares_one():
+    # a = mean|r| minimises ||r - a sign(r)||^2; check against a 1-D search
+    r = np.random.default_rng(32).standard_normal((3, 128))
+    bits, a = O.direct_sign_sketch(r)
+    sgn = 2.0 * bits - 1.0
+    for k in range(3):
+        grid = np.linspace(0.5 * a[k], 1.5 * a[k], 2001)
+        err = [np.sum((r[k] - g * sgn[k]) ** 2) for g in grid]
+        assert abs(grid[int(np.argmin(err))] - a[k]) <= 1e-3 * a[k]
+
+
+def test_direct_sign_error_variance_is_0_23_of_qjl_at_m_equal_d():
+    # the pages' ratio (1 - 2/pi)/(pi/2) = 0.231 for Gaussian residual
+    # coordinates, measured over 4000 (q, r, S) draws
+    rng = np.random.default_rng(33)
+    d = 128
+    e_ds, e_qjl = [], []
+    for _ in range(4000):
+        r = rng.standard_normal(d)
+        q = rng.standard_normal(d)
+        S = rng.standard_normal((d, d))
+        bits, a = O.direct_sign_sketch(r)
+        e_ds.append(O.direct_sign_estimate(q, bits, a) - q @ r)
+        qb, gamma, _ = O.qjl_sketch(r, S)
+        e_qjl.append(O.qjl_inner_product_estimate(q, qb, float(np.linalg.norm(r)), S) - q @ r)
+    ratio = np.var(e_ds) / np.var(e_qjl)
+    assert 0.20 < ratio < 0.26, ratio
+    assert (1 - 2 / math.pi) / (math.pi / 2) == pytest.approx(0.2313, abs=1e-4)
