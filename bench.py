@@ -174,7 +174,8 @@ def largest_divisor_at_most(n: int, cap: int) -> int:
 def packed_bytes(w):
     """Bytes of one packed key and one packed value vector (codes + norms [+ QJL])."""
     d = w.head_dim
-    kbytes = d * w.k_bits // 8 + 4 + ((w.qjl_m // 8 + 4) if w.k_qjl else 0)
+    kbytes = d * w.k_bits // 8 + 4 + ((w.qjl_m // 8 + 4) if w.k_qjl else 0) + \
+        ((d // 8 + 4) if w.k_sign else 0)
     vbytes = d * w.v_bits // 8 + 4
     return kbytes, vbytes
 
@@ -200,7 +201,8 @@ def build_state(B, w, device, layer=0):
     T, Wn = w.context, w.window
     nq = T - Wn
     cfg = B.Config(k_bits=w.k_bits, v_bits=w.v_bits, residual_window=Wn, seed=w.codec_seed,
-                   k_mode=B.TQ_MODE_MSE_QJL if w.k_qjl else B.TQ_MODE_MSE, qjl_m=w.qjl_m)
+                   k_mode=(B.TQ_MODE_MSE_QJL if w.k_qjl else
+                           B.TQ_MODE_MSE_SIGN if w.k_sign else B.TQ_MODE_MSE), qjl_m=w.qjl_m)
     tables = B.device_tables(cfg, device)
     K, V = WL.make_kv(w, layer=layer, device=device)
     kp = B.Planes(cfg, layer, 0, w.batch, w.n_kv_heads, nq, device)
@@ -428,7 +430,8 @@ def run_ours(args, w, rank, world, local):
         "config": {
             "workload": w.name, "batch": w.batch, "q_heads": w.n_q_heads,
             "kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "context": int(seq.max()),
-            "k_bits": w.k_bits, "v_bits": w.v_bits, "k_qjl": w.k_qjl, "window": Wn,
+            "k_bits": w.k_bits, "v_bits": w.v_bits, "k_qjl": w.k_qjl, "k_sign": w.k_sign,
+            "window": Wn,
             "new_tokens_per_step": 1, "parallelism": f"replicas x{world}",
             "l2": f"{R} cache replicas cycled ({R * cache_bytes / 1e6:.0f} MB > 4 x L2 {l2 / 1e6:.0f} MB)",
             "graph_steps": S,
@@ -488,6 +491,11 @@ def _oracle_cache(w, K, V, T):
         r = O.qjl_residual(qk["y"], qk["codes"], qk["norm64"], ck)
         bits, gamma, _ = O.qjl_sketch(r, S)
         qjl = dict(bits=bits, gamma=gamma, S=S)
+    dsign = None
+    if w.k_sign:
+        r = O.qjl_residual(qk["y"], qk["codes"], qk["norm64"], ck)
+        bits, scale = O.direct_sign_sketch(r)
+        dsign = dict(bits=bits, scale=scale)
     kw = vw = None
     if Wn:
         kw = np.zeros((1, K.shape[1], Wn, w.head_dim))
@@ -495,7 +503,8 @@ def _oracle_cache(w, K, V, T):
         for t in range(nq, T):
             kw[:, :, t % Wn] = K[:, :, t]
             vw[:, :, t % Wn] = V[:, :, t]
-    return dict(ck=ck, bk=bk, cv=cv, bv=bv, sk=sk, sv=sv, qk=qk, qv=qv, qjl=qjl, kw=kw, vw=vw)
+    return dict(ck=ck, bk=bk, cv=cv, bv=bv, sk=sk, sv=sv, qk=qk, qv=qv, qjl=qjl, dsign=dsign,
+                kw=kw, vw=vw)
 
 
 def _oracle_decode(w, c, qs, T):
@@ -503,7 +512,7 @@ def _oracle_decode(w, c, qs, T):
     return O.decode_attention(qs, c["qk"]["codes"], c["qk"]["norms"], c["qv"]["codes"],
                               c["qv"]["norms"], c["ck"], c["cv"], c["sk"], c["sv"], [T],
                               w.softmax_scale, window=w.window, k_win=c["kw"], v_win=c["vw"],
-                              qjl=c["qjl"])
+                              qjl=c["qjl"], dsign=c["dsign"])
 
 
 def sampled_parity(B, w, st, q, out, rep0, seq, decode):

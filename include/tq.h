@@ -76,7 +76,13 @@ typedef enum {
   TQ_ERR_BUFFER_TOO_SMALL = 7 /* workspace / table buffer smaller than required */
 } tq_status;
 
-typedef enum { TQ_MODE_MSE = 0, TQ_MODE_MSE_QJL = 1 } tq_mode;
+/* Key modes.  TQ_MODE_MSE_QJL: the 1-bit QJL sketch of the residual
+ * ("TurboQuant KV 캐시 압축 for llama.cpp", "QJL 보정 효과": TurboQuant_prod).
+ * TQ_MODE_MSE_SIGN: the Direct Sign residual of the same page's v1.1.0
+ * ("Direct Sign": the sign of each rotated residual coordinate is stored
+ * directly, no projection), with the scale a = mean_i |r_i|; the score gains
+ * a <q_rot, 2 bits - 1>. */
+typedef enum { TQ_MODE_MSE = 0, TQ_MODE_MSE_QJL = 1, TQ_MODE_MSE_SIGN = 2 } tq_mode;
 typedef enum { TQ_DENSITY_GAUSSIAN = 0, TQ_DENSITY_SPHERE_BETA = 1 } tq_density;
 typedef enum { TQ_BF16 = 0, TQ_F32 = 1 } tq_dtype;
 typedef enum { TQ_KIND_K = 0, TQ_KIND_V = 1 } tq_kind;
@@ -85,8 +91,9 @@ typedef enum { TQ_KIND_K = 0, TQ_KIND_V = 1 } tq_kind;
  *   head_dim         d; a power of two.  The GPU kernels implement d = 128.
  *   n_layers         number of attention layers (>= 1).
  *   k_bits, v_bits   MSE code bits of unprotected layers, in {1,2,3,4,8}.
- *   k_mode           TQ_MODE_MSE or TQ_MODE_MSE_QJL (keys only; values are
- *                    always MSE-only: the sketch corrects Q.K, not the V sum).
+ *   k_mode           TQ_MODE_MSE, TQ_MODE_MSE_QJL or TQ_MODE_MSE_SIGN (keys
+ *                    only; values are always MSE-only: the residual term
+ *                    corrects Q.K, not the V sum).
  *   qjl_m            QJL projections per key (multiple of 32, <= 256; 128 is
  *                    the only size the GPU kernels implement).
  *   n_protect_first, n_protect_last, protect_bits
@@ -122,8 +129,10 @@ typedef struct {
  * each plane laid out [batch][n_kv_heads][capacity][...] with no padding:
  *   codes      uint8 [.., code_bytes]  code_bytes = head_dim * bits / 8
  *   norms      fp32  [..]              ||x||
- *   qjl_signs  uint8 [.., qjl_m / 8]   QJL keys only, else NULL
- *   qjl_rnorm  fp32  [..]              gamma = ||r||, QJL keys only, else NULL
+ *   qjl_signs  uint8 [.., qjl_m / 8]   QJL keys: sketch bits; Direct Sign keys:
+ *                                      [.., head_dim / 8] residual signs; else NULL
+ *   qjl_rnorm  fp32  [..]              QJL keys: gamma = ||r||; Direct Sign keys:
+ *                                      a = mean |r_i|; else NULL
  *   capacity   tokens per (sequence, kv-head).
  * Every plane pointer must be 16-byte aligned (TQ_ERR_ALIGNMENT). */
 typedef struct {

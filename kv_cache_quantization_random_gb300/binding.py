@@ -24,7 +24,7 @@ TQ_ERR_NAMES = {
     4: "TQ_ERR_CUDA", 5: "TQ_ERR_DEVICE_TIMEOUT", 6: "TQ_ERR_DEVICE_BOUNDS",
     7: "TQ_ERR_BUFFER_TOO_SMALL",
 }
-TQ_MODE_MSE, TQ_MODE_MSE_QJL = 0, 1
+TQ_MODE_MSE, TQ_MODE_MSE_QJL, TQ_MODE_MSE_SIGN = 0, 1, 2
 TQ_DENSITY_GAUSSIAN, TQ_DENSITY_SPHERE_BETA = 0, 1
 TQ_BF16, TQ_F32 = 0, 1
 TQ_KIND_K, TQ_KIND_V = 0, 1
@@ -217,6 +217,7 @@ class Planes:
         kb, vb, mode = tq_layer_spec_get(cfg, layer)
         self.bits = kb if kind == TQ_KIND_K else vb
         self.qjl = kind == TQ_KIND_K and mode == TQ_MODE_MSE_QJL
+        self.dsign = kind == TQ_KIND_K and mode == TQ_MODE_MSE_SIGN
         alloc = lambda n: torch.zeros(max(n, 16), dtype=torch.uint8, device=device)
         self.codes = alloc(sizes[0])
         self.norms = alloc(sizes[1])
@@ -240,7 +241,7 @@ class Planes:
             torch.float32).view(self.batch, self.n_kv_heads, self.capacity)
 
     def signs_view(self):
-        m = self.cfg.qjl_m
+        m = self.cfg.head_dim if self.dsign else self.cfg.qjl_m
         return self.qjl_signs[: self.batch * self.n_kv_heads * self.capacity * m // 8].view(
             self.batch, self.n_kv_heads, self.capacity, m // 8)
 

@@ -1,7 +1,8 @@
 // Decode attention over a TurboQuant-compressed KV cache (sm_103a): the kernel
 // template, instantiated per (query heads per kv-head G, key bits, value bits,
-// QJL) in tq_decode_g{1,2,4,8}.cu so that each launch runs code for exactly
-// one storage format.
+// key residual term: none, QJL sketch or Direct Sign) in
+// tq_decode_g{1,2,4,8}.cu so that each launch runs code for exactly one
+// storage format.
 //
 // "TurboQuant KV 캐시 압축 for llama.cpp": v1.7.0 decision 4 (the decode kernel
 // applies the encoders' WHT to Q, so q_rot . k_rot = q . k by Parseval);
@@ -54,7 +55,9 @@ struct DecodeSmem {
   int qr, qo, sv, qjlb, sq, lutk4, warps, warp_stride;
   int kbuf, vbuf, kn, vn, sbuf, rn, ws, bar;   // offsets inside one warp's region
   int comb, total;
-  __host__ __device__ DecodeSmem(int G, int qjl, int kb, int vb) {
+  // res: 0 = MSE keys, 1 = QJL keys, 2 = Direct Sign keys
+  __host__ __device__ DecodeSmem(int G, int res, int kb, int vb) {
+    const bool qjl = res == 1, sres = res != 0;
     int off = 0;
     qr = off; off += kD2 * G * 4;                 // [128][G] rotated, scaled queries
     qo = off; off += kD2 * G * 4;                 // [128][G] original-domain queries
@@ -69,8 +72,8 @@ struct DecodeSmem {
     vbuf = w; w += ns * 32 * 16 * vb;
     kn = w; w += ns * 128;
     vn = w; w += ns * 128;
-    sbuf = w; w += qjl ? ns * 32 * 16 : 0;
-    rn = w; w += qjl ? ns * 128 : 0;
+    sbuf = w; w += sres ? ns * 32 * 16 : 0;     // 128 sign bits per token
+    rn = w; w += sres ? ns * 128 : 0;           // gamma (QJL) or scale (Direct Sign)
     ws = w; w += 8 * 32 * 2;                      // [8 heads][32 tokens] fp16 weights
     bar = w; w += 8 * ns;
     w = (w + 15) & ~15;
@@ -329,6 +332,23 @@ __device__ __forceinline__ void score_all(const KCodes<KB> (&c)[4], const uint32
   }
 }
 
+// Direct Sign: sum_i (2 bit_i - 1) q_rot,i for tokens ta, ta+8.  Bit i of
+// the token's 128-bit sign vector belongs to rotated coordinate i, and the
+// lane's 32 bits are coordinates 32 tig .. 32 tig + 31: the same k-index
+// permutation as the key scores, so B is the query operand bh / bl.
+__device__ __forceinline__ void sign_scores(uint32_t sa, uint32_t sb, const uint32_t* slut,
+                                            const uint32_t (&bh)[8][2],
+                                            const uint32_t (&bl)[8][2], float (&d)[4],
+                                            float (&dl)[4]) {
+#pragma unroll
+  for (int kt = 0; kt < 8; ++kt) {
+    const uint32_t a0 = slut[(sa >> (4 * kt)) & 3u], a1 = slut[(sb >> (4 * kt)) & 3u];
+    const uint32_t a2 = slut[(sa >> (4 * kt + 2)) & 3u], a3 = slut[(sb >> (4 * kt + 2)) & 3u];
+    mma16816(d, a0, a1, a2, a3, bh[kt][0], bh[kt][1]);
+    mma16816(dl, a0, a1, a2, a3, bl[kt][0], bl[kt][1]);
+  }
+}
+
 // QJL: sum_j (2 bit_j - 1) (S q)_j for tokens ta, ta+8: A = exact +-1 signs,
 // B = S q hi and lo (per lane, per k-tile, from shared memory).
 __device__ __forceinline__ void qjl_scores(uint32_t sa, uint32_t sb, const uint32_t* slut,
@@ -344,14 +364,17 @@ __device__ __forceinline__ void qjl_scores(uint32_t sa, uint32_t sb, const uint3
   }
 }
 
-template <int G, int KB, int VB, bool QJL>
+template <int G, int KB, int VB, int RES>
 __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
   constexpr int KROW = 16 * KB, VROW = 16 * VB;
   __shared__ __align__(16) uint32_t lutk[256];   // K centroid tables (see kpair)
   __shared__ __align__(16) uint32_t lutv[256];   // V fp16 centroids (pairs for 2/3 bits)
   __shared__ uint32_t slut[4];                   // (+-1, +-1) fp16 pairs of two sign bits
   extern __shared__ __align__(128) uint8_t smem[];
-  const DecodeSmem L(G, QJL ? 1 : 0, KB, VB);
+  constexpr bool QJL = RES == 1;        // QJL sketch of the key residual
+  constexpr bool SGN = RES == 2;        // Direct Sign key residual
+  constexpr bool HAS_RES = RES != 0;
+  const DecodeSmem L(G, RES, KB, VB);
   float* qr = (float*)(smem + L.qr);
   float* qo = (float*)(smem + L.qo);
   float* svs = (float*)(smem + L.sv);
@@ -420,8 +443,8 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
   const uint8_t* vc = a.vc + row0 * a.vcap * VROW;
   const float* knp = a.kn + row0 * a.kcap;
   const float* vnp = a.vn + row0 * a.vcap;
-  const uint8_t* ksp = QJL ? a.ks + row0 * a.kcap * 16 : nullptr;
-  const float* krp = QJL ? a.kr + row0 * a.kcap : nullptr;
+  const uint8_t* ksp = HAS_RES ? a.ks + row0 * a.kcap * 16 : nullptr;
+  const float* krp = HAS_RES ? a.kr + row0 * a.kcap : nullptr;
 
   // chunk c0 -> ring slot: codes by bulk copy; norms by bulk copy when the
   // 16-byte-rounded range stays inside the plane, else by plain loads
@@ -431,7 +454,7 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
     // bulk copies need 16-byte aligned sources: the norm rows of a (sequence,
     // head) start at row0 * capacity floats, aligned only if capacity % 4 == 0
     const bool aligned = (((uintptr_t)(knp + c0) | (uintptr_t)(vnp + c0) |
-                           (QJL ? (uintptr_t)(krp + c0) : (uintptr_t)0)) & 15u) == 0;
+                           (HAS_RES ? (uintptr_t)(krp + c0) : (uintptr_t)0)) & 15u) == 0;
     const bool bulk_norms =
         aligned && (long long)c0 + n4 <= a.kcap && (long long)c0 + n4 <= a.vcap;
     uint8_t* kb_ = wreg + L.kbuf + slot * 32 * KROW;
@@ -441,12 +464,12 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
     if (!bulk_norms && lane < nv) {
       kn_[lane] = knp[c0 + lane];
       vn_[lane] = vnp[c0 + lane];
-      if constexpr (QJL) ((float*)(wreg + L.rn + slot * 128))[lane] = krp[c0 + lane];
+      if constexpr (HAS_RES) ((float*)(wreg + L.rn + slot * 128))[lane] = krp[c0 + lane];
     }
     __syncwarp();
     if (lane == 0) {
       uint32_t bytes = nv * (KROW + VROW) + (bulk_norms ? 2 * n4 * 4 : 0);
-      if constexpr (QJL) bytes += nv * 16 + (bulk_norms ? n4 * 4 : 0);
+      if constexpr (HAS_RES) bytes += nv * 16 + (bulk_norms ? n4 * 4 : 0);
       // a.extra_tx is a test hook: bytes that never arrive, so the wait on
       // this chunk can only end by running out of polls
       mbar_arrive_expect_tx(bar + slot, bytes + a.extra_tx);
@@ -456,7 +479,7 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
         bulk_g2s(kn_, knp + c0, n4 * 4, bar + slot);
         bulk_g2s(vn_, vnp + c0, n4 * 4, bar + slot);
       }
-      if constexpr (QJL) {
+      if constexpr (HAS_RES) {
         bulk_g2s(wreg + L.sbuf + slot * 512, ksp + (long long)c0 * 16, nv * 16, bar + slot);
         if (bulk_norms) bulk_g2s(wreg + L.rn + slot * 128, krp + c0, n4 * 4, bar + slot);
       }
@@ -633,7 +656,9 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
     const uint32_t* klut = KB == 4 ? (const uint32_t*)(smem + L.lutk4 + 8 * (lane & 15)) : lutk;
     uint16_t* ws16 = (uint16_t*)(wreg + L.ws);   // [8 heads][32 tokens] fp16 weights
     const float kscale = 1.f / (kCScale * qsp);
-    const float qjl_scale = 1.2533141373155003f / (float)kQjlM / qsq;   // sqrt(pi/2)/m
+    // residual-term scale: QJL sqrt(pi/2)/m over the S q operand scale;
+    // Direct Sign 1 over the q operand scale
+    const float res_scale = QJL ? 1.2533141373155003f / (float)kQjlM / qsq : 1.f / qsp;
     const uint4* qjlb = QJL ? (const uint4*)(smem + L.qjlb) + lane * 8 : nullptr;
 
     int c0 = t_begin + 32 * warp;           // its copies were started in the prologue
@@ -672,14 +697,15 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
           sc[mt][1] = (hh[mt][1] + (lh[mt][1] + hl[mt][1])) * na;
           sc[mt][2] = (hh[mt][2] + (lh[mt][2] + hl[mt][2])) * nb;
           sc[mt][3] = (hh[mt][3] + (lh[mt][3] + hl[mt][3])) * nb;
-          if constexpr (QJL) {
+          if constexpr (HAS_RES) {
             const uint8_t* sb_ = wreg + L.sbuf + slot * 512;
             const float* rn_ = (const float*)(wreg + L.rn + slot * 128);
             const uint32_t sa = *(const uint32_t*)(sb_ + ta * 16 + 4 * tig);
             const uint32_t sbits = *(const uint32_t*)(sb_ + tb * 16 + 4 * tig);
             float qa[4] = {0.f, 0.f, 0.f, 0.f}, ql[4] = {0.f, 0.f, 0.f, 0.f};
-            qjl_scores(sa, sbits, slut, qjlb, qa, ql);
-            const float ga = rn_[ta] * qjl_scale, gb = rn_[tb] * qjl_scale;
+            if constexpr (QJL) qjl_scores(sa, sbits, slut, qjlb, qa, ql);
+            else sign_scores(sa, sbits, slut, bh, bl, qa, ql);
+            const float ga = rn_[ta] * res_scale, gb = rn_[tb] * res_scale;
             sc[mt][0] = fmaf(qa[0] + ql[0], ga, sc[mt][0]);
             sc[mt][1] = fmaf(qa[1] + ql[1], ga, sc[mt][1]);
             sc[mt][2] = fmaf(qa[2] + ql[2], gb, sc[mt][2]);
@@ -970,10 +996,10 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
 }
 
 
-template <int G, int KB, int VB, bool QJL>
+template <int G, int KB, int VB, int RES>
 int launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
-  auto k = decode_kernel<G, KB, VB, QJL>;
-  const size_t smem = (size_t)DecodeSmem(G, QJL ? 1 : 0, KB, VB).total;
+  auto k = decode_kernel<G, KB, VB, RES>;
+  const size_t smem = (size_t)DecodeSmem(G, RES, KB, VB).total;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return 1;
   // programmatic dependent launch: the CTAs may start while the previous
@@ -993,30 +1019,39 @@ int launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
   return cudaGetLastError() != cudaSuccess;
 }
 
-// Dispatch over (KB, VB, QJL) for one G; defined once per G translation unit.
+// Dispatch over (KB, VB, key residual) for one G; defined once per G
+// translation unit.  Keys with a residual term (QJL, Direct Sign) use 2-4 bit codes.
 template <int G>
 int launch_decode_g(const DecodeArgs& a, cudaStream_t s) {
-#define TQ_VB_CASES(KB_, QJL_)                                               \
+#define TQ_VB_CASES(KB_, RES_)                                               \
   switch (a.vb) {                                                          \
-    case 2: return launch_decode_t<G, KB_, 2, QJL_>(a, s);                 \
-    case 3: return launch_decode_t<G, KB_, 3, QJL_>(a, s);                 \
-    case 4: return launch_decode_t<G, KB_, 4, QJL_>(a, s);                 \
-    case 8: return launch_decode_t<G, KB_, 8, QJL_>(a, s);                 \
+    case 2: return launch_decode_t<G, KB_, 2, RES_>(a, s);                 \
+    case 3: return launch_decode_t<G, KB_, 3, RES_>(a, s);                 \
+    case 4: return launch_decode_t<G, KB_, 4, RES_>(a, s);                 \
+    case 8: return launch_decode_t<G, KB_, 8, RES_>(a, s);                 \
   }                                                                        \
   return 1;
-  if (a.qjl) {
-    switch (a.kb) {
-      case 2: { TQ_VB_CASES(2, true) }
-      case 3: { TQ_VB_CASES(3, true) }
-      case 4: { TQ_VB_CASES(4, true) }
+  if (a.qjl || a.dsign) {
+    if (a.qjl) {
+      switch (a.kb) {
+        case 2: { TQ_VB_CASES(2, 1) }
+        case 3: { TQ_VB_CASES(3, 1) }
+        case 4: { TQ_VB_CASES(4, 1) }
+      }
+    } else {
+      switch (a.kb) {
+        case 2: { TQ_VB_CASES(2, 2) }
+        case 3: { TQ_VB_CASES(3, 2) }
+        case 4: { TQ_VB_CASES(4, 2) }
+      }
     }
     return 1;
   }
   switch (a.kb) {
-    case 2: { TQ_VB_CASES(2, false) }
-    case 3: { TQ_VB_CASES(3, false) }
-    case 4: { TQ_VB_CASES(4, false) }
-    case 8: { TQ_VB_CASES(8, false) }
+    case 2: { TQ_VB_CASES(2, 0) }
+    case 3: { TQ_VB_CASES(3, 0) }
+    case 4: { TQ_VB_CASES(4, 0) }
+    case 8: { TQ_VB_CASES(8, 0) }
   }
 #undef TQ_VB_CASES
   return 1;

@@ -270,7 +270,9 @@ static tq_status check_config(const tq_config* cfg) {
   if (!pow2(cfg->head_dim) || cfg->head_dim > 1024) return TQ_ERR_INVALID_ARG;
   if (cfg->n_layers < 1 || cfg->n_layers > 4096) return TQ_ERR_INVALID_ARG;
   if (!valid_bits(cfg->k_bits) || !valid_bits(cfg->v_bits)) return TQ_ERR_INVALID_ARG;
-  if (cfg->k_mode != TQ_MODE_MSE && cfg->k_mode != TQ_MODE_MSE_QJL) return TQ_ERR_INVALID_ARG;
+  if (cfg->k_mode != TQ_MODE_MSE && cfg->k_mode != TQ_MODE_MSE_QJL &&
+      cfg->k_mode != TQ_MODE_MSE_SIGN)
+    return TQ_ERR_INVALID_ARG;
   if (cfg->k_mode == TQ_MODE_MSE_QJL &&
       (cfg->qjl_m < 32 || cfg->qjl_m > 256 || cfg->qjl_m % 32 != 0))
     return TQ_ERR_INVALID_ARG;
@@ -448,9 +450,10 @@ extern "C" tq_status tq_plane_bytes(const tq_config* cfg, int layer, int kind, i
   size_t rows = (size_t)batch * n_kv_heads * (size_t)capacity;
   sizes[0] = rows * code_bytes(cfg->head_dim, bits);
   sizes[1] = rows * sizeof(float);
-  bool qjl = kind == 0 && s.k_mode == TQ_MODE_MSE_QJL;
-  sizes[2] = qjl ? rows * (size_t)(cfg->qjl_m / 8) : 0;
-  sizes[3] = qjl ? rows * sizeof(float) : 0;
+  const bool qjl = kind == 0 && s.k_mode == TQ_MODE_MSE_QJL;
+  const bool dsign = kind == 0 && s.k_mode == TQ_MODE_MSE_SIGN;
+  sizes[2] = qjl ? rows * (size_t)(cfg->qjl_m / 8) : dsign ? rows * (size_t)(cfg->head_dim / 8) : 0;
+  sizes[3] = qjl || dsign ? rows * sizeof(float) : 0;
   return TQ_OK;
 }
 
@@ -528,7 +531,7 @@ static tq_status check_gpu_common(const tq_config* cfg, const void* tables, int 
 }
 static tq_status check_planes(const tq_config* cfg, int layer, int kind, const tq_planes& p) {
   tq_layer_spec s = spec_of(cfg, layer);
-  bool qjl = kind == 0 && s.k_mode == TQ_MODE_MSE_QJL;
+  const bool qjl = kind == 0 && s.k_mode != TQ_MODE_MSE;   // QJL or Direct Sign planes
   if (!p.codes || !p.norms || p.capacity < 0) return TQ_ERR_INVALID_ARG;
   if (qjl && (!p.qjl_signs || !p.qjl_rnorm)) return TQ_ERR_INVALID_ARG;
   if (!aligned16(p.codes) || !aligned16(p.norms)) return TQ_ERR_ALIGNMENT;
@@ -574,6 +577,7 @@ static void fill_quant_codec(QuantArgs& a, const tq_config* cfg, const void* tab
   a.boundaries = (const float*)cb + 256;
   a.rot_signs = tbl_signs(cfg, tables, layer, kind);
   a.qjl = kind == 0 && s.k_mode == TQ_MODE_MSE_QJL;
+  a.dsign = kind == 0 && s.k_mode == TQ_MODE_MSE_SIGN;
   a.S = a.qjl ? tbl_qjl(cfg, tables, layer) : nullptr;
   a.m = cfg->qjl_m;
   a.err = quant_error_ptr();
@@ -679,6 +683,7 @@ extern "C" tq_status tq_append_kv(const tq_config* cfg, const void* tables, int 
       a.rot_signs[kind] = q.rot_signs;
       if (kind == 0) {
         a.qjl = q.qjl;
+        a.dsign = q.dsign;
         a.S = q.S;
         a.qjl_signs = p.qjl_signs;
         a.qjl_rnorm = p.qjl_rnorm;
@@ -759,6 +764,7 @@ extern "C" tq_status tq_dequantize(const tq_config* cfg, const void* tables, int
   a.centroids = (const float*)tbl_codebook(tables, a.bits);
   a.rot_signs = tbl_signs(cfg, tables, layer, kind);
   a.qjl = include_qjl && kind == 0 && s.k_mode == TQ_MODE_MSE_QJL;
+  a.dsign = include_qjl && kind == 0 && s.k_mode == TQ_MODE_MSE_SIGN;
   a.S = a.qjl ? tbl_qjl(cfg, tables, layer) : nullptr;
   a.m = cfg->qjl_m;
   a.dst = dst;
@@ -815,6 +821,7 @@ extern "C" tq_status tq_decode_attention(const tq_config* cfg, const void* table
   a.kb = s.k_bits;
   a.vb = s.v_bits;
   a.qjl = s.k_mode == TQ_MODE_MSE_QJL;
+  a.dsign = s.k_mode == TQ_MODE_MSE_SIGN;
   a.m = cfg->qjl_m;
   a.kwin = k_win;
   a.vwin = v_win;

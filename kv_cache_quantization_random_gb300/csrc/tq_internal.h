@@ -58,6 +58,7 @@ struct QuantArgs {
   const float* boundaries;       // [256]
   const float* rot_signs;        // [d]
   int qjl;                       // 0 | 1
+  int dsign;                     // keys in Direct Sign mode: 0 | 1
   const uint16_t* S;             // bf16 [m][d]
   int m;
   unsigned* err;                 // device error word
@@ -112,6 +113,7 @@ struct AppendArgs {
   const float* boundaries[2];
   const float* rot_signs[2];
   int qjl;                       // K in MSE+QJL mode
+  int dsign;                     // K in Direct Sign mode
   const uint16_t* S;             // bf16 [m][d]
   unsigned* err;
 };
@@ -128,6 +130,7 @@ struct DequantArgs {
   const float* centroids;
   const float* rot_signs;
   int qjl;
+  int dsign;                     // add the Direct Sign residual a (2 bits - 1)
   const uint16_t* S;
   int m;
   float* dst;
@@ -142,6 +145,7 @@ struct DecodeArgs {
   const uint8_t* kc; const float* kn; const uint8_t* ks; const float* kr; int64_t kcap;
   const uint8_t* vc; const float* vn; int64_t vcap;
   int kb, vb, qjl, m;
+  int dsign;                     // keys in Direct Sign mode
   const uint16_t* kwin; const uint16_t* vwin; int W;
   const int32_t* seq_lens;
   int n_qsplits;                 // splits over the quantized tokens

@@ -22,11 +22,14 @@ __device__ unsigned g_quant_err;
 
 // dynamic shared memory of quantize_kernel: per warp two buffers of 32 rows,
 // the search grid and the boundaries
-__host__ __device__ constexpr size_t quant_smem_bytes(bool f32, int cells) {
-  return 2 * quant_rows_bytes(f32) + (size_t)cells * 8 + 256 * 4;
+__host__ __device__ constexpr size_t quant_smem_bytes(bool f32, int cells, bool sgn) {
+  return 2 * quant_rows_bytes(f32) + (size_t)cells * 8 + 256 * 4 + (sgn ? 256 * 4 : 0);
 }
 
-template <int BITS, bool F32, bool CLAMP>
+// SGN: keys in Direct Sign mode also get the sign of every rotated residual
+// coordinate and the scale mean |r_i| ("TurboQuant KV 캐시 압축 for
+// llama.cpp", v1.1.0 "Direct Sign").
+template <int BITS, bool F32, bool CLAMP, bool SGN>
 __global__ void __launch_bounds__(kQRows, 3) quantize_kernel(const QuantArgs a) {
   constexpr int kPitch = RowCfg<F32>::kPitch;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -35,7 +38,11 @@ __global__ void __launch_bounds__(kQRows, 3) quantize_kernel(const QuantArgs a) 
   uint8_t* wrows = smem + (size_t)warp * 2 * 32 * kPitch;
   float2* grid = (float2*)(smem + 2 * quant_rows_bytes(F32));
   float* bnd = (float*)(grid + a.grid_cells);
-  for (int i = tid; i < 256; i += kQRows) bnd[i] = a.boundaries[i];
+  float* cen = bnd + 256;                               // SGN only
+  for (int i = tid; i < 256; i += kQRows) {
+    bnd[i] = a.boundaries[i];
+    if constexpr (SGN) cen[i] = a.centroids[i];
+  }
   __syncthreads();
   build_grid<BITS>(a, bnd, grid, tid, kQRows);
   __syncthreads();
@@ -73,9 +80,22 @@ __global__ void __launch_bounds__(kQRows, 3) quantize_kernel(const QuantArgs a) 
     const uint8_t* rows = wrows + buf * 32 * kPitch;
     if (valid) {
       float2 p[64];
-      const float nrm = quantize_row<BITS, F32, CLAMP, false>(
-          a, rows + lane * kPitch, grid_base, kmax, nullptr, a.codes + drow * (16 * BITS), p);
+      const float nrm = quantize_row<BITS, F32, CLAMP, SGN>(
+          a, rows + lane * kPitch, grid_base, kmax, cen, a.codes + drow * (16 * BITS), p);
       a.norms[drow] = nrm;
+      if constexpr (SGN) {
+        // p[j] = (r_j, r_{j+64}): bit i of the 128-bit sign vector is [r_i >= 0]
+        uint32_t sw[4] = {0u, 0u, 0u, 0u};
+        float asum = 0.f;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          sw[j >> 5] |= (p[j].x >= 0.f ? 1u : 0u) << (j & 31);
+          sw[2 + (j >> 5)] |= (p[j].y >= 0.f ? 1u : 0u) << (j & 31);
+          asum += fabsf(p[j].x) + fabsf(p[j].y);
+        }
+        *(uint4*)(a.qjl_signs + drow * (kD / 8)) = make_uint4(sw[0], sw[1], sw[2], sw[3]);
+        a.qjl_rnorm[drow] = asum * (1.0f / kD);
+      }
     }
     __syncwarp();      // every lane is done with this buffer before it is refilled
     buf ^= 1;
@@ -168,6 +188,24 @@ __device__ __forceinline__ void append_quantize_row(const AppendArgs& a, int kin
                           words[4 * lane + 3]);
   }
   if (lane == 0) a.norms[kind][drow] = nrm;
+  if (kind == 0 && a.dsign) {
+    // Direct Sign: bit i = [r_i >= 0] (lane l holds coordinates 4l..4l+3),
+    // scale = mean |r_i|
+    uint32_t nib = 0u;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) nib |= (r[c] >= 0.f ? 1u : 0u) << c;
+    const float asum = warp_sum(fabsf(r[0]) + fabsf(r[1]) + fabsf(r[2]) + fabsf(r[3]));
+    // lanes 8w .. 8w+7 fill word w; gather with shuffles
+    uint32_t word = nib << (4 * (lane & 7));
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) word |= __shfl_xor_sync(0xffffffffu, word, o);
+    const uint32_t w0 = __shfl_sync(0xffffffffu, word, 0), w1 = __shfl_sync(0xffffffffu, word, 8);
+    const uint32_t w2 = __shfl_sync(0xffffffffu, word, 16), w3 = __shfl_sync(0xffffffffu, word, 24);
+    if (lane == 0) {
+      *(uint4*)(a.qjl_signs + drow * (kDim / 8)) = make_uint4(w0, w1, w2, w3);
+      a.qjl_rnorm[drow] = asum * (1.0f / kDim);
+    }
+  }
   if (kind == 0 && a.qjl) {
     float g = r[0] * r[0];
     g = fmaf(r[1], r[1], g);
@@ -294,6 +332,14 @@ __global__ void __launch_bounds__(128) dequantize_kernel(const DequantArgs a) {
     if ((p & 31) + BITS > 32) c |= w[(p >> 5) + 1] << (32 - (p & 31));
     y[i] = cen[c & ((1u << BITS) - 1u)] * nrm;
   }
+  if (a.dsign) {
+    // Direct Sign residual: r_i ~= a (2 bit_i - 1), rotated domain
+    const uint4 sb4 = *(const uint4*)(a.qjl_signs + row * (kD / 8));
+    const uint32_t sb[4] = {sb4.x, sb4.y, sb4.z, sb4.w};
+    const float sc = a.qjl_rnorm[row];
+#pragma unroll
+    for (int i = 0; i < kD; ++i) y[i] += ((sb[i >> 5] >> (i & 31)) & 1u) ? sc : -sc;
+  }
   if constexpr (QJL) {
     const uint4 sb4 = *(const uint4*)(a.qjl_signs + row * (kQjlM / 8));
     const uint32_t sb[4] = {sb4.x, sb4.y, sb4.z, sb4.w};
@@ -326,10 +372,10 @@ int sm_count() {
   return n;
 }
 
-template <int BITS, bool F32>
+template <int BITS, bool F32, bool SGN>
 static int launch_q(const QuantArgs& a, cudaStream_t s) {
-  auto k = quantize_kernel<BITS, F32, (BITS > 4)>;
-  const size_t smem = quant_smem_bytes(F32, a.grid_cells);
+  auto k = quantize_kernel<BITS, F32, (BITS > 4), SGN>;
+  const size_t smem = quant_smem_bytes(F32, a.grid_cells, SGN);
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return 1;
   int per_sm = 0;
@@ -347,7 +393,8 @@ static int launch_q(const QuantArgs& a, cudaStream_t s) {
 template <int BITS>
 static int launch_q_bits(const QuantArgs& a, cudaStream_t s) {
   if (a.qjl) return launch_quantize_qjl(a, s);
-  return a.src_f32 ? launch_q<BITS, true>(a, s) : launch_q<BITS, false>(a, s);
+  if (a.dsign) return a.src_f32 ? launch_q<BITS, true, true>(a, s) : launch_q<BITS, false, true>(a, s);
+  return a.src_f32 ? launch_q<BITS, true, false>(a, s) : launch_q<BITS, false, false>(a, s);
 }
 
 int launch_quantize(const QuantArgs& a, void* stream) {

@@ -16,6 +16,8 @@ The five workloads mirror the shapes on the TurboQuant pages:
   ("윈도우용 터보퀀트(TurboQuant) 구현을 개선하다", finding 2).
 * ``qjl_b16_8k``  batch 16, 32/8 heads, 8192 tokens, keys 2-bit + 1-bit QJL
   sketch (m = 128), values 3-bit, no window.
+* ``sign_b16_8k``  the same shapes and inputs with the keys' 1-bit residual
+  term stored as Direct Sign (128 residual signs + scale) instead of QJL.
 * ``long_1m``  batch 1, 64/8 heads, 1,048,576 tokens, K3/V3, window 256,
   streaming quantize in 4096-token chunks.
 * ``serving_36l``  36 layers, layers 0-3 and 32-35 at 8 bits, the rest K4/V2;
@@ -47,6 +49,7 @@ class Workload:
     k_bits: int
     v_bits: int
     k_qjl: bool = False
+    k_sign: bool = False               # keys with the Direct Sign residual
     qjl_m: int = 128
     window: int = 0
     n_layers: int = 1
@@ -85,6 +88,9 @@ WORKLOADS = {
     "qjl_b16_8k": Workload(
         name="qjl_b16_8k", batch=16, n_q_heads=32, n_kv_heads=8, head_dim=128,
         context=8192, k_bits=2, v_bits=3, k_qjl=True, qjl_m=128, data_seed=1002),
+    "sign_b16_8k": Workload(
+        name="sign_b16_8k", batch=16, n_q_heads=32, n_kv_heads=8, head_dim=128,
+        context=8192, k_bits=2, v_bits=3, k_sign=True, data_seed=1002),
     "long_1m": Workload(
         name="long_1m", batch=1, n_q_heads=64, n_kv_heads=8, head_dim=128,
         context=1048576, k_bits=3, v_bits=3, window=256, new_tokens=4096,

@@ -23,8 +23,9 @@ def B():
     return binding()
 
 
-def _decode_case(B, *, batch, hq, hkv, seq, kb, vb, W=0, qjl=False, layer=0, n_layers=1,
-                 protect=(0, 0), q_f32=False, seed=0, dist="llama", extra_cap=0, data_seed=5):
+def _decode_case(B, *, batch, hq, hkv, seq, kb, vb, W=0, qjl=False, dsign=False, layer=0,
+                 n_layers=1, protect=(0, 0), q_f32=False, seed=0, dist="llama", extra_cap=0,
+                 data_seed=5):
     """Build a cache from seeded inputs, quantize it with the oracle, upload the
     oracle's planes, run the CUDA decode, run the oracle decode, return both."""
     import torch
@@ -40,7 +41,8 @@ def _decode_case(B, *, batch, hq, hkv, seq, kb, vb, W=0, qjl=False, layer=0, n_l
         q = q.float()
     cfg = B.Config(k_bits=kb, v_bits=vb, residual_window=W, seed=seed, n_layers=n_layers,
                    n_protect_first=protect[0], n_protect_last=protect[1],
-                   k_mode=B.TQ_MODE_MSE_QJL if qjl else B.TQ_MODE_MSE)
+                   k_mode=(B.TQ_MODE_MSE_QJL if qjl else
+                           B.TQ_MODE_MSE_SIGN if dsign else B.TQ_MODE_MSE))
     kb_l, vb_l, mode = B.tq_layer_spec_get(cfg, layer)
     tables = B.device_tables(cfg)
     K64, V64 = to64(K), to64(V)
@@ -57,6 +59,11 @@ def _decode_case(B, *, batch, hq, hkv, seq, kb, vb, W=0, qjl=False, layer=0, n_l
             qj = oracle_qjl(oqk, seed, layer)
             kp.signs_view()[:, :, :nq].copy_(torch.from_numpy(qj["packed"]))
             kp.rnorm_view()[:, :, :nq].copy_(torch.from_numpy(qj["gamma"]))
+        if mode == B.TQ_MODE_MSE_SIGN:
+            r = O.qjl_residual(oqk["y"], oqk["codes"], oqk["norm64"], oqk["c32"])
+            dbits, dscale = O.direct_sign_sketch(r)
+            kp.signs_view()[:, :, :nq].copy_(torch.from_numpy(O.pack_bits(dbits)))
+            kp.rnorm_view()[:, :, :nq].copy_(torch.from_numpy(dscale))
     # window ring per sequence: token t in slot t mod W, for t in [T_b - W, T_b)
     kw = vw = None
     kw64 = vw64 = None
@@ -83,12 +90,19 @@ def _decode_case(B, *, batch, hq, hkv, seq, kb, vb, W=0, qjl=False, layer=0, n_l
         gam = np.zeros((batch, hkv, cap), np.float32)
         bits[:, :, :nq], gam[:, :, :nq] = qj["bits"], qj["gamma"]
         qjl_arg = dict(bits=bits, gamma=gam, S=qj["S"])
+    dsign_arg = None
+    if mode == B.TQ_MODE_MSE_SIGN:
+        bits_ = np.zeros((batch, hkv, cap, 128), np.int64)
+        sc_ = np.zeros((batch, hkv, cap), np.float32)
+        if nq:
+            bits_[:, :, :nq], sc_[:, :, :nq] = dbits, dscale
+        dsign_arg = dict(bits=bits_, scale=sc_)
     ck, _ = O.codebook_fp32(kb_l, 128)
     cv, _ = O.codebook_fp32(vb_l, 128)
     ref = O.decode_attention(to64(q), kcodes, kn, vcodes, vn, ck, cv,
                              O.rotation_signs(seed, layer, 0, 128),
                              O.rotation_signs(seed, layer, 1, 128), seq, w.softmax_scale,
-                             window=W, k_win=kw64, v_win=vw64, qjl=qjl_arg)
+                             window=W, k_win=kw64, v_win=vw64, qjl=qjl_arg, dsign=dsign_arg)
     out = torch.full((batch, hq, 128), float("nan"), device="cuda")
     ws = B.new_workspace(cfg, batch, hq, hkv, Tmax)
     seq_t = torch.tensor(seq, dtype=torch.int32, device="cuda")
@@ -166,6 +180,13 @@ def test_decode_ragged_no_window_and_empty(B):
 
 def test_decode_qjl_keys(B):
     out, ref, _ = _decode_case(B, batch=3, hq=8, hkv=2, seq=[900, 64, 1], kb=2, vb=3, qjl=True)
+    assert rel_l2_per_head(out, ref).max() < TOL
+
+
+@pytest.mark.parametrize("kb,vb,W", [(2, 3, 0), (3, 3, 64), (4, 2, 16)])
+def test_decode_direct_sign_keys(B, kb, vb, W):
+    out, ref, _ = _decode_case(B, batch=3, hq=8, hkv=2, seq=[900, 64, 1], kb=kb, vb=vb, W=W,
+                               dsign=True)
     assert rel_l2_per_head(out, ref).max() < TOL
 
 

@@ -150,6 +150,33 @@ def test_quantize_qjl_keys(B):
     assert not bad.any(), int(bad.sum())
 
 
+def _check_direct_sign(P, oq, bits, rows=None):
+    """GPU signs and scale against the oracle's Direct Sign of the residual of
+    the GPU's own codes (codes may differ inside the boundary band); a sign may
+    differ only where |r_i| <= 1e-6 ||x||."""
+    sl = (slice(None), slice(None), slice(None, rows))
+    gcodes = O.unpack_codes(P.codes_view()[sl].cpu().numpy(), bits, 128)
+    r = O.qjl_residual(oq["y"], gcodes, oq["norm64"], oq["c32"])
+    sb, scale = O.direct_sign_sketch(r)
+    gbits = O.unpack_bits(P.signs_view()[sl].cpu().numpy(), 128)
+    band = np.abs(r) <= 1e-6 * oq["norm64"][..., None]
+    assert not ((gbits != sb) & ~band).any()
+    compare_norms(P.rnorm_view()[sl].cpu().numpy(), scale, rel=1e-5)
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_quantize_direct_sign_keys(B, bits):
+    from kv_cache_quantization_random_gb300 import workloads as W
+    w = W.scaled(W.get("sign_b16_8k"), batch=2, context=333)
+    K, _ = W.make_kv(w)
+    cfg = B.Config(k_bits=bits, v_bits=3, k_mode=B.TQ_MODE_MSE_SIGN, seed=4)
+    planes = _run_quantize(B, cfg, 0, 0, K.cuda())
+    oq = oracle_quantize(to64(K), bits, 4, 0, 0)
+    compare_codes(planes.codes_view().cpu().numpy(), oq, bits)
+    compare_norms(planes.norms_view().cpu().numpy(), oq["norms"])
+    _check_direct_sign(planes, oq, bits)
+
+
 @pytest.mark.parametrize("bits,qjl", [(2, False), (3, False), (4, False), (8, False), (2, True)])
 def test_dequantize_matches_oracle(B, bits, qjl):
     import torch
@@ -220,7 +247,8 @@ def test_streaming_append_with_window(B, W_):
 
 
 @pytest.mark.parametrize("kb,vb,qjl,W_", [(3, 3, False, 8), (8, 8, False, 0), (2, 3, True, 0),
-                                        (4, 2, True, 32)])
+                                        (4, 2, True, 32), (2, 3, "sign", 0),
+                                        (3, 2, "sign", 16)])
 def test_append_one_launch_and_bulk_paths(B, kb, vb, qjl, W_):
     """Appends of at most 8 tokens per sequence run as one fused launch (warp
     per vector); larger ones take the bulk quantize kernel.  Both must give the
@@ -229,7 +257,8 @@ def test_append_one_launch_and_bulk_paths(B, kb, vb, qjl, W_):
     from kv_cache_quantization_random_gb300 import workloads as W
     Bsz, H, cap = 3, 2, 80
     cfg = B.Config(k_bits=kb, v_bits=vb, residual_window=W_, seed=11,
-                   k_mode=B.TQ_MODE_MSE_QJL if qjl else B.TQ_MODE_MSE)
+                   k_mode=(B.TQ_MODE_MSE_SIGN if qjl == "sign" else
+                           B.TQ_MODE_MSE_QJL if qjl else B.TQ_MODE_MSE))
     tables = B.device_tables(cfg)
     kp = B.Planes(cfg, 0, 0, Bsz, H, cap)
     vp = B.Planes(cfg, 0, 1, Bsz, H, cap)
@@ -255,7 +284,9 @@ def test_append_one_launch_and_bulk_paths(B, kb, vb, qjl, W_):
         oq = oracle_quantize(to64(X[:, :, :nq]), bits, 11, 0, kind)
         compare_codes(P.codes_view()[:, :, :nq].cpu().numpy(), oq, bits)
         compare_norms(P.norms_view()[:, :, :nq].cpu().numpy(), oq["norms"])
-        if kind == 0 and qjl:
+        if kind == 0 and qjl == "sign":
+            _check_direct_sign(P, oq, bits, rows=nq)
+        elif kind == 0 and qjl:
             # sketch of the oracle's residual of the GPU's own codes (codes may
             # differ inside the boundary band); a sign may differ only where
             # |z_j| <= 1e-5 ||S_j|| gamma
