@@ -194,7 +194,7 @@ def algorithmic_bytes(w, seq, W):
     return total
 
 
-def build_state(B, w, device, layer=0):
+def build_state(B, w, device, layer=0, sparse_v=0):
     """Inputs, planes and window ring of the workload's context (not yet quantized)."""
     import torch
     from kv_cache_quantization_random_gb300 import workloads as WL
@@ -202,7 +202,8 @@ def build_state(B, w, device, layer=0):
     nq = T - Wn
     cfg = B.Config(k_bits=w.k_bits, v_bits=w.v_bits, residual_window=Wn, seed=w.codec_seed,
                    k_mode=(B.TQ_MODE_MSE_QJL if w.k_qjl else
-                           B.TQ_MODE_MSE_SIGN if w.k_sign else B.TQ_MODE_MSE), qjl_m=w.qjl_m)
+                           B.TQ_MODE_MSE_SIGN if w.k_sign else B.TQ_MODE_MSE), qjl_m=w.qjl_m,
+                   sparse_v=sparse_v)
     tables = B.device_tables(cfg, device)
     K, V = WL.make_kv(w, layer=layer, device=device)
     kp = B.Planes(cfg, layer, 0, w.batch, w.n_kv_heads, nq, device)
@@ -239,7 +240,7 @@ def run_ours(args, w, rank, world, local):
     peaks, peak_kind = measured_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
 
-    st = build_state(B, w, device)
+    st = build_state(B, w, device, sparse_v=args.sparse_v)
     cfg, tables, kp, vp = st["cfg"], st["tables"], st["kp"], st["vp"]
     K, V, nq, Wn, T = st["K"], st["V"], st["nq"], w.window, w.context
 
@@ -433,6 +434,7 @@ def run_ours(args, w, rank, world, local):
             "k_bits": w.k_bits, "v_bits": w.v_bits, "k_qjl": w.k_qjl, "k_sign": w.k_sign,
             "window": Wn,
             "new_tokens_per_step": 1, "parallelism": f"replicas x{world}",
+            "sparse_v": args.sparse_v,
             "l2": f"{R} cache replicas cycled ({R * cache_bytes / 1e6:.0f} MB > 4 x L2 {l2 / 1e6:.0f} MB)",
             "graph_steps": S,
         },
@@ -632,6 +634,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-max-steps", type=int, default=200)
+    ap.add_argument("--sparse-v", type=int, default=0,
+                    help="skip a 32-token chunk's V sum when all its softmax weights are below "
+                         "2^-N of the running maximum (0: exact, the default)")
     ap.add_argument("--decode-traffic", type=float, default=None,
                     help="dram bytes per decode launch from an ncu capture of the current kernel")
     args = ap.parse_args()

@@ -101,6 +101,13 @@ typedef enum { TQ_KIND_K = 0, TQ_KIND_V = 1 } tq_kind;
  *   residual_window  W >= 0: the last W tokens of a sequence stay bf16.
  *   density          TQ_DENSITY_GAUSSIAN (N(0,1/d)); SPHERE_BETA is the exact
  *                    coordinate density of a uniform unit vector.
+ *   sparse_v         0: exact.  k in 1..120: decode skips the V sum of a 32-token
+ *                    chunk when every softmax weight of the chunk is below 2^-k
+ *                    of the running maximum (the sparse-V dequant skip that
+ *                    "[GitHub 탐방] TurboQuant 3-bit KV 캐시 압축 — 단일 GPU 재현
+ *                    기록" cites from a llama.cpp extension); the softmax
+ *                    denominator still counts those tokens.  MSE-only keys
+ *                    (TQ_ERR_UNSUPPORTED with a key residual term).
  *   seed             seeds every random sign vector and QJL matrix. */
 typedef struct {
   int32_t head_dim;
@@ -114,7 +121,7 @@ typedef struct {
   int32_t protect_bits;
   int32_t residual_window;
   int32_t density;
-  int32_t reserved;
+  int32_t sparse_v;
   uint64_t seed;
 } tq_config;
 

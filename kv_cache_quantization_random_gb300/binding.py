@@ -50,7 +50,7 @@ class tq_config(C.Structure):
                 ("v_bits", C.c_int32), ("k_mode", C.c_int32), ("qjl_m", C.c_int32),
                 ("n_protect_first", C.c_int32), ("n_protect_last", C.c_int32),
                 ("protect_bits", C.c_int32), ("residual_window", C.c_int32),
-                ("density", C.c_int32), ("reserved", C.c_int32), ("seed", C.c_uint64)]
+                ("density", C.c_int32), ("sparse_v", C.c_int32), ("seed", C.c_uint64)]
 
 
 class tq_layer_spec(C.Structure):
@@ -135,11 +135,12 @@ class Config:
     residual_window: int = 0
     density: int = TQ_DENSITY_GAUSSIAN
     seed: int = 0
+    sparse_v: int = 0
 
     def c(self) -> tq_config:
         return tq_config(self.head_dim, self.n_layers, self.k_bits, self.v_bits, self.k_mode,
                          self.qjl_m, self.n_protect_first, self.n_protect_last,
-                         self.protect_bits, self.residual_window, self.density, 0,
+                         self.protect_bits, self.residual_window, self.density, self.sparse_v,
                          self.seed & ((1 << 64) - 1))
 
 

@@ -364,7 +364,7 @@ __device__ __forceinline__ void qjl_scores(uint32_t sa, uint32_t sb, const uint3
   }
 }
 
-template <int G, int KB, int VB, int RES>
+template <int G, int KB, int VB, int RES, bool SPARSE>
 __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
   constexpr int KROW = 16 * KB, VROW = 16 * VB;
   __shared__ __align__(16) uint32_t lutk[256];   // K centroid tables (see kpair)
@@ -730,7 +730,7 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
       m0 = mn0;
       m1 = mn1;
       float w[2][4];
-      float wloc = 0.f, ps0 = 0.f, ps1 = 0.f;
+      float wloc = 0.f, ploc = 0.f, ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
         const int ta = 16 * mt + mg, tb = ta + 8;
@@ -739,6 +739,7 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
         const float p2 = exp2f(sc[mt][2] - mn0), p3 = exp2f(sc[mt][3] - mn1);
         ps0 += p0 + p2;
         ps1 += p1 + p3;
+        if constexpr (SPARSE) ploc = fmaxf(ploc, fmaxf(fmaxf(p0, p1), fmaxf(p2, p3)));
         w[mt][0] = p0 * va;
         w[mt][1] = p1 * va;
         w[mt][2] = p2 * vb;
@@ -747,6 +748,10 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
       }
       l0 = fmaf(l0, al0, ps0);
       l1 = fmaf(l1, al1, ps1);
+      // sparse V: when every weight of the chunk is below the threshold
+      // (relative to the running maximum), only the accumulator is rescaled
+      bool skip_v = false;
+      if constexpr (SPARSE) skip_v = warp_max(ploc) < a.sparse_thr;
       const float wmax = warp_max(wloc);
       // fp16 weights scaled into range: the largest is 16384 (capped at 2^64
       // so that the accumulator, kept in the scale of the latest chunk, stays finite)
@@ -754,11 +759,11 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
         const int ta = 16 * mt + mg, tb = ta + 8;
-        if (h0ok) {
+        if (h0ok && !skip_v) {
           ws16[(2 * tig) * 32 + ta] = (uint16_t)h16(w[mt][0] * scl);
           ws16[(2 * tig) * 32 + tb] = (uint16_t)h16(w[mt][2] * scl);
         }
-        if (h1ok) {
+        if (h1ok && !skip_v) {
           ws16[(2 * tig + 1) * 32 + ta] = (uint16_t)h16(w[mt][1] * scl);
           ws16[(2 * tig + 1) * 32 + tb] = (uint16_t)h16(w[mt][3] * scl);
         }
@@ -766,8 +771,8 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
       __syncwarp();
       // ---- rotated-domain V sum on the tensor cores: d holds the sum times
       // the current chunk's weight scale; rescale, then d += V^T W
-      const float rs = scl / dscale;
-      dscale = scl;
+      const float rs = skip_v ? 1.f : scl / dscale;
+      if (!skip_v) dscale = scl;
       const float2 pre = make_float2(al0 * rs, al1 * rs);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
@@ -777,7 +782,7 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
       }
       const uint8_t* vb_ = wreg + L.vbuf + slot * 32 * VROW;
 #pragma unroll
-      for (int kt = 0; kt < 2; ++kt) {
+      for (int kt = 0; kt < 2 && !skip_v; ++kt) {
         const uint32_t b0 = mg < G ? *(const uint32_t*)(ws16 + mg * 32 + 16 * kt + 2 * tig) : 0u;
         const uint32_t b1 = mg < G ? *(const uint32_t*)(ws16 + mg * 32 + 16 * kt + 2 * tig + 8) : 0u;
         vmma_ktile<VB>(vb_, lutv, kt, mg, tig, b0, b1, d);
@@ -996,9 +1001,9 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
 }
 
 
-template <int G, int KB, int VB, int RES>
+template <int G, int KB, int VB, int RES, bool SPARSE = false>
 int launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
-  auto k = decode_kernel<G, KB, VB, RES>;
+  auto k = decode_kernel<G, KB, VB, RES, SPARSE>;
   const size_t smem = (size_t)DecodeSmem(G, RES, KB, VB).total;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return 1;
@@ -1045,6 +1050,24 @@ int launch_decode_g(const DecodeArgs& a, cudaStream_t s) {
         case 4: { TQ_VB_CASES(4, 2) }
       }
     }
+    return 1;
+  }
+  if (a.sparse_thr > 0.f) {
+#define TQ_VB_SPARSE(KB_)                                                    \
+  switch (a.vb) {                                                          \
+    case 2: return launch_decode_t<G, KB_, 2, 0, true>(a, s);              \
+    case 3: return launch_decode_t<G, KB_, 3, 0, true>(a, s);              \
+    case 4: return launch_decode_t<G, KB_, 4, 0, true>(a, s);              \
+    case 8: return launch_decode_t<G, KB_, 8, 0, true>(a, s);              \
+  }                                                                        \
+  return 1;
+    switch (a.kb) {
+      case 2: { TQ_VB_SPARSE(2) }
+      case 3: { TQ_VB_SPARSE(3) }
+      case 4: { TQ_VB_SPARSE(4) }
+      case 8: { TQ_VB_SPARSE(8) }
+    }
+#undef TQ_VB_SPARSE
     return 1;
   }
   switch (a.kb) {

@@ -282,6 +282,7 @@ static tq_status check_config(const tq_config* cfg) {
   if (cfg->residual_window < 0 || cfg->residual_window > (1 << 20)) return TQ_ERR_INVALID_ARG;
   if (cfg->density != TQ_DENSITY_GAUSSIAN && cfg->density != TQ_DENSITY_SPHERE_BETA)
     return TQ_ERR_INVALID_ARG;
+  if (cfg->sparse_v < 0 || cfg->sparse_v > 120) return TQ_ERR_INVALID_ARG;
   return TQ_OK;
 }
 
@@ -822,6 +823,8 @@ extern "C" tq_status tq_decode_attention(const tq_config* cfg, const void* table
   a.vb = s.v_bits;
   a.qjl = s.k_mode == TQ_MODE_MSE_QJL;
   a.dsign = s.k_mode == TQ_MODE_MSE_SIGN;
+  a.sparse_thr = cfg->sparse_v > 0 ? std::ldexp(1.0f, -cfg->sparse_v) : 0.0f;
+  if (a.sparse_thr > 0.f && (a.qjl || a.dsign)) return TQ_ERR_UNSUPPORTED;   // MSE keys only
   a.m = cfg->qjl_m;
   a.kwin = k_win;
   a.vwin = v_win;

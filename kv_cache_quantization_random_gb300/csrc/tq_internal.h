@@ -146,6 +146,7 @@ struct DecodeArgs {
   const uint8_t* vc; const float* vn; int64_t vcap;
   int kb, vb, qjl, m;
   int dsign;                     // keys in Direct Sign mode
+  float sparse_thr;              // skip a chunk's V sum below this weight (0: never)
   const uint16_t* kwin; const uint16_t* vwin; int W;
   const int32_t* seq_lens;
   int n_qsplits;                 // splits over the quantized tokens

@@ -190,6 +190,27 @@ def test_decode_direct_sign_keys(B, kb, vb, W):
     assert rel_l2_per_head(out, ref).max() < TOL
 
 
+def test_decode_sparse_v_skip_stays_within_tolerance(B):
+    """sparse_v = 20: the V sum of a 32-token chunk whose softmax weights are
+    all below 2^-20 of the running maximum is skipped.  The output stays within
+    the parity bar of the exact oracle, and close to the exact GPU output."""
+    import copy
+    import torch
+    out, ref, c = _decode_case(B, batch=2, hq=8, hkv=2, seq=[4000, 2500], kb=4, vb=2, W=32)
+    scfg = copy.copy(c["cfg"])
+    scfg.sparse_v = 20
+    got = torch.empty(2, 8, 128, device="cuda")
+    B.tq_decode_attention(scfg, c["tables"], 0, c["q"].cuda(), c["scale"], c["kp"], c["vp"],
+                          c["seq_t"], c["Tmax"], got, c["ws"], k_win=c["kw"], v_win=c["vw"])
+    torch.cuda.synchronize()
+    assert B.tq_get_device_error() == B.TQ_OK
+    g = to64(got)
+    assert rel_l2_per_head(g, ref).max() < TOL
+    # the skipped weights are each below 2^-20 of the largest: the change is
+    # far below the codec's own error
+    assert rel_l2_per_head(g, out).max() < 1e-4
+
+
 def test_decode_protected_layers(B):
     for layer in (0, 5, 11):
         out, ref, _ = _decode_case(B, batch=2, hq=8, hkv=2, seq=[600, 1200], kb=4, vb=2,
