@@ -50,7 +50,7 @@ __all__ = [
     "quantize_vectors", "near_boundary", "pack_codes", "unpack_codes",
     "pack_bits", "unpack_bits", "qjl_residual", "qjl_sketch",
     "qjl_inner_product_estimate", "direct_sign_sketch", "direct_sign_estimate", "dequantize", "dequantize_qjl",
-    "layer_bits", "softmax", "decode_attention", "exact_attention",
+    "layer_bits", "softmax", "decode_attention", "decode_attention_multi", "exact_attention",
 ]
 
 # --------------------------------------------------------------------------
@@ -656,6 +656,57 @@ def decode_attention(q, k_codes, k_norms, v_codes, v_norms, ck32, cv32,
                 vw = np.asarray(v_win[b, kh, slots], dtype=np.float64)
                 o = o + p[nq:] @ vw
             out[b, h] = o
+    return out
+
+
+def decode_attention_multi(q, k_codes, k_norms, v_codes, v_norms, ck32, cv32,
+                           signs_k, signs_v, seq_lens, scale, window=0,
+                           k_win=None, v_win=None):
+    """Several query tokens per sequence at once (speculative verification,
+    chunked decode): q [B, Hq, n_q, d]; query j of sequence b is the token at
+    position T_b - n_q + j and attends causally to tokens t <= T_b - n_q + j.
+    The cache is the same as for decode_attention (tokens t < T_b - W in the
+    codes, the last W in the window ring).  Returns fp64 [B, Hq, n_q, d]."""
+    q = np.asarray(q, dtype=np.float64)
+    B, Hq, nQ, d = q.shape
+    Hkv = k_codes.shape[1]
+    g = Hq // Hkv
+    RK = rotation_matrix(np.asarray(signs_k, dtype=np.float64))
+    RV = rotation_matrix(np.asarray(signs_v, dtype=np.float64))
+    ck = np.asarray(ck32, dtype=np.float64)
+    cv = np.asarray(cv32, dtype=np.float64)
+    out = np.zeros((B, Hq, nQ, d))
+    for b in range(B):
+        T = int(seq_lens[b])
+        nq = max(T - window, 0)
+        for h in range(Hq):
+            kh = h // g
+            for j in range(nQ):
+                last = T - nQ + j                  # last visible position
+                if last < 0:
+                    continue
+                qv = q[b, h, j]
+                q_rot = RK @ qv
+                nqv = min(nq, last + 1)            # visible quantized tokens
+                win = [t for t in range(nq, T) if t <= last]
+                scores = []
+                if nqv > 0:
+                    kc = np.asarray(k_codes[b, kh, :nqv])
+                    scores.append(scale * np.asarray(k_norms[b, kh, :nqv], dtype=np.float64) *
+                                  (ck[kc] @ q_rot))
+                if win:
+                    kw = np.asarray(k_win[b, kh, [t % window for t in win]], dtype=np.float64)
+                    scores.append(scale * (kw @ qv))
+                p = softmax(np.concatenate(scores))
+                o = np.zeros(d)
+                if nqv > 0:
+                    vc = np.asarray(v_codes[b, kh, :nqv])
+                    w = p[:nqv] * np.asarray(v_norms[b, kh, :nqv], dtype=np.float64)
+                    o = o + RV.T @ (w @ cv[vc])
+                if win:
+                    vw = np.asarray(v_win[b, kh, [t % window for t in win]], dtype=np.float64)
+                    o = o + p[nqv:] @ vw
+                out[b, h, j] = o
     return out
 
 

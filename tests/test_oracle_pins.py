@@ -561,3 +561,50 @@ def test_direct_sign_error_variance_is_0_23_of_qjl_at_m_equal_d():
     ratio = np.var(e_ds) / np.var(e_qjl)
     assert 0.20 < ratio < 0.26, ratio
     assert (1 - 2 / math.pi) / (math.pi / 2) == pytest.approx(0.2313, abs=1e-4)
+
+
+# ------------------------------------------------------------ multi-query decode
+def _tiny_cache(T, W, d=16, seed=41):
+    rng = np.random.default_rng(seed)
+    K = rng.standard_normal((1, 1, T, d))
+    V = rng.standard_normal((1, 1, T, d))
+    ck, bk = O.codebook_fp32(3, d)
+    cv, bv = O.codebook_fp32(3, d)
+    sk = O.rotation_signs(1, 0, 0, d)
+    sv = O.rotation_signs(1, 0, 1, d)
+    nq = T - W
+    qk = O.quantize_vectors(K[:, :, :nq], ck, bk, sk)
+    qv = O.quantize_vectors(V[:, :, :nq], cv, bv, sv)
+    kw = np.zeros((1, 1, max(W, 1), d))
+    vw = np.zeros_like(kw)
+    for t in range(nq, T):
+        kw[0, 0, t % W] = K[0, 0, t]
+        vw[0, 0, t % W] = V[0, 0, t]
+    return dict(K=K, V=V, ck=ck, cv=cv, sk=sk, sv=sv, qk=qk, qv=qv, kw=kw, vw=vw, nq=nq)
+
+
+def test_multi_query_with_one_query_is_single_query_decode():
+    c = _tiny_cache(T=40, W=8)
+    q = np.random.default_rng(42).standard_normal((1, 2, 1, 16))
+    a = O.decode_attention_multi(q, c["qk"]["codes"], c["qk"]["norms"], c["qv"]["codes"],
+                                 c["qv"]["norms"], c["ck"], c["cv"], c["sk"], c["sv"], [40], 0.25,
+                                 window=8, k_win=c["kw"], v_win=c["vw"])
+    b = O.decode_attention(q[:, :, 0], c["qk"]["codes"], c["qk"]["norms"], c["qv"]["codes"],
+                           c["qv"]["norms"], c["ck"], c["cv"], c["sk"], c["sv"], [40], 0.25,
+                           window=8, k_win=c["kw"], v_win=c["vw"])
+    assert np.allclose(a[:, :, 0], b, rtol=0, atol=1e-14)
+
+
+def test_multi_query_is_causal_over_the_window():
+    # query j sees exactly the tokens up to T - n_q + j: with every token in
+    # the window (W >= T) this is exact causal attention, brute force
+    T, nQ = 12, 3
+    c = _tiny_cache(T=T, W=T)
+    q = np.random.default_rng(43).standard_normal((1, 1, nQ, 16))
+    got = O.decode_attention_multi(q, c["qk"]["codes"], c["qk"]["norms"], c["qv"]["codes"],
+                                   c["qv"]["norms"], c["ck"], c["cv"], c["sk"], c["sv"], [T], 0.3,
+                                   window=T, k_win=c["kw"], v_win=c["vw"])
+    for j in range(nQ):
+        last = T - nQ + j
+        ref = O.exact_attention(q[:, :, j], c["K"][:, :, :last + 1], c["V"][:, :, :last + 1], 0.3)
+        assert np.allclose(got[:, :, j], ref, rtol=0, atol=1e-12)
