@@ -259,6 +259,27 @@ tq_status tq_decode_attention(const tq_config* cfg, const void* tables, int laye
                               float* out, void* workspace, size_t workspace_bytes,
                               void* stream);
 
+/* Decode attention for n_queries query tokens per sequence at once
+ * (speculative-draft verification, chunked decode; the multi-column path of
+ * "TurboQuant KV 캐시 압축 for llama.cpp", v1.1.0 bug fixes: ncols = 2 for
+ * prompt evaluation).  Query token j
+ * of sequence b sits at position T_b - n_queries + j and attends causally to
+ * tokens t <= T_b - n_queries + j of the same cache.
+ *   q     device [batch][n_q_heads][n_queries][head_dim], dtype q_dtype.
+ *   out   device fp32 [batch][n_q_heads][n_queries][head_dim].
+ *   workspace  >= tq_workspace_bytes(cfg, batch, n_q_heads * n_queries,
+ *         n_kv_heads, max_seq_len).
+ * The tokens some query may not see must be window tokens: residual_window
+ * >= n_queries - 1, else TQ_ERR_UNSUPPORTED; (n_q_heads / n_kv_heads) *
+ * n_queries in {1, 2, 4, 8}, else TQ_ERR_UNSUPPORTED.  Other arguments and
+ * errors as tq_decode_attention (which is this call with n_queries = 1). */
+tq_status tq_decode_attention_multi(const tq_config* cfg, const void* tables, int layer,
+                                    const void* q, int q_dtype, float softmax_scale, int batch,
+                                    int n_q_heads, int n_kv_heads, int n_queries, tq_planes k,
+                                    tq_planes v, const uint16_t* k_win, const uint16_t* v_win,
+                                    const int32_t* seq_lens, int max_seq_len, float* out,
+                                    void* workspace, size_t workspace_bytes, void* stream);
+
 /* Synchronize `stream`, then read and clear the device error words.
  * Returns TQ_OK, TQ_ERR_DEVICE_TIMEOUT, TQ_ERR_DEVICE_BOUNDS or TQ_ERR_CUDA. */
 tq_status tq_get_device_error(void* stream);

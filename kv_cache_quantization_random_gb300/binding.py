@@ -35,7 +35,7 @@ EXPORTED = [
     "tq_make_qjl_matrix", "tq_tables_bytes", "tq_build_tables", "tq_plane_bytes",
     "tq_workspace_bytes", "tq_workspace_init", "tq_quantize_kv", "tq_append_kv",
     "tq_dequantize", "tq_decode_attention", "tq_get_device_error", "tq_set_wait_limit",
-    "tq_set_fault_injection", "tq_decode_attention_noalloc",
+    "tq_set_fault_injection", "tq_decode_attention_noalloc", "tq_decode_attention_multi",
 ]
 
 
@@ -106,6 +106,8 @@ def load(build_if_missing: bool = False):
         "tq_set_fault_injection": (None, [I]),
         "tq_decode_attention_noalloc": (I, [cfgp, P, I, P, I, F, I, I, I, tq_planes, tq_planes,
                                             P, P, P, I, P, P]),
+        "tq_decode_attention_multi": (I, [cfgp, P, I, P, I, F, I, I, I, I, tq_planes, tq_planes,
+                                          P, P, P, I, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -324,6 +326,20 @@ def tq_decode_attention(cfg: Config, tables, layer: int, q, softmax_scale: float
         seq_lens.data_ptr(), max_seq_len, out.data_ptr(), workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _stream_ptr(stream))
     _check(st, "tq_decode_attention")
+
+
+def tq_decode_attention_multi(cfg: Config, tables, layer: int, q, softmax_scale: float,
+                              k: Planes, v: Planes, seq_lens, max_seq_len: int, out, workspace,
+                              k_win=None, v_win=None, stream=None):
+    """q [B, Hq, n_queries, d] -> out [B, Hq, n_queries, d]: causal decode of
+    n_queries query tokens per sequence (workspace sized for Hq * n_queries)."""
+    B, Hq, nQ, _ = q.shape
+    st = load().tq_decode_attention_multi(
+        C.byref(cfg.c()), tables.data_ptr(), layer, q.data_ptr(), _dtype_code(q),
+        float(softmax_scale), B, Hq, k.n_kv_heads, nQ, k.c(), v.c(), _ptr(k_win), _ptr(v_win),
+        seq_lens.data_ptr(), max_seq_len, out.data_ptr(), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    _check(st, "tq_decode_attention_multi")
 
 
 def tq_decode_attention_noalloc(cfg: Config, tables, layer: int, q, softmax_scale: float,

@@ -873,6 +873,9 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
         const float vx[4] = {bf16lo(vw[u].x), bf16hi(vw[u].x), bf16lo(vw[u].y), bf16hi(vw[u].y)};
 #pragma unroll
         for (int g = 0; g < G; ++g) {
+          // several query tokens per sequence: column g is query token g % n_q
+          // at position T - n_q + g % n_q, which sees tokens up to itself
+          if (a.n_q > 1 && tw0 + k0 + u * kDWarps > T - a.n_q + g % a.n_q) continue;
           float part = 0.f;
 #pragma unroll
           for (int j = 0; j < 4; ++j) part = fmaf(qo[(4 * lane + j) * G + g], kx[j], part);

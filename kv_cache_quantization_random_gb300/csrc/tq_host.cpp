@@ -772,20 +772,28 @@ extern "C" tq_status tq_dequantize(const tq_config* cfg, const void* tables, int
   return launch_dequantize(a, stream) == 0 ? TQ_OK : TQ_ERR_CUDA;
 }
 
-extern "C" tq_status tq_decode_attention(const tq_config* cfg, const void* tables, int layer,
-                                         const void* q, int q_dtype, float softmax_scale,
-                                         int batch, int n_q_heads, int n_kv_heads, tq_planes k,
-                                         tq_planes v, const uint16_t* k_win,
-                                         const uint16_t* v_win, const int32_t* seq_lens,
-                                         int max_seq_len, float* out, void* workspace,
-                                         size_t workspace_bytes, void* stream) {
+// Decode with n_queries query tokens per sequence: the n_queries query
+// vectors of a query head are laid out contiguously ([B][Hq][n_queries][d]),
+// so the kernel sees n_q_heads * n_queries query columns in groups of
+// G * n_queries per kv-head, and masks window tokens causally per column.
+namespace tq {
+static tq_status decode_common(const tq_config* cfg, const void* tables, int layer, const void* q,
+                               int q_dtype, float softmax_scale, int batch, int n_q_heads,
+                               int n_kv_heads, int n_queries, tq_planes k, tq_planes v,
+                               const uint16_t* k_win, const uint16_t* v_win,
+                               const int32_t* seq_lens, int max_seq_len, float* out,
+                               void* workspace, size_t workspace_bytes, void* stream) {
   tq_status st = check_gpu_common(cfg, tables, layer);
   if (st != TQ_OK) return st;
   if (batch < 0 || n_kv_heads < 1 || n_q_heads < n_kv_heads || n_q_heads % n_kv_heads != 0 ||
-      max_seq_len < 0)
+      max_seq_len < 0 || n_queries < 1)
     return TQ_ERR_INVALID_ARG;
-  int G = n_q_heads / n_kv_heads;
+  const int G = n_q_heads / n_kv_heads * n_queries;   // query columns per kv-head
   if (G != 1 && G != 2 && G != 4 && G != 8) return TQ_ERR_UNSUPPORTED;
+  // the tokens that some query must not see (the last n_queries - 1) have to
+  // be window tokens
+  if (n_queries > 1 && cfg->residual_window < n_queries - 1) return TQ_ERR_UNSUPPORTED;
+  n_q_heads *= n_queries;
   if (q_dtype != TQ_BF16 && q_dtype != TQ_F32) return TQ_ERR_INVALID_ARG;
   if (!(std::isfinite(softmax_scale))) return TQ_ERR_INVALID_ARG;
   if (batch == 0) return TQ_OK;
@@ -844,6 +852,7 @@ extern "C" tq_status tq_decode_attention(const tq_config* cfg, const void* table
   a.err = decode_error_ptr();
   a.wait_limit = g_wait_limit;
   a.extra_tx = g_fault_injection == 1 ? 16u : 0u;
+  a.n_q = n_queries;
   if (p.n_splits == 0) {
     // every sequence is empty: the output is zero
     if (cudaMemsetAsync(out, 0, (size_t)batch * n_q_heads * kHeadDim * sizeof(float),
@@ -852,6 +861,29 @@ extern "C" tq_status tq_decode_attention(const tq_config* cfg, const void* table
     return TQ_OK;
   }
   return launch_decode(a, stream) == 0 ? TQ_OK : TQ_ERR_CUDA;
+}
+}  // namespace tq
+
+extern "C" tq_status tq_decode_attention(const tq_config* cfg, const void* tables, int layer,
+                                         const void* q, int q_dtype, float softmax_scale,
+                                         int batch, int n_q_heads, int n_kv_heads, tq_planes k,
+                                         tq_planes v, const uint16_t* k_win,
+                                         const uint16_t* v_win, const int32_t* seq_lens,
+                                         int max_seq_len, float* out, void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+  return decode_common(cfg, tables, layer, q, q_dtype, softmax_scale, batch, n_q_heads,
+                       n_kv_heads, 1, k, v, k_win, v_win, seq_lens, max_seq_len, out, workspace,
+                       workspace_bytes, stream);
+}
+
+extern "C" tq_status tq_decode_attention_multi(
+    const tq_config* cfg, const void* tables, int layer, const void* q, int q_dtype,
+    float softmax_scale, int batch, int n_q_heads, int n_kv_heads, int n_queries, tq_planes k,
+    tq_planes v, const uint16_t* k_win, const uint16_t* v_win, const int32_t* seq_lens,
+    int max_seq_len, float* out, void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_common(cfg, tables, layer, q, q_dtype, softmax_scale, batch, n_q_heads,
+                       n_kv_heads, n_queries, k, v, k_win, v_win, seq_lens, max_seq_len, out,
+                       workspace, workspace_bytes, stream);
 }
 
 extern "C" tq_status tq_get_device_error(void* stream) {

@@ -147,6 +147,7 @@ struct DecodeArgs {
   int kb, vb, qjl, m;
   int dsign;                     // keys in Direct Sign mode
   float sparse_thr;              // skip a chunk's V sum below this weight (0: never)
+  int n_q;                       // query tokens per sequence (columns g: token g % n_q)
   const uint16_t* kwin; const uint16_t* vwin; int W;
   const int32_t* seq_lens;
   int n_qsplits;                 // splits over the quantized tokens

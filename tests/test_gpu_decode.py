@@ -289,3 +289,70 @@ def test_fault_injection_times_out_and_context_stays_usable(B):
                           c["seq_t"], c["Tmax"], out, c["ws"], k_win=c["kw"], v_win=c["vw"])
     assert B.tq_get_device_error() == B.TQ_OK
     assert rel_l2_per_head(to64(out), ref).max() < TOL
+
+
+@pytest.mark.parametrize("hq,hkv,nq_tok,W", [(8, 2, 2, 16), (4, 2, 4, 8), (2, 2, 8, 64), (8, 8, 1, 0)])
+def test_decode_multi_query_matches_causal_oracle(B, hq, hkv, nq_tok, W):
+    """n_queries query tokens per sequence at once: query j sees tokens up to
+    T - n_queries + j; against the oracle's causal multi-query decode."""
+    import torch
+    from kv_cache_quantization_random_gb300 import workloads as W_
+    seq = np.array([700, 300, max(nq_tok, 5)], dtype=np.int64)
+    batch, Tmax = len(seq), int(seq.max())
+    w = W_.scaled(W_.get("llama8b_32k"), batch=batch, n_q_heads=hq, n_kv_heads=hkv,
+                  context=Tmax, data_seed=9)
+    K, V = W_.make_kv(w)
+    gen = torch.Generator().manual_seed(77)
+    q = torch.randn(batch, hq, nq_tok, 128, generator=gen).to(torch.bfloat16)
+    cfg = B.Config(k_bits=4, v_bits=2, residual_window=W, seed=3)
+    tables = B.device_tables(cfg)
+    nq = max(Tmax - W, 0)
+    kp = B.Planes(cfg, 0, 0, batch, hkv, max(nq, 1))
+    vp = B.Planes(cfg, 0, 1, batch, hkv, max(nq, 1))
+    if nq:
+        B.tq_quantize_kv(cfg, tables, 0, 0, K[:, :, :nq].cuda(), kp)
+        B.tq_quantize_kv(cfg, tables, 0, 1, V[:, :, :nq].cuda(), vp)
+    kw = vw = None
+    kw64 = vw64 = None
+    if W:
+        kw = torch.zeros(batch, hkv, W, 128, dtype=torch.bfloat16)
+        vw = torch.zeros_like(kw)
+        for b in range(batch):
+            for t in range(max(int(seq[b]) - W, 0), int(seq[b])):
+                kw[b, :, t % W] = K[b, :, t]
+                vw[b, :, t % W] = V[b, :, t]
+        kw64, vw64 = to64(kw), to64(vw)
+        kw, vw = kw.cuda(), vw.cuda()
+    out = torch.full((batch, hq, nq_tok, 128), float("nan"), device="cuda")
+    ws = B.new_workspace(cfg, batch, hq * nq_tok, hkv, Tmax)
+    seq_t = torch.tensor(seq, dtype=torch.int32, device="cuda")
+    B.tq_decode_attention_multi(cfg, tables, 0, q.cuda(), w.softmax_scale, kp, vp, seq_t, Tmax,
+                                out, ws, k_win=kw, v_win=vw)
+    torch.cuda.synchronize()
+    assert B.tq_get_device_error() == B.TQ_OK
+    oqk = oracle_quantize(to64(K[:, :, :nq]), 4, 3, 0, 0)
+    oqv = oracle_quantize(to64(V[:, :, :nq]), 2, 3, 0, 1)
+    ref = O.decode_attention_multi(to64(q), oqk["codes"], oqk["norms"], oqv["codes"],
+                                   oqv["norms"], oqk["c32"], oqv["c32"], oqk["signs"], oqv["signs"],
+                                   seq, w.softmax_scale, window=W, k_win=kw64, v_win=vw64)
+    got = to64(out)
+    assert np.all(np.isfinite(got))
+    rel = np.linalg.norm(got - ref, axis=-1) / np.linalg.norm(ref, axis=-1)
+    assert rel.max() < TOL
+
+
+def test_decode_multi_query_needs_the_hidden_tokens_in_the_window(B):
+    import torch
+    cfg = B.Config(k_bits=4, v_bits=2, residual_window=2)
+    tables = B.device_tables(cfg)
+    kp = B.Planes(cfg, 0, 0, 1, 2, 64)
+    vp = B.Planes(cfg, 0, 1, 1, 2, 64)
+    q = torch.zeros(1, 2, 4, 128, dtype=torch.bfloat16, device="cuda")     # 4 columns per kv-head
+    out = torch.empty(1, 2, 4, 128, device="cuda")
+    ws = B.new_workspace(cfg, 1, 8, 2, 66)
+    kw = torch.zeros(1, 2, 2, 128, dtype=torch.bfloat16, device="cuda")
+    seq = torch.tensor([66], dtype=torch.int32, device="cuda")
+    with pytest.raises(B.TQError) as e:      # n_queries = 4 needs W >= 3
+        B.tq_decode_attention_multi(cfg, tables, 0, q, 1.0, kp, vp, seq, 66, out, ws,
+                                    k_win=kw, v_win=kw)
+    assert e.value.status == 2
