@@ -384,6 +384,33 @@ def run_ours(args, w, rank, world, local):
         raise RuntimeError("device error during timed steps")
     dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
 
+    # ---- optional: several query tokens per sequence (speculative verify)
+    multi = None
+    if args.n_queries > 1:
+        nQ = args.n_queries
+        gq = torch.Generator(device=device)
+        gq.manual_seed(w.data_seed * 7 + nQ)
+        qm = torch.randn((w.batch, w.n_q_heads, nQ, w.head_dim), generator=gq, device=device,
+                         dtype=torch.float32).to(torch.bfloat16)
+        outm = torch.empty(w.batch, w.n_q_heads, nQ, w.head_dim, device=device)
+        wsm = B.new_workspace(cfg, w.batch, w.n_q_heads * nQ, w.n_kv_heads, Tmax, device)
+
+        def decode_multi(r):
+            kr, vr, kwr, vwr = reps[r]
+            B.tq_decode_attention_multi(cfg, tables, 0, qm, w.softmax_scale, kr, vr, seq_t, Tmax,
+                                        outm, wsm, k_win=kwr, v_win=vwr)
+
+        for i in range(3):
+            decode_multi(i % R)
+        g_multi = capture(lambda i: decode_multi(i % R))
+        g_multi.replay()
+        torch.cuda.synchronize()
+        mq_ms = time_graph(g_multi, reps_t)
+        mq_bytes = dec_bytes + len(seq) * w.n_q_heads * (nQ - 1) * w.head_dim * (2 + 4)
+        multi = {"n_queries": nQ, "ms": mq_ms, "gbs": mq_bytes / (mq_ms * 1e-3) / 1e9,
+                 "query_token_attends_per_s": nQ * tokens_per_step / (mq_ms * 1e-3),
+                 "vs_single_query_ms": dec_ms}
+
     # ---- end to end through the public API with host buffers
     qh = q.cpu().pin_memory()
     kh = knew.cpu().pin_memory()
@@ -459,6 +486,8 @@ def run_ours(args, w, rank, world, local):
         "clocks": clocks.summary(),
         "parity": parity,
     }
+    if multi is not None:
+        res["multi_query"] = multi
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w, st, q, seq, budget_s=args.cpu_seconds)
     return res
@@ -634,6 +663,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-max-steps", type=int, default=200)
+    ap.add_argument("--n-queries", type=int, default=1,
+                    help="also time decode of N query tokens per sequence (causal, in the window)")
     ap.add_argument("--sparse-v", type=int, default=0,
                     help="skip a 32-token chunk's V sum when all its softmax weights are below "
                          "2^-N of the running maximum (0: exact, the default)")
