@@ -676,6 +676,7 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
       const uint8_t* kb_ = wreg + L.kbuf + slot * 32 * KROW;
       const float* kn_ = (const float*)(wreg + L.kn + slot * 128);
       const float* vn_ = (const float*)(wreg + L.vn + slot * 128);
+      const float vmax = warp_max(lane < nv ? vn_[lane] : 0.f);
       // ---- scores on the tensor cores: sc[mt][0,1] token 16mt+mg, sc[mt][2,3] token +8;
       //      columns 0 / 1 are heads 2tig / 2tig+1
       float sc[2][4];
@@ -730,7 +731,7 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
       m0 = mn0;
       m1 = mn1;
       float w[2][4];
-      float wloc = 0.f, ploc = 0.f, ps0 = 0.f, ps1 = 0.f;
+      float ploc = 0.f, ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
         const int ta = 16 * mt + mg, tb = ta + 8;
@@ -744,7 +745,6 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
         w[mt][1] = p1 * va;
         w[mt][2] = p2 * vb;
         w[mt][3] = p3 * vb;
-        wloc = fmaxf(wloc, fmaxf(fmaxf(w[mt][0], w[mt][1]), fmaxf(w[mt][2], w[mt][3])));
       }
       l0 = fmaf(l0, al0, ps0);
       l1 = fmaf(l1, al1, ps1);
@@ -752,10 +752,12 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
       // (relative to the running maximum), only the accumulator is rescaled
       bool skip_v = false;
       if constexpr (SPARSE) skip_v = warp_max(ploc) < a.sparse_thr;
-      const float wmax = warp_max(wloc);
-      // fp16 weights scaled into range: the largest is 16384 (capped at 2^64
-      // so that the accumulator, kept in the scale of the latest chunk, stays finite)
-      const float scl = wmax > 0.f ? fminf(16384.f / wmax, 1.8446744073709552e19f) : 1.f;
+      // fp16 weights scaled into range: every weight p ||v|| is at most the
+      // chunk's largest value norm (p <= 1), which maps to 16384 (capped at
+      // 2^64 so that the accumulator, kept in the latest chunk's scale, stays
+      // finite); vmax was reduced right after the chunk arrived, off the
+      // softmax's dependency chain
+      const float scl = vmax > 0.f ? fminf(16384.f / vmax, 1.8446744073709552e19f) : 1.f;
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
         const int ta = 16 * mt + mg, tb = ta + 8;
@@ -871,18 +873,20 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
         if (k0 + u * kDWarps >= nw) break;
         const float kx[4] = {bf16lo(kw[u].x), bf16hi(kw[u].x), bf16lo(kw[u].y), bf16hi(kw[u].y)};
         const float vx[4] = {bf16lo(vw[u].x), bf16hi(vw[u].x), bf16lo(vw[u].y), bf16hi(vw[u].y)};
+        const int tpos = tw0 + k0 + u * kDWarps;      // token position
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           // several query tokens per sequence: column g is query token g % n_q
           // at position T - n_q + g % n_q, which sees tokens up to itself
-          if (a.n_q > 1 && tw0 + k0 + u * kDWarps > T - a.n_q + g % a.n_q) continue;
+          // (branch-free, so the per-column state stays in registers)
+          const bool vis = tpos <= T - a.n_q + g % a.n_q;
           float part = 0.f;
 #pragma unroll
           for (int j = 0; j < 4; ++j) part = fmaf(qo[(4 * lane + j) * G + g], kx[j], part);
           const float s = warp_sum(part);
-          const float mnew = fmaxf(m[g], s);
-          const float al = exp2f(m[g] - mnew);
-          const float p = exp2f(s - mnew);
+          const float mnew = vis ? fmaxf(m[g], s) : m[g];
+          const float al = vis ? exp2f(m[g] - mnew) : 1.f;
+          const float p = vis ? exp2f(s - mnew) : 0.f;
           l[g] = fmaf(l[g], al, p);
           m[g] = mnew;
 #pragma unroll
