@@ -23,7 +23,8 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 SOURCES = ["tq_host.cpp", "tq_quantize.cu", "tq_qjl.cu", "tq_decode.cu", "tq_decode_g1.cu", "tq_decode_g2.cu",
            "tq_decode_g4.cu", "tq_decode_g8.cu"]
-HEADERS = ["tq_internal.h", "tq_device.cuh", "tq_decode_kernel.cuh", "tq_quant_common.cuh"]
+HEADERS = ["tq_internal.h", "tq_device.cuh", "tq_decode_kernel.cuh", "tq_quant_common.cuh",
+           "tq_umma.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O3",

@@ -45,6 +45,9 @@ constexpr int kDT = kDWarps * 32;
 constexpr int kD2 = 128;
 constexpr float kNegBig = -1.0e30f;
 constexpr float kCScale = 64.f;   // centroids are scaled by 64 in the K tables
+// words per head row of the V-sum weight buffer (16 used): the B-operand
+// reads of the 8 heads x 4 lanes fall into 32 different banks
+constexpr int kWsStride = 20;
 
 // Chunks in each warp's ring: enough bytes in flight per SM to cover the HBM
 // latency (3 chunks ahead); formats with wide rows keep a 3-slot ring.
@@ -74,7 +77,7 @@ struct DecodeSmem {
     vn = w; w += ns * 128;
     sbuf = w; w += sres ? ns * 32 * 16 : 0;     // 128 sign bits per token
     rn = w; w += sres ? ns * 128 : 0;           // gamma (QJL) or scale (Direct Sign)
-    ws = w; w += 8 * 32 * 2;                      // [8 heads][32 tokens] fp16 weights
+    ws = w; w += 8 * kWsStride * 4;               // [8 heads][16 token pairs] fp16 weights
     bar = w; w += 8 * ns;
     w = (w + 15) & ~15;
     warp_stride = w;
@@ -87,6 +90,13 @@ struct DecodeSmem {
   }
 };
 
+// 2^x on the MUFU unit (relative error about 2^-22; results below the fp32
+// normal range flush to zero, as the softmax weights may)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ uint32_t byte_of(uint32_t x, int b) {
   return __byte_perm(x, 0u, 0x4440u | (uint32_t)b);
 }
@@ -106,13 +116,25 @@ __device__ __forceinline__ void pack_hilo(uint32_t e0, uint32_t e1, uint32_t& hi
   hi = __byte_perm(e0, e1, 0x5410);
   lo = __byte_perm(e0, e1, 0x7632);
 }
+// the same hi pair and lo pair of (x0, x1) from packed conversions: two
+// conversions for two values instead of four
+__device__ __forceinline__ void hilo2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(x0, x1);
+  const float2 f = __half22float2(h);
+  const __half2 l = __floats2half2_rn(x0 - f.x, x1 - f.y);
+  hi = *(const uint32_t*)&h;
+  lo = *(const uint32_t*)&l;
+}
 // ---- V sum on the tensor cores ------------------------------------------------
 // D[coords x heads] += V^T[coords x tokens] W[tokens x heads] with
 // mma.sync m16n8k16 (fp16 operands, fp32 accumulate).  The m index is a free
 // permutation of the coordinates: thread (g = lane/4, tig = lane%4) owns rows
 // g and g+8 of every m-tile k, mapped to coordinates 16g+2k and 16g+2k+1, so
-// its 16 coordinates are contiguous in a packed row.  Columns 2tig, 2tig+1
-// (and +8, +9) of a k-tile are tokens; B holds the fp16 softmax weights.
+// its 16 coordinates are contiguous in a packed row.  The k index is a free
+// permutation of the tokens: columns 2j, 2j+1 of k-tile kt are tokens
+// 16kt + j and 16kt + j + 8, the two tokens whose scores a lane of the score
+// MMA holds, so that lane packs both weights into one B register; B holds the
+// fp16 softmax weights.
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
   asm(
@@ -134,11 +156,13 @@ __device__ __forceinline__ void vmma_ktile(const uint8_t* vbuf, const uint32_t* 
                                            int g, int tig, uint32_t b0, uint32_t b1,
                                            float (&d)[8][4]) {
   constexpr int VROW = 16 * VB;
-  const int t0 = 16 * kt + 2 * tig;
+  // a0/a1: columns 2tig, 2tig+1 = tokens t0, t0 + 8; a2/a3: columns 2tig+8,
+  // 2tig+9 = tokens t0 + 4, t0 + 12
+  const int t0 = 16 * kt + tig;
   const uint8_t* r0 = vbuf + t0 * VROW;
-  const uint8_t* r1 = r0 + VROW;
-  const uint8_t* r2 = r0 + 8 * VROW;
-  const uint8_t* r3 = r2 + VROW;
+  const uint8_t* r1 = r0 + 8 * VROW;
+  const uint8_t* r2 = r0 + 4 * VROW;
+  const uint8_t* r3 = r0 + 12 * VROW;
   if constexpr (VB == 2) {
     const uint32_t x0 = *(const uint32_t*)(r0 + 4 * g), x1 = *(const uint32_t*)(r1 + 4 * g);
     const uint32_t x2 = *(const uint32_t*)(r2 + 4 * g), x3 = *(const uint32_t*)(r3 + 4 * g);
@@ -301,10 +325,10 @@ __device__ __forceinline__ void kpair(const KCodes<KB>& c, const uint32_t* lut, 
   }
 }
 
-// Scores of the chunk's 32 tokens for heads 2tig, 2tig+1: codes c[0..3] are
-// tokens g, g+8 (m-tile 0) and 16+g, 24+g (m-tile 1).  The hi*hi, lo*hi and
-// hi*lo products of each m-tile accumulate in separate chains, so six
-// independent MMA chains of eight run side by side instead of two of 24.
+// Scores of the chunk's 32 tokens: codes c[u] are token 8u + g.
+// G = 8: columns are heads; m-tile mt has rows g / g+8 = tokens 16mt + g /
+// 16mt + 8 + g, and the hi*hi, lo*hi and hi*lo products accumulate in
+// separate chains (six independent chains of eight).
 template <int KB, int KT>
 __device__ __forceinline__ void score_ktile(const KCodes<KB> (&c)[4], const uint32_t* lut,
                                             const uint32_t (&bh)[8][2], const uint32_t (&bl)[8][2],
@@ -332,10 +356,34 @@ __device__ __forceinline__ void score_all(const KCodes<KB> (&c)[4], const uint32
   }
 }
 
+// G <= 4 ("folded"): the free columns 4-7 carry the query's lo part (column
+// n is head n % 4, hi part for n < 4, lo part for n >= 4), and m-tile u holds
+// token 8u + g twice: row g its K hi part, row g+8 its K lo part.  One MMA
+// then yields hi*hi (row g, columns 0-3), hi*lo (row g, 4-7), lo*hi (row g+8,
+// 0-3) and a negligible lo*lo, and each (hi pair, lo pair) table entry is
+// the A operand pair (a0, a1) or (a2, a3) as loaded: 32 MMAs per chunk in
+// four chains, against 48 in six.
+template <int KB, int KT>
+__device__ __forceinline__ void score_all_folded(const KCodes<KB> (&c)[4], const uint32_t* lut,
+                                                 const uint32_t (&bq)[8][2], float (&acc)[4][4]) {
+  if constexpr (KT < 8) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      uint32_t h0, l0, h2, l2;
+      kpair<KB, 4 * KT>(c[u], lut, h0, l0);
+      kpair<KB, 4 * KT + 2>(c[u], lut, h2, l2);
+      mma16816(acc[u], h0, l0, h2, l2, bq[KT][0], bq[KT][1]);
+    }
+    score_all_folded<KB, KT + 1>(c, lut, bq, acc);
+  }
+}
+
 // Direct Sign: sum_i (2 bit_i - 1) q_rot,i for tokens ta, ta+8.  Bit i of
 // the token's 128-bit sign vector belongs to rotated coordinate i, and the
 // lane's 32 bits are coordinates 32 tig .. 32 tig + 31: the same k-index
-// permutation as the key scores, so B is the query operand bh / bl.
+// permutation as the key scores, so B is the query operand bh / bl (folded:
+// bh alone, whose columns already carry both parts).
+template <bool FOLD>
 __device__ __forceinline__ void sign_scores(uint32_t sa, uint32_t sb, const uint32_t* slut,
                                             const uint32_t (&bh)[8][2],
                                             const uint32_t (&bl)[8][2], float (&d)[4],
@@ -345,22 +393,30 @@ __device__ __forceinline__ void sign_scores(uint32_t sa, uint32_t sb, const uint
     const uint32_t a0 = slut[(sa >> (4 * kt)) & 3u], a1 = slut[(sb >> (4 * kt)) & 3u];
     const uint32_t a2 = slut[(sa >> (4 * kt + 2)) & 3u], a3 = slut[(sb >> (4 * kt + 2)) & 3u];
     mma16816(d, a0, a1, a2, a3, bh[kt][0], bh[kt][1]);
-    mma16816(dl, a0, a1, a2, a3, bl[kt][0], bl[kt][1]);
+    if constexpr (!FOLD) mma16816(dl, a0, a1, a2, a3, bl[kt][0], bl[kt][1]);
   }
 }
 
 // QJL: sum_j (2 bit_j - 1) (S q)_j for tokens ta, ta+8: A = exact +-1 signs,
-// B = S q hi and lo (per lane, per k-tile, from shared memory).
+// B = S q hi and lo (per lane, per k-tile, from shared memory: (b0 hi, b1 hi,
+// b0 lo, b1 lo)).  Folded, the lane's column is one part, chosen by `part`.
+template <bool FOLD>
 __device__ __forceinline__ void qjl_scores(uint32_t sa, uint32_t sb, const uint32_t* slut,
-                                           const uint4* qb, float (&d)[4], float (&dl)[4]) {
+                                           const uint4* qb, int part, float (&d)[4],
+                                           float (&dl)[4]) {
 #pragma unroll
   for (int kt = 0; kt < 8; ++kt) {
     // sign bits 4kt, 4kt+1 (pair 0) and 4kt+2, 4kt+3 (pair 1) of this lane's 32
     const uint32_t a0 = slut[(sa >> (4 * kt)) & 3u], a1 = slut[(sb >> (4 * kt)) & 3u];
     const uint32_t a2 = slut[(sa >> (4 * kt + 2)) & 3u], a3 = slut[(sb >> (4 * kt + 2)) & 3u];
-    const uint4 b = qb[kt];
-    mma16816(d, a0, a1, a2, a3, b.x, b.y);
-    mma16816(dl, a0, a1, a2, a3, b.z, b.w);
+    if constexpr (FOLD) {
+      const uint2 b = ((const uint2*)(qb + kt))[part];
+      mma16816(d, a0, a1, a2, a3, b.x, b.y);
+    } else {
+      const uint4 b = qb[kt];
+      mma16816(d, a0, a1, a2, a3, b.x, b.y);
+      mma16816(dl, a0, a1, a2, a3, b.z, b.w);
+    }
   }
 }
 
@@ -374,6 +430,9 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
   constexpr bool QJL = RES == 1;        // QJL sketch of the key residual
   constexpr bool SGN = RES == 2;        // Direct Sign key residual
   constexpr bool HAS_RES = RES != 0;
+  // G <= 4 query heads leave half of the 8 MMA columns free: they carry the
+  // query's lo part (see score_ktile)
+  constexpr bool FOLD = G <= 4;
   const DecodeSmem L(G, RES, KB, VB);
   float* qr = (float*)(smem + L.qr);
   float* qo = (float*)(smem + L.qo);
@@ -391,9 +450,7 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
   // and each warp starts the bulk copies of its first chunk before the query
   // is rotated, so the prologue costs about one memory round trip.
   __shared__ float cks[256], cvs[256];
-  const int T = a.seq_lens[b];
   const int W = a.W;
-  const int nq = T - W > 0 ? T - W : 0;
   const bool window_split = split >= a.n_qsplits;
   constexpr int GW = (G + kDWarps - 1) / kDWarps;   // query heads rotated per warp
   float ck0 = 0.f, ck1 = 0.f, cv0 = 0.f, cv1 = 0.f;
@@ -403,22 +460,6 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
   if (tid + kDT < (1 << VB)) cv1 = __ldg(a.cv + tid + kDT);
   const float svv = __ldg(a.sv + tid);
   const float4 sk4 = __ldg((const float4*)a.sk + lane);
-  const long long qbase = ((long long)b * a.Hq + (long long)kvh * G) * kD2;
-  float qv[GW][4];
-#pragma unroll
-  for (int j = 0; j < GW; ++j) {
-    const int g = warp + kDWarps * j;
-    qv[j][0] = qv[j][1] = qv[j][2] = qv[j][3] = 0.f;
-    if (g < G) {
-      if (a.q_f32) {
-        const float4 v = __ldg((const float4*)((const float*)a.q + qbase + g * kD2) + lane);
-        qv[j][0] = v.x; qv[j][1] = v.y; qv[j][2] = v.z; qv[j][3] = v.w;
-      } else {
-        const uint2 v = __ldg((const uint2*)((const uint16_t*)a.q + qbase + g * kD2) + lane);
-        qv[j][0] = bf16lo(v.x); qv[j][1] = bf16hi(v.x); qv[j][2] = bf16lo(v.y); qv[j][3] = bf16hi(v.y);
-      }
-    }
-  }
   cks[tid] = ck0;
   cks[tid + kDT] = ck1;
   cvs[tid] = cv0;
@@ -434,6 +475,12 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
   }
   __syncwarp();
 
+  // everything below may read what the previous kernel on the stream wrote
+  // (sequence lengths, query, planes, window ring, workspace): wait for it
+  // to finish; only the codec tables are read before
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int T = a.seq_lens[b];
+  const int nq = T - W > 0 ? T - W : 0;
   // this split's token range and plane rows (quantized splits)
   const int t_begin = split * a.split_tokens;
   int t_end = t_begin + a.split_tokens;
@@ -485,9 +532,22 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
       }
     }
   };
-  // everything below may read what the previous kernel on the stream wrote
-  // (planes, window ring, workspace): wait for it to finish
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const long long qbase = ((long long)b * a.Hq + (long long)kvh * G) * kD2;
+  float qv[GW][4];
+#pragma unroll
+  for (int j = 0; j < GW; ++j) {
+    const int g = warp + kDWarps * j;
+    qv[j][0] = qv[j][1] = qv[j][2] = qv[j][3] = 0.f;
+    if (g < G) {
+      if (a.q_f32) {
+        const float4 v = __ldg((const float4*)((const float*)a.q + qbase + g * kD2) + lane);
+        qv[j][0] = v.x; qv[j][1] = v.y; qv[j][2] = v.z; qv[j][3] = v.w;
+      } else {
+        const uint2 v = __ldg((const uint2*)((const uint16_t*)a.q + qbase + g * kD2) + lane);
+        qv[j][0] = bf16lo(v.x); qv[j][1] = bf16hi(v.x); qv[j][2] = bf16lo(v.y); qv[j][3] = bf16hi(v.y);
+      }
+    }
+  }
   // the warp's first NS - 1 chunks (c = t_begin + 32 warp + 128 j) go in flight now
   if (!window_split) {
 #pragma unroll
@@ -502,9 +562,8 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
     if constexpr (KB == 2 || KB == 3) {
       if (i < (1 << (2 * KB))) {
         const int msk = (1 << KB) - 1;
-        const uint32_t e0 = hilo(cks[i & msk] * kCScale), e1 = hilo(cks[(i >> KB) & msk] * kCScale);
         uint32_t hp, lp;
-        pack_hilo(e0, e1, hp, lp);
+        hilo2(cks[i & msk] * kCScale, cks[(i >> KB) & msk] * kCScale, hp, lp);
         lutk[2 * i] = hp;
         lutk[2 * i + 1] = lp;
       }
@@ -512,7 +571,7 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
       // pair i = c_lo | c_hi << 4 into all 16 replicas; at step j lane l
       // writes replica (l + j) % 16, so a half-warp's stores never collide
       uint32_t hp, lp;
-      pack_hilo(hilo(cks[i & 15] * kCScale), hilo(cks[i >> 4] * kCScale), hp, lp);
+      hilo2(cks[i & 15] * kCScale, cks[i >> 4] * kCScale, hp, lp);
       uint2* row = (uint2*)(smem + L.lutk4) + i * 16;
 #pragma unroll
       for (int j = 0; j < 16; ++j) row[(lane + j) & 15] = make_uint2(hp, lp);
@@ -572,18 +631,21 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
   int qe = 0;
   (void)frexpf(qmax, &qe);
   const float qsp = qmax > 0.f ? ldexpf(1.f, -qe) : 1.f;
-  // B operands (q hi/lo) of this lane: head mg, coordinates 32tig + 4kt + {0,1} / {2,3}
+  // B operands (q hi/lo) of this lane, coordinates 32tig + 4kt + {0,1} / {2,3}:
+  // unfolded, head mg in bh (hi) and bl (lo); folded, column mg is head mg % 4,
+  // its hi part for mg < 4 and its lo part for mg >= 4, all in bh
+  const int qhead = FOLD ? (mg & 3) : mg;
   uint32_t bh[8][2], bl[8][2];
 #pragma unroll
   for (int kt = 0; kt < 8; ++kt) {
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
       uint32_t hp = 0u, lp = 0u;
-      if (mg < G) {
+      if (qhead < G) {
         const int c = 32 * tig + 4 * kt + 2 * p;
-        pack_hilo(hilo(qr[c * G + mg] * qsp), hilo(qr[(c + 1) * G + mg] * qsp), hp, lp);
+        hilo2(qr[c * G + qhead] * qsp, qr[(c + 1) * G + qhead] * qsp, hp, lp);
       }
-      bh[kt][p] = hp;
+      bh[kt][p] = FOLD && mg >= 4 ? lp : hp;
       bl[kt][p] = lp;
     }
   }
@@ -622,16 +684,16 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
     int se = 0;
     (void)frexpf(smax, &se);
     qsq = smax > 0.f ? ldexpf(1.f, -se) : 1.f;
-    // per lane, per k-tile: (b0 hi, b1 hi, b0 lo, b1 lo) of head lane/4, sketch
-    // indices 32(lane%4) + 4kt + {0,1} / {2,3}
+    // per lane, per k-tile: (b0 hi, b1 hi, b0 lo, b1 lo) of head lane/4 (folded:
+    // (lane/4) % 4), sketch indices 32(lane%4) + 4kt + {0,1} / {2,3}
     uint4* qjlb = (uint4*)(smem + L.qjlb);
     for (int e = tid; e < 32 * 8; e += kDT) {
-      const int ln = e / 8, kt = e % 8, g = ln >> 2, tg = ln & 3;
+      const int ln = e / 8, kt = e % 8, g = FOLD ? (ln >> 2) & 3 : ln >> 2, tg = ln & 3;
       uint4 o = make_uint4(0u, 0u, 0u, 0u);
       if (g < G) {
         const int c = 32 * tg + 4 * kt;
-        pack_hilo(hilo(sq[g * kQjlM + c] * qsq), hilo(sq[g * kQjlM + c + 1] * qsq), o.x, o.z);
-        pack_hilo(hilo(sq[g * kQjlM + c + 2] * qsq), hilo(sq[g * kQjlM + c + 3] * qsq), o.y, o.w);
+        hilo2(sq[g * kQjlM + c] * qsq, sq[g * kQjlM + c + 1] * qsq, o.x, o.z);
+        hilo2(sq[g * kQjlM + c + 2] * qsq, sq[g * kQjlM + c + 3] * qsq, o.y, o.w);
       }
       qjlb[e] = o;
     }
@@ -654,7 +716,8 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
       for (int j = 0; j < 4; ++j) d[k][j] = 0.f;
     const bool h0ok = 2 * tig < G, h1ok = 2 * tig + 1 < G;
     const uint32_t* klut = KB == 4 ? (const uint32_t*)(smem + L.lutk4 + 8 * (lane & 15)) : lutk;
-    uint16_t* ws16 = (uint16_t*)(wreg + L.ws);   // [8 heads][32 tokens] fp16 weights
+    // [8 heads][16 pairs] fp16 weights: pair 8kt + j = tokens 16kt + j, 16kt + j + 8
+    uint32_t* ws32 = (uint32_t*)(wreg + L.ws);
     const float kscale = 1.f / (kCScale * qsp);
     // residual-term scale: QJL sqrt(pi/2)/m over the S q operand scale;
     // Direct Sign 1 over the q operand scale
@@ -684,38 +747,62 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
         KCodes<KB> c[4];
 #pragma unroll
         for (int r = 0; r < 4; ++r) load_kcodes<KB>(kb_ + (8 * r + mg) * KROW, tig, c[r]);
-        float hh[2][4], lh[2][4], hl[2][4];
+        // FOLD: acc[u] = token 8u + mg, [0,1] K hi rows, [2,3] K lo rows
+        float hh[2][4], lh[2][4], hl[2][4], acc[4][4];
+        if constexpr (FOLD) {
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
+          for (int u = 0; u < 4; ++u)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) hh[mt][j] = lh[mt][j] = hl[mt][j] = 0.f;
-        score_all<KB, 0>(c, klut, bh, bl, hh, lh, hl);
+            for (int j = 0; j < 4; ++j) acc[u][j] = 0.f;
+          score_all_folded<KB, 0>(c, klut, bh, acc);
+        } else {
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) hh[mt][j] = lh[mt][j] = hl[mt][j] = 0.f;
+          score_all<KB, 0>(c, klut, bh, bl, hh, lh, hl);
+        }
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
           const int ta = 16 * mt + mg, tb = ta + 8;
           const float na = kn_[ta] * kscale, nb = kn_[tb] * kscale;
-          sc[mt][0] = (hh[mt][0] + (lh[mt][0] + hl[mt][0])) * na;
-          sc[mt][1] = (hh[mt][1] + (lh[mt][1] + hl[mt][1])) * na;
-          sc[mt][2] = (hh[mt][2] + (lh[mt][2] + hl[mt][2])) * nb;
-          sc[mt][3] = (hh[mt][3] + (lh[mt][3] + hl[mt][3])) * nb;
+          if constexpr (FOLD) {
+            // this lane's part (hi for tig < 2, lo for tig >= 2) of heads
+            // 2(tig%2), 2(tig%2)+1; lane tig ^ 2 holds the other part
+            sc[mt][0] = (acc[2 * mt][0] + acc[2 * mt][2]) * na;
+            sc[mt][1] = (acc[2 * mt][1] + acc[2 * mt][3]) * na;
+            sc[mt][2] = (acc[2 * mt + 1][0] + acc[2 * mt + 1][2]) * nb;
+            sc[mt][3] = (acc[2 * mt + 1][1] + acc[2 * mt + 1][3]) * nb;
+          } else {
+            sc[mt][0] = (hh[mt][0] + (lh[mt][0] + hl[mt][0])) * na;
+            sc[mt][1] = (hh[mt][1] + (lh[mt][1] + hl[mt][1])) * na;
+            sc[mt][2] = (hh[mt][2] + (lh[mt][2] + hl[mt][2])) * nb;
+            sc[mt][3] = (hh[mt][3] + (lh[mt][3] + hl[mt][3])) * nb;
+          }
           if constexpr (HAS_RES) {
             const uint8_t* sb_ = wreg + L.sbuf + slot * 512;
             const float* rn_ = (const float*)(wreg + L.rn + slot * 128);
             const uint32_t sa = *(const uint32_t*)(sb_ + ta * 16 + 4 * tig);
             const uint32_t sbits = *(const uint32_t*)(sb_ + tb * 16 + 4 * tig);
             float qa[4] = {0.f, 0.f, 0.f, 0.f}, ql[4] = {0.f, 0.f, 0.f, 0.f};
-            if constexpr (QJL) qjl_scores(sa, sbits, slut, qjlb, qa, ql);
-            else sign_scores(sa, sbits, slut, bh, bl, qa, ql);
+            if constexpr (QJL) qjl_scores<FOLD>(sa, sbits, slut, qjlb, mg >> 2, qa, ql);
+            else sign_scores<FOLD>(sa, sbits, slut, bh, bl, qa, ql);
             const float ga = rn_[ta] * res_scale, gb = rn_[tb] * res_scale;
             sc[mt][0] = fmaf(qa[0] + ql[0], ga, sc[mt][0]);
             sc[mt][1] = fmaf(qa[1] + ql[1], ga, sc[mt][1]);
             sc[mt][2] = fmaf(qa[2] + ql[2], gb, sc[mt][2]);
             sc[mt][3] = fmaf(qa[3] + ql[3], gb, sc[mt][3]);
           }
-          if (ta >= nv || !h0ok) sc[mt][0] = kNegBig;
-          if (ta >= nv || !h1ok) sc[mt][1] = kNegBig;
-          if (tb >= nv || !h0ok) sc[mt][2] = kNegBig;
-          if (tb >= nv || !h1ok) sc[mt][3] = kNegBig;
+          if constexpr (FOLD) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) sc[mt][j] += __shfl_xor_sync(0xffffffffu, sc[mt][j], 2);
+          }
+          // tokens past the end of a partial chunk get no weight; columns of
+          // absent heads are never written or read back, so need no mask
+          if (nv < 32) {
+            if (ta >= nv) sc[mt][0] = sc[mt][1] = kNegBig;
+            if (tb >= nv) sc[mt][2] = sc[mt][3] = kNegBig;
+          }
         }
       }
       // ---- online softmax (log2 domain) per head column; reduce over mg
@@ -727,7 +814,7 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
         x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, o));
       }
       const float mn0 = fmaxf(m0, x0), mn1 = fmaxf(m1, x1);
-      const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+      const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
       m0 = mn0;
       m1 = mn1;
       float w[2][4];
@@ -736,11 +823,12 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
       for (int mt = 0; mt < 2; ++mt) {
         const int ta = 16 * mt + mg, tb = ta + 8;
         const float va = ta < nv ? vn_[ta] : 0.f, vb = tb < nv ? vn_[tb] : 0.f;
-        const float p0 = exp2f(sc[mt][0] - mn0), p1 = exp2f(sc[mt][1] - mn1);
-        const float p2 = exp2f(sc[mt][2] - mn0), p3 = exp2f(sc[mt][3] - mn1);
+        const float p0 = ex2(sc[mt][0] - mn0), p1 = ex2(sc[mt][1] - mn1);
+        const float p2 = ex2(sc[mt][2] - mn0), p3 = ex2(sc[mt][3] - mn1);
         ps0 += p0 + p2;
         ps1 += p1 + p3;
-        if constexpr (SPARSE) ploc = fmaxf(ploc, fmaxf(fmaxf(p0, p1), fmaxf(p2, p3)));
+        if constexpr (SPARSE)
+          ploc = fmaxf(ploc, fmaxf(h0ok ? fmaxf(p0, p2) : 0.f, h1ok ? fmaxf(p1, p3) : 0.f));
         w[mt][0] = p0 * va;
         w[mt][1] = p1 * va;
         w[mt][2] = p2 * vb;
@@ -760,14 +848,14 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
       const float scl = vmax > 0.f ? fminf(16384.f / vmax, 1.8446744073709552e19f) : 1.f;
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
-        const int ta = 16 * mt + mg, tb = ta + 8;
+        // tokens 16mt + mg and 16mt + mg + 8: weight pair 8mt + mg
         if (h0ok && !skip_v) {
-          ws16[(2 * tig) * 32 + ta] = (uint16_t)h16(w[mt][0] * scl);
-          ws16[(2 * tig) * 32 + tb] = (uint16_t)h16(w[mt][2] * scl);
+          const __half2 h = __floats2half2_rn(w[mt][0] * scl, w[mt][2] * scl);
+          ws32[(2 * tig) * kWsStride + 8 * mt + mg] = *(const uint32_t*)&h;
         }
         if (h1ok && !skip_v) {
-          ws16[(2 * tig + 1) * 32 + ta] = (uint16_t)h16(w[mt][1] * scl);
-          ws16[(2 * tig + 1) * 32 + tb] = (uint16_t)h16(w[mt][3] * scl);
+          const __half2 h = __floats2half2_rn(w[mt][1] * scl, w[mt][3] * scl);
+          ws32[(2 * tig + 1) * kWsStride + 8 * mt + mg] = *(const uint32_t*)&h;
         }
       }
       __syncwarp();
@@ -785,8 +873,8 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
       const uint8_t* vb_ = wreg + L.vbuf + slot * 32 * VROW;
 #pragma unroll
       for (int kt = 0; kt < 2 && !skip_v; ++kt) {
-        const uint32_t b0 = mg < G ? *(const uint32_t*)(ws16 + mg * 32 + 16 * kt + 2 * tig) : 0u;
-        const uint32_t b1 = mg < G ? *(const uint32_t*)(ws16 + mg * 32 + 16 * kt + 2 * tig + 8) : 0u;
+        const uint32_t b0 = mg < G ? ws32[mg * kWsStride + 8 * kt + tig] : 0u;
+        const uint32_t b1 = mg < G ? ws32[mg * kWsStride + 8 * kt + tig + 4] : 0u;
         vmma_ktile<VB>(vb_, lutv, kt, mg, tig, b0, b1, d);
       }
       __syncwarp();
@@ -885,8 +973,8 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
           for (int j = 0; j < 4; ++j) part = fmaf(qo[(4 * lane + j) * G + g], kx[j], part);
           const float s = warp_sum(part);
           const float mnew = vis ? fmaxf(m[g], s) : m[g];
-          const float al = vis ? exp2f(m[g] - mnew) : 1.f;
-          const float p = vis ? exp2f(s - mnew) : 0.f;
+          const float al = vis ? ex2(m[g] - mnew) : 1.f;
+          const float p = vis ? ex2(s - mnew) : 0.f;
           l[g] = fmaf(l[g], al, p);
           m[g] = mnew;
 #pragma unroll
@@ -919,7 +1007,7 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
     float O = 0.f, Lsum = 0.f;
 #pragma unroll
     for (int w = 0; w < kDWarps; ++w) {
-      const float f = exp2f(cm[w * G + g] - M);
+      const float f = ex2(cm[w * G + g] - M);
       O = fmaf(co[(w * G + g) * kD2 + tid], f, O);
       Lsum = fmaf(cl[w * G + g], f, Lsum);
     }
@@ -929,15 +1017,19 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
       part[g * stride + 1] = Lsum;
     }
   }
-  __threadfence();
+  // the CTA's partial writes are ordered before the counter update by the
+  // barrier and one gpu-scope fence (cumulative); the last CTA fences again
+  // before it reads the other splits' partials
   __syncthreads();
   if (tid == 0) {
+    __threadfence();
     const unsigned prev = atomicAdd(&a.counters[unit], 1u);
-    *is_last = prev == (unsigned)(a.n_splits - 1);
+    const bool last = prev == (unsigned)(a.n_splits - 1);
+    if (last) __threadfence();
+    *is_last = last;
   }
   __syncthreads();
   if (!*is_last) return;
-  __threadfence();
 
   // last CTA of this (sequence, kv-head): one warp per head merges the splits,
   // inverse-rotates (R^T = D_s H / sqrt(d)) in registers and writes the output
@@ -961,8 +1053,8 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
                    ? __ldcg((const float4*)(base + ((s0 + u) * G + g) * stride + 4) + lane)
                    : make_float4(0.f, 0.f, 0.f, 0.f);
       const float Mn = fmaxf(M, warp_max(ml));
-      const float r = exp2f(M - Mn);
-      const float fl = exp2f(ml - Mn);
+      const float r = ex2(M - Mn);
+      const float fl = ex2(ml - Mn);
       Lsum = fmaf(Lsum, r, warp_sum(ll * fl));
       rot = make_float4(rot.x * r, rot.y * r, rot.z * r, rot.w * r);
       win = make_float4(win.x * r, win.y * r, win.z * r, win.w * r);
@@ -1016,7 +1108,7 @@ int launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
     return 1;
   // programmatic dependent launch: the CTAs may start while the previous
   // kernel on the stream (the library's append) is still running; they read
-  // only q, seq_lens and the codec tables before griddepcontrol.wait
+  // only the codec tables before griddepcontrol.wait
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)a.n_splits, (unsigned)a.Hkv, (unsigned)a.B);
   cfg.blockDim = dim3(kDT, 1, 1);

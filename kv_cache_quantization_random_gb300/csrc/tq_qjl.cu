@@ -21,69 +21,9 @@
 #include <stdint.h>
 
 #include "tq_quant_common.cuh"
+#include "tq_umma.cuh"
 
 namespace tq {
-
-// ---- shared-memory operand layout for tcgen05 (K-major, no swizzle) -----------
-// A [128 rows][128 k] bf16: 8x8 core matrices of 128 contiguous bytes; the 16
-// core matrices of an 8-row group follow each other along K (leading byte
-// offset 128), 8-row groups are 2048 bytes apart (stride byte offset).
-constexpr uint32_t kCoreLbo = 128;
-constexpr uint32_t kCoreSbo = 2048;
-constexpr uint32_t kOpBytes = 128 * 128 * 2;   // one [128 x 128] bf16 operand
-
-__device__ __forceinline__ uint32_t op_offset(int row, int kchunk) {   // 8-element chunk
-  return (uint32_t)(row >> 3) * kCoreSbo + (uint32_t)kchunk * kCoreLbo + (uint32_t)(row & 7) * 16u;
-}
-
-// Shared-memory matrix descriptor: start address, leading and stride byte
-// offsets (all >> 4), descriptor version 1, no swizzle.
-__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) {
-  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((kCoreLbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((kCoreSbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
-}
-
-// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
-// K-major, N = 128, M = 128.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) |
-                            ((128u >> 4) << 24);
-
-__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
 
 __host__ __device__ constexpr size_t qjl_smem_bytes(bool f32, int cells) {
   return 1024                                    // alignment slack

@@ -62,7 +62,7 @@ __device__ __forceinline__ bool resolve_row(const QuantArgs& a, uint32_t v, cons
 
 __device__ __forceinline__ float2 lds64f(uint32_t addr) {
   float2 v;
-  asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+  asm("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
   return v;
 }
 
@@ -163,21 +163,23 @@ __device__ __forceinline__ void build_grid(const QuantArgs& a, const float* bnd,
   }
 }
 
-// Norm, rotation, code search and packing of the vector in `row` (shared
-// memory); the codes go to codes_dst (16 * BITS bytes).  Returns ||x||.  With
-// RESID, p holds the rotated-domain residual n (y - c[idx]) afterwards (pairs
-// (r_j, r_{j+64})), from the centroids `cen` in shared memory.
-template <int BITS, bool F32, bool CLAMP, bool RESID>
-__device__ __forceinline__ float quantize_row(const QuantArgs& a, const uint8_t* row,
-                                              uint32_t grid_base, uint32_t kmax,
-                                              const float* cen, uint8_t* codes_dst,
-                                              float2 (&p)[64]) {
+// Code search and packing of one vector from its unnormalised rotated
+// coordinates p (pairs (z_j, z_{j+64}) of z = H (s * x), H the +-1 Sylvester
+// matrix) and its norm: y = z / (||x|| sqrt(d)); the codes go to codes_dst
+// (16 * BITS bytes).  With RESID, p holds the rotated-domain residual
+// ||x|| (y - c[idx]) afterwards, from the centroids `cen` in shared memory.
+// GUARD bounds every grid index; without it the caller guarantees |y_i| <= 1
+// (up to rounding), inside the grid of a 2-4 bit codebook.
+template <int BITS, bool CLAMP, bool GUARD, bool RESID>
+__device__ __forceinline__ void search_pack_t(const QuantArgs& a, float2 (&p)[64], float nrm,
+                                              uint32_t grid_base, uint32_t kmax, const float* cen,
+                                              uint8_t* codes_dst) {
   constexpr int NW = 4 * BITS;         // 32-bit code words per vector (128 * BITS / 32)
-  const float nrm = load_rotate<F32>(a, row, p);
   const float inv = nrm > 0.f ? 1.0f / (nrm * 11.313708498984761f) : 0.f;
   const float2 inv2 = make_float2(inv, inv);
   const float2 gs2 = make_float2(a.grid_scale, a.grid_scale);
   const float2 gm2 = make_float2(a.grid_magic, a.grid_magic);
+  const uint32_t bias = grid_base - 0x4B400000u * 8u;
   uint32_t words[NW];
 #pragma unroll
   for (int k = 0; k < NW; ++k) words[k] = 0u;
@@ -190,10 +192,16 @@ __device__ __forceinline__ float quantize_row(const QuantArgs& a, const uint8_t*
       yc.y = fminf(fmaxf(y.y, -a.grid_clamp), a.grid_clamp);
     }
     const float2 t = __ffma2_rn(yc, gs2, gm2);
-    const uint32_t k0 = min(__float_as_uint(t.x) - 0x4B400000u, kmax);
-    const uint32_t k1 = min(__float_as_uint(t.y) - 0x4B400000u, kmax);
-    const float2 e0 = lds64f(grid_base + k0 * 8u);
-    const float2 e1 = lds64f(grid_base + k1 * 8u);
+    uint32_t a0, a1;                                 // grid entry addresses
+    if constexpr (GUARD) {
+      a0 = grid_base + min(__float_as_uint(t.x) - 0x4B400000u, kmax) * 8u;
+      a1 = grid_base + min(__float_as_uint(t.y) - 0x4B400000u, kmax) * 8u;
+    } else {
+      a0 = __float_as_uint(t.x) * 8u + bias;        // cell = bits(t) - bits(magic)
+      a1 = __float_as_uint(t.y) * 8u + bias;
+    }
+    const float2 e0 = lds64f(a0);
+    const float2 e1 = lds64f(a1);
     const uint32_t c0 = __float_as_uint(e0.y) + (e0.x < y.x ? 1u : 0u);
     const uint32_t c1 = __float_as_uint(e1.y) + (e1.x < y.y ? 1u : 0u);
 #pragma unroll
@@ -201,7 +209,8 @@ __device__ __forceinline__ float quantize_row(const QuantArgs& a, const uint8_t*
       const int i = j + 64 * half;                   // coordinate
       const uint32_t code = half ? c1 : c0;
       const int pb = i * BITS;
-      words[pb >> 5] |= code << (pb & 31);
+      // fields do not overlap: a multiply-add places the code
+      words[pb >> 5] = code * (1u << (pb & 31)) + words[pb >> 5];
       if ((pb & 31) + BITS > 32) words[(pb >> 5) + 1] |= code >> (32 - (pb & 31));
     }
     if constexpr (RESID) p[j] = make_float2(nrm * (y.x - cen[c0]), nrm * (y.y - cen[c1]));
@@ -210,7 +219,51 @@ __device__ __forceinline__ float quantize_row(const QuantArgs& a, const uint8_t*
 #pragma unroll
   for (int k = 0; k < BITS; ++k)
     dc[k] = make_uint4(words[4 * k], words[4 * k + 1], words[4 * k + 2], words[4 * k + 3]);
+}
+
+// A row whose norm is finite and of normal size has |y_i| <= 1 to within
+// rounding, inside the search grid of a 2-4 bit codebook (8-bit grids clamp
+// y): it takes the unguarded search.  Rows with inf or NaN, or so small that
+// the sum of squares loses precision, take the guarded one.
+template <int BITS, bool CLAMP, bool RESID>
+__device__ __forceinline__ void search_pack(const QuantArgs& a, float2 (&p)[64], float nrm,
+                                            uint32_t grid_base, uint32_t kmax, const float* cen,
+                                            uint8_t* codes_dst) {
+  if (!CLAMP && nrm <= 3.4e38f && nrm >= 1e-18f)
+    search_pack_t<BITS, CLAMP, false, RESID>(a, p, nrm, grid_base, kmax, cen, codes_dst);
+  else
+    search_pack_t<BITS, CLAMP, true, RESID>(a, p, nrm, grid_base, kmax, cen, codes_dst);
+}
+
+// Norm, rotation, code search and packing of the vector in `row` (shared
+// memory); the codes go to codes_dst (16 * BITS bytes).  Returns ||x||.  With
+// RESID, p holds the rotated-domain residual n (y - c[idx]) afterwards (pairs
+// (r_j, r_{j+64})), from the centroids `cen` in shared memory.
+template <int BITS, bool F32, bool CLAMP, bool RESID>
+__device__ __forceinline__ float quantize_row(const QuantArgs& a, const uint8_t* row,
+                                              uint32_t grid_base, uint32_t kmax,
+                                              const float* cen, uint8_t* codes_dst,
+                                              float2 (&p)[64]) {
+  const float nrm = load_rotate<F32>(a, row, p);
+  search_pack<BITS, CLAMP, RESID>(a, p, nrm, grid_base, kmax, cen, codes_dst);
   return nrm;
+}
+
+// Direct Sign sketch of a residual held as pairs p[j] = (r_j, r_{j+64}): bit
+// i of the 128-bit sign vector is [r_i >= 0]; the scale is mean |r_i|
+// ("TurboQuant KV 캐시 압축 for llama.cpp", v1.1.0 "Direct Sign").
+__device__ __forceinline__ void direct_sign(const float2 (&p)[64], uint8_t* signs_dst,
+                                            float* scale_dst) {
+  uint32_t sw[4] = {0u, 0u, 0u, 0u};
+  float asum = 0.f;
+#pragma unroll
+  for (int j = 0; j < 64; ++j) {
+    sw[j >> 5] |= (p[j].x >= 0.f ? 1u : 0u) << (j & 31);
+    sw[2 + (j >> 5)] |= (p[j].y >= 0.f ? 1u : 0u) << (j & 31);
+    asum += fabsf(p[j].x) + fabsf(p[j].y);
+  }
+  *(uint4*)signs_dst = make_uint4(sw[0], sw[1], sw[2], sw[3]);
+  *scale_dst = asum * (1.0f / kD);
 }
 
 }  // namespace tq

@@ -83,19 +83,7 @@ __global__ void __launch_bounds__(kQRows, 3) quantize_kernel(const QuantArgs a) 
       const float nrm = quantize_row<BITS, F32, CLAMP, SGN>(
           a, rows + lane * kPitch, grid_base, kmax, cen, a.codes + drow * (16 * BITS), p);
       a.norms[drow] = nrm;
-      if constexpr (SGN) {
-        // p[j] = (r_j, r_{j+64}): bit i of the 128-bit sign vector is [r_i >= 0]
-        uint32_t sw[4] = {0u, 0u, 0u, 0u};
-        float asum = 0.f;
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          sw[j >> 5] |= (p[j].x >= 0.f ? 1u : 0u) << (j & 31);
-          sw[2 + (j >> 5)] |= (p[j].y >= 0.f ? 1u : 0u) << (j & 31);
-          asum += fabsf(p[j].x) + fabsf(p[j].y);
-        }
-        *(uint4*)(a.qjl_signs + drow * (kD / 8)) = make_uint4(sw[0], sw[1], sw[2], sw[3]);
-        a.qjl_rnorm[drow] = asum * (1.0f / kD);
-      }
+      if constexpr (SGN) direct_sign(p, a.qjl_signs + drow * (kD / 8), a.qjl_rnorm + drow);
     }
     __syncwarp();      // every lane is done with this buffer before it is refilled
     buf ^= 1;

@@ -56,6 +56,30 @@ def test_quantize_bits_and_ragged_tiles_bf16(B, bits, n):
         compare_norms(planes.norms_view().cpu().numpy(), oq["norms"])
 
 
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_quantize_rows_of_extreme_magnitude(B, bits):
+    """Rows scaled by 1e-15 and 1e15 quantize like the oracle's (same unit
+    vector); zero rows, rows whose squares fall below the fp32 normal range,
+    and rows with inf or NaN take the bounded search and raise no error."""
+    import torch
+    g = torch.Generator().manual_seed(11)
+    base = torch.randn(1, 1, 8, 128, generator=g)
+    scales = torch.tensor([1.0, 1e-15, 1e15, 1e-3, 0.0, 1e-21, 1.0, 1.0]).view(1, 1, 8, 1)
+    X = (base * scales).to(torch.bfloat16)
+    X[0, 0, 6, 5] = float("inf")
+    X[0, 0, 7, 9] = float("nan")
+    cfg = B.Config(k_bits=bits, v_bits=bits, seed=3)
+    planes = _run_quantize(B, cfg, 0, 1, X.cuda())
+    codes = planes.codes_view().cpu().numpy()
+    fin = [0, 1, 2, 3]
+    oq = oracle_quantize(to64(X[:, :, fin]), bits, 3, 0, 1)
+    compare_codes(codes[:, :, fin], oq, bits)
+    compare_norms(planes.norms_view().cpu().numpy()[:, :, fin], oq["norms"])
+    got = O.unpack_codes(codes[0, 0], bits, 128)
+    assert (got >= 0).all() and (got < (1 << bits)).all()
+    assert planes.norms_view().cpu().numpy()[0, 0, 4] == 0.0
+
+
 @pytest.mark.parametrize("bits", [2, 4])
 def test_quantize_and_decode_with_the_sphere_density_codebook(B, bits):
     """Codebook from the exact coordinate density (TQ_DENSITY_SPHERE_BETA):
