@@ -11,7 +11,9 @@
 // items 1 and 2 (dequantized codes fed to tensor-core MMA; the QJL term is a
 // correction from the sign bits and the stored residual scale).
 //
-// One CTA = (split, kv-head, sequence), 4 warps.  Prologue: the G query heads
+// One CTA = (split, kv-head, sequence): one CTA of 12 (or 8) warps per SM
+// with G <= 4 query columns and MSE keys, two of 4 warps otherwise
+// (decode_warps).  Prologue: the G query heads
 // of the kv-head are scaled by softmax_scale*log2(e), rotated with the K sign
 // vector and split into fp16 hi + lo MMA operands held in registers; QJL keys
 // also get S q_rot as hi + lo operands.  Main loop, per warp and 32-token
@@ -40,55 +42,9 @@
 
 namespace tq {
 
-constexpr int kDWarps = 4;
-constexpr int kDT = kDWarps * 32;
 constexpr int kD2 = 128;
 constexpr float kNegBig = -1.0e30f;
 constexpr float kCScale = 64.f;   // centroids are scaled by 64 in the K tables
-// words per head row of the V-sum weight buffer (16 used): the B-operand
-// reads of the 8 heads x 4 lanes fall into 32 different banks
-constexpr int kWsStride = 20;
-
-// Chunks in each warp's ring: enough bytes in flight per SM to cover the HBM
-// latency (3 chunks ahead); formats with wide rows keep a 3-slot ring.
-__host__ __device__ constexpr int ring_slots(int kb, int vb) { return kb + vb <= 8 ? 4 : 3; }
-
-// Byte layout of the dynamic shared memory of a decode CTA.
-struct DecodeSmem {
-  int qr, qo, sv, qjlb, sq, lutk4, warps, warp_stride;
-  int kbuf, vbuf, kn, vn, sbuf, rn, ws, bar;   // offsets inside one warp's region
-  int comb, total;
-  // res: 0 = MSE keys, 1 = QJL keys, 2 = Direct Sign keys
-  __host__ __device__ DecodeSmem(int G, int res, int kb, int vb) {
-    const bool qjl = res == 1, sres = res != 0;
-    int off = 0;
-    qr = off; off += kD2 * G * 4;                 // [128][G] rotated, scaled queries
-    qo = off; off += kD2 * G * 4;                 // [128][G] original-domain queries
-    sv = off; off += kD2 * 4;
-    qjlb = off; off += qjl ? 32 * 8 * 16 : 0;     // per lane, per k-tile: S q hi/lo operands
-    sq = off; off += qjl ? G * kQjlM * 4 : 0;     // [G][m] S q_rot (QJL)
-    lutk4 = off; off += kb == 4 ? 256 * 16 * 8 : 0;   // 4-bit key pair table, 16 replicas
-    warps = off;
-    const int ns = ring_slots(kb, vb);
-    int w = 0;
-    kbuf = w; w += ns * 32 * 16 * kb;
-    vbuf = w; w += ns * 32 * 16 * vb;
-    kn = w; w += ns * 128;
-    vn = w; w += ns * 128;
-    sbuf = w; w += sres ? ns * 32 * 16 : 0;     // 128 sign bits per token
-    rn = w; w += sres ? ns * 128 : 0;           // gamma (QJL) or scale (Direct Sign)
-    ws = w; w += 8 * kWsStride * 4;               // [8 heads][16 token pairs] fp16 weights
-    bar = w; w += 8 * ns;
-    w = (w + 15) & ~15;
-    warp_stride = w;
-    int region = kDWarps * w;
-    const int comb_need = kDWarps * G * (2 + kD2) * 4;   // cm, cl, co
-    if (region < comb_need) region = comb_need;
-    comb = warps;
-    off += region;
-    total = off + 16;                             // + is-last flag
-  }
-};
 
 // 2^x on the MUFU unit (relative error about 2^-22; results below the fp32
 // normal range flush to zero, as the softmax weights may)
@@ -421,7 +377,11 @@ __device__ __forceinline__ void qjl_scores(uint32_t sa, uint32_t sb, const uint3
 }
 
 template <int G, int KB, int VB, int RES, bool SPARSE>
-__global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
+                                  decode_ctas_per_sm(decode_warps(G, KB, VB, RES)))
+    decode_kernel(const DecodeArgs a) {
+  constexpr int kDWarps = decode_warps(G, KB, VB, RES);   // warps of this CTA
+  constexpr int kDT = kDWarps * 32;
   constexpr int KROW = 16 * KB, VROW = 16 * VB;
   __shared__ __align__(16) uint32_t lutk[256];   // K centroid tables (see kpair)
   __shared__ __align__(16) uint32_t lutv[256];   // V fp16 centroids (pairs for 2/3 bits)
@@ -433,14 +393,33 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
   // G <= 4 query heads leave half of the 8 MMA columns free: they carry the
   // query's lo part (see score_ktile)
   constexpr bool FOLD = G <= 4;
-  const DecodeSmem L(G, RES, KB, VB);
+  constexpr DecodeSmem L(G, RES, KB, VB, kDWarps);
   float* qr = (float*)(smem + L.qr);
   float* qo = (float*)(smem + L.qo);
   float* svs = (float*)(smem + L.sv);
   int* is_last = (int*)(smem + L.total - 16);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  // 1-D grid.  Several waves: the long quantized splits of every (sequence,
+  // kv-head) first and the short window splits after them, so that CTAs start
+  // longest first; one wave: each pair's splits together.
+  int split, seq_head;
+  {
+    const int nq_total = a.B * a.Hkv * a.n_qsplits;
+    const int i = (int)blockIdx.x;
+    if (!a.long_first) {
+      seq_head = i / a.n_splits;
+      split = i - seq_head * a.n_splits;
+    } else if (i < nq_total) {
+      seq_head = i / a.n_qsplits;
+      split = i - seq_head * a.n_qsplits;
+    } else {
+      const int nws = a.n_splits - a.n_qsplits;
+      seq_head = (i - nq_total) / nws;
+      split = a.n_qsplits + (i - nq_total - seq_head * nws);
+    }
+  }
+  const int kvh = seq_head % a.Hkv, b = seq_head / a.Hkv;
   const int Hkv = a.Hkv;
   const uint32_t limit = a.wait_limit ? a.wait_limit : kDefaultWaitLimit;
   const int mg = lane >> 2, tig = lane & 3;   // MMA group / thread-in-group
@@ -453,18 +432,12 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
   const int W = a.W;
   const bool window_split = split >= a.n_qsplits;
   constexpr int GW = (G + kDWarps - 1) / kDWarps;   // query heads rotated per warp
-  float ck0 = 0.f, ck1 = 0.f, cv0 = 0.f, cv1 = 0.f;
-  if (tid < (1 << KB)) ck0 = __ldg(a.ck + tid);
-  if (tid + kDT < (1 << KB)) ck1 = __ldg(a.ck + tid + kDT);
-  if (tid < (1 << VB)) cv0 = __ldg(a.cv + tid);
-  if (tid + kDT < (1 << VB)) cv1 = __ldg(a.cv + tid + kDT);
-  const float svv = __ldg(a.sv + tid);
+  for (int i = tid; i < 256; i += kDT) {
+    cks[i] = i < (1 << KB) ? __ldg(a.ck + i) : 0.f;
+    cvs[i] = i < (1 << VB) ? __ldg(a.cv + i) : 0.f;
+  }
+  if (tid < kD2) svs[tid] = __ldg(a.sv + tid);
   const float4 sk4 = __ldg((const float4*)a.sk + lane);
-  cks[tid] = ck0;
-  cks[tid + kDT] = ck1;
-  cvs[tid] = cv0;
-  cvs[tid + kDT] = cv1;
-  svs[tid] = svv;
   uint8_t* wreg = smem + L.warps + warp * L.warp_stride;
   uint64_t* bar = (uint64_t*)(wreg + L.bar);
   constexpr int NS = ring_slots(KB, VB);
@@ -627,7 +600,8 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
   qmax = warp_max(qmax);
   if (lane == 0) red[warp] = qmax;
   __syncthreads();
-  qmax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+#pragma unroll
+  for (int w = 0; w < kDWarps; ++w) qmax = fmaxf(qmax, red[w]);
   int qe = 0;
   (void)frexpf(qmax, &qe);
   const float qsp = qmax > 0.f ? ldexpf(1.f, -qe) : 1.f;
@@ -680,7 +654,8 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
     __syncthreads();
     if (lane == 0) red[warp] = smax;
     __syncthreads();
-    smax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+#pragma unroll
+    for (int w = 0; w < kDWarps; ++w) smax = fmaxf(smax, red[w]);
     int se = 0;
     (void)frexpf(smax, &se);
     qsq = smax > 0.f ? ldexpf(1.f, -se) : 1.f;
@@ -940,11 +915,11 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
     }
     const int nw = T < W ? T : W;                     // window tokens of this sequence
     const int tw0 = T - nw;
-    const int kw0 = 32 * (split - a.n_qsplits);       // this split's 32 of them
-    const int kw1 = kw0 + 32 < nw ? kw0 + 32 : nw;
+    const int kw0 = a.wsplit_tokens * (split - a.n_qsplits);   // this split's share
+    const int kw1 = kw0 + a.wsplit_tokens < nw ? kw0 + a.wsplit_tokens : nw;
     const long long base = ((long long)b * Hkv + kvh) * W;
-    // warp w takes window tokens w, w+4, ...; 8 tokens' rows are loaded before
-    // any is used, so the loads overlap instead of paying one latency each
+    // warp w takes window tokens w, w + warps, ...; 8 tokens' rows are loaded
+    // before any is used, so the loads overlap instead of paying one latency each
     for (int k0 = kw0 + warp; k0 < kw1; k0 += 8 * kDWarps) {
       uint2 kw[8], vw[8];
 #pragma unroll
@@ -999,8 +974,9 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
   const long long unit = (long long)b * Hkv + kvh;
   const int stride = kPartialStride;
   float* part = a.partials + (unit * a.n_splits + split) * G * stride;
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
+  // thread e of the G x 128 outputs: head e / 128, coordinate e % 128
+  for (int e = tid; e < G * kD2; e += kDT) {
+    const int g = e / kD2, c = e % kD2;
     float M = kNegBig;
 #pragma unroll
     for (int w = 0; w < kDWarps; ++w) M = fmaxf(M, cm[w * G + g]);
@@ -1008,11 +984,11 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
 #pragma unroll
     for (int w = 0; w < kDWarps; ++w) {
       const float f = ex2(cm[w * G + g] - M);
-      O = fmaf(co[(w * G + g) * kD2 + tid], f, O);
+      O = fmaf(co[(w * G + g) * kD2 + c], f, O);
       Lsum = fmaf(cl[w * G + g], f, Lsum);
     }
-    part[g * stride + 4 + tid] = O;
-    if (tid == 0) {
+    part[g * stride + 4 + c] = O;
+    if (c == 0) {
       part[g * stride] = M;
       part[g * stride + 1] = Lsum;
     }
@@ -1103,15 +1079,16 @@ __global__ void __launch_bounds__(kDT, 2) decode_kernel(const DecodeArgs a) {
 template <int G, int KB, int VB, int RES, bool SPARSE = false>
 int launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
   auto k = decode_kernel<G, KB, VB, RES, SPARSE>;
-  const size_t smem = (size_t)DecodeSmem(G, RES, KB, VB).total;
+  constexpr int kWarps = decode_warps(G, KB, VB, RES);
+  const size_t smem = (size_t)DecodeSmem(G, RES, KB, VB, kWarps).total;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return 1;
   // programmatic dependent launch: the CTAs may start while the previous
   // kernel on the stream (the library's append) is still running; they read
   // only the codec tables before griddepcontrol.wait
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)a.n_splits, (unsigned)a.Hkv, (unsigned)a.B);
-  cfg.blockDim = dim3(kDT, 1, 1);
+  cfg.gridDim = dim3((unsigned)((long long)a.n_splits * a.Hkv * a.B), 1, 1);
+  cfg.blockDim = dim3(32 * kWarps, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

@@ -461,20 +461,29 @@ extern "C" tq_status tq_plane_bytes(const tq_config* cfg, int layer, int kind, i
 // ------------------------------------------------------------------ decode plan
 namespace tq {
 struct DecodePlan {
-  int n_qsplits, n_splits, split_tokens, G;
+  int n_qsplits, n_splits, split_tokens, wsplit_tokens, G, long_first;
   size_t partial_floats, counters_off, total;
 };
-static DecodePlan decode_plan(const tq_config* cfg, int batch, int n_q_heads, int n_kv_heads,
-                              int max_seq_len) {
+// Splits of one decode launch for a layer of format s: one wave of about
+// kDecodeSms x decode_ctas_per_sm CTAs of decode_warps(...) warps.  The window is
+// cut into splits of at most 16 tokens per warp; the quantized tokens of each
+// (sequence, kv-head) are split evenly in multiples of 32 tokens over the rest.
+static DecodePlan decode_plan(const tq_config* cfg, const tq_layer_spec& s, int batch,
+                              int n_q_heads, int n_kv_heads, int max_seq_len) {
   DecodePlan p;
-  int W = cfg->residual_window;
+  const int W = cfg->residual_window;
   long long max_nq = (long long)max_seq_len - W;
   if (max_nq < 0) max_nq = 0;
-  long long units = (long long)batch * n_kv_heads;
-  // the window: one split per 32 window tokens; the quantized tokens: one wave
-  // of about kTargetCtas CTAs in all, split evenly in multiples of 32 tokens
-  const int n_wsplits = W > 0 ? (W + 31) / 32 : 0;
-  long long slots = kTargetCtas - units * n_wsplits;
+  const long long units = (long long)batch * n_kv_heads;
+  p.G = n_kv_heads > 0 ? n_q_heads / n_kv_heads : 0;
+  const int res = s.k_mode == TQ_MODE_MSE_QJL ? 1 : s.k_mode == TQ_MODE_MSE_SIGN ? 2 : 0;
+  const int warps = decode_warps(p.G, s.k_bits, s.v_bits, res);
+  int wst = (W + 31) / 32 * 32;
+  if (wst > 16 * warps) wst = 16 * warps;
+  p.wsplit_tokens = wst > 0 ? wst : 1;
+  const int n_wsplits = W > 0 ? (W + wst - 1) / wst : 0;
+  const long long wave = (long long)kDecodeSms * decode_ctas_per_sm(warps);
+  long long slots = wave - units * n_wsplits;
   if (slots < units) slots = units;
   long long per = units > 0 ? (units * max_nq + slots - 1) / slots : 0;
   long long st = (per + 31) / 32 * 32;
@@ -482,7 +491,7 @@ static DecodePlan decode_plan(const tq_config* cfg, int batch, int n_q_heads, in
   p.split_tokens = (int)st;
   p.n_qsplits = (int)((max_nq + st - 1) / st);
   p.n_splits = p.n_qsplits + n_wsplits;
-  p.G = n_kv_heads > 0 ? n_q_heads / n_kv_heads : 0;
+  p.long_first = units * p.n_splits > wave;
   p.partial_floats = (size_t)units * p.n_splits * p.G * kPartialStride;
   p.counters_off = align256(p.partial_floats * sizeof(float));
   p.total = p.counters_off + align256((size_t)units * sizeof(unsigned));
@@ -495,7 +504,14 @@ extern "C" size_t tq_workspace_bytes(const tq_config* cfg, int batch, int n_q_he
   if (check_config(cfg) != TQ_OK || batch < 0 || n_kv_heads < 1 || n_q_heads < n_kv_heads ||
       max_seq_len < 0)
     return 0;
-  return decode_plan(cfg, batch, n_q_heads, n_kv_heads, max_seq_len).total;
+  // the largest plan over the layers' formats
+  size_t total = 0;
+  for (int layer = 0; layer < cfg->n_layers; ++layer) {
+    const size_t t =
+        decode_plan(cfg, spec_of(cfg, layer), batch, n_q_heads, n_kv_heads, max_seq_len).total;
+    if (t > total) total = t;
+  }
+  return total;
 }
 
 extern "C" tq_status tq_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
@@ -808,9 +824,10 @@ static tq_status decode_common(const tq_config* cfg, const void* tables, int lay
   }
   long long max_nq = (long long)max_seq_len - W;
   if (max_nq > k.capacity || max_nq > v.capacity) return TQ_ERR_INVALID_ARG;
-  DecodePlan p = decode_plan(cfg, batch, n_q_heads, n_kv_heads, max_seq_len);
-  if (workspace_bytes < p.total) return TQ_ERR_BUFFER_TOO_SMALL;
   tq_layer_spec s = spec_of(cfg, layer);
+  DecodePlan p = decode_plan(cfg, s, batch, n_q_heads, n_kv_heads, max_seq_len);
+  if (workspace_bytes < p.total) return TQ_ERR_BUFFER_TOO_SMALL;
+  if ((long long)p.n_splits * n_kv_heads * batch >= (1ll << 31)) return TQ_ERR_UNSUPPORTED;
   DecodeArgs a{};
   a.q = q;
   a.q_f32 = q_dtype == TQ_F32;
@@ -841,6 +858,8 @@ static tq_status decode_common(const tq_config* cfg, const void* tables, int lay
   a.n_qsplits = p.n_qsplits;
   a.n_splits = p.n_splits;
   a.split_tokens = p.split_tokens;
+  a.wsplit_tokens = p.wsplit_tokens;
+  a.long_first = p.long_first;
   a.ck = (const float*)tbl_codebook(tables, s.k_bits);
   a.cv = (const float*)tbl_codebook(tables, s.v_bits);
   a.sk = tbl_signs(cfg, tables, layer, 0);

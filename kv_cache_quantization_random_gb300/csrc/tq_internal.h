@@ -13,8 +13,71 @@ namespace tq {
 
 constexpr int kHeadDim = 128;          // the head_dim the kernels implement
 constexpr int kQjlM = 128;             // the QJL projection count the kernels implement
-constexpr int kTargetCtas = 2 * 152;   // decode grid target: 2 resident CTAs per GB300 SM
+constexpr int kDecodeSms = 152;         // decode grid target: one wave over the GB300's SMs
 constexpr int kPartialStride = 4 + kHeadDim;   // floats per (split, head): m, l, pad, pad, o[d]
+
+// ---- decode CTA shape, shared by the host's split plan and the kernel --------
+// words per head row of the V-sum weight buffer (16 used): the B-operand
+// reads of the 8 heads x 4 lanes fall into 32 different banks
+constexpr int kWsStride = 20;
+// 32-token chunks in each warp's staging ring: enough bytes in flight per SM
+// to cover the HBM latency; formats with wide rows keep 3.
+__host__ __device__ constexpr int ring_slots(int kb, int vb) { return kb + vb <= 8 ? 4 : 3; }
+
+// Byte layout of the dynamic shared memory of a decode CTA with nw warps
+// (G query columns per kv-head; res 0 = MSE keys, 1 = QJL, 2 = Direct Sign).
+struct DecodeSmem {
+  int qr = 0, qo = 0, sv = 0, qjlb = 0, sq = 0, lutk4 = 0, warps = 0, warp_stride = 0;
+  int kbuf = 0, vbuf = 0, kn = 0, vn = 0, sbuf = 0, rn = 0, ws = 0, bar = 0;   // inside one warp's region
+  int comb = 0, total = 0;
+  __host__ __device__ constexpr DecodeSmem(int G, int res, int kb, int vb, int nw) {
+    const bool qjl = res == 1, sres = res != 0;
+    int off = 0;
+    qr = off; off += kHeadDim * G * 4;            // [128][G] rotated, scaled queries
+    qo = off; off += kHeadDim * G * 4;            // [128][G] original-domain queries
+    sv = off; off += kHeadDim * 4;
+    qjlb = off; off += qjl ? 32 * 8 * 16 : 0;     // per lane, per k-tile: S q hi/lo operands
+    sq = off; off += qjl ? G * kQjlM * 4 : 0;     // [G][m] S q_rot (QJL)
+    lutk4 = off; off += kb == 4 ? 256 * 16 * 8 : 0;   // 4-bit key pair table, 16 replicas
+    warps = off;
+    const int ns = ring_slots(kb, vb);
+    int w = 0;
+    kbuf = w; w += ns * 32 * 16 * kb;
+    vbuf = w; w += ns * 32 * 16 * vb;
+    kn = w; w += ns * 128;
+    vn = w; w += ns * 128;
+    sbuf = w; w += sres ? ns * 32 * 16 : 0;       // 128 sign bits per token
+    rn = w; w += sres ? ns * 128 : 0;             // gamma (QJL) or scale (Direct Sign)
+    ws = w; w += 8 * kWsStride * 4;               // [8 heads][16 token pairs] fp16 weights
+    bar = w; w += 8 * ns;
+    w = (w + 15) & ~15;
+    warp_stride = w;
+    int region = nw * w;
+    const int comb_need = nw * G * (2 + kHeadDim) * 4;   // cm, cl, co
+    if (region < comb_need) region = comb_need;
+    comb = warps;
+    off += region;
+    total = off + 16;                             // + is-last flag
+  }
+};
+
+// dynamic shared memory a decode CTA may use (227 KB per CTA, less the
+// kernel's static tables)
+constexpr int kDecodeSmemBudget = 216 * 1024;
+
+// Warps of a decode CTA.  G <= 4 query columns with MSE keys (about 168
+// registers a thread): one CTA per SM of 12 warps, or 8 when 12 staging
+// rings do not fit.  Keys with a residual term and G = 8 (up to 255
+// registers): two CTAs of 4 warps per SM, so that one CTA's prologue runs
+// beside the other's main loop (measured faster for these formats).
+__host__ __device__ constexpr int decode_warps(int G, int kb, int vb, int res) {
+  return (G > 4 || res != 0)                                             ? 4
+         : DecodeSmem(G, res, kb, vb, 12).total <= kDecodeSmemBudget ? 12
+         : DecodeSmem(G, res, kb, vb, 8).total <= kDecodeSmemBudget  ? 8
+                                                                       : 4;
+}
+// resident decode CTAs per SM for a CTA of `warps` warps
+__host__ __device__ constexpr int decode_ctas_per_sm(int warps) { return warps == 4 ? 2 : 1; }
 
 // ---- device tables (built on the host by tq_build_tables) -------------------
 // [0, 256)                 header, int32 words (see kTbl*)
@@ -151,8 +214,11 @@ struct DecodeArgs {
   const uint16_t* kwin; const uint16_t* vwin; int W;
   const int32_t* seq_lens;
   int n_qsplits;                 // splits over the quantized tokens
-  int n_splits;                  // n_qsplits + one split per 32 window tokens
+  int n_splits;                  // n_qsplits + the window splits
   int split_tokens;              // tokens per quantized split (multiple of 32)
+  int wsplit_tokens;             // window tokens per window split
+  int long_first;                // CTA order: all quantized splits before the window
+                                 // splits (several waves), else split-major per pair
   // codec
   const float* ck; const float* cv;
   const float* sk; const float* sv;
