@@ -425,9 +425,10 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
   const int mg = lane >> 2, tig = lane & 3;   // MMA group / thread-in-group
 
   // ------------------------------------------------------------- prologue
-  // Every global load of the prologue is issued before any result is used,
-  // and each warp starts the bulk copies of its first chunk before the query
-  // is rotated, so the prologue costs about one memory round trip.
+  // The codec tables are loaded before the dependency wait, the sequence
+  // length and the bulk copy of each warp's first chunk right after it; the
+  // query and the tables' arithmetic overlap the copies' flight, so the
+  // prologue costs about one memory round trip.
   __shared__ float cks[256], cvs[256];
   const int W = a.W;
   const bool window_split = split >= a.n_qsplits;
@@ -450,7 +451,7 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
 
   // everything below may read what the previous kernel on the stream wrote
   // (sequence lengths, query, planes, window ring, workspace): wait for it
-  // to finish; only the codec tables are read before
+  // to finish
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int T = a.seq_lens[b];
   const int nq = T - W > 0 ? T - W : 0;
@@ -473,20 +474,23 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
     const int n4 = (nv + 3) & ~3;
     // bulk copies need 16-byte aligned sources: the norm rows of a (sequence,
     // head) start at row0 * capacity floats, aligned only if capacity % 4 == 0
-    const bool aligned = (((uintptr_t)(knp + c0) | (uintptr_t)(vnp + c0) |
-                           (HAS_RES ? (uintptr_t)(krp + c0) : (uintptr_t)0)) & 15u) == 0;
+    // (chunks start at multiples of 32 tokens, so this holds for all or none)
+    const bool norms_aligned = (((uintptr_t)knp | (uintptr_t)vnp |
+                                 (HAS_RES ? (uintptr_t)krp : (uintptr_t)0)) & 15u) == 0;
     const bool bulk_norms =
-        aligned && (long long)c0 + n4 <= a.kcap && (long long)c0 + n4 <= a.vcap;
+        norms_aligned && (long long)c0 + n4 <= a.kcap && (long long)c0 + n4 <= a.vcap;
     uint8_t* kb_ = wreg + L.kbuf + slot * 32 * KROW;
     uint8_t* vb_ = wreg + L.vbuf + slot * 32 * VROW;
     float* kn_ = (float*)(wreg + L.kn + slot * 128);
     float* vn_ = (float*)(wreg + L.vn + slot * 128);
-    if (!bulk_norms && lane < nv) {
-      kn_[lane] = knp[c0 + lane];
-      vn_[lane] = vnp[c0 + lane];
-      if constexpr (HAS_RES) ((float*)(wreg + L.rn + slot * 128))[lane] = krp[c0 + lane];
+    if (!bulk_norms) {                     // warp-uniform
+      if (lane < nv) {
+        kn_[lane] = knp[c0 + lane];
+        vn_[lane] = vnp[c0 + lane];
+        if constexpr (HAS_RES) ((float*)(wreg + L.rn + slot * 128))[lane] = krp[c0 + lane];
+      }
+      __syncwarp();
     }
-    __syncwarp();
     if (lane == 0) {
       uint32_t bytes = nv * (KROW + VROW) + (bulk_norms ? 2 * n4 * 4 : 0);
       if constexpr (HAS_RES) bytes += nv * 16 + (bulk_norms ? n4 * 4 : 0);
@@ -521,16 +525,19 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
       }
     }
   }
-  // the warp's first NS - 1 chunks (c = t_begin + 32 warp + 128 j) go in flight now
+  // every warp's first chunk (c = t_begin + 32 warp) goes in flight now; its
+  // next NS - 2 follow after the CTA barrier below, so that the first chunks
+  // of all warps are not queued behind the later ones
+  if (!window_split && t_begin + 32 * warp < t_end) issue(t_begin + 32 * warp, 0);
+
+  __syncthreads();                                   // cks, cvs, svs
   if (!window_split) {
 #pragma unroll
-    for (int j = 0; j < NS - 1; ++j) {
+    for (int j = 1; j < NS - 1; ++j) {
       const int c = t_begin + 32 * warp + 32 * kDWarps * j;
       if (c < t_end) issue(c, j);
     }
   }
-
-  __syncthreads();                                   // cks, cvs, svs
   for (int i = tid; i < 256; i += kDT) {
     if constexpr (KB == 2 || KB == 3) {
       if (i < (1 << (2 * KB))) {
@@ -683,7 +690,7 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
   if (!window_split) {
     // online-softmax state of heads 2tig, 2tig+1 (accumulator columns)
     float m0 = kNegBig, m1 = kNegBig, l0 = 0.f, l1 = 0.f;
-    float dscale = 1.f;      // d holds the V sum times dscale
+    float inv_d = 1.f;       // d holds the V sum divided by inv_d (a power of two)
     float d[8][4];           // fp32 V-sum accumulators (MMA layout)
 #pragma unroll
     for (int k = 0; k < 8; ++k)
@@ -792,12 +799,19 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
       const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
       m0 = mn0;
       m1 = mn1;
+      // fp16 weights scaled into range by a power of two: every weight
+      // p ||v|| is at most the chunk's largest value norm (p <= 1), which maps
+      // below 2^15; the exponent is clamped to [2^-60, 2^64] so that the
+      // accumulator, kept in the latest chunk's scale, stays finite
+      int sexp = 141 - (int)((__float_as_uint(vmax) >> 23) & 0xFFu);   // 14 - floor(log2 vmax)
+      sexp = sexp > 64 ? 64 : sexp < -60 ? -60 : sexp;
+      const float scl = __int_as_float((127 + sexp) << 23);
       float w[2][4];
       float ploc = 0.f, ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
         const int ta = 16 * mt + mg, tb = ta + 8;
-        const float va = ta < nv ? vn_[ta] : 0.f, vb = tb < nv ? vn_[tb] : 0.f;
+        const float va = ta < nv ? vn_[ta] * scl : 0.f, vb = tb < nv ? vn_[tb] * scl : 0.f;
         const float p0 = ex2(sc[mt][0] - mn0), p1 = ex2(sc[mt][1] - mn1);
         const float p2 = ex2(sc[mt][2] - mn0), p3 = ex2(sc[mt][3] - mn1);
         ps0 += p0 + p2;
@@ -815,29 +829,23 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
       // (relative to the running maximum), only the accumulator is rescaled
       bool skip_v = false;
       if constexpr (SPARSE) skip_v = warp_max(ploc) < a.sparse_thr;
-      // fp16 weights scaled into range: every weight p ||v|| is at most the
-      // chunk's largest value norm (p <= 1), which maps to 16384 (capped at
-      // 2^64 so that the accumulator, kept in the latest chunk's scale, stays
-      // finite); vmax was reduced right after the chunk arrived, off the
-      // softmax's dependency chain
-      const float scl = vmax > 0.f ? fminf(16384.f / vmax, 1.8446744073709552e19f) : 1.f;
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
         // tokens 16mt + mg and 16mt + mg + 8: weight pair 8mt + mg
         if (h0ok && !skip_v) {
-          const __half2 h = __floats2half2_rn(w[mt][0] * scl, w[mt][2] * scl);
+          const __half2 h = __floats2half2_rn(w[mt][0], w[mt][2]);
           ws32[(2 * tig) * kWsStride + 8 * mt + mg] = *(const uint32_t*)&h;
         }
         if (h1ok && !skip_v) {
-          const __half2 h = __floats2half2_rn(w[mt][1] * scl, w[mt][3] * scl);
+          const __half2 h = __floats2half2_rn(w[mt][1], w[mt][3]);
           ws32[(2 * tig + 1) * kWsStride + 8 * mt + mg] = *(const uint32_t*)&h;
         }
       }
       __syncwarp();
       // ---- rotated-domain V sum on the tensor cores: d holds the sum times
       // the current chunk's weight scale; rescale, then d += V^T W
-      const float rs = skip_v ? 1.f : scl / dscale;
-      if (!skip_v) dscale = scl;
+      const float rs = skip_v ? 1.f : scl * inv_d;     // a power of two, exact
+      if (!skip_v) inv_d = __uint_as_float(0x7F000000u - __float_as_uint(scl));   // 1 / scl
       const float2 pre = make_float2(al0 * rs, al1 * rs);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
@@ -855,7 +863,7 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
       __syncwarp();
     }
     {
-      const float inv = 1.f / dscale;             // back to the unscaled sum
+      const float inv = inv_d;                    // back to the unscaled sum
 #pragma unroll
       for (int k = 0; k < 8; ++k)
 #pragma unroll
@@ -994,15 +1002,16 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
     }
   }
   // the CTA's partial writes are ordered before the counter update by the
-  // barrier and one gpu-scope fence (cumulative); the last CTA fences again
-  // before it reads the other splits' partials
+  // barrier and the update's release semantics (cumulative, gpu scope); its
+  // acquire side orders the last CTA's reads of the other splits' partials
   __syncthreads();
   if (tid == 0) {
-    __threadfence();
-    const unsigned prev = atomicAdd(&a.counters[unit], 1u);
-    const bool last = prev == (unsigned)(a.n_splits - 1);
-    if (last) __threadfence();
-    *is_last = last;
+    unsigned prev;
+    asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;"
+                 : "=r"(prev)
+                 : "l"(a.counters + unit)
+                 : "memory");
+    *is_last = prev == (unsigned)(a.n_splits - 1);
   }
   __syncthreads();
   if (!*is_last) return;
