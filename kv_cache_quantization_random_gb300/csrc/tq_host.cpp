@@ -466,7 +466,7 @@ struct DecodePlan {
 };
 // Splits of one decode launch for a layer of format s: one wave of about
 // kDecodeSms x decode_ctas_per_sm CTAs of decode_warps(...) warps.  The window is
-// cut into splits of at most 16 tokens per warp; the quantized tokens of each
+// cut into splits of at most 32 tokens per warp; the quantized tokens of each
 // (sequence, kv-head) are split evenly in multiples of 32 tokens over the rest.
 static DecodePlan decode_plan(const tq_config* cfg, const tq_layer_spec& s, int batch,
                               int n_q_heads, int n_kv_heads, int max_seq_len) {
@@ -479,12 +479,16 @@ static DecodePlan decode_plan(const tq_config* cfg, const tq_layer_spec& s, int 
   const int res = s.k_mode == TQ_MODE_MSE_QJL ? 1 : s.k_mode == TQ_MODE_MSE_SIGN ? 2 : 0;
   const int warps = decode_warps(p.G, s.k_bits, s.v_bits, res);
   int wst = (W + 31) / 32 * 32;
-  if (wst > 16 * warps) wst = 16 * warps;
+  if (wst > 32 * warps) wst = 32 * warps;
   p.wsplit_tokens = wst > 0 ? wst : 1;
   const int n_wsplits = W > 0 ? (W + wst - 1) / wst : 0;
   const long long wave = (long long)kDecodeSms * decode_ctas_per_sm(warps);
   long long slots = wave - units * n_wsplits;
-  if (slots < units) slots = units;
+  if (slots < units) {
+    // more than one wave: the quantized splits alone fill the wave (the short
+    // window splits run after them, longest first), at least one per pair
+    slots = (wave / units > 0 ? wave / units : 1) * units;
+  }
   long long per = units > 0 ? (units * max_nq + slots - 1) / slots : 0;
   long long st = (per + 31) / 32 * 32;
   if (st < 256) st = 256;

@@ -162,10 +162,11 @@ def test_decode_ragged_edges_with_window(B):
     assert rel_l2_per_head(out[1:], ref[1:]).max() < TOL
 
 
-@pytest.mark.parametrize("W", [100, 256])
+@pytest.mark.parametrize("W", [100, 256, 520])
 def test_decode_window_spread_over_several_splits(B, W):
-    """A window of W tokens is split 32 tokens per CTA; sequences shorter than
-    the window leave some of those splits partly or wholly empty."""
+    """A window of W tokens is split at most 32 tokens per warp of a CTA (520
+    tokens take two 12-warp CTAs); sequences shorter than the window leave
+    some of those splits partly or wholly empty."""
     seq = [5, 31, 33, 64, W - 1, W, W + 1, W + 64, 900]
     out, ref, _ = _decode_case(B, batch=len(seq), hq=8, hkv=2, seq=seq, kb=4, vb=2, W=W)
     assert rel_l2_per_head(out, ref).max() < TOL
