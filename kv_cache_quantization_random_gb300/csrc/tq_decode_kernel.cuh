@@ -142,24 +142,37 @@ __device__ __forceinline__ void vmma_ktile(const uint8_t* vbuf, const uint32_t* 
       mma16816(d[k], a0, a1, a2, a3, b0, b1);
     }
   } else if constexpr (VB == 3) {
-    // 48 bits of coordinates 16g..16g+15 start at byte 6g of a 48-byte row
+    // 48 bits of coordinates 16g..16g+15 start at byte 6g of a 48-byte row;
+    // as two words: lo = bits 0-31, hi = bits 32-47
     const int bo = 6 * g;
     const int sh = 8 * (bo & 3);
-    auto bits48 = [&](const uint8_t* r) {
+    auto bits48 = [&](const uint8_t* r, uint32_t& lo, uint32_t& hi) {
       const uint32_t* w = (const uint32_t*)(r + (bo & ~3));
-      return (((uint64_t)w[1] << 32) | w[0]) >> sh;
+      lo = __funnelshift_r(w[0], w[1], sh);
+      hi = w[1] >> sh;
     };
-    const uint64_t v0 = bits48(r0), v1 = bits48(r1), v2 = bits48(r2), v3 = bits48(r3);
-    auto pair_off = [](uint64_t va, uint64_t vb, int i) {
-      const uint32_t x = (uint32_t)(va >> (3 * i)), y = (uint32_t)(vb >> (3 * i));
-      return ((x << 2) & 0x1Cu) | ((y << 5) & 0xE0u);
+    uint32_t l0, h0, l1, h1, l2, h2, l3, h3;
+    bits48(r0, l0, h0);
+    bits48(r1, l1, h1);
+    bits48(r2, l2, h2);
+    bits48(r3, l3, h3);
+    // the 3-bit field at bit P of (hi:lo) moved to bit Q (compile-time P, Q)
+    auto field = [](uint32_t lo, uint32_t hi, int P, int Q) -> uint32_t {
+      if (P < Q) return lo << (Q - P);
+      if (P - Q < 32) return __funnelshift_r(lo, hi, P - Q);
+      return hi >> (P - Q - 32);
+    };
+    // byte offset 4e of pair entry e = x | y << 3 for codes x (first token)
+    // and y (second token)
+    auto pair_off = [&](uint32_t la, uint32_t ha, uint32_t lb, uint32_t hb, int i) {
+      return (field(la, ha, 3 * i, 2) & 0x1Cu) | (field(lb, hb, 3 * i, 5) & 0xE0u);
     };
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const uint32_t a0 = lut_u32(lutp, pair_off(v0, v1, 2 * k));
-      const uint32_t a1 = lut_u32(lutp, pair_off(v0, v1, 2 * k + 1));
-      const uint32_t a2 = lut_u32(lutp, pair_off(v2, v3, 2 * k));
-      const uint32_t a3 = lut_u32(lutp, pair_off(v2, v3, 2 * k + 1));
+      const uint32_t a0 = lut_u32(lutp, pair_off(l0, h0, l1, h1, 2 * k));
+      const uint32_t a1 = lut_u32(lutp, pair_off(l0, h0, l1, h1, 2 * k + 1));
+      const uint32_t a2 = lut_u32(lutp, pair_off(l2, h2, l3, h3, 2 * k));
+      const uint32_t a3 = lut_u32(lutp, pair_off(l2, h2, l3, h3, 2 * k + 1));
       mma16816(d[k], a0, a1, a2, a3, b0, b1);
     }
   } else if constexpr (VB == 4) {
@@ -205,9 +218,10 @@ __device__ __forceinline__ void vmma_ktile(const uint8_t* vbuf, const uint32_t* 
 // 2tig+1 (and 2tig+8, 2tig+9) of k-tile kt, mapped to coordinates 32tig+4kt,
 // +1 (and +2, +3), so its 32 coordinates are contiguous in a packed row.
 // Key tables (centroids x kCScale): 2, 3 and 4 bits: uint2 (hi pair, lo pair)
-// indexed by the code pair (c_i | c_{i+1} << KB); the 4-bit table (256 pairs)
-// is kept in 16 replicas interleaved 8 bytes apart, lane l reading replica
-// l % 16, so the 16 lanes of a half-warp always hit 16 different bank pairs;
+// indexed by the code pair (c_i | c_{i+1} << KB); the 3- and 4-bit tables (64
+// and 256 pairs) are kept in 16 replicas interleaved 8 bytes apart, lane l
+// reading replica l % 16, so the 16 lanes of a half-warp always hit 16
+// different bank pairs;
 // 8 bits: u32 hi | lo << 16 per code.
 template <int KB>
 struct KCodes {  // one token's 32 codes for this thread, as table offsets
@@ -249,20 +263,19 @@ __device__ __forceinline__ void kpair(const KCodes<KB>& c, const uint32_t* lut, 
     hi = e.x;
     lo = e.y;
   } else if constexpr (KB == 3) {
-    constexpr int o = 3 * I;                     // bit offset of the pair (6 bits)
+    // the pair's 6 bits start at bit o of the 96 code bits; the 64-entry table
+    // is kept in 16 replicas like the 4-bit one (entries 128 B apart, lut at
+    // this lane's replica), so the offset is the field moved to bit 7
+    constexpr int o = 3 * I, wi = o / 32, b = o % 32;
     uint32_t v;
-    if constexpr (o + 6 <= 32) {
-      v = c.w[0] >> o;
-    } else if constexpr (o < 32) {
-      v = (c.w[0] >> o) | (c.w[1] << (32 - o));
-    } else if constexpr (o + 6 <= 64) {
-      v = c.w[1] >> (o - 32);
-    } else if constexpr (o < 64) {
-      v = (c.w[1] >> (o - 32)) | (c.w[2] << (64 - o));
+    if constexpr (b < 7) {
+      v = c.w[wi] << (7 - b);
+    } else if constexpr (b + 6 <= 32) {
+      v = c.w[wi] >> (b - 7);
     } else {
-      v = c.w[2] >> (o - 64);
+      v = __funnelshift_r(c.w[wi], c.w[wi + 1], b - 7);
     }
-    const uint2 e = *(const uint2*)((const char*)lut + ((v << 3) & 0x1F8u));
+    const uint2 e = *(const uint2*)((const char*)lut + (v & 0x1F80u));
     hi = e.x;
     lo = e.y;
   } else if constexpr (KB == 4) {
@@ -354,11 +367,12 @@ __device__ __forceinline__ void sign_scores(uint32_t sa, uint32_t sb, const uint
 }
 
 // QJL: sum_j (2 bit_j - 1) (S q)_j for tokens ta, ta+8: A = exact +-1 signs,
-// B = S q hi and lo (per lane, per k-tile, from shared memory: (b0 hi, b1 hi,
-// b0 lo, b1 lo)).  Folded, the lane's column is one part, chosen by `part`.
+// B = S q hi and lo from shared memory, k-tile-major so that a warp's 32
+// lanes read contiguous words: unfolded, uint4 (b0 hi, b1 hi, b0 lo, b1 lo)
+// at [kt][lane]; folded, the lane's part (hi or lo) as uint2 at [kt][lane].
 template <bool FOLD>
 __device__ __forceinline__ void qjl_scores(uint32_t sa, uint32_t sb, const uint32_t* slut,
-                                           const uint4* qb, int part, float (&d)[4],
+                                           const void* qb, int lane, float (&d)[4],
                                            float (&dl)[4]) {
 #pragma unroll
   for (int kt = 0; kt < 8; ++kt) {
@@ -366,10 +380,10 @@ __device__ __forceinline__ void qjl_scores(uint32_t sa, uint32_t sb, const uint3
     const uint32_t a0 = slut[(sa >> (4 * kt)) & 3u], a1 = slut[(sb >> (4 * kt)) & 3u];
     const uint32_t a2 = slut[(sa >> (4 * kt + 2)) & 3u], a3 = slut[(sb >> (4 * kt + 2)) & 3u];
     if constexpr (FOLD) {
-      const uint2 b = ((const uint2*)(qb + kt))[part];
+      const uint2 b = ((const uint2*)qb)[kt * 32 + lane];
       mma16816(d, a0, a1, a2, a3, b.x, b.y);
     } else {
-      const uint4 b = qb[kt];
+      const uint4 b = ((const uint4*)qb)[kt * 32 + lane];
       mma16816(d, a0, a1, a2, a3, b.x, b.y);
       mma16816(dl, a0, a1, a2, a3, b.z, b.w);
     }
@@ -539,22 +553,24 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
     }
   }
   for (int i = tid; i < 256; i += kDT) {
-    if constexpr (KB == 2 || KB == 3) {
-      if (i < (1 << (2 * KB))) {
-        const int msk = (1 << KB) - 1;
+    if constexpr (KB == 2) {
+      if (i < 16) {
         uint32_t hp, lp;
-        hilo2(cks[i & msk] * kCScale, cks[(i >> KB) & msk] * kCScale, hp, lp);
+        hilo2(cks[i & 3] * kCScale, cks[(i >> 2) & 3] * kCScale, hp, lp);
         lutk[2 * i] = hp;
         lutk[2 * i + 1] = lp;
       }
-    } else if constexpr (KB == 4) {
-      // pair i = c_lo | c_hi << 4 into all 16 replicas; at step j lane l
+    } else if constexpr (KB == 3 || KB == 4) {
+      // pair i = c_lo | c_hi << KB into all 16 replicas; at step j lane l
       // writes replica (l + j) % 16, so a half-warp's stores never collide
-      uint32_t hp, lp;
-      hilo2(cks[i & 15] * kCScale, cks[i >> 4] * kCScale, hp, lp);
-      uint2* row = (uint2*)(smem + L.lutk4) + i * 16;
+      if (i < (1 << (2 * KB))) {
+        constexpr int msk = (1 << KB) - 1;
+        uint32_t hp, lp;
+        hilo2(cks[i & msk] * kCScale, cks[i >> KB] * kCScale, hp, lp);
+        uint2* row = (uint2*)(smem + L.lutk4) + i * 16;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) row[(lane + j) & 15] = make_uint2(hp, lp);
+        for (int j = 0; j < 16; ++j) row[(lane + j) & 15] = make_uint2(hp, lp);
+      }
     } else {
       lutk[i] = hilo(cks[i] * kCScale);
     }
@@ -666,18 +682,21 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
     int se = 0;
     (void)frexpf(smax, &se);
     qsq = smax > 0.f ? ldexpf(1.f, -se) : 1.f;
-    // per lane, per k-tile: (b0 hi, b1 hi, b0 lo, b1 lo) of head lane/4 (folded:
-    // (lane/4) % 4), sketch indices 32(lane%4) + 4kt + {0,1} / {2,3}
-    uint4* qjlb = (uint4*)(smem + L.qjlb);
+    // per k-tile, per lane: (b0 hi, b1 hi, b0 lo, b1 lo) of head lane/4 (folded:
+    // (lane/4) % 4, and only the lane's part), sketch indices 32(lane%4) + 4kt
+    // + {0,1} / {2,3}
     for (int e = tid; e < 32 * 8; e += kDT) {
-      const int ln = e / 8, kt = e % 8, g = FOLD ? (ln >> 2) & 3 : ln >> 2, tg = ln & 3;
+      const int kt = e / 32, ln = e % 32, g = FOLD ? (ln >> 2) & 3 : ln >> 2, tg = ln & 3;
       uint4 o = make_uint4(0u, 0u, 0u, 0u);
       if (g < G) {
         const int c = 32 * tg + 4 * kt;
         hilo2(sq[g * kQjlM + c] * qsq, sq[g * kQjlM + c + 1] * qsq, o.x, o.z);
         hilo2(sq[g * kQjlM + c + 2] * qsq, sq[g * kQjlM + c + 3] * qsq, o.y, o.w);
       }
-      qjlb[e] = o;
+      if constexpr (FOLD)
+        ((uint2*)(smem + L.qjlb))[e] = (ln >> 4) ? make_uint2(o.z, o.w) : make_uint2(o.x, o.y);
+      else
+        ((uint4*)(smem + L.qjlb))[e] = o;
     }
   }
   __syncthreads();
@@ -697,14 +716,15 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
 #pragma unroll
       for (int j = 0; j < 4; ++j) d[k][j] = 0.f;
     const bool h0ok = 2 * tig < G, h1ok = 2 * tig + 1 < G;
-    const uint32_t* klut = KB == 4 ? (const uint32_t*)(smem + L.lutk4 + 8 * (lane & 15)) : lutk;
+    const uint32_t* klut =
+        KB == 3 || KB == 4 ? (const uint32_t*)(smem + L.lutk4 + 8 * (lane & 15)) : lutk;
     // [8 heads][16 pairs] fp16 weights: pair 8kt + j = tokens 16kt + j, 16kt + j + 8
     uint32_t* ws32 = (uint32_t*)(wreg + L.ws);
     const float kscale = 1.f / (kCScale * qsp);
     // residual-term scale: QJL sqrt(pi/2)/m over the S q operand scale;
     // Direct Sign 1 over the q operand scale
     const float res_scale = QJL ? 1.2533141373155003f / (float)kQjlM / qsq : 1.f / qsp;
-    const uint4* qjlb = QJL ? (const uint4*)(smem + L.qjlb) + lane * 8 : nullptr;
+    const void* qjlb = QJL ? (const void*)(smem + L.qjlb) : nullptr;
 
     int c0 = t_begin + 32 * warp;           // its copies were started in the prologue
     bool ok = true;
@@ -767,7 +787,7 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
             const uint32_t sa = *(const uint32_t*)(sb_ + ta * 16 + 4 * tig);
             const uint32_t sbits = *(const uint32_t*)(sb_ + tb * 16 + 4 * tig);
             float qa[4] = {0.f, 0.f, 0.f, 0.f}, ql[4] = {0.f, 0.f, 0.f, 0.f};
-            if constexpr (QJL) qjl_scores<FOLD>(sa, sbits, slut, qjlb, mg >> 2, qa, ql);
+            if constexpr (QJL) qjl_scores<FOLD>(sa, sbits, slut, qjlb, lane, qa, ql);
             else sign_scores<FOLD>(sa, sbits, slut, bh, bl, qa, ql);
             const float ga = rn_[ta] * res_scale, gb = rn_[tb] * res_scale;
             sc[mt][0] = fmaf(qa[0] + ql[0], ga, sc[mt][0]);

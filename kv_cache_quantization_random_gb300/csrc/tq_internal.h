@@ -38,7 +38,7 @@ struct DecodeSmem {
     sv = off; off += kHeadDim * 4;
     qjlb = off; off += qjl ? 32 * 8 * 16 : 0;     // per lane, per k-tile: S q hi/lo operands
     sq = off; off += qjl ? G * kQjlM * 4 : 0;     // [G][m] S q_rot (QJL)
-    lutk4 = off; off += kb == 4 ? 256 * 16 * 8 : 0;   // 4-bit key pair table, 16 replicas
+    lutk4 = off; off += kb == 4 ? 256 * 16 * 8 : kb == 3 ? 64 * 16 * 8 : 0;   // 3/4-bit key pairs, 16 replicas
     warps = off;
     const int ns = ring_slots(kb, vb);
     int w = 0;
