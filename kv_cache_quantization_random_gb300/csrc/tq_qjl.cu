@@ -16,6 +16,9 @@
 // stays in shared memory for the whole launch.  TMEM lane t holds z for key
 // t, so after the commit each warp reads its 32 lanes with tcgen05.ld and
 // every thread turns its own 128 projections into 4 words of sign bits.
+// bf16 rows are staged in the R lo tile itself (a CTA barrier separates the
+// last read of a row from the first residual write), which leaves room for
+// two CTAs per SM; fp32 rows keep a buffer of their own and one CTA per SM.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -25,16 +28,18 @@
 
 namespace tq {
 
+// bf16 rows are staged in the R lo tile (read into registers before R lo is
+// written), so a CTA fits twice on an SM; fp32 rows need their own buffer.
 __host__ __device__ constexpr size_t qjl_smem_bytes(bool f32, int cells) {
   return 1024                                    // alignment slack
          + 3 * (size_t)kOpBytes                  // R hi, R lo, S
-         + quant_rows_bytes(f32)                 // staged rows (one tile)
+         + (f32 ? quant_rows_bytes(true) : 0)    // staged fp32 rows (one tile)
          + (size_t)cells * 8 + 2 * 256 * 4       // grid, boundaries, centroids
          + 16;                                   // mbarrier + TMEM address
 }
 
 template <int BITS, bool F32>
-__global__ void __launch_bounds__(kQRows, 1) quantize_qjl_kernel(const QuantArgs a) {
+__global__ void __launch_bounds__(kQRows, F32 ? 1 : 2) quantize_qjl_kernel(const QuantArgs a) {
   constexpr int kPitch = RowCfg<F32>::kPitch;
   extern __shared__ uint8_t smem_raw[];
   // operand tiles on a 1 KB boundary
@@ -42,8 +47,8 @@ __global__ void __launch_bounds__(kQRows, 1) quantize_qjl_kernel(const QuantArgs
   uint8_t* ahi = base;
   uint8_t* alo = base + kOpBytes;
   uint8_t* sop = base + 2 * kOpBytes;
-  uint8_t* rows = base + 3 * kOpBytes;
-  float2* grid = (float2*)(rows + quant_rows_bytes(F32));
+  uint8_t* rows = F32 ? base + 3 * kOpBytes : alo;
+  float2* grid = (float2*)(base + 3 * kOpBytes + (F32 ? quant_rows_bytes(true) : 0));
   float* bnd = (float*)(grid + a.grid_cells);
   float* cen = bnd + 256;
   uint64_t* bar = (uint64_t*)(cen + 256);
@@ -90,7 +95,8 @@ __global__ void __launch_bounds__(kQRows, 1) quantize_qjl_kernel(const QuantArgs
     const void* src = nullptr;
     long long drow = 0;
     const bool valid = v < total && resolve_row(a, v, &src, &drow);
-    stage_rows<F32>(src, valid, rows + warp * 32 * kPitch, lane);
+    if constexpr (F32) stage_rows<F32>(src, valid, rows + warp * 32 * kPitch, lane);
+    else stage_rows_swz(src, valid, rows, 32 * warp, lane);
     cp_async_commit();
     cp_async_wait<0>();
     __syncwarp();
@@ -99,8 +105,9 @@ __global__ void __launch_bounds__(kQRows, 1) quantize_qjl_kernel(const QuantArgs
     {
       float2 p[64];
       if (valid) {
-        const float nrm = quantize_row<BITS, F32, (BITS > 4), true>(
-            a, rows + tid * kPitch, grid_base, kmax, cen, a.codes + drow * (16 * BITS), p);
+        const float nrm = quantize_row<BITS, F32, (BITS > 4), true, !F32>(
+            a, rows + tid * (F32 ? kPitch : 256), grid_base, kmax, cen,
+            a.codes + drow * (16 * BITS), p, tid & 7);
         a.norms[drow] = nrm;
         float2 g2 = make_float2(0.f, 0.f);
 #pragma unroll
@@ -110,6 +117,8 @@ __global__ void __launch_bounds__(kQRows, 1) quantize_qjl_kernel(const QuantArgs
 #pragma unroll
         for (int j = 0; j < 64; ++j) p[j] = make_float2(0.f, 0.f);
       }
+      // bf16 rows live in the R lo tile: every thread has read its row
+      if constexpr (!F32) __syncthreads();
       // p[j] = (r_j, r_{j+64}); chunk c of the row holds coordinates 8c .. 8c+7
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
@@ -119,11 +128,12 @@ __global__ void __launch_bounds__(kQRows, 1) quantize_qjl_kernel(const QuantArgs
           const int i0 = 8 * c + 2 * u;                 // coordinates i0, i0 + 1
           const float r0 = i0 < 64 ? p[i0].x : p[i0 - 64].y;
           const float r1 = i0 + 1 < 64 ? p[i0 + 1].x : p[i0 + 1 - 64].y;
-          const __nv_bfloat16 h0 = __float2bfloat16_rn(r0), h1 = __float2bfloat16_rn(r1);
-          const __nv_bfloat16 l0 = __float2bfloat16_rn(r0 - __bfloat162float(h0));
-          const __nv_bfloat16 l1 = __float2bfloat16_rn(r1 - __bfloat162float(h1));
-          hw[u] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-          lw[u] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+          // packed conversions: hi = bf16(r), lo = bf16(r - hi)
+          const __nv_bfloat162 h = __floats2bfloat162_rn(r0, r1);
+          const float2 hf = __bfloat1622float2(h);
+          const __nv_bfloat162 l = __floats2bfloat162_rn(r0 - hf.x, r1 - hf.y);
+          hw[u] = *(const uint32_t*)&h;
+          lw[u] = *(const uint32_t*)&l;
         }
         *(uint4*)(ahi + op_offset(tid, c)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
         *(uint4*)(alo + op_offset(tid, c)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
@@ -190,7 +200,7 @@ static int launch_qjl_t(const QuantArgs& a, cudaStream_t s) {
     return 1;
   const long long total = (long long)a.B * a.H * a.n;
   const long long ntiles = (total + kQRows - 1) / kQRows;
-  long long grid = sm_count();              // one CTA per SM (shared memory bound)
+  long long grid = (long long)sm_count() * (F32 ? 1 : 2);   // CTAs resident per SM
   if (grid > ntiles) grid = ntiles;
   k<<<(unsigned)grid, kQRows, smem, s>>>(a);
   return cudaGetLastError() != cudaSuccess;

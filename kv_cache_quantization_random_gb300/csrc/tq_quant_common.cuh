@@ -86,11 +86,32 @@ __device__ __forceinline__ void stage_rows(const void* src, bool valid, uint8_t*
   }
 }
 
+// bf16 rows packed 256 bytes apart with their 16-byte chunks permuted: chunk
+// c of row r sits at position (c & 8) | ((c ^ r) & 7), so that the 32 lanes
+// of a warp, reading the same chunk of 32 consecutive rows, hit 8 different
+// bank groups per quarter-warp.  A tile of 128 such rows fills 32 KB.
+__device__ __forceinline__ int swz_chunk(int c, int r) { return (c & 8) | ((c ^ r) & 7); }
+
+// stage_rows for the permuted bf16 layout (rows 256 bytes apart)
+__device__ __forceinline__ void stage_rows_swz(const void* src, bool valid, uint8_t* rows,
+                                               int row0, int lane) {
+  const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+  const int c = lane % 16;
+#pragma unroll 4
+  for (int pass = 0; pass < 16; ++pass) {
+    const int r = pass * 2 + lane / 16;
+    const uint8_t* sp = (const uint8_t*)__shfl_sync(0xffffffffu, (unsigned long long)src, r);
+    if ((vmask >> r) & 1u)
+      cp_async16(rows + (row0 + r) * 256 + 16 * swz_chunk(c, row0 + r), sp + 16 * c);
+  }
+}
+
 // Rotated coordinates of one vector, held as pairs (y_j, y_{j+64}), j < 64,
 // so that six of the seven butterfly stages run on packed fp32 pairs.
-template <bool F32>
+// SWZ: bf16 row in the permuted layout, rsw = its row index (mod 8).
+template <bool F32, bool SWZ = false>
 __device__ __forceinline__ float load_rotate(const QuantArgs& a, const uint8_t* row,
-                                             float2 (&p)[64]) {
+                                             float2 (&p)[64], int rsw = 0) {
   if constexpr (F32) {
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
@@ -104,8 +125,9 @@ __device__ __forceinline__ float load_rotate(const QuantArgs& a, const uint8_t* 
   } else {
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-      const uint4 lo = lds128(row + 16 * c);            // coordinates 8c .. 8c+7
-      const uint4 hi = lds128(row + 128 + 16 * c);      // coordinates 64+8c ..
+      const int pc = SWZ ? (c ^ rsw) & 7 : c;           // chunk position in the row
+      const uint4 lo = lds128(row + 16 * pc);           // coordinates 8c .. 8c+7
+      const uint4 hi = lds128(row + 128 + 16 * pc);     // coordinates 64+8c ..
       const uint32_t l[4] = {lo.x, lo.y, lo.z, lo.w};
       const uint32_t h[4] = {hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
@@ -239,12 +261,12 @@ __device__ __forceinline__ void search_pack(const QuantArgs& a, float2 (&p)[64],
 // memory); the codes go to codes_dst (16 * BITS bytes).  Returns ||x||.  With
 // RESID, p holds the rotated-domain residual n (y - c[idx]) afterwards (pairs
 // (r_j, r_{j+64})), from the centroids `cen` in shared memory.
-template <int BITS, bool F32, bool CLAMP, bool RESID>
+template <int BITS, bool F32, bool CLAMP, bool RESID, bool SWZ = false>
 __device__ __forceinline__ float quantize_row(const QuantArgs& a, const uint8_t* row,
                                               uint32_t grid_base, uint32_t kmax,
                                               const float* cen, uint8_t* codes_dst,
-                                              float2 (&p)[64]) {
-  const float nrm = load_rotate<F32>(a, row, p);
+                                              float2 (&p)[64], int rsw = 0) {
+  const float nrm = load_rotate<F32, SWZ>(a, row, p, rsw);
   search_pack<BITS, CLAMP, RESID>(a, p, nrm, grid_base, kmax, cen, codes_dst);
   return nrm;
 }
