@@ -252,28 +252,46 @@ def run_ours(args, w, rank, world, local):
     for _ in range(3):
         quantize_all()
     torch.cuda.synchronize()
-    # device time of the two launches, without the host's per-call overhead:
+    # device time of the launches, without the host's per-call overhead:
     # qiters calls replayed from one CUDA graph, best of 5 replays
     qiters = 10
-    gq = torch.cuda.CUDAGraph()
-    sq = torch.cuda.Stream()
-    sq.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(sq):
-        with torch.cuda.graph(gq, stream=sq):
-            for _ in range(qiters):
-                quantize_all()
-    torch.cuda.current_stream().wait_stream(sq)
-    gq.replay()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    q_ms = float("inf")
-    for _ in range(5):
-        e0.record()
+
+    def graph_ms(fn):
+        gq = torch.cuda.CUDAGraph()
+        sq = torch.cuda.Stream()
+        sq.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(sq):
+            with torch.cuda.graph(gq, stream=sq):
+                for _ in range(qiters):
+                    fn()
+        torch.cuda.current_stream().wait_stream(sq)
         gq.replay()
-        e1.record()
         torch.cuda.synchronize()
-        q_ms = min(q_ms, e0.elapsed_time(e1) / qiters)
-    del gq
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        best = float("inf")
+        for _ in range(5):
+            e0.record()
+            gq.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1) / qiters)
+        return best
+
+    q_ms = graph_ms(quantize_all)
+    # keys in MSE+QJL mode: the QJL kernel alone, and the rate of its
+    # projection, 2 (hi, lo) x 2 x keys x m x d flops on the tensor cores
+    qjl_proj = None
+    if w.k_qjl:
+        k_ms = graph_ms(lambda: B.tq_quantize_kv(cfg, tables, 0, 0, K[:, :, :nq], kp))
+        n_keys = w.batch * w.n_kv_heads * nq
+        flops = 2 * 2 * n_keys * w.qjl_m * w.head_dim
+        tflops = flops / (k_ms * 1e-3) / 1e12
+        bf16_peak = float(peaks["bf16_tflops"])
+        qjl_proj = {"kernel": "tq::quantize_qjl_kernel", "ms": k_ms, "gflop": flops / 1e9,
+                    "tflops": tflops, "bf16_peak_tflops": bf16_peak,
+                    "frac_of_bf16_peak": tflops / bf16_peak, "peak_source": f"{peak_kind} bf16_tflops",
+                    "note": "projection flops over the whole kernel's time (codes, norms and residuals "
+                            "included); ncu's sm__pipe_tensor_cycles_active is in profiles/"}
     n_vec = w.batch * w.n_kv_heads * nq
     in_b = w.head_dim * (4 if w.in_dtype == "fp32" else 2)
     kbts, vbts = packed_bytes(w)
@@ -515,6 +533,8 @@ def run_ours(args, w, rank, world, local):
     }
     if multi is not None:
         res["multi_query"] = multi
+    if qjl_proj is not None:
+        res["qjl_projection"] = qjl_proj
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w, st, q, seq, budget_s=args.cpu_seconds)
     return res

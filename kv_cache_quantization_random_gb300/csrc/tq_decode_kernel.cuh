@@ -953,7 +953,7 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int k = k0 + u * kDWarps;
-        if (k < nw) {
+        if (k < kw1) {
           const long long slotrow = (base + (tw0 + k) % W) * kD2;
           kw[u] = *(const uint2*)(a.kwin + slotrow + 4 * lane);
           vw[u] = *(const uint2*)(a.vwin + slotrow + 4 * lane);
@@ -961,7 +961,7 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        if (k0 + u * kDWarps >= nw) break;
+        if (k0 + u * kDWarps >= kw1) break;
         const float kx[4] = {bf16lo(kw[u].x), bf16hi(kw[u].x), bf16lo(kw[u].y), bf16hi(kw[u].y)};
         const float vx[4] = {bf16lo(vw[u].x), bf16hi(vw[u].x), bf16lo(vw[u].y), bf16hi(vw[u].y)};
         const int tpos = tw0 + k0 + u * kDWarps;      // token position
