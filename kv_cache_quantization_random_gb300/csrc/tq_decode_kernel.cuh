@@ -11,9 +11,9 @@
 // items 1 and 2 (dequantized codes fed to tensor-core MMA; the QJL term is a
 // correction from the sign bits and the stored residual scale).
 //
-// One CTA = (split, kv-head, sequence): one CTA of 12 (or 8) warps per SM
-// with G <= 4 query columns and MSE keys, two of 4 warps otherwise
-// (decode_warps).  Prologue: the G query heads
+// One CTA = (split, kv-head, sequence): with MSE keys one CTA per SM of 12
+// (or 8) warps for G <= 4 query columns and of 8 warps for G = 8; with a key
+// residual term two of 4 warps (decode_warps).  Prologue: the G query heads
 // of the kv-head are scaled by softmax_scale*log2(e), rotated with the K sign
 // vector and split into fp16 hi + lo MMA operands held in registers; QJL keys
 // also get S q_rot as hi + lo operands.  Main loop, per warp and 32-token

@@ -67,11 +67,14 @@ constexpr int kDecodeSmemBudget = 216 * 1024;
 
 // Warps of a decode CTA.  G <= 4 query columns with MSE keys (about 168
 // registers a thread): one CTA per SM of 12 warps, or 8 when 12 staging
-// rings do not fit.  Keys with a residual term and G = 8 (up to 255
-// registers): two CTAs of 4 warps per SM, so that one CTA's prologue runs
-// beside the other's main loop (measured faster for these formats).
+// rings do not fit.  G = 8 with MSE keys (about 240 registers): one CTA of 8
+// warps.  Keys with a residual term: two CTAs of 4 warps per SM, so that one
+// CTA's prologue runs beside the other's main loop (measured faster for these
+// formats).  Fewer, wider CTAs build the SM's lookup tables once and leave
+// half as many splits to merge.
 __host__ __device__ constexpr int decode_warps(int G, int kb, int vb, int res) {
-  return (G > 4 || res != 0)                                             ? 4
+  return res != 0                                                        ? 4
+         : G > 4 ? (DecodeSmem(G, res, kb, vb, 8).total <= kDecodeSmemBudget ? 8 : 4)
          : DecodeSmem(G, res, kb, vb, 12).total <= kDecodeSmemBudget ? 12
          : DecodeSmem(G, res, kb, vb, 8).total <= kDecodeSmemBudget  ? 8
                                                                        : 4;
