@@ -227,6 +227,19 @@ def reset_window(st, w):
         st["vw"][:, :, idx % Wn] = st["V"][:, :, nq:T]
 
 
+def window_before_step(st, w, seq):
+    """Window ring as it stands before a step appends token T-1: the slot of
+    token T-1 still holds token T-1-W, which the step's append quantizes."""
+    Wn = w.window
+    if not Wn:
+        return
+    for b, T in enumerate(seq):
+        t = int(T) - 1 - Wn
+        if t >= 0:
+            st["kw"][b, :, t % Wn] = st["K"][b, :, t]
+            st["vw"][b, :, t % Wn] = st["V"][b, :, t]
+
+
 def run_ours(args, w, rank, world, local):
     import numpy as np
     import torch
@@ -344,10 +357,12 @@ def run_ours(args, w, rank, world, local):
                               k_win=kwr, v_win=vwr)
 
     def step(i):
-        append(i % R)
-        decode(i % R)
+        # tq_decode_step: the append and the decode that overlaps it
+        kr, vr, kwr, vwr = reps[i % R]
+        B.tq_decode_step(cfg, tables, 0, q, w.softmax_scale, knew, vnew, seq_before, Tmax, kr, vr,
+                         out, ws, k_win=kwr, v_win=vwr)
 
-    # one fused append launch (one new token per sequence) + one decode launch
+    # one append launch (one new token per sequence) + one decode launch
     launches_per_step = 2
 
     # ---- warmup (direct launches), then capture graphs of S steps
@@ -464,9 +479,8 @@ def run_ours(args, w, rank, world, local):
     def e2e_step(i):
         dbuf.copy_(hbuf, non_blocking=True)
         kr, vr, kwr, vwr = reps[i % R]
-        B.tq_append_kv(cfg, tables, 0, kd, vd, seq_before, kwr, vwr, kr, vr)
-        B.tq_decode_attention(cfg, tables, 0, qd, w.softmax_scale, kr, vr, seq_t, Tmax, out, ws,
-                              k_win=kwr, v_win=vwr)
+        B.tq_decode_step(cfg, tables, 0, qd, w.softmax_scale, kd, vd, seq_before, Tmax, kr, vr,
+                         out, ws, k_win=kwr, v_win=vwr)
         outh.copy_(out, non_blocking=True)
 
     for i in range(3):
@@ -519,9 +533,8 @@ def run_ours(args, w, rank, world, local):
                         sc.wait_event(ev_out[i - 2])           # outs[j] has been read back
                     qd_, kd_, vd_ = dviews[j]
                     kr, vr, kwr, vwr = reps[i % R]
-                    B.tq_append_kv(cfg, tables, 0, kd_, vd_, seq_before, kwr, vwr, kr, vr)
-                    B.tq_decode_attention(cfg, tables, 0, qd_, w.softmax_scale, kr, vr, seq_t, Tmax,
-                                          outs[j], ws, k_win=kwr, v_win=vwr)
+                    B.tq_decode_step(cfg, tables, 0, qd_, w.softmax_scale, kd_, vd_, seq_before, Tmax,
+                                     kr, vr, outs[j], ws, k_win=kwr, v_win=vwr)
                     ev_done.append(torch.cuda.Event())
                     ev_done[i].record(sc)
                     with torch.cuda.stream(cout):
@@ -557,10 +570,12 @@ def run_ours(args, w, rank, world, local):
     parity = None
     if not args.no_parity and rank == 0:
         # the timed steps rewrote one row and one window slot of every replica:
-        # restore replica 0 from the inputs before checking it
+        # restore replica 0 from the inputs, as it stands before the step's
+        # append, and check the output of one step
         quantize_all()
         reset_window(st, w)
-        parity = sampled_parity(B, w, st, q, out, reps[0], seq, decode)
+        window_before_step(st, w, seq)
+        parity = sampled_parity(B, w, st, q, out, reps[0], seq, step)
 
     res = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,

@@ -280,6 +280,26 @@ tq_status tq_decode_attention_multi(const tq_config* cfg, const void* tables, in
                                     const int32_t* seq_lens, int max_seq_len, float* out,
                                     void* workspace, size_t workspace_bytes, void* stream);
 
+/* One decode step of a serving loop: tq_append_kv of one new token per
+ * (sequence, kv-head) (k_new, v_new: [batch][n_kv_heads][1][head_dim] with
+ * src_strides, as there), then tq_decode_attention over the seq_lens_before[b]
+ * + 1 tokens of every sequence, with the same arguments and results as those
+ * two calls ("[GitHub 탐방] TurboQuant 3-bit KV 캐시 압축 — 단일 GPU 재현 기록",
+ * "실험 설계": the newest tokens stay in the bf16 window).  max_seq_len bounds
+ * seq_lens_before[b] + 1.  Two launches: the decode starts while the append
+ * runs and waits for it only before it reads what the append writes (the
+ * window ring, the plane rows from max(seq_lens_before[b] - W, 0) on); with at
+ * most 16 (sequence, kv-head) pairs and short splits the decode leaves the
+ * append's CTA slots free.  The planes, ring and workspace must not be used by other work on the
+ * device meanwhile. */
+tq_status tq_decode_step(const tq_config* cfg, const void* tables, int layer, const void* q,
+                         int q_dtype, float softmax_scale, int batch, int n_q_heads,
+                         int n_kv_heads, const void* k_new, const void* v_new, int src_dtype,
+                         const int64_t src_strides[3], const int32_t* seq_lens_before,
+                         int max_seq_len, uint16_t* k_win, uint16_t* v_win, tq_planes k,
+                         tq_planes v, float* out, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
 /* Synchronize `stream`, then read and clear the device error words.
  * Returns TQ_OK, TQ_ERR_DEVICE_TIMEOUT, TQ_ERR_DEVICE_BOUNDS or TQ_ERR_CUDA. */
 tq_status tq_get_device_error(void* stream);

@@ -36,6 +36,7 @@ EXPORTED = [
     "tq_workspace_bytes", "tq_workspace_init", "tq_quantize_kv", "tq_append_kv",
     "tq_dequantize", "tq_decode_attention", "tq_get_device_error", "tq_set_wait_limit",
     "tq_set_fault_injection", "tq_decode_attention_noalloc", "tq_decode_attention_multi",
+    "tq_decode_step",
 ]
 
 
@@ -108,6 +109,8 @@ def load(build_if_missing: bool = False):
                                             P, P, P, I, P, P]),
         "tq_decode_attention_multi": (I, [cfgp, P, I, P, I, F, I, I, I, I, tq_planes, tq_planes,
                                           P, P, P, I, P, P, SZ, P]),
+        "tq_decode_step": (I, [cfgp, P, I, P, I, F, I, I, I, P, P, I, C.POINTER(I64), P, I, P, P,
+                               tq_planes, tq_planes, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -340,6 +343,25 @@ def tq_decode_attention_multi(cfg: Config, tables, layer: int, q, softmax_scale:
         seq_lens.data_ptr(), max_seq_len, out.data_ptr(), workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _stream_ptr(stream))
     _check(st, "tq_decode_attention_multi")
+
+
+def tq_decode_step(cfg: Config, tables, layer: int, q, softmax_scale: float, k_new, v_new,
+                   seq_lens_before, max_seq_len: int, k: Planes, v: Planes, out, workspace,
+                   k_win=None, v_win=None, stream=None):
+    """tq_append_kv of one token per (sequence, kv-head) (k_new, v_new
+    [B, Hkv, 1, d]) followed by tq_decode_attention over seq_lens_before + 1
+    tokens, as one call (the decode overlaps the append)."""
+    B, Hq, _ = q.shape
+    H = k_new.shape[1]
+    if v_new.shape != k_new.shape or v_new.stride() != k_new.stride() or k_new.shape[2] != 1:
+        raise ValueError("k_new and v_new must be [B, Hkv, 1, d] with the same strides")
+    st = load().tq_decode_step(
+        C.byref(cfg.c()), tables.data_ptr(), layer, q.data_ptr(), _dtype_code(q),
+        float(softmax_scale), B, Hq, H, k_new.data_ptr(), v_new.data_ptr(), _dtype_code(k_new),
+        _strides3(k_new), seq_lens_before.data_ptr(), max_seq_len, _ptr(k_win), _ptr(v_win),
+        k.c(), v.c(), out.data_ptr(), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    _check(st, "tq_decode_step")
 
 
 def tq_decode_attention_noalloc(cfg: Config, tables, layer: int, q, softmax_scale: float,

@@ -465,10 +465,15 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
 
   // everything below may read what the previous kernel on the stream wrote
   // (sequence lengths, query, planes, window ring, workspace): wait for it
-  // to finish
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int T = a.seq_lens[b];
+  // to finish.  In a decode step (a.step_new > 0) the previous kernel is the
+  // step's append, which writes only the window ring and the plane rows from
+  // dep_row0 on: window splits wait here, quantized splits only before the
+  // copy of a chunk that reaches row dep_row0 (see issue).
+  const bool step_mode = a.step_new > 0;
+  if (!step_mode || window_split) asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int T = a.seq_lens[b] + a.step_new;
   const int nq = T - W > 0 ? T - W : 0;
+  const int dep_row0 = T - a.step_new - W > 0 ? T - a.step_new - W : 0;
   // this split's token range and plane rows (quantized splits)
   const int t_begin = split * a.split_tokens;
   int t_end = t_begin + a.split_tokens;
@@ -486,6 +491,9 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
   auto issue = [&](int c0, int slot) {
     const int nv = t_end - c0 < 32 ? t_end - c0 : 32;
     const int n4 = (nv + 3) & ~3;
+    // warp-uniform: rows the step's append may still be writing
+    if (step_mode && !window_split && c0 + n4 > dep_row0)
+      asm volatile("griddepcontrol.wait;" ::: "memory");
     // bulk copies need 16-byte aligned sources: the norm rows of a (sequence,
     // head) start at row0 * capacity floats, aligned only if capacity % 4 == 0
     // (chunks start at multiples of 32 tokens, so this holds for all or none)
@@ -1113,8 +1121,9 @@ int launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return 1;
   // programmatic dependent launch: the CTAs may start while the previous
-  // kernel on the stream (the library's append) is still running; they read
-  // only the codec tables before griddepcontrol.wait
+  // kernel on the stream is still running; they read only the codec tables
+  // before griddepcontrol.wait (in a decode step, also the data the step's
+  // append does not write)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((long long)a.n_splits * a.Hkv * a.B), 1, 1);
   cfg.blockDim = dim3(32 * kWarps, 1, 1);

@@ -468,8 +468,11 @@ struct DecodePlan {
 // kDecodeSms x decode_ctas_per_sm CTAs of decode_warps(...) warps.  The window is
 // cut into splits of at most 32 tokens per warp; the quantized tokens of each
 // (sequence, kv-head) are split evenly in multiples of 32 tokens over the rest.
+// reserve: CTA slots of the wave left to a kernel that runs beside the decode
+// (the append of a decode step)
+constexpr int kStepReserveMaxSplit = 4096;   // tokens per quantized split
 static DecodePlan decode_plan(const tq_config* cfg, const tq_layer_spec& s, int batch,
-                              int n_q_heads, int n_kv_heads, int max_seq_len) {
+                              int n_q_heads, int n_kv_heads, int max_seq_len, int reserve = 0) {
   DecodePlan p;
   const int W = cfg->residual_window;
   long long max_nq = (long long)max_seq_len - W;
@@ -482,7 +485,8 @@ static DecodePlan decode_plan(const tq_config* cfg, const tq_layer_spec& s, int 
   if (wst > 32 * warps) wst = 32 * warps;
   p.wsplit_tokens = wst > 0 ? wst : 1;
   const int n_wsplits = W > 0 ? (W + wst - 1) / wst : 0;
-  const long long wave = (long long)kDecodeSms * decode_ctas_per_sm(warps);
+  long long wave = (long long)kDecodeSms * decode_ctas_per_sm(warps) - reserve;
+  if (wave < 1) wave = 1;
   long long slots = wave - units * n_wsplits;
   if (slots < units) {
     // more than one wave: the quantized splits alone fill the wave (the short
@@ -797,12 +801,16 @@ extern "C" tq_status tq_dequantize(const tq_config* cfg, const void* tables, int
 // so the kernel sees n_q_heads * n_queries query columns in groups of
 // G * n_queries per kv-head, and masks window tokens causally per column.
 namespace tq {
-static tq_status decode_common(const tq_config* cfg, const void* tables, int layer, const void* q,
-                               int q_dtype, float softmax_scale, int batch, int n_q_heads,
-                               int n_kv_heads, int n_queries, tq_planes k, tq_planes v,
-                               const uint16_t* k_win, const uint16_t* v_win,
-                               const int32_t* seq_lens, int max_seq_len, float* out,
-                               void* workspace, size_t workspace_bytes, void* stream) {
+// Checks and launch arguments of a decode; *empty: every sequence is empty
+// (nothing to launch, the output is zero).
+static tq_status decode_prepare(const tq_config* cfg, const void* tables, int layer, const void* q,
+                                int q_dtype, float softmax_scale, int batch, int n_q_heads,
+                                int n_kv_heads, int n_queries, tq_planes k, tq_planes v,
+                                const uint16_t* k_win, const uint16_t* v_win,
+                                const int32_t* seq_lens, int max_seq_len, float* out,
+                                void* workspace, size_t workspace_bytes, int step_new,
+                                int reserve, DecodeArgs* args, bool* empty) {
+  *empty = false;
   tq_status st = check_gpu_common(cfg, tables, layer);
   if (st != TQ_OK) return st;
   if (batch < 0 || n_kv_heads < 1 || n_q_heads < n_kv_heads || n_q_heads % n_kv_heads != 0 ||
@@ -816,7 +824,10 @@ static tq_status decode_common(const tq_config* cfg, const void* tables, int lay
   n_q_heads *= n_queries;
   if (q_dtype != TQ_BF16 && q_dtype != TQ_F32) return TQ_ERR_INVALID_ARG;
   if (!(std::isfinite(softmax_scale))) return TQ_ERR_INVALID_ARG;
-  if (batch == 0) return TQ_OK;
+  if (batch == 0) {
+    *empty = true;
+    return TQ_OK;
+  }
   if (!q || !seq_lens || !out || !workspace) return TQ_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(out) || !aligned16(workspace)) return TQ_ERR_ALIGNMENT;
   const int W = cfg->residual_window;
@@ -830,6 +841,11 @@ static tq_status decode_common(const tq_config* cfg, const void* tables, int lay
   if (max_nq > k.capacity || max_nq > v.capacity) return TQ_ERR_INVALID_ARG;
   tq_layer_spec s = spec_of(cfg, layer);
   DecodePlan p = decode_plan(cfg, s, batch, n_q_heads, n_kv_heads, max_seq_len);
+  // a decode step leaves the append's CTA slots free only when its splits are
+  // short: then the append's latency weighs more than the share of the
+  // decode's work that those slots would have taken
+  if (reserve > 0 && p.split_tokens <= kStepReserveMaxSplit)
+    p = decode_plan(cfg, s, batch, n_q_heads, n_kv_heads, max_seq_len, reserve);
   if (workspace_bytes < p.total) return TQ_ERR_BUFFER_TOO_SMALL;
   if ((long long)p.n_splits * n_kv_heads * batch >= (1ll << 31)) return TQ_ERR_UNSUPPORTED;
   DecodeArgs a{};
@@ -876,9 +892,28 @@ static tq_status decode_common(const tq_config* cfg, const void* tables, int lay
   a.wait_limit = g_wait_limit;
   a.extra_tx = g_fault_injection == 1 ? 16u : 0u;
   a.n_q = n_queries;
-  if (p.n_splits == 0) {
+  a.step_new = step_new;
+  *empty = p.n_splits == 0;
+  *args = a;
+  return TQ_OK;
+}
+
+static tq_status decode_common(const tq_config* cfg, const void* tables, int layer, const void* q,
+                               int q_dtype, float softmax_scale, int batch, int n_q_heads,
+                               int n_kv_heads, int n_queries, tq_planes k, tq_planes v,
+                               const uint16_t* k_win, const uint16_t* v_win,
+                               const int32_t* seq_lens, int max_seq_len, float* out,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  DecodeArgs a{};
+  bool empty = false;
+  tq_status st = decode_prepare(cfg, tables, layer, q, q_dtype, softmax_scale, batch, n_q_heads,
+                                n_kv_heads, n_queries, k, v, k_win, v_win, seq_lens, max_seq_len,
+                                out, workspace, workspace_bytes, 0, 0, &a, &empty);
+  if (st != TQ_OK) return st;
+  if (batch == 0) return TQ_OK;
+  if (empty) {
     // every sequence is empty: the output is zero
-    if (cudaMemsetAsync(out, 0, (size_t)batch * n_q_heads * kHeadDim * sizeof(float),
+    if (cudaMemsetAsync(out, 0, (size_t)batch * n_q_heads * n_queries * kHeadDim * sizeof(float),
                         (cudaStream_t)stream) != cudaSuccess)
       return TQ_ERR_CUDA;
     return TQ_OK;
@@ -907,6 +942,34 @@ extern "C" tq_status tq_decode_attention_multi(
   return decode_common(cfg, tables, layer, q, q_dtype, softmax_scale, batch, n_q_heads,
                        n_kv_heads, n_queries, k, v, k_win, v_win, seq_lens, max_seq_len, out,
                        workspace, workspace_bytes, stream);
+}
+
+extern "C" tq_status tq_decode_step(const tq_config* cfg, const void* tables, int layer,
+                                    const void* q, int q_dtype, float softmax_scale, int batch,
+                                    int n_q_heads, int n_kv_heads, const void* k_new,
+                                    const void* v_new, int src_dtype, const int64_t src_strides[3],
+                                    const int32_t* seq_lens_before, int max_seq_len,
+                                    uint16_t* k_win, uint16_t* v_win, tq_planes k, tq_planes v,
+                                    float* out, void* workspace, size_t workspace_bytes,
+                                    void* stream) {
+  if (batch == 0) return TQ_OK;
+  if (max_seq_len < 1) return TQ_ERR_INVALID_ARG;
+  // the append's CTAs (one per sequence and kv-head) run beside the decode's
+  // first wave: with few of them and short splits, the decode leaves their
+  // slots free
+  const long long units = (long long)batch * n_kv_heads;
+  const int reserve = units > 0 && units <= 16 ? (int)units : 0;
+  DecodeArgs a{};
+  bool empty = false;
+  tq_status st = decode_prepare(cfg, tables, layer, q, q_dtype, softmax_scale, batch, n_q_heads,
+                                n_kv_heads, 1, k, v, k_win, v_win, seq_lens_before, max_seq_len,
+                                out, workspace, workspace_bytes, 1, reserve, &a, &empty);
+  if (st != TQ_OK) return st;
+  if (empty) return TQ_ERR_INVALID_ARG;              // unreachable with max_seq_len >= 1
+  st = tq_append_kv(cfg, tables, layer, k_new, v_new, src_dtype, src_strides, batch, n_kv_heads,
+                    1, seq_lens_before, k_win, v_win, k, v, stream);
+  if (st != TQ_OK) return st;
+  return launch_decode(a, stream) == 0 ? TQ_OK : TQ_ERR_CUDA;
 }
 
 extern "C" tq_status tq_get_device_error(void* stream) {

@@ -214,6 +214,9 @@ struct DecodeArgs {
   int dsign;                     // keys in Direct Sign mode
   float sparse_thr;              // skip a chunk's V sum below this weight (0: never)
   int n_q;                       // query tokens per sequence (columns g: token g % n_q)
+  int step_new;                  // > 0: decode step.  seq_lens are the lengths before
+                                 // step_new tokens that the kernel launched just before
+                                 // this one appends (tq_decode_step); T = seq_lens + step_new
   const uint16_t* kwin; const uint16_t* vwin; int W;
   const int32_t* seq_lens;
   int n_qsplits;                 // splits over the quantized tokens

@@ -357,3 +357,71 @@ def test_decode_multi_query_needs_the_hidden_tokens_in_the_window(B):
         B.tq_decode_attention_multi(cfg, tables, 0, q, 1.0, kp, vp, seq, 66, out, ws,
                                     k_win=kw, v_win=kw)
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("kb,vb,mode,W", [(4, 2, "mse", 16), (3, 3, "mse", 0), (2, 3, "qjl", 0),
+                                         (2, 3, "sign", 16), (8, 8, "mse", 8), (4, 2, "mse", 128)])
+def test_decode_step_matches_append_then_decode(B, kb, vb, mode, W):
+    """tq_decode_step (append of one token per sequence, then decode, in two
+    overlapping launches) writes the same planes and ring as tq_append_kv and
+    returns the output of tq_decode_attention after it.  The plane rows the
+    append writes are zeroed beforehand, so a decode that read them before the
+    append finished would differ."""
+    import torch
+    from kv_cache_quantization_random_gb300 import workloads as W_
+    T0 = np.array([699, max(W - 1, 0), W, 0, 37, 300], dtype=np.int64)
+    batch, hkv, hq, C = len(T0), 2, 8, 700
+    w = W_.scaled(W_.get("llama8b_32k"), batch=batch, n_q_heads=hq, n_kv_heads=hkv, context=C,
+                  data_seed=17)
+    K, V = W_.make_kv(w)
+    q = W_.make_q(w).cuda()
+    km = {"mse": B.TQ_MODE_MSE, "sign": B.TQ_MODE_MSE_SIGN, "qjl": B.TQ_MODE_MSE_QJL}[mode]
+    cfg = B.Config(k_bits=kb, v_bits=vb, k_mode=km, residual_window=W, seed=6)
+    tables = B.device_tables(cfg)
+    Kd, Vd = K.cuda(), V.cuda()
+    caches = []
+    for _ in range(2):
+        kp, vp = B.Planes(cfg, 0, 0, batch, hkv, C), B.Planes(cfg, 0, 1, batch, hkv, C)
+        B.tq_quantize_kv(cfg, tables, 0, 0, Kd[:, :, :C - 1], kp)
+        B.tq_quantize_kv(cfg, tables, 0, 1, Vd[:, :, :C - 1], vp)
+        for b in range(batch):                    # rows the step's append writes, and later ones
+            r0 = max(int(T0[b]) - W, 0)
+            for P in (kp, vp):
+                P.codes_view()[b, :, r0:] = 0
+                P.norms_view()[b, :, r0:] = 0
+                if P.qjl_signs is not None:
+                    P.signs_view()[b, :, r0:] = 0
+                    P.rnorm_view()[b, :, r0:] = 0
+        kw = torch.zeros(batch, hkv, max(W, 1), 128, dtype=torch.bfloat16, device="cuda")
+        vw = torch.zeros_like(kw)
+        for b in range(batch):
+            for t in range(max(int(T0[b]) - W, 0), int(T0[b])):
+                kw[b, :, t % W] = Kd[b, :, t]
+                vw[b, :, t % W] = Vd[b, :, t]
+        caches.append((kp, vp, kw if W else None, vw if W else None))
+    kn = torch.stack([K[b, :, int(T0[b]):int(T0[b]) + 1] for b in range(batch)]).cuda()
+    vn = torch.stack([V[b, :, int(T0[b]):int(T0[b]) + 1] for b in range(batch)]).cuda()
+    before = torch.tensor(T0, dtype=torch.int32, device="cuda")
+    after = before + 1
+    ws = B.new_workspace(cfg, batch, hq, hkv, C)
+    outs = [torch.empty(batch, hq, 128, device="cuda") for _ in range(2)]
+    kp, vp, kw, vw = caches[0]
+    B.tq_append_kv(cfg, tables, 0, kn, vn, before, kw, vw, kp, vp)
+    B.tq_decode_attention(cfg, tables, 0, q, w.softmax_scale, kp, vp, after, C, outs[0], ws,
+                          k_win=kw, v_win=vw)
+    kp, vp, kw, vw = caches[1]
+    B.tq_decode_step(cfg, tables, 0, q, w.softmax_scale, kn, vn, before, C, kp, vp, outs[1], ws,
+                     k_win=kw, v_win=vw)
+    torch.cuda.synchronize()
+    assert B.tq_get_device_error() == B.TQ_OK
+    (ka, va, kwa, vwa), (kb_, vb_, kwb, vwb) = caches
+    for Pa, Pb in ((ka, kb_), (va, vb_)):
+        assert torch.equal(Pa.codes.cpu(), Pb.codes.cpu())
+        assert torch.equal(Pa.norms.cpu(), Pb.norms.cpu())
+        if Pa.qjl_signs is not None:
+            assert torch.equal(Pa.qjl_signs.cpu(), Pb.qjl_signs.cpu())
+            assert torch.equal(Pa.qjl_rnorm.cpu(), Pb.qjl_rnorm.cpu())
+    if W:
+        assert torch.equal(kwa.cpu(), kwb.cpu()) and torch.equal(vwa.cpu(), vwb.cpu())
+    a, b = to64(outs[0]), to64(outs[1])
+    assert rel_l2_per_head(b, a).max() < 1e-5
