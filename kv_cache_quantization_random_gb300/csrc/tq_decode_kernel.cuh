@@ -467,13 +467,12 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
   // (sequence lengths, query, planes, window ring, workspace): wait for it
   // to finish.  In a decode step (a.step_new > 0) the previous kernel is the
   // step's append, which writes only the window ring and the plane rows from
-  // dep_row0 on: window splits wait here, quantized splits only before the
-  // copy of a chunk that reaches row dep_row0 (see issue).
-  const bool step_mode = a.step_new > 0;
-  if (!step_mode || window_split) asm volatile("griddepcontrol.wait;" ::: "memory");
+  // max(nq - step_new, 0) on: window splits wait here, quantized splits only
+  // before the copy of a chunk that reaches row t_end - step_new of their
+  // range (see issue; t_end <= nq, so that covers those rows).
+  if (a.step_new == 0 || window_split) asm volatile("griddepcontrol.wait;" ::: "memory");
   const int T = a.seq_lens[b] + a.step_new;
   const int nq = T - W > 0 ? T - W : 0;
-  const int dep_row0 = T - a.step_new - W > 0 ? T - a.step_new - W : 0;
   // this split's token range and plane rows (quantized splits)
   const int t_begin = split * a.split_tokens;
   int t_end = t_begin + a.split_tokens;
@@ -492,7 +491,7 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
     const int nv = t_end - c0 < 32 ? t_end - c0 : 32;
     const int n4 = (nv + 3) & ~3;
     // warp-uniform: rows the step's append may still be writing
-    if (step_mode && !window_split && c0 + n4 > dep_row0)
+    if (a.step_new > 0 && c0 + n4 > t_end - a.step_new)
       asm volatile("griddepcontrol.wait;" ::: "memory");
     // bulk copies need 16-byte aligned sources: the norm rows of a (sequence,
     // head) start at row0 * capacity floats, aligned only if capacity % 4 == 0
