@@ -163,3 +163,30 @@ def test_argument_validation_rejects_before_launch(B):
     rc = lib.tq_decode_attention(C.byref(wcfg.c()), 4096, 0, 16384, 0, 1.0, 1, 8, 8, planes,
                                  planes, None, None, 20480, 10, out, 65536, 1 << 20, None)
     assert rc == 1                                     # window buffers missing
+
+
+def test_decode_step_validates_both_calls_before_launch(B):
+    """tq_decode_step checks the decode's arguments and the append's before it
+    launches either (so no half-done step): each rejection below returns
+    before any CUDA call, which would fail on a host without a GPU."""
+    import ctypes as C
+    lib = B.load()
+    cfg = B.Config()
+    planes = B.tq_planes(4096, 8192, None, None, 100)
+    strides = (C.c_int64 * 3)(128, 128, 128)
+
+    def step(c=cfg, ws_bytes=1 << 20, max_len=10, knew=20480, dt=0, hq=8, tables=4096):
+        return lib.tq_decode_step(C.byref(c.c()), tables, 0, 16384, 0, 1.0, 1, hq, 8, knew, 24576,
+                                  dt, strides, 28672, max_len, None, None, planes, planes, 32768,
+                                  65536, ws_bytes, None)
+
+    assert step(max_len=0) == 1                        # the step adds a token: max_seq_len >= 1
+    assert step(ws_bytes=16) == 7                      # workspace too small
+    assert step(hq=24) == 2                            # group size 3
+    assert step(tables=4100) == 3                      # misaligned tables
+    assert step(B.Config(residual_window=16)) == 1     # window buffers missing
+    assert step(knew=20482) == 3                       # misaligned new keys (append's check)
+    assert step(dt=7) == 1                             # bad source dtype (append's check)
+    assert lib.tq_decode_step(C.byref(cfg.c()), 4096, 0, 16384, 0, 1.0, 0, 8, 8, 20480, 24576, 0,
+                              strides, 28672, 10, None, None, planes, planes, 32768, 65536,
+                              1 << 20, None) == 0      # empty batch: nothing to do
