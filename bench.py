@@ -1,14 +1,16 @@
 #!/usr/bin/env python3
 """Benchmark of the TurboQuant hot path on one GB300 (or N replicas).
 
-A step is one decode step of a serving loop over the workload's cache:
+A step is one decode step of a serving loop over the workload's cache, one
+tq_decode_step call:
   append   one new token per (sequence, kv-head): the token leaving the
            residual window is quantized into the planes and the new token is
            written into the window ring (norm, rotation, code search, packing,
            window bookkeeping);
   decode   attention of every query head over the whole compressed context
            (query rotation, compressed-domain scoring, softmax, rotated V sum,
-           split merge and inverse rotation).
+           split merge and inverse rotation), launched so that it overlaps the
+           append.
 The headline value is context tokens attended per second.  Bulk quantize of
 the whole context (K and V) is measured separately and reported in GB/s.
 
