@@ -359,17 +359,20 @@ def test_decode_multi_query_needs_the_hidden_tokens_in_the_window(B):
     assert e.value.status == 2
 
 
-@pytest.mark.parametrize("kb,vb,mode,W", [(4, 2, "mse", 16), (3, 3, "mse", 0), (2, 3, "qjl", 0),
-                                         (2, 3, "sign", 16), (8, 8, "mse", 8), (4, 2, "mse", 128)])
-def test_decode_step_matches_append_then_decode(B, kb, vb, mode, W):
+@pytest.mark.parametrize("kb,vb,mode,W,rep", [(4, 2, "mse", 16, 1), (3, 3, "mse", 0, 1),
+                                             (2, 3, "qjl", 0, 1), (2, 3, "sign", 16, 1),
+                                             (8, 8, "mse", 8, 1), (4, 2, "mse", 128, 1),
+                                             (4, 2, "mse", 16, 2)])
+def test_decode_step_matches_append_then_decode(B, kb, vb, mode, W, rep):
     """tq_decode_step (append of one token per sequence, then decode, in two
     overlapping launches) writes the same planes and ring as tq_append_kv and
     returns the output of tq_decode_attention after it.  The plane rows the
     append writes are zeroed beforehand, so a decode that read them before the
-    append finished would differ."""
+    append finished would differ.  rep = 2 gives 24 (sequence, kv-head) pairs:
+    the decode then keeps all CTA slots."""
     import torch
     from kv_cache_quantization_random_gb300 import workloads as W_
-    T0 = np.array([699, max(W - 1, 0), W, 0, 37, 300], dtype=np.int64)
+    T0 = np.tile(np.array([699, max(W - 1, 0), W, 0, 37, 300], dtype=np.int64), rep)
     batch, hkv, hq, C = len(T0), 2, 8, 700
     w = W_.scaled(W_.get("llama8b_32k"), batch=batch, n_q_heads=hq, n_kv_heads=hkv, context=C,
                   data_seed=17)
