@@ -117,12 +117,18 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# the files that define the decode kernel, its launch and its split plan
+DECODE_SOURCES = ("tq_decode.cu", "tq_decode_g1.cu", "tq_decode_g2.cu", "tq_decode_g4.cu",
+                  "tq_decode_g8.cu", "tq_decode_kernel.cuh", "tq_device.cuh", "tq_internal.h",
+                  "tq_host.cpp")
+
+
 def sources_digest() -> str:
-    """sha256 of the concatenated CUDA/C++ sources (sorted by name)."""
+    """sha256 of the concatenated decode sources (DECODE_SOURCES, in that order)."""
     import hashlib
     d = os.path.join(ROOT, "kv_cache_quantization_random_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(d)):
+    for name in DECODE_SOURCES:
         with open(os.path.join(d, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
