@@ -44,8 +44,9 @@
  *
  * Memory and ownership: the caller allocates every buffer (device memory for
  * planes, tables, workspace, inputs and outputs); the library allocates
- * nothing and keeps no state besides one device error word per translation
- * unit.  Every device call is asynchronous on the caller's stream (a
+ * nothing at run time.  Its device state is one error word per translation
+ * unit plus, on every GPU that loads it, the fixed 8 MiB scratch array of
+ * tq_decode_attention_noalloc (reserved at load time, held until exit).  Every device call is asynchronous on the caller's stream (a
  * cudaStream_t passed as void*; NULL = legacy default stream).
  *
  * Errors: arguments are validated on the host before any launch; a bad
@@ -187,18 +188,33 @@ tq_status tq_build_tables(const tq_config* cfg, void* host_buf, size_t bytes);
 
 /* Bytes of the four planes of layer/kind for batch x n_kv_heads x capacity
  * vectors: sizes[0] codes, [1] norms, [2] qjl_signs, [3] qjl_rnorm (0 when
- * the plane is not used). */
+ * the plane is not used).  A b-bit vector of head_dim coordinates takes
+ * head_dim*b/8 code bytes plus a 4-byte norm ("윈도우용 터보퀀트(TurboQuant)
+ * 구현을 개선하다", finding 3: 3 bits x 128 = 48 B + 4 B = 52 B); QJL keys add
+ * m/8 sign bytes and a 4-byte residual norm ("TurboQuant KV 캐시 압축 for
+ * llama.cpp", v1.4.2 item 2), Direct Sign keys head_dim/8 and a 4-byte scale
+ * (v1.1.0).  Host only; returns TQ_ERR_INVALID_ARG for a bad config, layer,
+ * kind or a negative size. */
 tq_status tq_plane_bytes(const tq_config* cfg, int layer, int kind, int batch, int n_kv_heads,
                          int64_t capacity, size_t sizes[4]);
 
-/* Device workspace needed by tq_decode_attention for these shapes. */
+/* Bytes of device workspace that tq_decode_attention needs for these shapes
+ * (the largest over the config's layers): the split partials (m, l, o) of
+ * the split-K decode and one split counter per (sequence, kv-head).  The
+ * log-sum-exp merge of per-split softmax partials is the combine step of the
+ * pages' flash-decoding kernels ("TurboQuant KV 캐시 압축 for llama.cpp",
+ * v1.5.2 items 1-2: partial sums accumulate in fp32).  Host only; 0 for
+ * invalid arguments. */
 size_t tq_workspace_bytes(const tq_config* cfg, int batch, int n_q_heads, int n_kv_heads,
                           int max_seq_len);
 
 /* -------------------------------------------------------------- device */
 
-/* Zero the workspace's split counters (async on stream).  Needed once after
- * allocation; decode leaves the counters at zero when it completes. */
+/* Zero a decode workspace (async on stream; the workspace is the one
+ * tq_workspace_bytes sizes for the split-K combine described there).  Needed
+ * once after allocation; every decode leaves its split counters at zero when
+ * it completes, including one whose bounded waits ran out.
+ * TQ_ERR_INVALID_ARG for a NULL workspace, TQ_ERR_CUDA if the memset fails. */
 tq_status tq_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
 
 /* Quantize src[b, h, j, :] for j < n_tokens into plane row
@@ -232,9 +248,16 @@ tq_status tq_append_kv(const tq_config* cfg, const void* tables, int layer, cons
                        uint16_t* k_win, uint16_t* v_win, tq_planes k, tq_planes v,
                        void* stream);
 
-/* dst[b, h, j, :] (fp32, device, contiguous [batch][n_kv_heads][n_tokens][d])
- * = n R^T c[idx] for plane rows j < n_tokens; with include_qjl != 0 and a
- * QJL key plane, plus R^T (sqrt(pi/2)/m) gamma S^T (2 bits - 1). */
+/* Reconstruct vectors from their planes (inspection and tests; decode never
+ * materialises them).  dst[b, h, j, :] (fp32, device, contiguous
+ * [batch][n_kv_heads][n_tokens][d]) = n R^T c[idx] for plane rows
+ * j < n_tokens: the centroid lookup, the inverse WHT and the norm
+ * ("TurboQuant KV 캐시 압축 for llama.cpp", v1.7.0 decision 4: the decoder
+ * undoes the encoder's sign flip + butterfly; "윈도우용 터보퀀트(TurboQuant)
+ * 구현을 개선하다", recap).  With include_qjl != 0 and a QJL key plane, plus
+ * R^T (sqrt(pi/2)/m) gamma S^T (2 bits - 1) (v1.4.2 item 2); with a Direct
+ * Sign key plane, plus R^T a (2 bits - 1).  Arguments are checked as for
+ * tq_quantize_kv; n_tokens <= capacity. */
 tq_status tq_dequantize(const tq_config* cfg, const void* tables, int layer, int kind,
                         tq_planes src, int batch, int n_kv_heads, int n_tokens,
                         int include_qjl, float* dst, void* stream);
@@ -245,7 +268,9 @@ tq_status tq_dequantize(const tq_config* cfg, const void* tables, int layer, int
  *   k_win, v_win  device bf16 [batch][n_kv_heads][W][head_dim] ring, token t
  *            in slot t mod W (NULL when W = 0).
  *   seq_lens device int32 [batch]: T per sequence, window included;
- *            each T <= max_seq_len (host bound used to size the grid).
+ *            each T <= max_seq_len (host bound used to size the grid).  A T
+ *            outside [0, max_seq_len] is decoded as an empty sequence (zeros)
+ *            and sets TQ_ERR_DEVICE_BOUNDS (tq_get_device_error).
  *   out      device fp32 [batch][n_q_heads][head_dim].
  *   Query head h reads kv-head h / (n_q_heads / n_kv_heads).  Scores are
  *   softmax_scale * q.k; a sequence with T = 0 writes zeros.
@@ -300,7 +325,13 @@ tq_status tq_decode_step(const tq_config* cfg, const void* tables, int layer, co
                          tq_planes v, float* out, void* workspace, size_t workspace_bytes,
                          void* stream);
 
-/* Synchronize `stream`, then read and clear the device error words.
+/* Synchronize `stream`, then read and clear the device error words that the
+ * kernels set instead of faulting: a bounded wait that ran out
+ * (TQ_ERR_DEVICE_TIMEOUT) or an index check (TQ_ERR_DEVICE_BOUNDS: a plane
+ * row past capacity, a sequence length outside [0, max_seq_len]).  The pages
+ * have no counterpart; the __syncthreads race on the query-WHT shared memory
+ * that they fixed ("TurboQuant KV 캐시 압축 for llama.cpp", v1.1.0 bug fixes)
+ * is the kind of fault such checks make visible without taking the GPU down.
  * Returns TQ_OK, TQ_ERR_DEVICE_TIMEOUT, TQ_ERR_DEVICE_BOUNDS or TQ_ERR_CUDA. */
 tq_status tq_get_device_error(void* stream);
 
@@ -335,8 +366,12 @@ void tq_set_fault_injection(int mode);
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     outside any stream capture.
- *   - Each call clears the part of the array it uses (an async memset on
- *     `stream`) before the decode launch.
+ *   - Each call clears the array's split counters for its shapes (an async
+ *     memset of a few bytes on `stream`) before the decode launch; the
+ *     split partials are always written before they are read.
+ *   - The array's device address is cached per device for the life of the
+ *     process: after cudaDeviceReset (or a new primary context) on that
+ *     device the entry point may not be used again.
  *   - Every call on a device shares the one array: calls whose work can
  *     overlap on the GPU (different streams, no ordering between them) race
  *     and give wrong results.  Order them on one stream or by events. */

@@ -19,6 +19,8 @@ import numpy as np
 from . import build as _build
 
 TQ_OK = 0
+TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_ALIGNMENT, TQ_ERR_CUDA = 1, 2, 3, 4
+TQ_ERR_DEVICE_TIMEOUT, TQ_ERR_DEVICE_BOUNDS, TQ_ERR_BUFFER_TOO_SMALL = 5, 6, 7
 TQ_ERR_NAMES = {
     0: "TQ_OK", 1: "TQ_ERR_INVALID_ARG", 2: "TQ_ERR_UNSUPPORTED", 3: "TQ_ERR_ALIGNMENT",
     4: "TQ_ERR_CUDA", 5: "TQ_ERR_DEVICE_TIMEOUT", 6: "TQ_ERR_DEVICE_BOUNDS",

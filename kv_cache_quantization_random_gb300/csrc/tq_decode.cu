@@ -94,9 +94,15 @@ extern "C" tq_status tq_decode_attention_noalloc(
   void* scratch = nullptr;
   tq_status st = tq::static_scratch_address(&scratch);
   if (st != TQ_OK) return st;
-  // the array keeps whatever the previous call left; the split counters must
-  // start at zero, so clear the part this call uses
-  if (need > 0 && cudaMemsetAsync(scratch, 0, need, (cudaStream_t)stream) != cudaSuccess)
+  // the array keeps whatever the previous call left (another call's partials
+  // may lie where this call's split counters go); the counters must start at
+  // zero, so clear them.  The partials are written before they are read.
+  size_t coff = 0, cbytes = 0;
+  tq_status cst = tq::decode_counters_range(cfg, layer, batch, n_q_heads, n_kv_heads,
+                                            max_seq_len, &coff, &cbytes);
+  if (cst != TQ_OK) return cst;
+  if (cbytes > 0 && cudaMemsetAsync((unsigned char*)scratch + coff, 0, cbytes,
+                                    (cudaStream_t)stream) != cudaSuccess)
     return TQ_ERR_CUDA;
   return tq_decode_attention(cfg, tables, layer, q, q_dtype, softmax_scale, batch, n_q_heads,
                              n_kv_heads, k, v, k_win, v_win, seq_lens, max_seq_len, out, scratch,

@@ -471,7 +471,13 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
   // before the copy of a chunk that reaches row t_end - step_new of their
   // range (see issue; t_end <= nq, so that covers those rows).
   if (a.step_new == 0 || window_split) asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int T = a.seq_lens[b] + a.step_new;
+  int T = a.seq_lens[b] + a.step_new;
+  // a length outside the plan's range would read past this pair's plane rows
+  // or ring: flag it and decode the sequence as empty
+  if (T < 0 || T > a.max_seq_len) {
+    if (tid == 0) atomicOr(a.err, kErrBounds);
+    T = 0;
+  }
   const int nq = T - W > 0 ? T - W : 0;
   // this split's token range and plane rows (quantized splits)
   const int t_begin = split * a.split_tokens;
@@ -897,11 +903,16 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
         for (int j = 0; j < 4; ++j) d[k][j] *= inv;
     }
     if (!ok) {
-      // a staging wait ran out (error word set): give the copies still in
-      // flight (chunks kq .. kq + NS - 1, one per ring slot) a bounded wait, then stop
+      // a staging wait ran out (error word set): wait for the copies still in
+      // flight (chunks kq .. kq + NS - 1, one per ring slot) to land, each
+      // wait bounded, then stop.  Under fault injection each barrier expects
+      // a.extra_tx bytes that no copy delivers: retire them first, so that
+      // the barrier completes exactly when the real copies have landed.
       for (int dd = 0; dd < NS; ++dd) {
         const int kk = kq + dd;
         if (t_begin + 32 * warp + kk * 32 * kDWarps >= t_end) break;
+        if (lane == 0 && a.extra_tx != 0) mbar_complete_tx(bar + kk % NS, a.extra_tx);
+        __syncwarp();
         for (uint32_t i = 0; i < limit && !mbar_try_wait(bar + kk % NS, (kk / NS) & 1); ++i) {
         }
       }

@@ -522,6 +522,24 @@ extern "C" size_t tq_workspace_bytes(const tq_config* cfg, int batch, int n_q_he
   return total;
 }
 
+namespace tq {
+// Byte range [*off, *off + *bytes) of the split counters in the workspace of a
+// tq_decode_attention call with these shapes: the only part of the workspace
+// that must be zero when the decode starts (the partials are written before
+// they are read).
+tq_status decode_counters_range(const tq_config* cfg, int layer, int batch, int n_q_heads,
+                                int n_kv_heads, int max_seq_len, size_t* off, size_t* bytes) {
+  if (check_config(cfg) != TQ_OK || layer < 0 || layer >= cfg->n_layers || batch < 0 ||
+      n_kv_heads < 1 || n_q_heads < n_kv_heads || max_seq_len < 0)
+    return TQ_ERR_INVALID_ARG;
+  const DecodePlan p =
+      decode_plan(cfg, spec_of(cfg, layer), batch, n_q_heads, n_kv_heads, max_seq_len);
+  *off = p.counters_off;
+  *bytes = p.total - p.counters_off;
+  return TQ_OK;
+}
+}  // namespace tq
+
 extern "C" tq_status tq_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
   if (!workspace) return TQ_ERR_INVALID_ARG;
   if (cudaMemsetAsync(workspace, 0, workspace_bytes, (cudaStream_t)stream) != cudaSuccess)
@@ -875,6 +893,7 @@ static tq_status decode_prepare(const tq_config* cfg, const void* tables, int la
   a.vwin = v_win;
   a.W = W;
   a.seq_lens = seq_lens;
+  a.max_seq_len = max_seq_len;
   a.n_qsplits = p.n_qsplits;
   a.n_splits = p.n_splits;
   a.split_tokens = p.split_tokens;

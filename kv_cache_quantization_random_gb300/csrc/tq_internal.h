@@ -219,6 +219,8 @@ struct DecodeArgs {
                                  // this one appends (tq_decode_step); T = seq_lens + step_new
   const uint16_t* kwin; const uint16_t* vwin; int W;
   const int32_t* seq_lens;
+  int max_seq_len;               // host bound on every T: a T outside [0, max_seq_len]
+                                 // sets kErrBounds and is decoded as an empty sequence
   int n_qsplits;                 // splits over the quantized tokens
   int n_splits;                  // n_qsplits + the window splits
   int split_tokens;              // tokens per quantized split (multiple of 32)
@@ -246,6 +248,10 @@ int launch_window_scatter(const WindowScatterArgs& a, void* stream);
 int launch_append(const AppendArgs& a, void* stream);
 int launch_dequantize(const DequantArgs& a, void* stream);
 int launch_decode(const DecodeArgs& a, void* stream);
+
+// the split counters' byte range in a decode workspace (tq_host.cpp)
+tq_status decode_counters_range(const tq_config* cfg, int layer, int batch, int n_q_heads,
+                                int n_kv_heads, int max_seq_len, size_t* off, size_t* bytes);
 
 // device error words: each .cu owns one; these read-and-clear them
 int quant_read_error(unsigned* out);

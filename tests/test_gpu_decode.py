@@ -292,6 +292,29 @@ def test_fault_injection_times_out_and_context_stays_usable(B):
     assert rel_l2_per_head(to64(out), ref).max() < TOL
 
 
+def test_decode_flags_lengths_outside_the_plan(B):
+    """A sequence length above max_seq_len (or below zero) would make the
+    kernel read past the pair's plane rows or window ring.  The kernel checks
+    every length it reads: such a sequence is decoded as empty (zeros) and the
+    call reports TQ_ERR_DEVICE_BOUNDS; the other sequences are unaffected, and
+    the next call is clean."""
+    import torch
+    got, ref, c = _decode_case(B, batch=3, hq=8, hkv=2, seq=[700, 333, 512], kb=4, vb=2, W=16)
+    assert rel_l2_per_head(got, ref).max() < TOL
+    bad = torch.tensor([700, 5000, -3], dtype=torch.int32, device="cuda")
+    out = torch.full((3, 8, 128), float("nan"), device="cuda")
+    B.tq_decode_attention(c["cfg"], c["tables"], 0, c["q"].cuda(), c["scale"], c["kp"], c["vp"],
+                          bad, c["Tmax"], out, c["ws"], k_win=c["kw"], v_win=c["vw"])
+    assert B.tq_get_device_error() == B.TQ_ERR_DEVICE_BOUNDS
+    o = to64(out)
+    assert np.array_equal(o[0], got[0])           # same plan, same splits: bit-identical
+    assert np.all(o[1:] == 0.0)
+    B.tq_decode_attention(c["cfg"], c["tables"], 0, c["q"].cuda(), c["scale"], c["kp"], c["vp"],
+                          c["seq_t"], c["Tmax"], out, c["ws"], k_win=c["kw"], v_win=c["vw"])
+    assert B.tq_get_device_error() == B.TQ_OK
+    assert np.array_equal(to64(out), got)
+
+
 @pytest.mark.parametrize("hq,hkv,nq_tok,W", [(8, 2, 2, 16), (4, 2, 4, 8), (2, 2, 8, 64), (8, 8, 1, 0)])
 def test_decode_multi_query_matches_causal_oracle(B, hq, hkv, nq_tok, W):
     """n_queries query tokens per sequence at once: query j sees tokens up to
