@@ -23,7 +23,11 @@ The five workloads mirror the shapes on the TurboQuant pages:
 * ``serving_36l``  36 layers, layers 0-3 and 32-35 at 8 bits, the rest K4/V2;
   batch 64, 32/8 heads, contexts uniform in [4096, 16384], 64 new tokens per
   sequence per step.
-The last three reuse the key/value distributions of ``llama8b_32k``.
+The QJL, Direct Sign, long-context and serving workloads draw their keys and
+values from the first workload's distributions (N(0,1) with 4 outlier channels
+x20, keys and values alike), in bf16, with a query N(0,1) and softmax scale
+1/sqrt(d).  ``with_llama_kv`` gives the same shapes with the Llama-shaped
+key/value distributions instead (a bench option).
 """
 
 from __future__ import annotations
@@ -35,7 +39,7 @@ from typing import Optional, Tuple
 import numpy as np
 
 __all__ = ["Workload", "WORKLOADS", "get", "seq_lens", "kv_params", "make_kv", "make_q",
-           "scaled"]
+           "scaled", "with_llama_kv"]
 
 
 @dataclass(frozen=True)
@@ -87,23 +91,34 @@ WORKLOADS = {
         context=32768, k_bits=4, v_bits=2, window=128, data_seed=1001),
     "qjl_b16_8k": Workload(
         name="qjl_b16_8k", batch=16, n_q_heads=32, n_kv_heads=8, head_dim=128,
-        context=8192, k_bits=2, v_bits=3, k_qjl=True, qjl_m=128, data_seed=1002),
+        context=8192, k_bits=2, v_bits=3, k_qjl=True, qjl_m=128, data_seed=1002,
+        dist="gauss_outlier", n_outliers=4),
     "sign_b16_8k": Workload(
         name="sign_b16_8k", batch=16, n_q_heads=32, n_kv_heads=8, head_dim=128,
-        context=8192, k_bits=2, v_bits=3, k_sign=True, data_seed=1002),
+        context=8192, k_bits=2, v_bits=3, k_sign=True, data_seed=1002,
+        dist="gauss_outlier", n_outliers=4),
     "long_1m": Workload(
         name="long_1m", batch=1, n_q_heads=64, n_kv_heads=8, head_dim=128,
         context=1048576, k_bits=3, v_bits=3, window=256, new_tokens=4096,
-        data_seed=1003),
+        data_seed=1003,
+        dist="gauss_outlier", n_outliers=4),
     "serving_36l": Workload(
         name="serving_36l", batch=64, n_q_heads=32, n_kv_heads=8, head_dim=128,
         context=16384, k_bits=4, v_bits=2, n_layers=36, protect_first=4,
-        protect_last=4, ragged=(4096, 16384), new_tokens=64, data_seed=1004),
+        protect_last=4, ragged=(4096, 16384), new_tokens=64, data_seed=1004,
+        dist="gauss_outlier", n_outliers=4),
 }
 
 
 def get(name: str) -> Workload:
     return WORKLOADS[name]
+
+
+def with_llama_kv(w: Workload) -> Workload:
+    """The same shapes with the Llama-shaped key/value distributions
+    (log-normal key channels, 6 outliers, mean key norm 170, values
+    N(0, 0.25^2))."""
+    return replace(w, dist="llama", n_outliers=6)
 
 
 def scaled(w: Workload, **kw) -> Workload:
