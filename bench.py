@@ -439,8 +439,11 @@ def run_single(args, w, rank, world, local):
     dec_bytes = decode_bytes(w, seq)
     cache_bytes = sum(t.numel() for t in (kp.codes, kp.norms, vp.codes, vp.norms)) + \
         (2 * st["kw"].numel() * 2 if Wn else 0)
-    flush_mode = 4 * cache_bytes < l2
-    R = 1 if flush_mode else max(2, min(64, math.ceil(4 * l2 / max(cache_bytes, 1)) + 1))
+    # replicas cover 4x L2 with at most 64 copies; a smaller cache (the
+    # single-head workload) is timed one step at a time with L2 flushed
+    R = max(2, math.ceil(4 * l2 / max(cache_bytes, 1)) + 1)
+    flush_mode = R > 64
+    R = 1 if flush_mode else R
     reps = []
     for r in range(R):
         if r == 0:

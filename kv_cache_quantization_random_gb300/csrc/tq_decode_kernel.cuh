@@ -103,12 +103,28 @@ __device__ __forceinline__ uint32_t lut_u32(const uint32_t* lut, uint32_t byte_o
   return *(const uint32_t*)((const char*)lut + byte_off);
 }
 
-// A operands of k-tile kt for the 8 m-tiles, then the 8 MMAs.  lutp: for 2-
-// and 3-bit values, half2 (c[i0], c[i1]) indexed by the pair (i0 | i1 << VB)
-// of the codes of the two tokens of an operand register; for 4- and 8-bit
+// Coordinate of accumulator row g (hi = 0) or g + 8 (hi = 1) of m-tile k for
+// lane group g: 2-bit values pair coordinates c and c + 2 in one code byte
+// (see vmma_ktile), wider values c and c + 1.
+template <int VB>
+__device__ __forceinline__ int vrow_coord(int g, int k, int hi) {
+  if constexpr (VB == 2) return 16 * g + 4 * (k >> 1) + (k & 1) + 2 * hi;
+  else return 16 * g + 2 * k + hi;
+}
+
+// A operands of k-tile kt for the 8 m-tiles, then the 8 MMAs.
+// 2-bit values: vtab is the value half of the shared pair table (entry b at
+// byte 256 b, lane l's replica 8 (l % 16) bytes into it, laneV = 128 + 8 (l %
+// 16) being that replica's offset in the row): for a byte b of the codes of two
+// tokens (bits 0-1 / 2-3: coordinate c of the first / second token, bits 4-5 /
+// 6-7: coordinate c + 2), entry b is the operand pair (a0, a1) or (a2, a3) as
+// loaded: half2 (c_V of the two tokens) for c and for c + 2.
+// lutp: for 3-bit values, half2 (c[i0], c[i1]) indexed by the pair (i0 | i1 <<
+// 3) of the codes of the two tokens of an operand register; for 4- and 8-bit
 // values, fp16 c[i] in the low half (pairs are packed with a byte permute).
 template <int VB>
-__device__ __forceinline__ void vmma_ktile(const uint8_t* vbuf, const uint32_t* lutp, int kt,
+__device__ __forceinline__ void vmma_ktile(const uint8_t* vbuf, const uint32_t* lutp,
+                                           const uint8_t* vtab, uint32_t laneV, int kt,
                                            int g, int tig, uint32_t b0, uint32_t b1,
                                            float (&d)[8][4]) {
   constexpr int VROW = 16 * VB;
@@ -122,24 +138,20 @@ __device__ __forceinline__ void vmma_ktile(const uint8_t* vbuf, const uint32_t* 
   if constexpr (VB == 2) {
     const uint32_t x0 = *(const uint32_t*)(r0 + 4 * g), x1 = *(const uint32_t*)(r1 + 4 * g);
     const uint32_t x2 = *(const uint32_t*)(r2 + 4 * g), x3 = *(const uint32_t*)(r3 + 4 * g);
-    // nibble k of zA: codes of coordinate 16g+2k for tokens t0 (bits 0-1) and t0+1 (bits 2-3);
-    // zA2 the same for coordinate 16g+2k+1
+    // byte b of zA: codes of coordinates 16g + 4b (bits 0-3) and 16g + 4b + 2
+    // (bits 4-7) of tokens t0 and t0 + 8; zA2 the same for 16g + 4b + 1 and
+    // + 3; zB, zB2 for tokens t0 + 4, t0 + 12.  m-tile k reads byte k / 2 of
+    // zA (k even) or zA2 (k odd): rows g / g + 8 are coordinates c / c + 2.
     const uint32_t zA = (x0 & 0x33333333u) | ((x1 & 0x33333333u) << 2);
     const uint32_t zA2 = ((x0 >> 2) & 0x33333333u) | (x1 & 0xCCCCCCCCu);
     const uint32_t zB = (x2 & 0x33333333u) | ((x3 & 0x33333333u) << 2);
     const uint32_t zB2 = ((x2 >> 2) & 0x33333333u) | (x3 & 0xCCCCCCCCu);
-    const uint32_t eA = (zA << 2) & 0x3C3C3C3Cu, oA = (zA >> 2) & 0x3C3C3C3Cu;
-    const uint32_t eA2 = (zA2 << 2) & 0x3C3C3C3Cu, oA2 = (zA2 >> 2) & 0x3C3C3C3Cu;
-    const uint32_t eB = (zB << 2) & 0x3C3C3C3Cu, oB = (zB >> 2) & 0x3C3C3C3Cu;
-    const uint32_t eB2 = (zB2 << 2) & 0x3C3C3C3Cu, oB2 = (zB2 >> 2) & 0x3C3C3C3Cu;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const int by = k >> 1;
-      const uint32_t a0 = lut_u32(lutp, byte_of((k & 1) ? oA : eA, by));
-      const uint32_t a1 = lut_u32(lutp, byte_of((k & 1) ? oA2 : eA2, by));
-      const uint32_t a2 = lut_u32(lutp, byte_of((k & 1) ? oB : eB, by));
-      const uint32_t a3 = lut_u32(lutp, byte_of((k & 1) ? oB2 : eB2, by));
-      mma16816(d[k], a0, a1, a2, a3, b0, b1);
+      const uint32_t sel = 0x5504u | ((uint32_t)(k >> 1) << 4);
+      const uint2 ea = *(const uint2*)(vtab + __byte_perm((k & 1) ? zA2 : zA, laneV, sel));
+      const uint2 eb = *(const uint2*)(vtab + __byte_perm((k & 1) ? zB2 : zB, laneV, sel));
+      mma16816(d[k], ea.x, ea.y, eb.x, eb.y, b0, b1);
     }
   } else if constexpr (VB == 3) {
     // 48 bits of coordinates 16g..16g+15 start at byte 6g of a 48-byte row;
@@ -219,9 +231,8 @@ __device__ __forceinline__ void vmma_ktile(const uint8_t* vbuf, const uint32_t* 
 // +1 (and +2, +3), so its 32 coordinates are contiguous in a packed row.
 // Key tables (centroids x kCScale): 2, 3 and 4 bits: uint2 (hi pair, lo pair)
 // indexed by the code pair (c_i | c_{i+1} << KB); the 3- and 4-bit tables (64
-// and 256 pairs) are kept in 16 replicas interleaved 8 bytes apart, lane l
-// reading replica l % 16, so the 16 lanes of a half-warp always hit 16
-// different bank pairs;
+// and 256 pairs) are kept in 32 replicas interleaved 8 bytes apart (256 bytes
+// per pair), lane l reading replica l, so a warp's 32 lookups never collide;
 // 8 bits: u32 hi | lo << 16 per code.
 template <int KB>
 struct KCodes {  // one token's 32 codes for this thread, as table offsets
@@ -250,10 +261,14 @@ __device__ __forceinline__ void load_kcodes(const uint8_t* row, int tig, KCodes<
   }
 }
 
-// (hi pair, lo pair) operand of coordinates 32tig + i, i+1 (i even, compile time)
+// (hi pair, lo pair) operand of coordinates 32tig + i, i+1 (i even, compile time).
+// 3- and 4-bit keys: lut is the base of the replicated pair table (entry p at
+// byte 256 p, lane l's replica 8 l bytes into it) and lane8 = 8 * lane, so
+// the byte offset (p << 8) | lane8 is one byte permute (4 bits: the pair is a
+// byte of the codes) or one shift and one masked OR (3 bits) away from the codes.
 template <int KB, int I>
-__device__ __forceinline__ void kpair(const KCodes<KB>& c, const uint32_t* lut, uint32_t& hi,
-                                      uint32_t& lo) {
+__device__ __forceinline__ void kpair(const KCodes<KB>& c, const uint32_t* lut, uint32_t lane8,
+                                      uint32_t& hi, uint32_t& lo) {
   if constexpr (KB == 2) {
     // nibble I/2 of the 64 code bits: byte (I/4) % 4 of word I/16, low or high nibble
     const uint32_t w = c.w[I / 16];
@@ -263,26 +278,25 @@ __device__ __forceinline__ void kpair(const KCodes<KB>& c, const uint32_t* lut, 
     hi = e.x;
     lo = e.y;
   } else if constexpr (KB == 3) {
-    // the pair's 6 bits start at bit o of the 96 code bits; the 64-entry table
-    // is kept in 16 replicas like the 4-bit one (entries 128 B apart, lut at
-    // this lane's replica), so the offset is the field moved to bit 7
+    // the pair's 6 bits start at bit o of the 96 code bits: the field moved to
+    // bit 8, masked, OR the lane's replica offset
     constexpr int o = 3 * I, wi = o / 32, b = o % 32;
     uint32_t v;
-    if constexpr (b < 7) {
-      v = c.w[wi] << (7 - b);
+    if constexpr (b < 8) {
+      v = c.w[wi] << (8 - b);
     } else if constexpr (b + 6 <= 32) {
-      v = c.w[wi] >> (b - 7);
+      v = c.w[wi] >> (b - 8);
     } else {
-      v = __funnelshift_r(c.w[wi], c.w[wi + 1], b - 7);
+      v = __funnelshift_r(c.w[wi], c.w[wi + 1], b - 8);
     }
-    const uint2 e = *(const uint2*)((const char*)lut + (v & 0x1F80u));
+    const uint2 e = *(const uint2*)((const char*)lut + ((v & 0x3F00u) | lane8));
     hi = e.x;
     lo = e.y;
   } else if constexpr (KB == 4) {
     // byte I/2 of the 128 code bits (word I/8, byte (I/2)%4) is the pair index
-    // c_I | c_{I+1} << 4; lut points at this lane's replica, entries 128 B apart
-    const uint32_t p = __byte_perm(c.w[I / 8], 0u, 0x4440u | ((I / 2) % 4));
-    const uint2 e = *(const uint2*)((const char*)lut + p * 128u);
+    // c_I | c_{I+1} << 4: the permute puts it in byte 1 and lane8 in byte 0
+    const uint32_t off = __byte_perm(c.w[I / 8], lane8, 0x5504u | (((I / 2) % 4) << 4));
+    const uint2 e = *(const uint2*)((const char*)lut + off);
     hi = e.x;
     lo = e.y;
   } else {
@@ -300,15 +314,16 @@ __device__ __forceinline__ void kpair(const KCodes<KB>& c, const uint32_t* lut, 
 // separate chains (six independent chains of eight).
 template <int KB, int KT>
 __device__ __forceinline__ void score_ktile(const KCodes<KB> (&c)[4], const uint32_t* lut,
+                                            uint32_t lane8,
                                             const uint32_t (&bh)[8][2], const uint32_t (&bl)[8][2],
                                             float (&hh)[2][4], float (&lh)[2][4], float (&hl)[2][4]) {
 #pragma unroll
   for (int mt = 0; mt < 2; ++mt) {
     uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
-    kpair<KB, 4 * KT>(c[2 * mt], lut, h0, l0);
-    kpair<KB, 4 * KT>(c[2 * mt + 1], lut, h1, l1);
-    kpair<KB, 4 * KT + 2>(c[2 * mt], lut, h2, l2);
-    kpair<KB, 4 * KT + 2>(c[2 * mt + 1], lut, h3, l3);
+    kpair<KB, 4 * KT>(c[2 * mt], lut, lane8, h0, l0);
+    kpair<KB, 4 * KT>(c[2 * mt + 1], lut, lane8, h1, l1);
+    kpair<KB, 4 * KT + 2>(c[2 * mt], lut, lane8, h2, l2);
+    kpair<KB, 4 * KT + 2>(c[2 * mt + 1], lut, lane8, h3, l3);
     mma16816(hh[mt], h0, h1, h2, h3, bh[KT][0], bh[KT][1]);
     mma16816(lh[mt], l0, l1, l2, l3, bh[KT][0], bh[KT][1]);
     mma16816(hl[mt], h0, h1, h2, h3, bl[KT][0], bl[KT][1]);
@@ -317,33 +332,35 @@ __device__ __forceinline__ void score_ktile(const KCodes<KB> (&c)[4], const uint
 
 template <int KB, int KT>
 __device__ __forceinline__ void score_all(const KCodes<KB> (&c)[4], const uint32_t* lut,
+                                          uint32_t lane8,
                                           const uint32_t (&bh)[8][2], const uint32_t (&bl)[8][2],
                                           float (&hh)[2][4], float (&lh)[2][4], float (&hl)[2][4]) {
   if constexpr (KT < 8) {
-    score_ktile<KB, KT>(c, lut, bh, bl, hh, lh, hl);
-    score_all<KB, KT + 1>(c, lut, bh, bl, hh, lh, hl);
+    score_ktile<KB, KT>(c, lut, lane8, bh, bl, hh, lh, hl);
+    score_all<KB, KT + 1>(c, lut, lane8, bh, bl, hh, lh, hl);
   }
 }
 
-// G <= 4 ("folded"): the free columns 4-7 carry the query's lo part (column
-// n is head n % 4, hi part for n < 4, lo part for n >= 4), and m-tile u holds
+// G <= 4 ("folded"): the 8 MMA columns hold G heads twice, column 2h the
+// query's hi part of head h and column 2h + 1 its lo part, and m-tile u holds
 // token 8u + g twice: row g its K hi part, row g+8 its K lo part.  One MMA
-// then yields hi*hi (row g, columns 0-3), hi*lo (row g, 4-7), lo*hi (row g+8,
-// 0-3) and a negligible lo*lo, and each (hi pair, lo pair) table entry is
-// the A operand pair (a0, a1) or (a2, a3) as loaded: 32 MMAs per chunk in
-// four chains, against 48 in six.
+// then yields hi*hi (row g, even columns), hi*lo (row g, odd), lo*hi (row
+// g+8, even) and a negligible lo*lo, all of head tig in lane (g, tig), and
+// each (hi pair, lo pair) table entry is the A operand pair (a0, a1) or
+// (a2, a3) as loaded: 32 MMAs per chunk in four chains, against 48 in six.
 template <int KB, int KT>
 __device__ __forceinline__ void score_all_folded(const KCodes<KB> (&c)[4], const uint32_t* lut,
-                                                 const uint32_t (&bq)[8][2], float (&acc)[4][4]) {
+                                                 uint32_t lane8, const uint32_t (&bq)[8][2],
+                                                 float (&acc)[4][4]) {
   if constexpr (KT < 8) {
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       uint32_t h0, l0, h2, l2;
-      kpair<KB, 4 * KT>(c[u], lut, h0, l0);
-      kpair<KB, 4 * KT + 2>(c[u], lut, h2, l2);
+      kpair<KB, 4 * KT>(c[u], lut, lane8, h0, l0);
+      kpair<KB, 4 * KT + 2>(c[u], lut, lane8, h2, l2);
       mma16816(acc[u], h0, l0, h2, l2, bq[KT][0], bq[KT][1]);
     }
-    score_all_folded<KB, KT + 1>(c, lut, bq, acc);
+    score_all_folded<KB, KT + 1>(c, lut, lane8, bq, acc);
   }
 }
 
@@ -392,7 +409,7 @@ __device__ __forceinline__ void qjl_scores(uint32_t sa, uint32_t sb, const uint3
 
 template <int G, int KB, int VB, int RES, bool SPARSE>
 __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
-                                  decode_ctas_per_sm(decode_warps(G, KB, VB, RES)))
+                                  decode_ctas_per_sm(G, KB, VB, RES))
     decode_kernel(const DecodeArgs a) {
   constexpr int kDWarps = decode_warps(G, KB, VB, RES);   // warps of this CTA
   constexpr int kDT = kDWarps * 32;
@@ -574,18 +591,29 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
         lutk[2 * i + 1] = lp;
       }
     } else if constexpr (KB == 3 || KB == 4) {
-      // pair i = c_lo | c_hi << KB into all 16 replicas; at step j lane l
-      // writes replica (l + j) % 16, so a half-warp's stores never collide
+      // pair i = c_lo | c_hi << KB into the 16 key replicas of row i; at
+      // step j lane l writes replica (l + j) % 16
       if (i < (1 << (2 * KB))) {
         constexpr int msk = (1 << KB) - 1;
         uint32_t hp, lp;
         hilo2(cks[i & msk] * kCScale, cks[i >> KB] * kCScale, hp, lp);
-        uint2* row = (uint2*)(smem + L.lutk4) + i * 16;
+        uint2* row = (uint2*)(smem + L.lutk4) + i * 32;
 #pragma unroll
         for (int j = 0; j < 16; ++j) row[(lane + j) & 15] = make_uint2(hp, lp);
       }
     } else {
       lutk[i] = hilo(cks[i] * kCScale);
+    }
+    if constexpr (VB == 2) {
+      // value entry i of the pair table: (half2 of coordinate c, half2 of c + 2)
+      // for the code byte i (see vmma_ktile), into replicas 16-31 of row i
+      auto pe = [&](int n) {   // n = code of the first token | code of the second << 2
+        return (h16(cvs[(n >> 2) & 3]) << 16) | h16(cvs[n & 3]);
+      };
+      const uint2 ve = make_uint2(pe(i & 15), pe(i >> 4));
+      uint2* row = (uint2*)(smem + L.lutk4) + i * 32 + 16;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) row[(lane + j) & 15] = ve;
     }
     uint32_t e;
     if constexpr (VB == 2 || VB == 3) {
@@ -642,9 +670,9 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
   (void)frexpf(qmax, &qe);
   const float qsp = qmax > 0.f ? ldexpf(1.f, -qe) : 1.f;
   // B operands (q hi/lo) of this lane, coordinates 32tig + 4kt + {0,1} / {2,3}:
-  // unfolded, head mg in bh (hi) and bl (lo); folded, column mg is head mg % 4,
-  // its hi part for mg < 4 and its lo part for mg >= 4, all in bh
-  const int qhead = FOLD ? (mg & 3) : mg;
+  // unfolded, head mg in bh (hi) and bl (lo); folded, column mg is head mg / 2,
+  // its hi part for even mg and its lo part for odd mg, all in bh
+  const int qhead = FOLD ? (mg >> 1) : mg;
   uint32_t bh[8][2], bl[8][2];
 #pragma unroll
   for (int kt = 0; kt < 8; ++kt) {
@@ -655,7 +683,7 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
         const int c = 32 * tig + 4 * kt + 2 * p;
         hilo2(qr[c * G + qhead] * qsp, qr[(c + 1) * G + qhead] * qsp, hp, lp);
       }
-      bh[kt][p] = FOLD && mg >= 4 ? lp : hp;
+      bh[kt][p] = FOLD && (mg & 1) ? lp : hp;
       bl[kt][p] = lp;
     }
   }
@@ -696,10 +724,10 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
     (void)frexpf(smax, &se);
     qsq = smax > 0.f ? ldexpf(1.f, -se) : 1.f;
     // per k-tile, per lane: (b0 hi, b1 hi, b0 lo, b1 lo) of head lane/4 (folded:
-    // (lane/4) % 4, and only the lane's part), sketch indices 32(lane%4) + 4kt
-    // + {0,1} / {2,3}
+    // head lane/8, and only the lane's part, hi for even lane/4), sketch
+    // indices 32(lane%4) + 4kt + {0,1} / {2,3}
     for (int e = tid; e < 32 * 8; e += kDT) {
-      const int kt = e / 32, ln = e % 32, g = FOLD ? (ln >> 2) & 3 : ln >> 2, tg = ln & 3;
+      const int kt = e / 32, ln = e % 32, g = FOLD ? ln >> 3 : ln >> 2, tg = ln & 3;
       uint4 o = make_uint4(0u, 0u, 0u, 0u);
       if (g < G) {
         const int c = 32 * tg + 4 * kt;
@@ -707,7 +735,7 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
         hilo2(sq[g * kQjlM + c + 2] * qsq, sq[g * kQjlM + c + 3] * qsq, o.y, o.w);
       }
       if constexpr (FOLD)
-        ((uint2*)(smem + L.qjlb))[e] = (ln >> 4) ? make_uint2(o.z, o.w) : make_uint2(o.x, o.y);
+        ((uint2*)(smem + L.qjlb))[e] = ((ln >> 2) & 1) ? make_uint2(o.z, o.w) : make_uint2(o.x, o.y);
       else
         ((uint4*)(smem + L.qjlb))[e] = o;
     }
@@ -720,7 +748,9 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
   float* co = cl + kDWarps * G;          // [warps][G][128]
 
   if (!window_split) {
-    // online-softmax state of heads 2tig, 2tig+1 (accumulator columns)
+    // online-softmax state: folded, of head tig (mfold, lfold); unfolded, of heads
+    // 2tig, 2tig+1 (the accumulator columns)
+    float mfold = kNegBig, lfold = 0.f;
     float m0 = kNegBig, m1 = kNegBig, l0 = 0.f, l1 = 0.f;
     float inv_d = 1.f;       // d holds the V sum divided by inv_d (a power of two)
     float d[8][4];           // fp32 V-sum accumulators (MMA layout)
@@ -729,8 +759,14 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
 #pragma unroll
       for (int j = 0; j < 4; ++j) d[k][j] = 0.f;
     const bool h0ok = 2 * tig < G, h1ok = 2 * tig + 1 < G;
-    const uint32_t* klut =
-        KB == 3 || KB == 4 ? (const uint32_t*)(smem + L.lutk4 + 8 * (lane & 15)) : lutk;
+    // the shared pair table: row p (256 bytes) holds 16 replicas of the key
+    // pair entry p (bytes 0-127) and, for 2-bit values, 16 of the value entry p
+    // (bytes 128-255); lane l reads replica l % 16, so a half-warp's 16
+    // lookups hit 16 different bank pairs
+    const uint8_t* ptab = smem + L.lutk4;
+    const uint32_t* klut = KB == 3 || KB == 4 ? (const uint32_t*)ptab : lutk;
+    const uint32_t lane8 = 8u * (uint32_t)(lane & 15);          // key replica offset
+    const uint32_t laneV = 128u + 8u * (uint32_t)(lane & 15);   // value replica offset
     // [8 heads][16 pairs] fp16 weights: pair 8kt + j = tokens 16kt + j, 16kt + j + 8
     uint32_t* ws32 = (uint32_t*)(wreg + L.ws);
     const float kscale = 1.f / (kCScale * qsp);
@@ -755,6 +791,112 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
       const float* kn_ = (const float*)(wreg + L.kn + slot * 128);
       const float* vn_ = (const float*)(wreg + L.vn + slot * 128);
       const float vmax = warp_max(lane < nv ? vn_[lane] : 0.f);
+      if constexpr (FOLD) {
+        // ---- scores on the tensor cores: MMA column 2h is head h's query hi
+        // part and column 2h + 1 its lo part, so lane (mg, tig) holds both
+        // parts of head tig for the tokens of its rows.  m-tile u holds token
+        // 8u + mg twice (row mg: K hi, row mg + 8: K lo), and
+        //   score = hi*hi (acc[0]) + hi*lo (acc[1]) + lo*hi (acc[2])
+        // (lo*lo, acc[3], is below fp32 rounding and dropped).
+        float s4[4];
+        {
+          KCodes<KB> c[4];
+#pragma unroll
+          for (int r = 0; r < 4; ++r) load_kcodes<KB>(kb_ + (8 * r + mg) * KROW, tig, c[r]);
+          float acc[4][4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[u][j] = 0.f;
+          score_all_folded<KB, 0>(c, klut, lane8, bh, acc);
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            s4[u] = (acc[u][0] + acc[u][1] + acc[u][2]) * (kn_[8 * u + mg] * kscale);
+        }
+        if constexpr (HAS_RES) {
+          // the residual MMA's rows are two tokens (16mt + mg, 16mt + mg + 8),
+          // its columns the same hi / lo pairs
+          const uint8_t* sb_ = wreg + L.sbuf + slot * 512;
+          const float* rn_ = (const float*)(wreg + L.rn + slot * 128);
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) {
+            const int ta = 16 * mt + mg, tb = ta + 8;
+            const uint32_t sa = *(const uint32_t*)(sb_ + ta * 16 + 4 * tig);
+            const uint32_t sbits = *(const uint32_t*)(sb_ + tb * 16 + 4 * tig);
+            float qa[4] = {0.f, 0.f, 0.f, 0.f}, ql[4] = {0.f, 0.f, 0.f, 0.f};
+            if constexpr (QJL) qjl_scores<true>(sa, sbits, slut, qjlb, lane, qa, ql);
+            else sign_scores<true>(sa, sbits, slut, bh, bl, qa, ql);
+            s4[2 * mt] = fmaf(qa[0] + qa[1], rn_[ta] * res_scale, s4[2 * mt]);
+            s4[2 * mt + 1] = fmaf(qa[2] + qa[3], rn_[tb] * res_scale, s4[2 * mt + 1]);
+          }
+        }
+        // tokens past the end of a partial chunk get no weight; lanes of
+        // absent heads (tig >= G) compute values that are never used
+        if (nv < 32) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (8 * u + mg >= nv) s4[u] = kNegBig;
+        }
+        // ---- online softmax of head tig (log2 domain): max over the lane's 4
+        // tokens, then over the 8 lanes of the head
+        float x = fmaxf(fmaxf(s4[0], s4[1]), fmaxf(s4[2], s4[3]));
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+        const float mn = fmaxf(mfold, x);
+        const float al = ex2(mfold - mn);
+        mfold = mn;
+        int sexp = 141 - (int)((__float_as_uint(vmax) >> 23) & 0xFFu);   // 14 - floor(log2 vmax)
+        sexp = sexp > 64 ? 64 : sexp < -60 ? -60 : sexp;
+        const float scl = __int_as_float((127 + sexp) << 23);
+        float p[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) p[u] = ex2(s4[u] - mn);
+        lfold = fmaf(lfold, al, (p[0] + p[1]) + (p[2] + p[3]));
+        bool skip_v = false;
+        if constexpr (SPARSE)
+          skip_v = warp_max(tig < G ? fmaxf(fmaxf(p[0], p[1]), fmaxf(p[2], p[3])) : 0.f) <
+                   a.sparse_thr;
+        // fp16 weights p ||v|| scaled into range by a power of two (see
+        // below); pairs (tokens 8u + mg, 8u + 8 + mg) for u = 0, 2
+        uint32_t pk[2];
+#pragma unroll
+        for (int kt = 0; kt < 2; ++kt) {
+          const int ta = 16 * kt + mg, tb = ta + 8;
+          const float va = ta < nv ? vn_[ta] * scl : 0.f, vb = tb < nv ? vn_[tb] * scl : 0.f;
+          const __half2 h = __floats2half2_rn(p[2 * kt] * va, p[2 * kt + 1] * vb);
+          pk[kt] = *(const uint32_t*)&h;
+        }
+        // ---- rotated-domain V sum on the tensor cores: accumulator columns
+        // 2tig, 2tig + 1 are heads 2tig, 2tig + 1, whose rescale factors the
+        // score lanes of those heads hold
+        const float al0 = __shfl_sync(0xffffffffu, al, 2 * tig);
+        const float al1 = __shfl_sync(0xffffffffu, al, 2 * tig + 1);
+        const float rs = skip_v ? 1.f : scl * inv_d;     // a power of two, exact
+        if (!skip_v) inv_d = __uint_as_float(0x7F000000u - __float_as_uint(scl));   // 1 / scl
+        const float2 pre = make_float2(al0 * rs, al1 * rs);
+        // once the running maxima and the weight scale settle, most chunks
+        // leave the accumulator's scale unchanged: skip the multiply then
+        if (__any_sync(0xffffffffu, pre.x != 1.f || pre.y != 1.f)) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float2 lo = __fmul2_rn(make_float2(d[k][0], d[k][1]), pre);
+            const float2 hi = __fmul2_rn(make_float2(d[k][2], d[k][3]), pre);
+            d[k][0] = lo.x; d[k][1] = lo.y; d[k][2] = hi.x; d[k][3] = hi.y;
+          }
+        }
+        // B operand of k-tile kt, lane (mg, tig): head mg's weight pairs
+        // tig and tig + 4, i.e. tokens (16kt + tig, 16kt + tig + 8) and
+        // (16kt + tig + 4, 16kt + tig + 12), packed by score lanes 4 tig + mg
+        // and 4 (tig + 4) + mg
+        const uint8_t* vb_ = wreg + L.vbuf + slot * 32 * VROW;
+#pragma unroll
+        for (int kt = 0; kt < 2; ++kt) {
+          uint32_t b0 = __shfl_sync(0xffffffffu, pk[kt], 4 * tig + mg);
+          uint32_t b1 = __shfl_sync(0xffffffffu, pk[kt], 4 * tig + mg + 16);
+          if (mg >= G) b0 = b1 = 0u;
+          if (!skip_v) vmma_ktile<VB>(vb_, lutv, ptab, laneV, kt, mg, tig, b0, b1, d);
+        }
+      } else {
       // ---- scores on the tensor cores: sc[mt][0,1] token 16mt+mg, sc[mt][2,3] token +8;
       //      columns 0 / 1 are heads 2tig / 2tig+1
       float sc[2][4];
@@ -769,13 +911,13 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
           for (int u = 0; u < 4; ++u)
 #pragma unroll
             for (int j = 0; j < 4; ++j) acc[u][j] = 0.f;
-          score_all_folded<KB, 0>(c, klut, bh, acc);
+          score_all_folded<KB, 0>(c, klut, lane8, bh, acc);
         } else {
 #pragma unroll
           for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
             for (int j = 0; j < 4; ++j) hh[mt][j] = lh[mt][j] = hl[mt][j] = 0.f;
-          score_all<KB, 0>(c, klut, bh, bl, hh, lh, hl);
+          score_all<KB, 0>(c, klut, lane8, bh, bl, hh, lh, hl);
         }
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
@@ -891,9 +1033,10 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
       for (int kt = 0; kt < 2 && !skip_v; ++kt) {
         const uint32_t b0 = mg < G ? ws32[mg * kWsStride + 8 * kt + tig] : 0u;
         const uint32_t b1 = mg < G ? ws32[mg * kWsStride + 8 * kt + tig + 4] : 0u;
-        vmma_ktile<VB>(vb_, lutv, kt, mg, tig, b0, b1, d);
+        vmma_ktile<VB>(vb_, lutv, ptab, laneV, kt, mg, tig, b0, b1, d);
       }
       __syncwarp();
+      }
     }
     {
       const float inv = inv_d;                    // back to the unscaled sum
@@ -920,11 +1063,20 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
     // per-head l: sum over the 8 lanes of each column group
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
-      l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+      if constexpr (FOLD) {
+        lfold += __shfl_xor_sync(0xffffffffu, lfold, o);
+      } else {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+      }
     }
     __syncthreads();                     // every warp is done with its ring buffers
-    if (mg == 0) {
+    if constexpr (FOLD) {
+      if (mg == 0 && tig < G) {
+        cm[warp * G + tig] = mfold;
+        cl[warp * G + tig] = lfold;
+      }
+    } else if (mg == 0) {
       if (h0ok) {
         cm[warp * G + 2 * tig] = m0;
         cl[warp * G + 2 * tig] = l0;
@@ -934,19 +1086,20 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
         cl[warp * G + 2 * tig + 1] = l1;
       }
     }
-    // thread (mg, tig): m-tile k rows -> coordinates 16mg+2k (+1); columns -> heads 2tig (+1)
+    // thread (mg, tig): m-tile k rows mg, mg + 8 -> coordinates vrow_coord;
+    // columns -> heads 2tig (+1)
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const int c = 16 * mg + 2 * k;
+      const int c0 = vrow_coord<VB>(mg, k, 0), c1 = vrow_coord<VB>(mg, k, 1);
       if (h0ok) {
-        float* dst = co + (warp * G + 2 * tig) * kD2 + c;
-        dst[0] = d[k][0];
-        dst[1] = d[k][2];
+        float* dst = co + (warp * G + 2 * tig) * kD2;
+        dst[c0] = d[k][0];
+        dst[c1] = d[k][2];
       }
       if (h1ok) {
-        float* dst = co + (warp * G + 2 * tig + 1) * kD2 + c;
-        dst[0] = d[k][1];
-        dst[1] = d[k][3];
+        float* dst = co + (warp * G + 2 * tig + 1) * kD2;
+        dst[c0] = d[k][1];
+        dst[c1] = d[k][3];
       }
     }
   } else {

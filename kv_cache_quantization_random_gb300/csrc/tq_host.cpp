@@ -485,7 +485,7 @@ static DecodePlan decode_plan(const tq_config* cfg, const tq_layer_spec& s, int 
   if (wst > 32 * warps) wst = 32 * warps;
   p.wsplit_tokens = wst > 0 ? wst : 1;
   const int n_wsplits = W > 0 ? (W + wst - 1) / wst : 0;
-  long long wave = (long long)kDecodeSms * decode_ctas_per_sm(warps) - reserve;
+  long long wave = (long long)kDecodeSms * decode_ctas_per_sm(p.G, s.k_bits, s.v_bits, res) - reserve;
   if (wave < 1) wave = 1;
   long long slots = wave - units * n_wsplits;
   if (slots < units) {

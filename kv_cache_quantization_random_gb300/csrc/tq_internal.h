@@ -21,8 +21,11 @@ constexpr int kPartialStride = 4 + kHeadDim;   // floats per (split, head): m, l
 // reads of the 8 heads x 4 lanes fall into 32 different banks
 constexpr int kWsStride = 20;
 // 32-token chunks in each warp's staging ring: enough bytes in flight per SM
-// to cover the HBM latency; formats with wide rows keep 3.
-__host__ __device__ constexpr int ring_slots(int kb, int vb) { return kb + vb <= 8 ? 4 : 3; }
+// to cover the HBM latency (3 slots of 12 warps hold about 120 KB for 3- and
+// 4-bit keys); formats with 2-bit keys and narrow rows keep 4.
+__host__ __device__ constexpr int ring_slots(int kb, int vb) {
+  return kb <= 2 && kb + vb <= 8 ? 4 : 3;
+}
 
 // Byte layout of the dynamic shared memory of a decode CTA with nw warps
 // (G query columns per kv-head; res 0 = MSE keys, 1 = QJL, 2 = Direct Sign).
@@ -38,7 +41,8 @@ struct DecodeSmem {
     sv = off; off += kHeadDim * 4;
     qjlb = off; off += qjl ? 32 * 8 * 16 : 0;     // per lane, per k-tile: S q hi/lo operands
     sq = off; off += qjl ? G * kQjlM * 4 : 0;     // [G][m] S q_rot (QJL)
-    lutk4 = off; off += kb == 4 ? 256 * 16 * 8 : kb == 3 ? 64 * 16 * 8 : 0;   // 3/4-bit key pairs, 16 replicas
+    // pair table: 256-byte rows, 16 key replicas then 16 value replicas (2-bit values)
+    lutk4 = off; off += vb == 2 || kb == 4 ? 256 * 256 : kb == 3 ? 64 * 256 : 0;
     warps = off;
     const int ns = ring_slots(kb, vb);
     int w = 0;
@@ -79,8 +83,14 @@ __host__ __device__ constexpr int decode_warps(int G, int kb, int vb, int res) {
          : DecodeSmem(G, res, kb, vb, 8).total <= kDecodeSmemBudget  ? 8
                                                                        : 4;
 }
-// resident decode CTAs per SM for a CTA of `warps` warps
-__host__ __device__ constexpr int decode_ctas_per_sm(int warps) { return warps == 4 ? 2 : 1; }
+// resident decode CTAs per SM: two CTAs of 4 warps when both fit in the SM's
+// shared memory (227 KB usable, less the kernel's 3 KB of static tables), else one
+__host__ __device__ constexpr int decode_ctas_per_sm(int G, int kb, int vb, int res) {
+  return decode_warps(G, kb, vb, res) == 4 &&
+                 2 * (DecodeSmem(G, res, kb, vb, 4).total + 4 * 1024) <= 227 * 1024
+             ? 2
+             : 1;
+}
 
 // ---- device tables (built on the host by tq_build_tables) -------------------
 // [0, 256)                 header, int32 words (see kTbl*)
