@@ -69,7 +69,9 @@ _LIB = None
 
 
 def lib_path() -> str:
-    return _build.LIB_PATH
+    """The library this process loads: libtq.so, or with TQ_LIB_VARIANT=debug
+    the bounds-checked libtq_debug.so."""
+    return _build.lib_path()
 
 
 def load(build_if_missing: bool = False):

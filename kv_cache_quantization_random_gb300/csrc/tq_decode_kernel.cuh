@@ -45,6 +45,9 @@ namespace tq {
 constexpr int kD2 = 128;
 constexpr float kNegBig = -1.0e30f;
 constexpr float kCScale = 64.f;   // centroids are scaled by 64 in the K tables
+// the running softmax maxima are raised only when a score exceeds them by
+// more than this (log2 units), so softmax weights are at most 2^kLazyMax
+constexpr float kLazyMax = 8.f;
 
 // 2^x on the MUFU unit (relative error about 2^-22; results below the fp32
 // normal range flush to zero, as the softmax weights may)
@@ -99,10 +102,6 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ uint32_t lut_u32(const uint32_t* lut, uint32_t byte_off) {
-  return *(const uint32_t*)((const char*)lut + byte_off);
-}
-
 // Coordinate of accumulator row g (hi = 0) or g + 8 (hi = 1) of m-tile k for
 // lane group g: 2-bit values pair coordinates c and c + 2 in one code byte
 // (see vmma_ktile), wider values c and c + 1.
@@ -126,15 +125,19 @@ template <int VB>
 __device__ __forceinline__ void vmma_ktile(const uint8_t* vbuf, const uint32_t* lutp,
                                            const uint8_t* vtab, uint32_t laneV, int kt,
                                            int g, int tig, uint32_t b0, uint32_t b1,
-                                           float (&d)[8][4]) {
+                                           float (&d)[8][4], unsigned* err) {
   constexpr int VROW = 16 * VB;
   // a0/a1: columns 2tig, 2tig+1 = tokens t0, t0 + 8; a2/a3: columns 2tig+8,
-  // 2tig+9 = tokens t0 + 4, t0 + 12
+  // 2tig+9 = tokens t0 + 4, t0 + 12 (rows of the chunk's 32-row slot)
   const int t0 = 16 * kt + tig;
-  const uint8_t* r0 = vbuf + t0 * VROW;
-  const uint8_t* r1 = r0 + 8 * VROW;
-  const uint8_t* r2 = r0 + 4 * VROW;
-  const uint8_t* r3 = r0 + 12 * VROW;
+  const uint8_t* r0 = bchk((const uint8_t(*)[VROW])(vbuf + t0 * VROW), vbuf, 32 * VROW, err)[0];
+  const uint8_t* r1 = bchk((const uint8_t(*)[VROW])(vbuf + (t0 + 8) * VROW), vbuf, 32 * VROW, err)[0];
+  const uint8_t* r2 = bchk((const uint8_t(*)[VROW])(vbuf + (t0 + 4) * VROW), vbuf, 32 * VROW, err)[0];
+  const uint8_t* r3 = bchk((const uint8_t(*)[VROW])(vbuf + (t0 + 12) * VROW), vbuf, 32 * VROW, err)[0];
+  // lookups stay inside the 256-entry tables
+  auto lut_u32 = [&](const uint32_t* lut, uint32_t off) {
+    return *bchk((const uint32_t*)((const char*)lut + off), lut, 256 * 4, err);
+  };
   if constexpr (VB == 2) {
     const uint32_t x0 = *(const uint32_t*)(r0 + 4 * g), x1 = *(const uint32_t*)(r1 + 4 * g);
     const uint32_t x2 = *(const uint32_t*)(r2 + 4 * g), x3 = *(const uint32_t*)(r3 + 4 * g);
@@ -149,8 +152,10 @@ __device__ __forceinline__ void vmma_ktile(const uint8_t* vbuf, const uint32_t* 
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const uint32_t sel = 0x5504u | ((uint32_t)(k >> 1) << 4);
-      const uint2 ea = *(const uint2*)(vtab + __byte_perm((k & 1) ? zA2 : zA, laneV, sel));
-      const uint2 eb = *(const uint2*)(vtab + __byte_perm((k & 1) ? zB2 : zB, laneV, sel));
+      const uint2 ea = *bchk((const uint2*)(vtab + __byte_perm((k & 1) ? zA2 : zA, laneV, sel)),
+                             vtab, 256 * 256, err);
+      const uint2 eb = *bchk((const uint2*)(vtab + __byte_perm((k & 1) ? zB2 : zB, laneV, sel)),
+                             vtab, 256 * 256, err);
       mma16816(d[k], ea.x, ea.y, eb.x, eb.y, b0, b1);
     }
   } else if constexpr (VB == 3) {
@@ -231,16 +236,20 @@ __device__ __forceinline__ void vmma_ktile(const uint8_t* vbuf, const uint32_t* 
 // +1 (and +2, +3), so its 32 coordinates are contiguous in a packed row.
 // Key tables (centroids x kCScale): 2, 3 and 4 bits: uint2 (hi pair, lo pair)
 // indexed by the code pair (c_i | c_{i+1} << KB); the 3- and 4-bit tables (64
-// and 256 pairs) are kept in 32 replicas interleaved 8 bytes apart (256 bytes
-// per pair), lane l reading replica l, so a warp's 32 lookups never collide;
-// 8 bits: u32 hi | lo << 16 per code.
+// and 256 pairs) are the key halves of the shared pair table: 16 replicas
+// interleaved 8 bytes apart in 256-byte rows, lane l reading replica l % 16,
+// so a half-warp's 16 lookups never collide; 8 bits: u32 hi | lo << 16 per code.
 template <int KB>
 struct KCodes {  // one token's 32 codes for this thread, as table offsets
   uint32_t w[KB];
 };
 
 template <int KB>
-__device__ __forceinline__ void load_kcodes(const uint8_t* row, int tig, KCodes<KB>& c) {
+__device__ __forceinline__ void load_kcodes(const uint8_t* slot, int r, int tig, KCodes<KB>& c,
+                                            unsigned* err) {
+  // row r of the chunk's 32-row slot
+  const uint8_t* row =
+      bchk((const uint8_t(*)[16 * KB])(slot + r * 16 * KB), slot, 32 * 16 * KB, err)[0];
   if constexpr (KB == 2) {
     const uint2 x = *(const uint2*)(row + 8 * tig);
     c.w[0] = x.x;
@@ -262,19 +271,22 @@ __device__ __forceinline__ void load_kcodes(const uint8_t* row, int tig, KCodes<
 }
 
 // (hi pair, lo pair) operand of coordinates 32tig + i, i+1 (i even, compile time).
-// 3- and 4-bit keys: lut is the base of the replicated pair table (entry p at
-// byte 256 p, lane l's replica 8 l bytes into it) and lane8 = 8 * lane, so
-// the byte offset (p << 8) | lane8 is one byte permute (4 bits: the pair is a
+// 3- and 4-bit keys: lut is the base of the pair table (entry p at byte 256 p,
+// lane l's replica 8 (l % 16) bytes into it) and lane8 = 8 (lane % 16), so the
+// byte offset (p << 8) | lane8 is one byte permute (4 bits: the pair is a
 // byte of the codes) or one shift and one masked OR (3 bits) away from the codes.
 template <int KB, int I>
 __device__ __forceinline__ void kpair(const KCodes<KB>& c, const uint32_t* lut, uint32_t lane8,
-                                      uint32_t& hi, uint32_t& lo) {
+                                      uint32_t& hi, uint32_t& lo, unsigned* err) {
+  // extent of the table this format reads: the 3/4-bit pair table's key rows
+  // (256-byte rows), else the kernel's 256-word table
+  constexpr size_t kLutBytes = KB == 4 ? 256 * 256 : KB == 3 ? 64 * 256 : 256 * 4;
   if constexpr (KB == 2) {
     // nibble I/2 of the 64 code bits: byte (I/4) % 4 of word I/16, low or high nibble
     const uint32_t w = c.w[I / 16];
     const uint32_t off = (I / 2) % 2 == 0 ? byte_of((w << 3) & 0x78787878u, (I / 4) % 4)
                                           : byte_of((w >> 1) & 0x78787878u, (I / 4) % 4);
-    const uint2 e = *(const uint2*)((const char*)lut + off);
+    const uint2 e = *bchk((const uint2*)((const char*)lut + off), lut, kLutBytes, err);
     hi = e.x;
     lo = e.y;
   } else if constexpr (KB == 3) {
@@ -289,21 +301,22 @@ __device__ __forceinline__ void kpair(const KCodes<KB>& c, const uint32_t* lut, 
     } else {
       v = __funnelshift_r(c.w[wi], c.w[wi + 1], b - 8);
     }
-    const uint2 e = *(const uint2*)((const char*)lut + ((v & 0x3F00u) | lane8));
+    const uint2 e =
+        *bchk((const uint2*)((const char*)lut + ((v & 0x3F00u) | lane8)), lut, kLutBytes, err);
     hi = e.x;
     lo = e.y;
   } else if constexpr (KB == 4) {
     // byte I/2 of the 128 code bits (word I/8, byte (I/2)%4) is the pair index
     // c_I | c_{I+1} << 4: the permute puts it in byte 1 and lane8 in byte 0
     const uint32_t off = __byte_perm(c.w[I / 8], lane8, 0x5504u | (((I / 2) % 4) << 4));
-    const uint2 e = *(const uint2*)((const char*)lut + off);
+    const uint2 e = *bchk((const uint2*)((const char*)lut + off), lut, kLutBytes, err);
     hi = e.x;
     lo = e.y;
   } else {
     // bytes I, I+1 of the 256 code bits: word I/4, half (I/2)%2
     const uint32_t w = c.w[I / 4];
-    const uint32_t e0 = *(const uint32_t*)((const char*)lut + half_of((w << 2) & 0x03FC03FCu, (I / 2) % 2));
-    const uint32_t e1 = *(const uint32_t*)((const char*)lut + half_of((w >> 6) & 0x03FC03FCu, (I / 2) % 2));
+    const uint32_t e0 = *bchk((const uint32_t*)((const char*)lut + half_of((w << 2) & 0x03FC03FCu, (I / 2) % 2)), lut, kLutBytes, err);
+    const uint32_t e1 = *bchk((const uint32_t*)((const char*)lut + half_of((w >> 6) & 0x03FC03FCu, (I / 2) % 2)), lut, kLutBytes, err);
     pack_hilo(e0, e1, hi, lo);
   }
 }
@@ -314,16 +327,16 @@ __device__ __forceinline__ void kpair(const KCodes<KB>& c, const uint32_t* lut, 
 // separate chains (six independent chains of eight).
 template <int KB, int KT>
 __device__ __forceinline__ void score_ktile(const KCodes<KB> (&c)[4], const uint32_t* lut,
-                                            uint32_t lane8,
+                                            uint32_t lane8, unsigned* err,
                                             const uint32_t (&bh)[8][2], const uint32_t (&bl)[8][2],
                                             float (&hh)[2][4], float (&lh)[2][4], float (&hl)[2][4]) {
 #pragma unroll
   for (int mt = 0; mt < 2; ++mt) {
     uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
-    kpair<KB, 4 * KT>(c[2 * mt], lut, lane8, h0, l0);
-    kpair<KB, 4 * KT>(c[2 * mt + 1], lut, lane8, h1, l1);
-    kpair<KB, 4 * KT + 2>(c[2 * mt], lut, lane8, h2, l2);
-    kpair<KB, 4 * KT + 2>(c[2 * mt + 1], lut, lane8, h3, l3);
+    kpair<KB, 4 * KT>(c[2 * mt], lut, lane8, h0, l0, err);
+    kpair<KB, 4 * KT>(c[2 * mt + 1], lut, lane8, h1, l1, err);
+    kpair<KB, 4 * KT + 2>(c[2 * mt], lut, lane8, h2, l2, err);
+    kpair<KB, 4 * KT + 2>(c[2 * mt + 1], lut, lane8, h3, l3, err);
     mma16816(hh[mt], h0, h1, h2, h3, bh[KT][0], bh[KT][1]);
     mma16816(lh[mt], l0, l1, l2, l3, bh[KT][0], bh[KT][1]);
     mma16816(hl[mt], h0, h1, h2, h3, bl[KT][0], bl[KT][1]);
@@ -332,12 +345,12 @@ __device__ __forceinline__ void score_ktile(const KCodes<KB> (&c)[4], const uint
 
 template <int KB, int KT>
 __device__ __forceinline__ void score_all(const KCodes<KB> (&c)[4], const uint32_t* lut,
-                                          uint32_t lane8,
+                                          uint32_t lane8, unsigned* err,
                                           const uint32_t (&bh)[8][2], const uint32_t (&bl)[8][2],
                                           float (&hh)[2][4], float (&lh)[2][4], float (&hl)[2][4]) {
   if constexpr (KT < 8) {
-    score_ktile<KB, KT>(c, lut, lane8, bh, bl, hh, lh, hl);
-    score_all<KB, KT + 1>(c, lut, lane8, bh, bl, hh, lh, hl);
+    score_ktile<KB, KT>(c, lut, lane8, err, bh, bl, hh, lh, hl);
+    score_all<KB, KT + 1>(c, lut, lane8, err, bh, bl, hh, lh, hl);
   }
 }
 
@@ -350,17 +363,17 @@ __device__ __forceinline__ void score_all(const KCodes<KB> (&c)[4], const uint32
 // (a2, a3) as loaded: 32 MMAs per chunk in four chains, against 48 in six.
 template <int KB, int KT>
 __device__ __forceinline__ void score_all_folded(const KCodes<KB> (&c)[4], const uint32_t* lut,
-                                                 uint32_t lane8, const uint32_t (&bq)[8][2],
-                                                 float (&acc)[4][4]) {
+                                                 uint32_t lane8, unsigned* err,
+                                                 const uint32_t (&bq)[8][2], float (&acc)[4][4]) {
   if constexpr (KT < 8) {
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       uint32_t h0, l0, h2, l2;
-      kpair<KB, 4 * KT>(c[u], lut, lane8, h0, l0);
-      kpair<KB, 4 * KT + 2>(c[u], lut, lane8, h2, l2);
+      kpair<KB, 4 * KT>(c[u], lut, lane8, h0, l0, err);
+      kpair<KB, 4 * KT + 2>(c[u], lut, lane8, h2, l2, err);
       mma16816(acc[u], h0, l0, h2, l2, bq[KT][0], bq[KT][1]);
     }
-    score_all_folded<KB, KT + 1>(c, lut, lane8, bq, acc);
+    score_all_folded<KB, KT + 1>(c, lut, lane8, err, bq, acc);
   }
 }
 
@@ -488,7 +501,7 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
   // before the copy of a chunk that reaches row t_end - step_new of their
   // range (see issue; t_end <= nq, so that covers those rows).
   if (a.step_new == 0 || window_split) asm volatile("griddepcontrol.wait;" ::: "memory");
-  int T = a.seq_lens[b] + a.step_new;
+  int T = *bchk(a.seq_lens + b, a.seq_lens, (size_t)a.B * 4, a.err) + a.step_new;
   // a length outside the plan's range would read past this pair's plane rows
   // or ring: flag it and decode the sequence as empty
   if (T < 0 || T > a.max_seq_len) {
@@ -529,9 +542,11 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
     float* vn_ = (float*)(wreg + L.vn + slot * 128);
     if (!bulk_norms) {                     // warp-uniform
       if (lane < nv) {
-        kn_[lane] = knp[c0 + lane];
-        vn_[lane] = vnp[c0 + lane];
-        if constexpr (HAS_RES) ((float*)(wreg + L.rn + slot * 128))[lane] = krp[c0 + lane];
+        *bchk(kn_ + lane, kn_, 128, a.err) = *bchk(knp + c0 + lane, knp, (size_t)a.kcap * 4, a.err);
+        *bchk(vn_ + lane, vn_, 128, a.err) = *bchk(vnp + c0 + lane, vnp, (size_t)a.vcap * 4, a.err);
+        if constexpr (HAS_RES)
+          *bchk((float*)(wreg + L.rn + slot * 128) + lane, wreg + L.rn + slot * 128, 128, a.err) =
+              *bchk(krp + c0 + lane, krp, (size_t)a.kcap * 4, a.err);
       }
       __syncwarp();
     }
@@ -541,15 +556,28 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
       // a.extra_tx is a test hook: bytes that never arrive, so the wait on
       // this chunk can only end by running out of polls
       mbar_arrive_expect_tx(bar + slot, bytes + a.extra_tx);
-      bulk_g2s(kb_, kc + (long long)c0 * KROW, nv * KROW, bar + slot);
-      bulk_g2s(vb_, vc + (long long)c0 * VROW, nv * VROW, bar + slot);
+      // a copy whose source leaves this pair's plane rows, or whose
+      // destination leaves the slot, is dropped (bounds-checked build)
+      auto copy = [&](void* dst, const void* dbase, size_t dbytes, const void* src,
+                      const void* sbase, size_t sbytes, uint32_t n) {
+        if (bchk_range(dst, n, dbase, dbytes, a.err) && bchk_range(src, n, sbase, sbytes, a.err))
+          bulk_g2s(dst, src, n, bar + slot);
+        else
+          mbar_complete_tx(bar + slot, n);
+      };
+      copy(kb_, kb_, 32 * KROW, kc + (long long)c0 * KROW, kc, (size_t)a.kcap * KROW, nv * KROW);
+      copy(vb_, vb_, 32 * VROW, vc + (long long)c0 * VROW, vc, (size_t)a.vcap * VROW, nv * VROW);
       if (bulk_norms) {
-        bulk_g2s(kn_, knp + c0, n4 * 4, bar + slot);
-        bulk_g2s(vn_, vnp + c0, n4 * 4, bar + slot);
+        copy(kn_, kn_, 128, knp + c0, knp, (size_t)a.kcap * 4, n4 * 4);
+        copy(vn_, vn_, 128, vnp + c0, vnp, (size_t)a.vcap * 4, n4 * 4);
       }
       if constexpr (HAS_RES) {
-        bulk_g2s(wreg + L.sbuf + slot * 512, ksp + (long long)c0 * 16, nv * 16, bar + slot);
-        if (bulk_norms) bulk_g2s(wreg + L.rn + slot * 128, krp + c0, n4 * 4, bar + slot);
+        uint8_t* sdst = wreg + L.sbuf + slot * 512;
+        copy(sdst, sdst, 512, ksp + (long long)c0 * 16, ksp, (size_t)a.kcap * 16, nv * 16);
+        if (bulk_norms) {
+          uint8_t* rdst = wreg + L.rn + slot * 128;
+          copy(rdst, rdst, 128, krp + c0, krp, (size_t)a.kcap * 4, n4 * 4);
+        }
       }
     }
   };
@@ -561,10 +589,12 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
     qv[j][0] = qv[j][1] = qv[j][2] = qv[j][3] = 0.f;
     if (g < G) {
       if (a.q_f32) {
-        const float4 v = __ldg((const float4*)((const float*)a.q + qbase + g * kD2) + lane);
+        const float4 v = __ldg(bchk((const float4*)((const float*)a.q + qbase + g * kD2) + lane,
+                                    a.q, (size_t)a.B * a.Hq * kD2 * 4, a.err));
         qv[j][0] = v.x; qv[j][1] = v.y; qv[j][2] = v.z; qv[j][3] = v.w;
       } else {
-        const uint2 v = __ldg((const uint2*)((const uint16_t*)a.q + qbase + g * kD2) + lane);
+        const uint2 v = __ldg(bchk((const uint2*)((const uint16_t*)a.q + qbase + g * kD2) + lane,
+                                   a.q, (size_t)a.B * a.Hq * kD2 * 2, a.err));
         qv[j][0] = bf16lo(v.x); qv[j][1] = bf16hi(v.x); qv[j][2] = bf16lo(v.y); qv[j][3] = bf16hi(v.y);
       }
     }
@@ -599,7 +629,9 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
         hilo2(cks[i & msk] * kCScale, cks[i >> KB] * kCScale, hp, lp);
         uint2* row = (uint2*)(smem + L.lutk4) + i * 32;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) row[(lane + j) & 15] = make_uint2(hp, lp);
+        for (int j = 0; j < 16; ++j)
+          *bchk(row + ((lane + j) & 15), smem + L.lutk4, L.warps - L.lutk4, a.err) =
+              make_uint2(hp, lp);
       }
     } else {
       lutk[i] = hilo(cks[i] * kCScale);
@@ -613,7 +645,8 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
       const uint2 ve = make_uint2(pe(i & 15), pe(i >> 4));
       uint2* row = (uint2*)(smem + L.lutk4) + i * 32 + 16;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) row[(lane + j) & 15] = ve;
+      for (int j = 0; j < 16; ++j)
+        *bchk(row + ((lane + j) & 15), smem + L.lutk4, L.warps - L.lutk4, a.err) = ve;
     }
     uint32_t e;
     if constexpr (VB == 2 || VB == 3) {
@@ -637,7 +670,7 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const float v = qv[j][c] * a.qscale;
-        qo[(4 * lane + c) * G + g] = v;
+        *bchk(qo + (4 * lane + c) * G + g, qo, kD2 * G * 4, a.err) = v;
         x[c] = v * sgs[c];
       }
       const float u0 = x[0] + x[1], u1 = x[0] - x[1], u2 = x[2] + x[3], u3 = x[2] - x[3];
@@ -654,7 +687,7 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const float v = x[c] * 0.08838834764831845f;   // 1/sqrt(128)
-        qr[(4 * lane + c) * G + g] = v;
+        *bchk(qr + (4 * lane + c) * G + g, qr, kD2 * G * 4, a.err) = v;
         qmax = fmaxf(qmax, fabsf(v));
       }
     }
@@ -681,7 +714,8 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
       uint32_t hp = 0u, lp = 0u;
       if (qhead < G) {
         const int c = 32 * tig + 4 * kt + 2 * p;
-        hilo2(qr[c * G + qhead] * qsp, qr[(c + 1) * G + qhead] * qsp, hp, lp);
+        hilo2(*bchk(qr + c * G + qhead, qr, kD2 * G * 4, a.err) * qsp,
+              *bchk(qr + (c + 1) * G + qhead, qr, kD2 * G * 4, a.err) * qsp, hp, lp);
       }
       bh[kt][p] = FOLD && (mg & 1) ? lp : hp;
       bl[kt][p] = lp;
@@ -710,7 +744,7 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
       }
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        sq[g * kQjlM + j] = acc[g];
+        *bchk(sq + g * kQjlM + j, sq, G * kQjlM * 4, a.err) = acc[g];
         smax = fmaxf(smax, fabsf(acc[g]));
       }
     }
@@ -731,13 +765,15 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
       uint4 o = make_uint4(0u, 0u, 0u, 0u);
       if (g < G) {
         const int c = 32 * tg + 4 * kt;
-        hilo2(sq[g * kQjlM + c] * qsq, sq[g * kQjlM + c + 1] * qsq, o.x, o.z);
-        hilo2(sq[g * kQjlM + c + 2] * qsq, sq[g * kQjlM + c + 3] * qsq, o.y, o.w);
+        const float4 s4q = *bchk((const float4*)(sq + g * kQjlM + c), sq, G * kQjlM * 4, a.err);
+        hilo2(s4q.x * qsq, s4q.y * qsq, o.x, o.z);
+        hilo2(s4q.z * qsq, s4q.w * qsq, o.y, o.w);
       }
       if constexpr (FOLD)
-        ((uint2*)(smem + L.qjlb))[e] = ((ln >> 2) & 1) ? make_uint2(o.z, o.w) : make_uint2(o.x, o.y);
+        *bchk((uint2*)(smem + L.qjlb) + e, smem + L.qjlb, 32 * 8 * 16, a.err) =
+            ((ln >> 2) & 1) ? make_uint2(o.z, o.w) : make_uint2(o.x, o.y);
       else
-        ((uint4*)(smem + L.qjlb))[e] = o;
+        *bchk((uint4*)(smem + L.qjlb) + e, smem + L.qjlb, 32 * 8 * 16, a.err) = o;
     }
   }
   __syncthreads();
@@ -746,6 +782,11 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
   float* cm = (float*)(smem + L.comb);   // [warps][G]      (merge area, after the loop)
   float* cl = cm + kDWarps * G;          // [warps][G]
   float* co = cl + kDWarps * G;          // [warps][G][128]
+  constexpr size_t kCombBytes = (size_t)kDWarps * G * (2 + kD2) * 4;
+  // bounds-checked accessors of the merge area (plain references otherwise)
+  auto CM = [&](int i) -> float& { return *bchk(cm + i, cm, kCombBytes, a.err); };
+  auto CL = [&](int i) -> float& { return *bchk(cl + i, cm, kCombBytes, a.err); };
+  auto CO = [&](long long i) -> float& { return *bchk(co + i, cm, kCombBytes, a.err); };
 
   if (!window_split) {
     // online-softmax state: folded, of head tig (mfold, lfold); unfolded, of heads
@@ -753,6 +794,8 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
     float mfold = kNegBig, lfold = 0.f;
     float m0 = kNegBig, m1 = kNegBig, l0 = 0.f, l1 = 0.f;
     float inv_d = 1.f;       // d holds the V sum divided by inv_d (a power of two)
+    float scl = 1.f;         // folded path: fp16 weight scale (a power of two), inv_d = 1 / scl
+    float vcap = 0.f;        // folded path: value-norm bound of the current weight scale
     float d[8][4];           // fp32 V-sum accumulators (MMA layout)
 #pragma unroll
     for (int k = 0; k < 8; ++k)
@@ -790,8 +833,32 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
       const uint8_t* kb_ = wreg + L.kbuf + slot * 32 * KROW;
       const float* kn_ = (const float*)(wreg + L.kn + slot * 128);
       const float* vn_ = (const float*)(wreg + L.vn + slot * 128);
-      const float vmax = warp_max(lane < nv ? vn_[lane] : 0.f);
       if constexpr (FOLD) {
+        // value norms of this lane's tokens 8u + mg (u = 0..3; 0 past the end)
+        float vn4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          vn4[u] = 8 * u + mg < nv ? *bchk(vn_ + 8 * u + mg, vn_, 128, a.err) : 0.f;
+        // lazy weight scale: raised only when a norm exceeds the bound vcap
+        float rs = 1.f;
+        {
+          const float nmax = fmaxf(fmaxf(vn4[0], vn4[1]), fmaxf(vn4[2], vn4[3]));
+          if (__any_sync(0xffffffffu, nmax > vcap)) {
+            const float wm = warp_max(nmax);
+            // wm in [2^e, 2^(e+1)): vcap = 2^(e+1) and scl = 2^(6-e), so that
+            // every weight p ||v|| scl (p <= 2^kLazyMax) stays below 2^15; the
+            // exponent is clamped to [2^-60, 2^64] so that the accumulator, kept
+            // in the current scale, stays finite
+            const int be = (int)((__float_as_uint(wm) >> 23) & 0xFFu);
+            int sexp = 133 - be;
+            sexp = sexp > 64 ? 64 : sexp < -60 ? -60 : sexp;
+            vcap = __int_as_float(((be < 253 ? be : 253) + 1) << 23);
+            const float scl_new = __int_as_float((127 + sexp) << 23);
+            rs = scl_new * inv_d;                    // a power of two, exact
+            scl = scl_new;
+            inv_d = __uint_as_float(0x7F000000u - __float_as_uint(scl));   // 1 / scl
+          }
+        }
         // ---- scores on the tensor cores: MMA column 2h is head h's query hi
         // part and column 2h + 1 its lo part, so lane (mg, tig) holds both
         // parts of head tig for the tokens of its rows.  m-tile u holds token
@@ -802,16 +869,17 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
         {
           KCodes<KB> c[4];
 #pragma unroll
-          for (int r = 0; r < 4; ++r) load_kcodes<KB>(kb_ + (8 * r + mg) * KROW, tig, c[r]);
+          for (int r = 0; r < 4; ++r) load_kcodes<KB>(kb_, 8 * r + mg, tig, c[r], a.err);
           float acc[4][4];
 #pragma unroll
           for (int u = 0; u < 4; ++u)
 #pragma unroll
             for (int j = 0; j < 4; ++j) acc[u][j] = 0.f;
-          score_all_folded<KB, 0>(c, klut, lane8, bh, acc);
+          score_all_folded<KB, 0>(c, klut, lane8, a.err, bh, acc);
 #pragma unroll
           for (int u = 0; u < 4; ++u)
-            s4[u] = (acc[u][0] + acc[u][1] + acc[u][2]) * (kn_[8 * u + mg] * kscale);
+            s4[u] = (acc[u][0] + acc[u][1] + acc[u][2]) *
+                    (*bchk(kn_ + 8 * u + mg, kn_, 128, a.err) * kscale);
         }
         if constexpr (HAS_RES) {
           // the residual MMA's rows are two tokens (16mt + mg, 16mt + mg + 8),
@@ -821,13 +889,16 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
 #pragma unroll
           for (int mt = 0; mt < 2; ++mt) {
             const int ta = 16 * mt + mg, tb = ta + 8;
-            const uint32_t sa = *(const uint32_t*)(sb_ + ta * 16 + 4 * tig);
-            const uint32_t sbits = *(const uint32_t*)(sb_ + tb * 16 + 4 * tig);
+            const uint32_t sa = *bchk((const uint32_t*)(sb_ + ta * 16 + 4 * tig), sb_, 512, a.err);
+            const uint32_t sbits =
+                *bchk((const uint32_t*)(sb_ + tb * 16 + 4 * tig), sb_, 512, a.err);
             float qa[4] = {0.f, 0.f, 0.f, 0.f}, ql[4] = {0.f, 0.f, 0.f, 0.f};
             if constexpr (QJL) qjl_scores<true>(sa, sbits, slut, qjlb, lane, qa, ql);
             else sign_scores<true>(sa, sbits, slut, bh, bl, qa, ql);
-            s4[2 * mt] = fmaf(qa[0] + qa[1], rn_[ta] * res_scale, s4[2 * mt]);
-            s4[2 * mt + 1] = fmaf(qa[2] + qa[3], rn_[tb] * res_scale, s4[2 * mt + 1]);
+            s4[2 * mt] =
+                fmaf(qa[0] + qa[1], *bchk(rn_ + ta, rn_, 128, a.err) * res_scale, s4[2 * mt]);
+            s4[2 * mt + 1] = fmaf(qa[2] + qa[3], *bchk(rn_ + tb, rn_, 128, a.err) * res_scale,
+                                  s4[2 * mt + 1]);
           }
         }
         // tokens past the end of a partial chunk get no weight; lanes of
@@ -837,45 +908,44 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
           for (int u = 0; u < 4; ++u)
             if (8 * u + mg >= nv) s4[u] = kNegBig;
         }
-        // ---- online softmax of head tig (log2 domain): max over the lane's 4
-        // tokens, then over the 8 lanes of the head
-        float x = fmaxf(fmaxf(s4[0], s4[1]), fmaxf(s4[2], s4[3]));
+        // ---- online softmax of head tig (log2 domain) with a lazy maximum:
+        // mfold (uniform over the head's 8 lanes) is raised only when a score
+        // exceeds it by more than kLazyMax (a warp vote), so the weights
+        // p = 2^(s - mfold) are at most 2^kLazyMax and most chunks need no
+        // reduction over lanes and no rescale
+        const float smax = fmaxf(fmaxf(s4[0], s4[1]), fmaxf(s4[2], s4[3]));
+        float al = 1.f, al0 = 1.f, al1 = 1.f;
+        if (__any_sync(0xffffffffu, smax > mfold + kLazyMax)) {
+          float x = smax;
 #pragma unroll
-        for (int o = 4; o < 32; o <<= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-        const float mn = fmaxf(mfold, x);
-        const float al = ex2(mfold - mn);
-        mfold = mn;
-        int sexp = 141 - (int)((__float_as_uint(vmax) >> 23) & 0xFFu);   // 14 - floor(log2 vmax)
-        sexp = sexp > 64 ? 64 : sexp < -60 ? -60 : sexp;
-        const float scl = __int_as_float((127 + sexp) << 23);
+          for (int o = 4; o < 32; o <<= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+          const float mn = fmaxf(mfold, x);
+          al = ex2(mfold - mn);
+          mfold = mn;
+          // accumulator columns 2tig, 2tig + 1 are heads 2tig, 2tig + 1, whose
+          // factors the score lanes of those heads hold
+          al0 = __shfl_sync(0xffffffffu, al, 2 * tig);
+          al1 = __shfl_sync(0xffffffffu, al, 2 * tig + 1);
+        }
         float p[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) p[u] = ex2(s4[u] - mn);
+        for (int u = 0; u < 4; ++u) p[u] = ex2(s4[u] - mfold);
         lfold = fmaf(lfold, al, (p[0] + p[1]) + (p[2] + p[3]));
         bool skip_v = false;
         if constexpr (SPARSE)
           skip_v = warp_max(tig < G ? fmaxf(fmaxf(p[0], p[1]), fmaxf(p[2], p[3])) : 0.f) <
                    a.sparse_thr;
-        // fp16 weights p ||v|| scaled into range by a power of two (see
-        // below); pairs (tokens 8u + mg, 8u + 8 + mg) for u = 0, 2
+        // fp16 weights p ||v|| scl; pairs (tokens 8u + mg, 8u + 8 + mg) for u = 0, 2
         uint32_t pk[2];
 #pragma unroll
         for (int kt = 0; kt < 2; ++kt) {
-          const int ta = 16 * kt + mg, tb = ta + 8;
-          const float va = ta < nv ? vn_[ta] * scl : 0.f, vb = tb < nv ? vn_[tb] * scl : 0.f;
-          const __half2 h = __floats2half2_rn(p[2 * kt] * va, p[2 * kt + 1] * vb);
+          const __half2 h = __floats2half2_rn(p[2 * kt] * (vn4[2 * kt] * scl),
+                                              p[2 * kt + 1] * (vn4[2 * kt + 1] * scl));
           pk[kt] = *(const uint32_t*)&h;
         }
-        // ---- rotated-domain V sum on the tensor cores: accumulator columns
-        // 2tig, 2tig + 1 are heads 2tig, 2tig + 1, whose rescale factors the
-        // score lanes of those heads hold
-        const float al0 = __shfl_sync(0xffffffffu, al, 2 * tig);
-        const float al1 = __shfl_sync(0xffffffffu, al, 2 * tig + 1);
-        const float rs = skip_v ? 1.f : scl * inv_d;     // a power of two, exact
-        if (!skip_v) inv_d = __uint_as_float(0x7F000000u - __float_as_uint(scl));   // 1 / scl
+        // ---- rotated-domain V sum on the tensor cores: bring the accumulator
+        // to the current maximum and scale first (rarely needed)
         const float2 pre = make_float2(al0 * rs, al1 * rs);
-        // once the running maxima and the weight scale settle, most chunks
-        // leave the accumulator's scale unchanged: skip the multiply then
         if (__any_sync(0xffffffffu, pre.x != 1.f || pre.y != 1.f)) {
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
@@ -894,7 +964,7 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
           uint32_t b0 = __shfl_sync(0xffffffffu, pk[kt], 4 * tig + mg);
           uint32_t b1 = __shfl_sync(0xffffffffu, pk[kt], 4 * tig + mg + 16);
           if (mg >= G) b0 = b1 = 0u;
-          if (!skip_v) vmma_ktile<VB>(vb_, lutv, ptab, laneV, kt, mg, tig, b0, b1, d);
+          if (!skip_v) vmma_ktile<VB>(vb_, lutv, ptab, laneV, kt, mg, tig, b0, b1, d, a.err);
         }
       } else {
       // ---- scores on the tensor cores: sc[mt][0,1] token 16mt+mg, sc[mt][2,3] token +8;
@@ -903,56 +973,37 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
       {
         KCodes<KB> c[4];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) load_kcodes<KB>(kb_ + (8 * r + mg) * KROW, tig, c[r]);
-        // FOLD: acc[u] = token 8u + mg, [0,1] K hi rows, [2,3] K lo rows
-        float hh[2][4], lh[2][4], hl[2][4], acc[4][4];
-        if constexpr (FOLD) {
+        for (int r = 0; r < 4; ++r) load_kcodes<KB>(kb_, 8 * r + mg, tig, c[r], a.err);
+        float hh[2][4], lh[2][4], hl[2][4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
+        for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) acc[u][j] = 0.f;
-          score_all_folded<KB, 0>(c, klut, lane8, bh, acc);
-        } else {
-#pragma unroll
-          for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) hh[mt][j] = lh[mt][j] = hl[mt][j] = 0.f;
-          score_all<KB, 0>(c, klut, lane8, bh, bl, hh, lh, hl);
-        }
+          for (int j = 0; j < 4; ++j) hh[mt][j] = lh[mt][j] = hl[mt][j] = 0.f;
+        score_all<KB, 0>(c, klut, lane8, a.err, bh, bl, hh, lh, hl);
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
           const int ta = 16 * mt + mg, tb = ta + 8;
-          const float na = kn_[ta] * kscale, nb = kn_[tb] * kscale;
-          if constexpr (FOLD) {
-            // this lane's part (hi for tig < 2, lo for tig >= 2) of heads
-            // 2(tig%2), 2(tig%2)+1; lane tig ^ 2 holds the other part
-            sc[mt][0] = (acc[2 * mt][0] + acc[2 * mt][2]) * na;
-            sc[mt][1] = (acc[2 * mt][1] + acc[2 * mt][3]) * na;
-            sc[mt][2] = (acc[2 * mt + 1][0] + acc[2 * mt + 1][2]) * nb;
-            sc[mt][3] = (acc[2 * mt + 1][1] + acc[2 * mt + 1][3]) * nb;
-          } else {
-            sc[mt][0] = (hh[mt][0] + (lh[mt][0] + hl[mt][0])) * na;
-            sc[mt][1] = (hh[mt][1] + (lh[mt][1] + hl[mt][1])) * na;
-            sc[mt][2] = (hh[mt][2] + (lh[mt][2] + hl[mt][2])) * nb;
-            sc[mt][3] = (hh[mt][3] + (lh[mt][3] + hl[mt][3])) * nb;
-          }
+          const float na = *bchk(kn_ + ta, kn_, 128, a.err) * kscale;
+          const float nb = *bchk(kn_ + tb, kn_, 128, a.err) * kscale;
+          sc[mt][0] = (hh[mt][0] + (lh[mt][0] + hl[mt][0])) * na;
+          sc[mt][1] = (hh[mt][1] + (lh[mt][1] + hl[mt][1])) * na;
+          sc[mt][2] = (hh[mt][2] + (lh[mt][2] + hl[mt][2])) * nb;
+          sc[mt][3] = (hh[mt][3] + (lh[mt][3] + hl[mt][3])) * nb;
           if constexpr (HAS_RES) {
             const uint8_t* sb_ = wreg + L.sbuf + slot * 512;
             const float* rn_ = (const float*)(wreg + L.rn + slot * 128);
-            const uint32_t sa = *(const uint32_t*)(sb_ + ta * 16 + 4 * tig);
-            const uint32_t sbits = *(const uint32_t*)(sb_ + tb * 16 + 4 * tig);
+            const uint32_t sa = *bchk((const uint32_t*)(sb_ + ta * 16 + 4 * tig), sb_, 512, a.err);
+            const uint32_t sbits =
+                *bchk((const uint32_t*)(sb_ + tb * 16 + 4 * tig), sb_, 512, a.err);
             float qa[4] = {0.f, 0.f, 0.f, 0.f}, ql[4] = {0.f, 0.f, 0.f, 0.f};
-            if constexpr (QJL) qjl_scores<FOLD>(sa, sbits, slut, qjlb, lane, qa, ql);
-            else sign_scores<FOLD>(sa, sbits, slut, bh, bl, qa, ql);
-            const float ga = rn_[ta] * res_scale, gb = rn_[tb] * res_scale;
+            if constexpr (QJL) qjl_scores<false>(sa, sbits, slut, qjlb, lane, qa, ql);
+            else sign_scores<false>(sa, sbits, slut, bh, bl, qa, ql);
+            const float ga = *bchk(rn_ + ta, rn_, 128, a.err) * res_scale;
+            const float gb = *bchk(rn_ + tb, rn_, 128, a.err) * res_scale;
             sc[mt][0] = fmaf(qa[0] + ql[0], ga, sc[mt][0]);
             sc[mt][1] = fmaf(qa[1] + ql[1], ga, sc[mt][1]);
             sc[mt][2] = fmaf(qa[2] + ql[2], gb, sc[mt][2]);
             sc[mt][3] = fmaf(qa[3] + ql[3], gb, sc[mt][3]);
-          }
-          if constexpr (FOLD) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) sc[mt][j] += __shfl_xor_sync(0xffffffffu, sc[mt][j], 2);
           }
           // tokens past the end of a partial chunk get no weight; columns of
           // absent heads are never written or read back, so need no mask
@@ -962,7 +1013,10 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
           }
         }
       }
-      // ---- online softmax (log2 domain) per head column; reduce over mg
+      // ---- online softmax (log2 domain) per head column; reduce over mg.
+      // (The lazy maxima of the folded path measured slower here: the
+      // branches split the chunk's body, which the wider unfolded path needs
+      // whole for its schedule.)
       float x0 = fmaxf(fmaxf(sc[0][0], sc[0][2]), fmaxf(sc[1][0], sc[1][2]));
       float x1 = fmaxf(fmaxf(sc[0][1], sc[0][3]), fmaxf(sc[1][1], sc[1][3]));
 #pragma unroll
@@ -978,6 +1032,7 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
       // p ||v|| is at most the chunk's largest value norm (p <= 1), which maps
       // below 2^15; the exponent is clamped to [2^-60, 2^64] so that the
       // accumulator, kept in the latest chunk's scale, stays finite
+      const float vmax = warp_max(lane < nv ? *bchk(vn_ + lane, vn_, 128, a.err) : 0.f);
       int sexp = 141 - (int)((__float_as_uint(vmax) >> 23) & 0xFFu);   // 14 - floor(log2 vmax)
       sexp = sexp > 64 ? 64 : sexp < -60 ? -60 : sexp;
       const float scl = __int_as_float((127 + sexp) << 23);
@@ -986,7 +1041,8 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
         const int ta = 16 * mt + mg, tb = ta + 8;
-        const float va = ta < nv ? vn_[ta] * scl : 0.f, vb = tb < nv ? vn_[tb] * scl : 0.f;
+        const float va = ta < nv ? *bchk(vn_ + ta, vn_, 128, a.err) * scl : 0.f;
+        const float vb = tb < nv ? *bchk(vn_ + tb, vn_, 128, a.err) * scl : 0.f;
         const float p0 = ex2(sc[mt][0] - mn0), p1 = ex2(sc[mt][1] - mn1);
         const float p2 = ex2(sc[mt][2] - mn0), p3 = ex2(sc[mt][3] - mn1);
         ps0 += p0 + p2;
@@ -1009,11 +1065,13 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
         // tokens 16mt + mg and 16mt + mg + 8: weight pair 8mt + mg
         if (h0ok && !skip_v) {
           const __half2 h = __floats2half2_rn(w[mt][0], w[mt][2]);
-          ws32[(2 * tig) * kWsStride + 8 * mt + mg] = *(const uint32_t*)&h;
+          *bchk(ws32 + (2 * tig) * kWsStride + 8 * mt + mg, ws32, 8 * kWsStride * 4, a.err) =
+              *(const uint32_t*)&h;
         }
         if (h1ok && !skip_v) {
           const __half2 h = __floats2half2_rn(w[mt][1], w[mt][3]);
-          ws32[(2 * tig + 1) * kWsStride + 8 * mt + mg] = *(const uint32_t*)&h;
+          *bchk(ws32 + (2 * tig + 1) * kWsStride + 8 * mt + mg, ws32, 8 * kWsStride * 4, a.err) =
+              *(const uint32_t*)&h;
         }
       }
       __syncwarp();
@@ -1031,9 +1089,12 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
       const uint8_t* vb_ = wreg + L.vbuf + slot * 32 * VROW;
 #pragma unroll
       for (int kt = 0; kt < 2 && !skip_v; ++kt) {
-        const uint32_t b0 = mg < G ? ws32[mg * kWsStride + 8 * kt + tig] : 0u;
-        const uint32_t b1 = mg < G ? ws32[mg * kWsStride + 8 * kt + tig + 4] : 0u;
-        vmma_ktile<VB>(vb_, lutv, ptab, laneV, kt, mg, tig, b0, b1, d);
+        const uint32_t b0 =
+            mg < G ? *bchk(ws32 + mg * kWsStride + 8 * kt + tig, ws32, 8 * kWsStride * 4, a.err) : 0u;
+        const uint32_t b1 =
+            mg < G ? *bchk(ws32 + mg * kWsStride + 8 * kt + tig + 4, ws32, 8 * kWsStride * 4, a.err)
+                   : 0u;
+        vmma_ktile<VB>(vb_, lutv, ptab, laneV, kt, mg, tig, b0, b1, d, a.err);
       }
       __syncwarp();
       }
@@ -1073,17 +1134,17 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
     __syncthreads();                     // every warp is done with its ring buffers
     if constexpr (FOLD) {
       if (mg == 0 && tig < G) {
-        cm[warp * G + tig] = mfold;
-        cl[warp * G + tig] = lfold;
+        CM(warp * G + tig) = mfold;
+        CL(warp * G + tig) = lfold;
       }
     } else if (mg == 0) {
       if (h0ok) {
-        cm[warp * G + 2 * tig] = m0;
-        cl[warp * G + 2 * tig] = l0;
+        CM(warp * G + 2 * tig) = m0;
+        CL(warp * G + 2 * tig) = l0;
       }
       if (h1ok) {
-        cm[warp * G + 2 * tig + 1] = m1;
-        cl[warp * G + 2 * tig + 1] = l1;
+        CM(warp * G + 2 * tig + 1) = m1;
+        CL(warp * G + 2 * tig + 1) = l1;
       }
     }
     // thread (mg, tig): m-tile k rows mg, mg + 8 -> coordinates vrow_coord;
@@ -1092,14 +1153,14 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
     for (int k = 0; k < 8; ++k) {
       const int c0 = vrow_coord<VB>(mg, k, 0), c1 = vrow_coord<VB>(mg, k, 1);
       if (h0ok) {
-        float* dst = co + (warp * G + 2 * tig) * kD2;
-        dst[c0] = d[k][0];
-        dst[c1] = d[k][2];
+        const long long r = (long long)(warp * G + 2 * tig) * kD2;
+        CO(r + c0) = d[k][0];
+        CO(r + c1) = d[k][2];
       }
       if (h1ok) {
-        float* dst = co + (warp * G + 2 * tig + 1) * kD2;
-        dst[c0] = d[k][1];
-        dst[c1] = d[k][3];
+        const long long r = (long long)(warp * G + 2 * tig + 1) * kD2;
+        CO(r + c0) = d[k][1];
+        CO(r + c1) = d[k][3];
       }
     }
   } else {
@@ -1126,8 +1187,11 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
         const int k = k0 + u * kDWarps;
         if (k < kw1) {
           const long long slotrow = (base + (tw0 + k) % W) * kD2;
-          kw[u] = *(const uint2*)(a.kwin + slotrow + 4 * lane);
-          vw[u] = *(const uint2*)(a.vwin + slotrow + 4 * lane);
+          // this pair's W ring rows
+          kw[u] = *bchk((const uint2*)(a.kwin + slotrow + 4 * lane), a.kwin + base * kD2,
+                        (size_t)W * kD2 * 2, a.err);
+          vw[u] = *bchk((const uint2*)(a.vwin + slotrow + 4 * lane), a.vwin + base * kD2,
+                        (size_t)W * kD2 * 2, a.err);
         }
       }
 #pragma unroll
@@ -1144,7 +1208,8 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
           const bool vis = tpos <= T - a.n_q + g % a.n_q;
           float part = 0.f;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) part = fmaf(qo[(4 * lane + j) * G + g], kx[j], part);
+          for (int j = 0; j < 4; ++j)
+            part = fmaf(*bchk(qo + (4 * lane + j) * G + g, qo, kD2 * G * 4, a.err), kx[j], part);
           const float s = warp_sum(part);
           const float mnew = vis ? fmaxf(m[g], s) : m[g];
           const float al = vis ? ex2(m[g] - mnew) : 1.f;
@@ -1160,10 +1225,10 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       if (lane == 0) {
-        cm[warp * G + g] = m[g];
-        cl[warp * G + g] = l[g];
+        CM(warp * G + g) = m[g];
+        CL(warp * G + g) = l[g];
       }
-      *(float4*)(co + (warp * G + g) * kD2 + 4 * lane) =
+      *bchk((float4*)(co + (warp * G + g) * kD2 + 4 * lane), cm, kCombBytes, a.err) =
           make_float4(ow[g][0], ow[g][1], ow[g][2], ow[g][3]);
     }
   }
@@ -1173,23 +1238,25 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
   const long long unit = (long long)b * Hkv + kvh;
   const int stride = kPartialStride;
   float* part = a.partials + (unit * a.n_splits + split) * G * stride;
+  const size_t part_bytes = (size_t)a.B * Hkv * a.n_splits * G * stride * 4;
+  auto PART = [&](int i) -> float& { return *bchk(part + i, a.partials, part_bytes, a.err); };
   // thread e of the G x 128 outputs: head e / 128, coordinate e % 128
   for (int e = tid; e < G * kD2; e += kDT) {
     const int g = e / kD2, c = e % kD2;
     float M = kNegBig;
 #pragma unroll
-    for (int w = 0; w < kDWarps; ++w) M = fmaxf(M, cm[w * G + g]);
+    for (int w = 0; w < kDWarps; ++w) M = fmaxf(M, CM(w * G + g));
     float O = 0.f, Lsum = 0.f;
 #pragma unroll
     for (int w = 0; w < kDWarps; ++w) {
-      const float f = ex2(cm[w * G + g] - M);
-      O = fmaf(co[(w * G + g) * kD2 + c], f, O);
-      Lsum = fmaf(cl[w * G + g], f, Lsum);
+      const float f = ex2(CM(w * G + g) - M);
+      O = fmaf(CO((long long)(w * G + g) * kD2 + c), f, O);
+      Lsum = fmaf(CL(w * G + g), f, Lsum);
     }
-    part[g * stride + 4 + c] = O;
+    PART(g * stride + 4 + c) = O;
     if (c == 0) {
-      part[g * stride] = M;
-      part[g * stride + 1] = Lsum;
+      PART(g * stride) = M;
+      PART(g * stride + 1) = Lsum;
     }
   }
   // the CTA's partial writes are ordered before the counter update by the
@@ -1200,7 +1267,7 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
     unsigned prev;
     asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;"
                  : "=r"(prev)
-                 : "l"(a.counters + unit)
+                 : "l"(bchk(a.counters + unit, a.counters, (size_t)a.B * Hkv * 4, a.err))
                  : "memory");
     *is_last = prev == (unsigned)(a.n_splits - 1);
   }
@@ -1219,14 +1286,16 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
     float4 rot = make_float4(0.f, 0.f, 0.f, 0.f), win = rot;
     for (int s0 = 0; s0 < a.n_splits; s0 += 32) {
       const int sl = s0 + lane;
-      const float* pl = base + (sl * G + g) * stride;
+      const float* pl = bchk(base + (sl < a.n_splits ? sl : 0) * G * stride + g * stride,
+                             a.partials, part_bytes, a.err);
       const float ml = sl < a.n_splits ? __ldcg(pl) : kNegBig;
       const float ll = sl < a.n_splits ? __ldcg(pl + 1) : 0.f;
       float4 v[32];
 #pragma unroll
       for (int u = 0; u < 32; ++u)
         v[u] = s0 + u < a.n_splits
-                   ? __ldcg((const float4*)(base + ((s0 + u) * G + g) * stride + 4) + lane)
+                   ? __ldcg(bchk((const float4*)(base + ((s0 + u) * G + g) * stride + 4) + lane,
+                                 a.partials, part_bytes, a.err))
                    : make_float4(0.f, 0.f, 0.f, 0.f);
       const float Mn = fmaxf(M, warp_max(ml));
       const float r = ex2(M - Mn);
@@ -1270,9 +1339,11 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
     const float inv = Lsum > 0.f ? 1.0f / Lsum : 0.f;
     const float4 res = make_float4((x[0] * r * sv4.x + win.x) * inv, (x[1] * r * sv4.y + win.y) * inv,
                                    (x[2] * r * sv4.z + win.z) * inv, (x[3] * r * sv4.w + win.w) * inv);
-    *(float4*)(a.out + ((long long)b * a.Hq + (long long)kvh * G + g) * kD2 + 4 * lane) = res;
+    *bchk((float4*)(a.out + ((long long)b * a.Hq + (long long)kvh * G + g) * kD2 + 4 * lane), a.out,
+          (size_t)a.B * a.Hq * kD2 * 4, a.err) = res;
   }
-  if (tid == 0) a.counters[unit] = 0u;   // leave the counter ready for the next call
+  if (tid == 0)   // leave the counter ready for the next call
+    *bchk(a.counters + unit, a.counters, (size_t)a.B * Hkv * 4, a.err) = 0u;
 }
 
 

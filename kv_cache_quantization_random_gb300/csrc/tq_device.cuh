@@ -13,6 +13,44 @@ namespace tq {
 
 constexpr uint32_t kDefaultWaitLimit = 1u << 26;   // ~ seconds of polling
 
+// ---- bounds-checked build ------------------------------------------------------
+// Compiled with TQ_DEBUG_BOUNDS, every index a kernel computes into shared or
+// global memory is checked against the extent of the buffer it addresses: an
+// index outside it sets kErrBounds in the kernel's error word, and the access
+// goes to the buffer's first element instead (a copy is dropped and its bytes
+// are retired from its barrier), so nothing outside the buffer is touched and
+// no wait is left hanging.  The normal build compiles the checks away.
+#ifdef TQ_DEBUG_BOUNDS
+constexpr bool kBoundsChecks = true;
+#else
+constexpr bool kBoundsChecks = false;
+#endif
+
+// p, or base when [p, p + sizeof(T)) leaves [base, base + bytes)
+template <class T>
+__device__ __forceinline__ T* bchk(T* p, const void* base, size_t bytes, unsigned* err) {
+  if constexpr (kBoundsChecks) {
+    const uintptr_t q = (uintptr_t)p, b0 = (uintptr_t)base;
+    if (q < b0 || q + sizeof(T) > b0 + bytes) {
+      atomicOr(err, kErrBounds);
+      return (T*)base;
+    }
+  }
+  return p;
+}
+// whether [p, p + n) lies inside [base, base + bytes) (always, in the normal build)
+__device__ __forceinline__ bool bchk_range(const void* p, size_t n, const void* base,
+                                           size_t bytes, unsigned* err) {
+  if constexpr (kBoundsChecks) {
+    const uintptr_t q = (uintptr_t)p, b0 = (uintptr_t)base;
+    if (q < b0 || q + n > b0 + bytes) {
+      atomicOr(err, kErrBounds);
+      return false;
+    }
+  }
+  return true;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }

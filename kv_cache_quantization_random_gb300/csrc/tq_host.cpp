@@ -811,6 +811,7 @@ extern "C" tq_status tq_dequantize(const tq_config* cfg, const void* tables, int
   a.S = a.qjl ? tbl_qjl(cfg, tables, layer) : nullptr;
   a.m = cfg->qjl_m;
   a.dst = dst;
+  a.err = quant_error_ptr();
   return launch_dequantize(a, stream) == 0 ? TQ_OK : TQ_ERR_CUDA;
 }
 

@@ -210,6 +210,7 @@ struct DequantArgs {
   const uint16_t* S;
   int m;
   float* dst;
+  unsigned* err;                 // device error word (bounds-checked build)
 };
 
 struct DecodeArgs {

@@ -23,6 +23,17 @@ __host__ __device__ constexpr size_t quant_rows_bytes(bool f32) {
   return (size_t)kQRows * (f32 ? RowCfg<true>::kPitch : RowCfg<false>::kPitch);
 }
 
+// Bytes spanned by the source tensor [B][H][n][d] of a quantize (strides in
+// elements, non-negative), and by a bf16 window ring [B][H][W][d].
+__device__ __forceinline__ size_t src_extent_bytes(const QuantArgs& a) {
+  const long long e = (long long)(a.B - 1) * a.sb + (long long)(a.H - 1) * a.sh +
+                      (long long)(a.n - 1) * a.st + kD;
+  return (size_t)e * (a.src_f32 ? 4 : 2);
+}
+__device__ __forceinline__ size_t ring_bytes(int B, int H, int W) {
+  return (size_t)B * H * W * kD * 2;
+}
+
 // Resolve vector v of the launch: its plane row and, for the stager, its
 // source address.  All index arithmetic is 32-bit (a launch covers fewer than
 // 2^31 vectors, checked on the host).
@@ -55,6 +66,15 @@ __device__ __forceinline__ bool resolve_row(const QuantArgs& a, uint32_t v, cons
   if (pos < 0 || pos >= a.cap) {
     atomicOr(a.err, kErrBounds);
     return false;
+  }
+  // the source row lies inside the input tensor or the window ring
+  // (bounds-checked build; a row outside is not quantized)
+  if (kBoundsChecks) {
+    const bool from_ring = a.append && pos < (long long)a.seq_before[b];
+    const void* base = from_ring ? (const void*)a.win : a.src;
+    const size_t bytes = from_ring ? ring_bytes(a.B, a.H, a.W) : src_extent_bytes(a);
+    if (!bchk_range(*src, (size_t)kD * (a.src_f32 && !from_ring ? 4 : 2), base, bytes, a.err))
+      return false;
   }
   *dst_row = ((long long)bh) * a.cap + pos;
   return true;
@@ -167,6 +187,42 @@ __device__ __forceinline__ float load_rotate(const QuantArgs& a, const uint8_t* 
   return sqrtf(s.x + s.y);
 }
 
+// load_rotate for a bf16 row held in registers: w[k] packs coordinates 2k
+// (low half) and 2k + 1 (high half), as the row lies in memory.
+__device__ __forceinline__ float load_rotate_regs(const QuantArgs& a, const uint32_t (&w)[64],
+                                                  float2 (&p)[64]) {
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    const int i = 2 * k;
+    p[i] = make_float2(__uint_as_float(w[k] * 65536u + a.smask[i]),
+                       __uint_as_float(w[32 + k] * 65536u + a.smask[64 + i]));
+    p[i + 1] = make_float2(__uint_as_float((w[k] & 0xFFFF0000u) ^ a.smask[i + 1]),
+                           __uint_as_float((w[32 + k] & 0xFFFF0000u) ^ a.smask[64 + i + 1]));
+  }
+  float2 s0 = make_float2(0.f, 0.f), s1 = s0;
+#pragma unroll
+  for (int j = 0; j < 64; j += 2) {
+    s0 = __ffma2_rn(p[j], p[j], s0);
+    s1 = __ffma2_rn(p[j + 1], p[j + 1], s1);
+  }
+  const float2 s = __fadd2_rn(s0, s1);
+  const float2 neg1 = make_float2(-1.f, -1.f);
+#pragma unroll
+  for (int hs = 1; hs < 64; hs <<= 1) {
+#pragma unroll
+    for (int j = 0; j < 64; ++j) {
+      if ((j & hs) == 0) {
+        const float2 u = p[j], v = p[j + hs];
+        p[j] = __fadd2_rn(u, v);
+        p[j + hs] = __ffma2_rn(v, neg1, u);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 64; ++j) p[j] = make_float2(p[j].x + p[j].y, p[j].x - p[j].y);
+  return sqrtf(s.x + s.y);
+}
+
 // Search-grid table (see SearchGrid in tq_internal.h) from the boundaries in
 // shared memory: entry k = (first boundary at or above the lower edge of cells
 // k-1..k+1, number of boundaries below that edge).  Called by all threads of
@@ -221,6 +277,13 @@ __device__ __forceinline__ void search_pack_t(const QuantArgs& a, float2 (&p)[64
     } else {
       a0 = __float_as_uint(t.x) * 8u + bias;        // cell = bits(t) - bits(magic)
       a1 = __float_as_uint(t.y) * 8u + bias;
+    }
+    if constexpr (kBoundsChecks) {   // grid entries of this launch's table
+      const uint32_t end = grid_base + (kmax + 1u) * 8u;
+      if (a0 < grid_base || a0 + 8u > end || a1 < grid_base || a1 + 8u > end) {
+        atomicOr(a.err, kErrBounds);
+        a0 = a1 = grid_base;
+      }
     }
     const float2 e0 = lds64f(a0);
     const float2 e1 = lds64f(a1);

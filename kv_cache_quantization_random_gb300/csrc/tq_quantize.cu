@@ -268,6 +268,16 @@ __global__ void __launch_bounds__(64) append_kernel(const AppendArgs a) {
       if (lane == 0) atomicOr(a.err, kErrBounds);
       continue;
     }
+    // bounds-checked build: the row lies inside the ring or the new input
+    if (kBoundsChecks) {
+      const bool ring = pos < T0;
+      const size_t bytes = ring ? (size_t)a.B * a.H * a.W * kD * 2
+                                : (size_t)((long long)(a.B - 1) * a.sb + (long long)(a.H - 1) * a.sh +
+                                           (long long)(a.n - 1) * a.st + kD) * esz;
+      if (!bchk_range(src, (size_t)kD * (ring ? 2 : esz), ring ? (const void*)a.win[kind] : a.src[kind],
+                      bytes, a.err))
+        continue;
+    }
     const long long drow = ((long long)b * a.H + h) * a.cap[kind] + pos;
     append_quantize_row(a, kind, src, f32, drow, bnd[kind], cen[kind], sg, words[kind], rbuf, lane);
   }
@@ -282,7 +292,7 @@ __global__ void __launch_bounds__(64) append_kernel(const AppendArgs a) {
     const uint4* s4 = (const uint4*)((const uint8_t*)a.src[k2] +
                                      (b * a.sb + h * a.sh + (t - T0) * a.st) * 2);
     uint4* d4 = (uint4*)(a.win[k2] + (((long long)b * a.H + h) * a.W + t % a.W) * kD);
-    d4[part] = s4[part];
+    *bchk(d4 + part, a.win[k2], (size_t)a.B * a.H * a.W * kD * 2, a.err) = s4[part];
   }
 }
 
@@ -305,7 +315,8 @@ __global__ void __launch_bounds__(128) dequantize_kernel(const DequantArgs a) {
   const long long bh = v / a.n;
   const long long row = bh * a.cap + j;
   uint32_t w[NW];
-  const uint4* src = (const uint4*)(a.codes + row * (16 * BITS));
+  const uint4* src = bchk((const uint4(*)[BITS])(a.codes + row * (16 * BITS)), a.codes,
+                          (size_t)a.B * a.H * a.cap * 16 * BITS, a.err)[0];
 #pragma unroll
   for (int k = 0; k < BITS; ++k) {
     uint4 t = src[k];

@@ -120,6 +120,15 @@ def test_decode_bits(B, kb, vb):
     assert rel_l2_per_head(out, ref).max() < TOL
 
 
+@pytest.mark.parametrize("seq,W", [([1], 0), ([2], 0), ([31], 0), ([33], 16), ([255, 256, 257], 0),
+                                   ([511, 512, 513], 8), ([1, 2, 3], 4), ([32, 64], 32)])
+def test_decode_tiny_and_split_boundary_lengths(B, seq, W):
+    """Tiny contexts and contexts one token either side of a split boundary
+    (splits are multiples of 256 tokens here), with and without a window."""
+    out, ref, _ = _decode_case(B, batch=len(seq), hq=8, hkv=2, seq=seq, kb=4, vb=2, W=W)
+    assert rel_l2_per_head(out, ref).max() < TOL
+
+
 @pytest.mark.parametrize("g", [1, 2, 4, 8])
 def test_decode_group_sizes(B, g):
     out, ref, _ = _decode_case(B, batch=1, hq=2 * g, hkv=2, seq=[1500], kb=3, vb=3)
