@@ -16,10 +16,9 @@
 // stays in shared memory for the whole launch.  TMEM lane t holds z for key
 // t, so after the commit each warp reads its 32 lanes with tcgen05.ld and
 // every thread turns its own 128 projections into 4 words of sign bits.
-// bf16 rows go straight from global memory into the registers of the thread
-// that owns the key, one tile ahead: the loads of tile i+1 are in flight while
-// tile i is quantized, projected and signed, and two CTAs fit on an SM; fp32
-// rows are staged in a shared-memory buffer of their own (one CTA per SM).
+// bf16 rows are staged in the R lo tile itself (a CTA barrier separates the
+// last read of a row from the first residual write), which leaves room for
+// two CTAs per SM; fp32 rows keep a buffer of their own and one CTA per SM.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -29,25 +28,14 @@
 
 namespace tq {
 
-// bf16 rows are read into registers, so a CTA fits twice on an SM; fp32 rows
-// need a staging buffer of their own.
+// bf16 rows are staged in the R lo tile (read into registers before R lo is
+// written), so a CTA fits twice on an SM; fp32 rows need their own buffer.
 __host__ __device__ constexpr size_t qjl_smem_bytes(bool f32, int cells) {
   return 1024                                    // alignment slack
          + 3 * (size_t)kOpBytes                  // R hi, R lo, S
          + (f32 ? quant_rows_bytes(true) : 0)    // staged fp32 rows (one tile)
          + (size_t)cells * 8 + 2 * 256 * 4       // grid, boundaries, centroids
          + 16;                                   // mbarrier + TMEM address
-}
-
-// this thread's bf16 row (256 bytes) into 64 registers, or zeros; the loads
-// complete while the caller works on the previous row
-__device__ __forceinline__ void load_row_regs(const void* src, bool valid, uint32_t (&w)[64]) {
-  const uint4* s = (const uint4*)src;
-#pragma unroll
-  for (int c = 0; c < 16; ++c) {
-    const uint4 v = valid ? __ldg(s + c) : make_uint4(0u, 0u, 0u, 0u);
-    w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
-  }
 }
 
 template <int BITS, bool F32>
@@ -59,7 +47,7 @@ __global__ void __launch_bounds__(kQRows, F32 ? 1 : 2) quantize_qjl_kernel(const
   uint8_t* ahi = base;
   uint8_t* alo = base + kOpBytes;
   uint8_t* sop = base + 2 * kOpBytes;
-  uint8_t* rows = base + 3 * kOpBytes;                 // fp32 staging (unused for bf16)
+  uint8_t* rows = F32 ? base + 3 * kOpBytes : alo;
   float2* grid = (float2*)(base + 3 * kOpBytes + (F32 ? quant_rows_bytes(true) : 0));
   float* bnd = (float*)(grid + a.grid_cells);
   float* cen = bnd + 256;
@@ -101,52 +89,25 @@ __global__ void __launch_bounds__(kQRows, F32 ? 1 : 2) quantize_qjl_kernel(const
   const uint32_t ntiles = (total + kQRows - 1) / kQRows;
   uint32_t phase = 0;
   bool failed = false;
-  // this thread's key of the current tile: source row, plane row, and (bf16)
-  // the row itself in registers
-  const void* src = nullptr;
-  long long drow = 0;
-  bool valid = false;
-  uint32_t rw[64];
-  {
-    const uint32_t v = blockIdx.x * kQRows + tid;
-    valid = blockIdx.x < ntiles && v < total && resolve_row(a, v, &src, &drow);
-    if constexpr (!F32) load_row_regs(src, valid, rw);
-  }
   for (uint32_t tile = blockIdx.x; tile < ntiles && !failed; tile += gridDim.x, phase ^= 1u) {
-    // ---- the next tile's key: resolved now, its bf16 row loaded into
-    // registers while this tile is processed
-    const void* nsrc = nullptr;
-    long long ndrow = 0;
-    bool nvalid = false;
-    uint32_t nw[64];
-    {
-      const uint32_t nt = tile + gridDim.x;
-      const uint32_t v = nt * kQRows + tid;
-      nvalid = nt < ntiles && v < total && resolve_row(a, v, &nsrc, &ndrow);
-      if constexpr (!F32) load_row_regs(nsrc, nvalid, nw);
-    }
-    if constexpr (F32) {
-      // ---- stage: warp w copies rows 32w .. 32w+31 of the tile
-      stage_rows<F32>(src, valid, rows + warp * 32 * kPitch, lane);
-      cp_async_commit();
-      cp_async_wait<0>();
-      __syncwarp();
-    }
+    // ---- stage: warp w copies rows 32w .. 32w+31 of the tile
+    const uint32_t v = tile * kQRows + tid;
+    const void* src = nullptr;
+    long long drow = 0;
+    const bool valid = v < total && resolve_row(a, v, &src, &drow);
+    if constexpr (F32) stage_rows<F32>(src, valid, rows + warp * 32 * kPitch, lane);
+    else stage_rows_swz(src, valid, rows, 32 * warp, lane);
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncwarp();
     // ---- codes, norm and residual of this thread's key; residual rows of R
     float gamma = 0.f;
     {
       float2 p[64];
       if (valid) {
-        float nrm;
-        if constexpr (F32) {
-          nrm = quantize_row<BITS, F32, (BITS > 4), true>(a, rows + tid * kPitch, grid_base,
-                                                         kmax, cen, a.codes + drow * (16 * BITS),
-                                                         p);
-        } else {
-          nrm = load_rotate_regs(a, rw, p);
-          search_pack<BITS, (BITS > 4), true>(a, p, nrm, grid_base, kmax, cen,
-                                              a.codes + drow * (16 * BITS));
-        }
+        const float nrm = quantize_row<BITS, F32, (BITS > 4), true, !F32>(
+            a, rows + tid * (F32 ? kPitch : 256), grid_base, kmax, cen,
+            a.codes + drow * (16 * BITS), p, tid & 7);
         a.norms[drow] = nrm;
         float2 g2 = make_float2(0.f, 0.f);
 #pragma unroll
@@ -156,6 +117,8 @@ __global__ void __launch_bounds__(kQRows, F32 ? 1 : 2) quantize_qjl_kernel(const
 #pragma unroll
         for (int j = 0; j < 64; ++j) p[j] = make_float2(0.f, 0.f);
       }
+      // bf16 rows live in the R lo tile: every thread has read its row
+      if constexpr (!F32) __syncthreads();
       // p[j] = (r_j, r_{j+64}); chunk c of the row holds coordinates 8c .. 8c+7
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
@@ -220,13 +183,6 @@ __global__ void __launch_bounds__(kQRows, F32 ? 1 : 2) quantize_qjl_kernel(const
     }
     tc_fence_before();
     __syncthreads();   // TMEM, R tiles and rows are reused by the next tile
-    src = nsrc;
-    drow = ndrow;
-    valid = nvalid;
-    if constexpr (!F32) {
-#pragma unroll
-      for (int k = 0; k < 64; ++k) rw[k] = nw[k];
-    }
   }
   (void)failed;
   tc_fence_before();

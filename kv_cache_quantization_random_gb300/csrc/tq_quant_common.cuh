@@ -187,42 +187,6 @@ __device__ __forceinline__ float load_rotate(const QuantArgs& a, const uint8_t* 
   return sqrtf(s.x + s.y);
 }
 
-// load_rotate for a bf16 row held in registers: w[k] packs coordinates 2k
-// (low half) and 2k + 1 (high half), as the row lies in memory.
-__device__ __forceinline__ float load_rotate_regs(const QuantArgs& a, const uint32_t (&w)[64],
-                                                  float2 (&p)[64]) {
-#pragma unroll
-  for (int k = 0; k < 32; ++k) {
-    const int i = 2 * k;
-    p[i] = make_float2(__uint_as_float(w[k] * 65536u + a.smask[i]),
-                       __uint_as_float(w[32 + k] * 65536u + a.smask[64 + i]));
-    p[i + 1] = make_float2(__uint_as_float((w[k] & 0xFFFF0000u) ^ a.smask[i + 1]),
-                           __uint_as_float((w[32 + k] & 0xFFFF0000u) ^ a.smask[64 + i + 1]));
-  }
-  float2 s0 = make_float2(0.f, 0.f), s1 = s0;
-#pragma unroll
-  for (int j = 0; j < 64; j += 2) {
-    s0 = __ffma2_rn(p[j], p[j], s0);
-    s1 = __ffma2_rn(p[j + 1], p[j + 1], s1);
-  }
-  const float2 s = __fadd2_rn(s0, s1);
-  const float2 neg1 = make_float2(-1.f, -1.f);
-#pragma unroll
-  for (int hs = 1; hs < 64; hs <<= 1) {
-#pragma unroll
-    for (int j = 0; j < 64; ++j) {
-      if ((j & hs) == 0) {
-        const float2 u = p[j], v = p[j + hs];
-        p[j] = __fadd2_rn(u, v);
-        p[j + hs] = __ffma2_rn(v, neg1, u);
-      }
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < 64; ++j) p[j] = make_float2(p[j].x + p[j].y, p[j].x - p[j].y);
-  return sqrtf(s.x + s.y);
-}
-
 // Search-grid table (see SearchGrid in tq_internal.h) from the boundaries in
 // shared memory: entry k = (first boundary at or above the lower edge of cells
 // k-1..k+1, number of boundaries below that edge).  Called by all threads of
