@@ -469,10 +469,11 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
   const int mg = lane >> 2, tig = lane & 3;   // MMA group / thread-in-group
 
   // ------------------------------------------------------------- prologue
-  // The codec tables are loaded before the dependency wait, the sequence
-  // length and the bulk copy of each warp's first chunk right after it; the
-  // query and the tables' arithmetic overlap the copies' flight, so the
-  // prologue costs about one memory round trip.
+  // The codec tables are loaded and the lookup tables built before the
+  // dependency wait; the sequence length and the bulk copy of each warp's
+  // first chunk come right after it, the query rotation overlaps the copies'
+  // flight, and each warp's later chunks follow the CTA barrier of the query
+  // scale, so that the first chunks of all warps are not queued behind them.
   __shared__ float cks[256], cvs[256];
   const int W = a.W;
   const bool window_split = split >= a.n_qsplits;
@@ -491,7 +492,57 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
     for (int i = 0; i < NS; ++i) mbar_init(bar + i, 1);
     fence_mbarrier_init();
   }
-  __syncwarp();
+  __syncthreads();                                   // cks, cvs, svs
+  // the shared lookup tables, built before the dependency wait so that they
+  // overlap the previous kernel's tail (the tables buffer is written by the
+  // host, never by a kernel on the stream)
+  for (int i = tid; i < 256; i += kDT) {
+    if constexpr (KB == 2) {
+      if (i < 16) {
+        uint32_t hp, lp;
+        hilo2(cks[i & 3] * kCScale, cks[(i >> 2) & 3] * kCScale, hp, lp);
+        lutk[2 * i] = hp;
+        lutk[2 * i + 1] = lp;
+      }
+    } else if constexpr (KB == 3 || KB == 4) {
+      // pair i = c_lo | c_hi << KB into the 16 key replicas of row i; at
+      // step j lane l writes replica (l + j) % 16
+      if (i < (1 << (2 * KB))) {
+        constexpr int msk = (1 << KB) - 1;
+        uint32_t hp, lp;
+        hilo2(cks[i & msk] * kCScale, cks[i >> KB] * kCScale, hp, lp);
+        uint2* row = (uint2*)(smem + L.lutk4) + i * 32;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          *bchk(row + ((lane + j) & 15), smem + L.lutk4, L.warps - L.lutk4, a.err) =
+              make_uint2(hp, lp);
+      }
+    } else {
+      lutk[i] = hilo(cks[i] * kCScale);
+    }
+    if constexpr (VB == 2) {
+      // value entry i of the pair table: (half2 of coordinate c, half2 of c + 2)
+      // for the code byte i (see vmma_ktile), into replicas 16-31 of row i
+      auto pe = [&](int n) {   // n = code of the first token | code of the second << 2
+        return (h16(cvs[(n >> 2) & 3]) << 16) | h16(cvs[n & 3]);
+      };
+      const uint2 ve = make_uint2(pe(i & 15), pe(i >> 4));
+      uint2* row = (uint2*)(smem + L.lutk4) + i * 32 + 16;
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        *bchk(row + ((lane + j) & 15), smem + L.lutk4, L.warps - L.lutk4, a.err) = ve;
+    }
+    uint32_t e;
+    if constexpr (VB == 2 || VB == 3) {
+      const int msk = (1 << VB) - 1;
+      e = (h16(cvs[(i >> VB) & msk]) << 16) | h16(cvs[i & msk]);
+    } else {
+      e = h16(cvs[i]);
+    }
+    lutv[i] = e;
+  }
+  if (tid < 4) slut[tid] = ((tid & 2) ? 0x3C000000u : 0xBC000000u) | ((tid & 1) ? 0x3C00u : 0xBC00u);
+
 
   // everything below may read what the previous kernel on the stream wrote
   // (sequence lengths, query, planes, window ring, workspace): wait for it
@@ -604,60 +655,6 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
   // of all warps are not queued behind the later ones
   if (!window_split && t_begin + 32 * warp < t_end) issue(t_begin + 32 * warp, 0);
 
-  __syncthreads();                                   // cks, cvs, svs
-  if (!window_split) {
-#pragma unroll
-    for (int j = 1; j < NS - 1; ++j) {
-      const int c = t_begin + 32 * warp + 32 * kDWarps * j;
-      if (c < t_end) issue(c, j);
-    }
-  }
-  for (int i = tid; i < 256; i += kDT) {
-    if constexpr (KB == 2) {
-      if (i < 16) {
-        uint32_t hp, lp;
-        hilo2(cks[i & 3] * kCScale, cks[(i >> 2) & 3] * kCScale, hp, lp);
-        lutk[2 * i] = hp;
-        lutk[2 * i + 1] = lp;
-      }
-    } else if constexpr (KB == 3 || KB == 4) {
-      // pair i = c_lo | c_hi << KB into the 16 key replicas of row i; at
-      // step j lane l writes replica (l + j) % 16
-      if (i < (1 << (2 * KB))) {
-        constexpr int msk = (1 << KB) - 1;
-        uint32_t hp, lp;
-        hilo2(cks[i & msk] * kCScale, cks[i >> KB] * kCScale, hp, lp);
-        uint2* row = (uint2*)(smem + L.lutk4) + i * 32;
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          *bchk(row + ((lane + j) & 15), smem + L.lutk4, L.warps - L.lutk4, a.err) =
-              make_uint2(hp, lp);
-      }
-    } else {
-      lutk[i] = hilo(cks[i] * kCScale);
-    }
-    if constexpr (VB == 2) {
-      // value entry i of the pair table: (half2 of coordinate c, half2 of c + 2)
-      // for the code byte i (see vmma_ktile), into replicas 16-31 of row i
-      auto pe = [&](int n) {   // n = code of the first token | code of the second << 2
-        return (h16(cvs[(n >> 2) & 3]) << 16) | h16(cvs[n & 3]);
-      };
-      const uint2 ve = make_uint2(pe(i & 15), pe(i >> 4));
-      uint2* row = (uint2*)(smem + L.lutk4) + i * 32 + 16;
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        *bchk(row + ((lane + j) & 15), smem + L.lutk4, L.warps - L.lutk4, a.err) = ve;
-    }
-    uint32_t e;
-    if constexpr (VB == 2 || VB == 3) {
-      const int msk = (1 << VB) - 1;
-      e = (h16(cvs[(i >> VB) & msk]) << 16) | h16(cvs[i & msk]);
-    } else {
-      e = h16(cvs[i]);
-    }
-    lutv[i] = e;
-  }
-  if (tid < 4) slut[tid] = ((tid & 2) ? 0x3C000000u : 0xBC000000u) | ((tid & 1) ? 0x3C00u : 0xBC00u);
   // query rotation in registers: warp w rotates heads w (and w + 4), lane l
   // holds coordinates 4l .. 4l+3; two butterfly stages in the lane, five by shuffles
   float qmax = 0.f;
@@ -697,6 +694,13 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
   qmax = warp_max(qmax);
   if (lane == 0) red[warp] = qmax;
   __syncthreads();
+  if (!window_split) {
+#pragma unroll
+    for (int j = 1; j < NS - 1; ++j) {
+      const int c = t_begin + 32 * warp + 32 * kDWarps * j;
+      if (c < t_end) issue(c, j);
+    }
+  }
 #pragma unroll
   for (int w = 0; w < kDWarps; ++w) qmax = fmaxf(qmax, red[w]);
   int qe = 0;
@@ -1274,29 +1278,43 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
   __syncthreads();
   if (!*is_last) return;
 
-  // last CTA of this (sequence, kv-head): one warp per head merges the splits,
-  // inverse-rotates (R^T = D_s H / sqrt(d)) in registers and writes the output
+  // last CTA of this (sequence, kv-head): every warp takes a share of the
+  // merge.  Head g gets WH = kDWarps / G warps (at least one); warp k of the
+  // head merges splits k, k + WH, ... in one pass with online rescaling
+  // (lane s holds (m, l) of the batch's split s, every lane its 4 coordinates
+  // of every row; NB rows in flight per batch).  Rows of quantized splits are
+  // rotated-domain sums, rows of window splits original-domain sums: two
+  // accumulators.  The WH warps of a head then combine through shared memory,
+  // and the head's first warp inverse-rotates (R^T = D_s H / sqrt(d)) in
+  // registers and writes the output.
+  constexpr int WH = kDWarps / G > 0 ? kDWarps / G : 1;    // warps per head
+  constexpr int NB = WH == 1 ? 32 : 8;                       // split rows per batch
   const float* base = a.partials + unit * a.n_splits * G * stride;
-  for (int g = warp; g < G; g += kDWarps) {
-    // one pass over the splits, 32 split rows in flight per batch, with online
-    // rescaling: lane s holds (m, l) of split s0 + s, every lane its 4
-    // coordinates of all 32 rows.  Rows of quantized splits are rotated-domain
-    // sums, rows of window splits original-domain sums: two accumulators.
+  float* mres = (float*)(smem + L.comb);     // [kDWarps][M, L, pad, pad, rot[128], win[128]]
+  constexpr int kMres = 4 + 2 * kD2;
+  auto MR = [&](int i) -> float& {
+    return *bchk(mres + i, mres, (size_t)kDWarps * kMres * 4, a.err);
+  };
+  for (int g0 = warp / WH; g0 < G; g0 += kDWarps / WH) {
+    const int g = g0, k = warp % WH;
     float M = kNegBig, Lsum = 0.f;
     float4 rot = make_float4(0.f, 0.f, 0.f, 0.f), win = rot;
-    for (int s0 = 0; s0 < a.n_splits; s0 += 32) {
-      const int sl = s0 + lane;
-      const float* pl = bchk(base + (sl < a.n_splits ? sl : 0) * G * stride + g * stride,
-                             a.partials, part_bytes, a.err);
-      const float ml = sl < a.n_splits ? __ldcg(pl) : kNegBig;
-      const float ll = sl < a.n_splits ? __ldcg(pl + 1) : 0.f;
-      float4 v[32];
+    for (int s0 = k; s0 < a.n_splits; s0 += WH * NB) {
+      const int sl = s0 + WH * lane;                // this lane's (m, l) row
+      const bool lv = lane < NB && sl < a.n_splits;
+      const float* pl = bchk(base + (lv ? sl : 0) * G * stride + g * stride, a.partials,
+                             part_bytes, a.err);
+      const float ml = lv ? __ldcg(pl) : kNegBig;
+      const float ll = lv ? __ldcg(pl + 1) : 0.f;
+      float4 v[NB];
 #pragma unroll
-      for (int u = 0; u < 32; ++u)
-        v[u] = s0 + u < a.n_splits
-                   ? __ldcg(bchk((const float4*)(base + ((s0 + u) * G + g) * stride + 4) + lane,
+      for (int u = 0; u < NB; ++u) {
+        const int su = s0 + WH * u;
+        v[u] = su < a.n_splits
+                   ? __ldcg(bchk((const float4*)(base + (su * G + g) * stride + 4) + lane,
                                  a.partials, part_bytes, a.err))
                    : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
       const float Mn = fmaxf(M, warp_max(ml));
       const float r = ex2(M - Mn);
       const float fl = ex2(ml - Mn);
@@ -1304,9 +1322,9 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
       rot = make_float4(rot.x * r, rot.y * r, rot.z * r, rot.w * r);
       win = make_float4(win.x * r, win.y * r, win.z * r, win.w * r);
 #pragma unroll
-      for (int u = 0; u < 32; ++u) {
+      for (int u = 0; u < NB; ++u) {
         const float f = __shfl_sync(0xffffffffu, fl, u);
-        const bool q = s0 + u < a.n_qsplits;
+        const bool q = s0 + WH * u < a.n_qsplits;
         const float fq = q ? f : 0.f, fw = q ? 0.f : f;
         rot.x = fmaf(v[u].x, fq, rot.x);
         rot.y = fmaf(v[u].y, fq, rot.y);
@@ -1319,28 +1337,86 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
       }
       M = Mn;
     }
-    // butterfly over 128 values, 4 per lane (coordinates 4*lane .. 4*lane+3)
-    float x[4] = {rot.x, rot.y, rot.z, rot.w};
-    {
-      float u0 = x[0] + x[1], u1 = x[0] - x[1], u2 = x[2] + x[3], u3 = x[2] - x[3];
-      x[0] = u0 + u2; x[2] = u0 - u2; x[1] = u1 + u3; x[3] = u1 - u3;
-    }
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const bool upper = (lane & o) != 0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float other = __shfl_xor_sync(0xffffffffu, x[j], o);
-        x[j] = upper ? other - x[j] : x[j] + other;
+    if constexpr (WH > 1) {
+      if (lane == 0) {
+        MR(warp * kMres) = M;
+        MR(warp * kMres + 1) = Lsum;
       }
+      *bchk((float4*)(mres + warp * kMres + 4) + lane, mres, (size_t)kDWarps * kMres * 4, a.err) = rot;
+      *bchk((float4*)(mres + warp * kMres + 4 + kD2) + lane, mres, (size_t)kDWarps * kMres * 4,
+            a.err) = win;
     }
-    const float4 sv4 = *(const float4*)(svs + 4 * lane);
-    const float r = 0.08838834764831845f;
-    const float inv = Lsum > 0.f ? 1.0f / Lsum : 0.f;
-    const float4 res = make_float4((x[0] * r * sv4.x + win.x) * inv, (x[1] * r * sv4.y + win.y) * inv,
-                                   (x[2] * r * sv4.z + win.z) * inv, (x[3] * r * sv4.w + win.w) * inv);
-    *bchk((float4*)(a.out + ((long long)b * a.Hq + (long long)kvh * G + g) * kD2 + 4 * lane), a.out,
-          (size_t)a.B * a.Hq * kD2 * 4, a.err) = res;
+    if constexpr (WH == 1) {
+      // one warp per head: no combine step
+      float x[4] = {rot.x, rot.y, rot.z, rot.w};
+      {
+        float u0 = x[0] + x[1], u1 = x[0] - x[1], u2 = x[2] + x[3], u3 = x[2] - x[3];
+        x[0] = u0 + u2; x[2] = u0 - u2; x[1] = u1 + u3; x[3] = u1 - u3;
+      }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float other = __shfl_xor_sync(0xffffffffu, x[j], o);
+          x[j] = upper ? other - x[j] : x[j] + other;
+        }
+      }
+      const float4 sv4 = *(const float4*)(svs + 4 * lane);
+      const float rr = 0.08838834764831845f;
+      const float inv = Lsum > 0.f ? 1.0f / Lsum : 0.f;
+      const float4 res = make_float4((x[0] * rr * sv4.x + win.x) * inv, (x[1] * rr * sv4.y + win.y) * inv,
+                                     (x[2] * rr * sv4.z + win.z) * inv, (x[3] * rr * sv4.w + win.w) * inv);
+      *bchk((float4*)(a.out + ((long long)b * a.Hq + (long long)kvh * G + g) * kD2 + 4 * lane), a.out,
+            (size_t)a.B * a.Hq * kD2 * 4, a.err) = res;
+    }
+  }
+  if constexpr (WH > 1) {
+    __syncthreads();
+    // the first warp of each head combines its head's WH partial merges
+    if (warp % WH == 0 && warp / WH < G) {
+      const int g = warp / WH;
+      float M = kNegBig;
+#pragma unroll
+      for (int k = 0; k < WH; ++k) M = fmaxf(M, MR((warp + k) * kMres));
+      float Lsum = 0.f;
+      float4 rot = make_float4(0.f, 0.f, 0.f, 0.f), win = rot;
+#pragma unroll
+      for (int k = 0; k < WH; ++k) {
+        const float f = ex2(MR((warp + k) * kMres) - M);
+        Lsum = fmaf(MR((warp + k) * kMres + 1), f, Lsum);
+        const float4 rk = *bchk((const float4*)(mres + (warp + k) * kMres + 4) + lane, mres,
+                                (size_t)kDWarps * kMres * 4, a.err);
+        const float4 wk = *bchk((const float4*)(mres + (warp + k) * kMres + 4 + kD2) + lane, mres,
+                                (size_t)kDWarps * kMres * 4, a.err);
+        rot = make_float4(fmaf(rk.x, f, rot.x), fmaf(rk.y, f, rot.y), fmaf(rk.z, f, rot.z),
+                          fmaf(rk.w, f, rot.w));
+        win = make_float4(fmaf(wk.x, f, win.x), fmaf(wk.y, f, win.y), fmaf(wk.z, f, win.z),
+                          fmaf(wk.w, f, win.w));
+      }
+      // butterfly over 128 values, 4 per lane (coordinates 4*lane .. 4*lane+3)
+      float x[4] = {rot.x, rot.y, rot.z, rot.w};
+      {
+        float u0 = x[0] + x[1], u1 = x[0] - x[1], u2 = x[2] + x[3], u3 = x[2] - x[3];
+        x[0] = u0 + u2; x[2] = u0 - u2; x[1] = u1 + u3; x[3] = u1 - u3;
+      }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float other = __shfl_xor_sync(0xffffffffu, x[j], o);
+          x[j] = upper ? other - x[j] : x[j] + other;
+        }
+      }
+      const float4 sv4 = *(const float4*)(svs + 4 * lane);
+      const float rr = 0.08838834764831845f;
+      const float inv = Lsum > 0.f ? 1.0f / Lsum : 0.f;
+      const float4 res = make_float4((x[0] * rr * sv4.x + win.x) * inv, (x[1] * rr * sv4.y + win.y) * inv,
+                                     (x[2] * rr * sv4.z + win.z) * inv, (x[3] * rr * sv4.w + win.w) * inv);
+      *bchk((float4*)(a.out + ((long long)b * a.Hq + (long long)kvh * G + g) * kD2 + 4 * lane), a.out,
+            (size_t)a.B * a.Hq * kD2 * 4, a.err) = res;
+    }
   }
   if (tid == 0)   // leave the counter ready for the next call
     *bchk(a.counters + unit, a.counters, (size_t)a.B * Hkv * 4, a.err) = 0u;

@@ -58,7 +58,9 @@ struct DecodeSmem {
     warp_stride = w;
     int region = nw * w;
     const int comb_need = nw * G * (2 + kHeadDim) * 4;   // cm, cl, co
+    const int merge_need = nw * (4 + 2 * kHeadDim) * 4;  // the last CTA's per-warp merges
     if (region < comb_need) region = comb_need;
+    if (region < merge_need) region = merge_need;
     comb = warps;
     off += region;
     total = off + 16;                             // + is-last flag
