@@ -536,6 +536,26 @@ def run_single(args, w, rank, world, local):
         raise RuntimeError("device error during timed steps")
     dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
 
+    # ---- sparse V: the exact decode of the same cache for comparison, and an
+    # upper bound of the share of 32-token chunks whose V sum the kernel may
+    # skip (all weights of the chunk below 2^-sparse_v of the head's final
+    # maximum; the kernel compares with the running maximum, which is lower,
+    # so it skips at most this share), from the oracle's scores of kv-head 0
+    sparse = None
+    if args.sparse_v > 0:
+        cfg_exact = make_config(B, w, 0)
+
+        def decode_exact(r):
+            kr, vr, kwr, vwr = reps[r]
+            B.tq_decode_attention(cfg_exact, tables, 0, q, w.softmax_scale, kr, vr, seq_t, Tmax,
+                                  out, ws, k_win=kwr, v_win=vwr)
+
+        for i in range(3):
+            decode_exact(i % R)
+        ex_ms = graph_ms(graph_of(lambda i: decode_exact(i % R), S), S)
+        sparse = {"sparse_v": args.sparse_v, "decode_ms": dec_ms, "exact_decode_ms": ex_ms,
+                  "skippable_chunks_upper_bound": sparse_skip_bound(w, st, q, seq, args.sparse_v)}
+
     # ---- optional: several query tokens per sequence (speculative verify)
     multi = None
     if args.n_queries > 1:
@@ -642,6 +662,8 @@ def run_single(args, w, rank, world, local):
     }
     if chunk is not None:
         res["chunk_quantize"] = chunk
+    if sparse is not None:
+        res["sparse_v"] = sparse
     if multi is not None:
         res["multi_query"] = multi
     if qjl_proj is not None:
@@ -1049,6 +1071,26 @@ def score_quality(w, K, qs, c, T):
             "score_cosine_similarity_min": float(np.min(sims)),
             "top1_agreement": float(np.mean(top1)), "query_heads": len(sims),
             "what": "MSE codes only (no residual term); synthetic keys, not a model's"}
+
+
+def sparse_skip_bound(w, st, q, seq, k):
+    """Share of the 32-token chunks of kv-head 0 (sequence 0) whose softmax
+    weights are all below 2^-k of each query head's final maximum, from the
+    oracle's compressed-domain scores."""
+    import numpy as np
+    import oracle as O
+    K, V, qs = _oracle_inputs(w, st, q, [0])
+    T = int(seq[0])
+    c = _oracle_cache(w, K, V, T)
+    nq = T - w.window
+    RK = O.rotation_matrix(c["sk"])
+    keys = c["qk"]["norms"][0, 0, :nq].astype(np.float64)[:, None] * c["ck"].astype(np.float64)[c["qk"]["codes"][0, 0, :nq]]
+    s = np.stack([keys @ (RK @ qs[0, j]) for j in range(w.group)]) * w.softmax_scale   # [G, nq]
+    s2 = s / math.log(2.0)                                                              # log2 units
+    below = s2 < (s2.max(axis=1, keepdims=True) - k)
+    n = nq // 32
+    chunks = below[:, :n * 32].reshape(w.group, n, 32).all(axis=(0, 2))
+    return float(chunks.mean()) if n else 0.0
 
 
 def sampled_parity(B, w, st, q, out, rep0, seq, step):

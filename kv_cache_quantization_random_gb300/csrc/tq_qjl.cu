@@ -89,15 +89,21 @@ __global__ void __launch_bounds__(kQRows, F32 ? 1 : 2) quantize_qjl_kernel(const
   const uint32_t ntiles = (total + kQRows - 1) / kQRows;
   uint32_t phase = 0;
   bool failed = false;
-  for (uint32_t tile = blockIdx.x; tile < ntiles && !failed; tile += gridDim.x, phase ^= 1u) {
-    // ---- stage: warp w copies rows 32w .. 32w+31 of the tile
-    const uint32_t v = tile * kQRows + tid;
-    const void* src = nullptr;
-    long long drow = 0;
-    const bool valid = v < total && resolve_row(a, v, &src, &drow);
-    if constexpr (F32) stage_rows<F32>(src, valid, rows + warp * 32 * kPitch, lane);
-    else stage_rows_swz(src, valid, rows, 32 * warp, lane);
+  // stage: warp w copies rows 32w .. 32w+31 of a tile (the rows its threads
+  // quantize); the next tile's rows are staged as soon as the tensor cores
+  // have read this tile's R tiles, so their loads overlap the signs and stores
+  auto stage = [&](uint32_t t, const void** src, long long* drow, bool* valid) {
+    const uint32_t v = t * kQRows + tid;
+    *valid = t < ntiles && v < total && resolve_row(a, v, src, drow);
+    if constexpr (F32) stage_rows<F32>(*src, *valid, rows + warp * 32 * kPitch, lane);
+    else stage_rows_swz(*src, *valid, rows, 32 * warp, lane);
     cp_async_commit();
+  };
+  const void* src = nullptr;
+  long long drow = 0;
+  bool valid = false;
+  stage(blockIdx.x, &src, &drow, &valid);
+  for (uint32_t tile = blockIdx.x; tile < ntiles && !failed; tile += gridDim.x, phase ^= 1u) {
     cp_async_wait<0>();
     __syncwarp();
     // ---- codes, norm and residual of this thread's key; residual rows of R
@@ -165,6 +171,12 @@ __global__ void __launch_bounds__(kQRows, F32 ? 1 : 2) quantize_qjl_kernel(const
       break;
     }
     tc_fence_after();
+    // the tensor cores are done with R lo, which holds the staged bf16 rows:
+    // stage the next tile now (fp32 rows have their own buffer, read already)
+    const void* nsrc = nullptr;
+    long long ndrow = 0;
+    bool nvalid = false;
+    stage(tile + gridDim.x, &nsrc, &ndrow, &nvalid);
     // ---- signs: warp w reads TMEM lanes 32w .. 32w+31 (its threads' keys)
     uint32_t sbits[4];
 #pragma unroll
@@ -182,8 +194,12 @@ __global__ void __launch_bounds__(kQRows, F32 ? 1 : 2) quantize_qjl_kernel(const
       a.qjl_rnorm[drow] = gamma;
     }
     tc_fence_before();
-    __syncthreads();   // TMEM, R tiles and rows are reused by the next tile
+    __syncthreads();   // TMEM and the R tiles are reused by the next tile
+    src = nsrc;
+    drow = ndrow;
+    valid = nvalid;
   }
+  cp_async_wait<0>();
   (void)failed;
   tc_fence_before();
   __syncthreads();
