@@ -589,22 +589,31 @@ def run_single(args, w, rank, world, local):
     chunk = None
     if w.new_tokens > 8:
         n_new = w.new_tokens
-        kch = K[:, :, T - n_new:T]
-        vch = V[:, :, T - n_new:T]
-        sb = torch.tensor(seq - n_new, dtype=torch.int32, device=device)
+        nv = w.batch * w.n_kv_heads * n_new
+        c_bytes = nv * (2 * in_bytes_per_vector(w) + kbts + vbts) + \
+            w.batch * w.n_kv_heads * min(n_new, Wn) * w.head_dim * 2 * 2
+        # chunk r appends tokens [T - (r+1) n_new, T - r n_new) at that position:
+        # Rc distinct input slices and plane rows, more than 4x L2 in all, so
+        # that consecutive appends find neither their inputs nor their
+        # destination rows in L2
+        Rc = max(1, min(int(math.ceil(4 * l2 / c_bytes)) + 1, (int(seq.min()) - Wn) // n_new - 1))
+        chunks = []
+        for r in range(Rc):
+            t1 = T - r * n_new
+            chunks.append((K[:, :, t1 - n_new:t1], V[:, :, t1 - n_new:t1],
+                           torch.tensor(seq - (r + 1) * n_new, dtype=torch.int32, device=device)))
 
         def chunk_append(i):
+            kch, vch, sb = chunks[i % Rc]
             B.tq_append_kv(cfg, tables, 0, kch, vch, sb, st["kw"], st["vw"], kp, vp)
 
         for i in range(3):
             chunk_append(i)
-        c_ms = graph_ms(graph_of(chunk_append, 4), 4)
-        nv = w.batch * w.n_kv_heads * n_new
-        c_bytes = nv * (2 * in_bytes_per_vector(w) + kbts + vbts) + \
-            w.batch * w.n_kv_heads * min(n_new, Wn) * w.head_dim * 2 * 2
+        c_ms = graph_ms(graph_of(chunk_append, Rc), Rc)
         chunk = {"new_tokens": n_new, "ms": c_ms, "bytes": c_bytes,
                  "gbs": c_bytes / (c_ms * 1e-3) / 1e9,
                  "frac_of_peak": c_bytes / (c_ms * 1e-3) / 1e9 / hbm_peak,
+                 "l2": f"{Rc} chunks at distinct positions cycled ({Rc * c_bytes / 1e6:.0f} MB)",
                  "what": "tq_append_kv of one streaming chunk per (sequence, kv-head): quantize "
                          "of the tokens leaving the window (bf16 in, packed out) and the ring "
                          "update (bf16 out)"}

@@ -760,23 +760,6 @@ extern "C" tq_status tq_append_kv(const tq_config* cfg, const void* tables, int 
     if (a.grid_cells <= 0 || a.grid_cells > kMaxGridCells) return TQ_ERR_UNSUPPORTED;
     if (launch_quantize(a, stream) != 0) return TQ_ERR_CUDA;
   }
-  if (W > 0) {
-    for (int kind = 0; kind < 2; ++kind) {
-      WindowScatterArgs w{};
-      w.src = kind == 0 ? k_new : v_new;
-      w.src_f32 = 0;
-      w.sb = src_strides[0];
-      w.sh = src_strides[1];
-      w.st = src_strides[2];
-      w.B = batch;
-      w.H = n_kv_heads;
-      w.n = n_new;
-      w.seq_before = seq_lens_before;
-      w.W = W;
-      w.win = kind == 0 ? k_win : v_win;
-      if (launch_window_scatter(w, stream) != 0) return TQ_ERR_CUDA;
-    }
-  }
   return TQ_OK;
 }
 

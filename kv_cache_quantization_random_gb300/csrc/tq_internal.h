@@ -123,7 +123,8 @@ struct QuantArgs {
   int append;
   const int32_t* seq_before;     // T0 per sequence
   int W;
-  const uint16_t* win;           // bf16 ring [B][H][W][d]
+  uint16_t* win;                 // bf16 ring [B][H][W][d]: leaving tokens are read from it,
+                                 // the new tokens that stay are written into it
   // destination planes
   uint8_t* codes;
   float* norms;
@@ -160,16 +161,6 @@ struct SearchGrid {
   int cells;
 };
 constexpr int kMaxGridCells = 2560;
-
-struct WindowScatterArgs {
-  const void* src;
-  int src_f32;
-  int64_t sb, sh, st;
-  int B, H, n;
-  const int32_t* seq_before;
-  int W;
-  uint16_t* win;
-};
 
 // tq_append_kv for a few new tokens per sequence: one launch does the K and
 // V quantize of the tokens leaving the window and the window ring update.
@@ -257,7 +248,6 @@ struct DecodeArgs {
 int launch_quantize(const QuantArgs& a, void* stream);
 int launch_quantize_qjl(const QuantArgs& a, cudaStream_t stream);   // keys in MSE+QJL mode
 int sm_count();
-int launch_window_scatter(const WindowScatterArgs& a, void* stream);
 int launch_append(const AppendArgs& a, void* stream);
 int launch_dequantize(const DequantArgs& a, void* stream);
 int launch_decode(const DecodeArgs& a, void* stream);

@@ -106,6 +106,8 @@ __global__ void __launch_bounds__(kQRows, F32 ? 1 : 2) quantize_qjl_kernel(const
   for (uint32_t tile = blockIdx.x; tile < ntiles && !failed; tile += gridDim.x, phase ^= 1u) {
     cp_async_wait<0>();
     __syncwarp();
+    // append mode: the ring slots whose tokens this tile has read take the new tokens
+    if (a.append && a.W > 0) ring_copies(a, tile * kQRows + tid, tile * kQRows + tid < total, lane);
     // ---- codes, norm and residual of this thread's key; residual rows of R
     float gamma = 0.f;
     {

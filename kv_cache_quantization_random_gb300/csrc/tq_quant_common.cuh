@@ -80,6 +80,74 @@ __device__ __forceinline__ bool resolve_row(const QuantArgs& a, uint32_t v, cons
   return true;
 }
 
+// Append mode with a window ring: which new token the launch writes into the
+// ring for vector index v, and where.  Slot s of a (sequence, head) ring
+// receives the newest token t of the append with t = s (mod W), if t is among
+// the W newest.  Before the append the slot held the token tau = t - kW just
+// below T0 (if tau >= 0): that token leaves the window, is quantized from the
+// ring by this launch, and the lane that quantizes it writes t once its row
+// has been read.  A slot that held no token (T0 < W) has no reader: the
+// vector indices past the quantized range, one for each such slot, write those.
+// So every slot has one writer, and none is written before its old token has
+// been read.
+__device__ __forceinline__ bool ring_copy_of(const QuantArgs& a, uint32_t v, const uint8_t** csrc,
+                                             uint16_t** cdst) {
+  const uint32_t n = (uint32_t)a.n;
+  const uint32_t bh = v / n;
+  const uint32_t j = v - bh * n;
+  const uint32_t b = bh / (uint32_t)a.H;
+  const uint32_t h = bh - b * (uint32_t)a.H;
+  const long long W = a.W;
+  const long long T0 = a.seq_before[b];
+  const long long T1 = T0 + n;
+  const long long q0 = T0 - W > 0 ? T0 - W : 0;
+  const long long q1 = T1 - W > 0 ? T1 - W : 0;
+  const long long pos = q0 + j;
+  long long slot, t;
+  if (pos < q1) {                          // a quantized token
+    if (pos >= T0 || T1 - 1 - pos < W) return false;   // not in the ring, or no successor
+    slot = pos % W;
+    t = pos + W * ((T1 - 1 - pos) / W);
+  } else {                                 // index j - (q1 - q0) of the empty slots
+    slot = T0 + (pos - q1);
+    if (slot >= W || slot >= T1) return false;
+    t = slot + W * ((T1 - 1 - slot) / W);
+  }
+  *csrc = (const uint8_t*)a.src + ((long long)b * a.sb + (long long)h * a.sh + (t - T0) * a.st) * 2;
+  *cdst = a.win + (((long long)b * a.H + h) * W + slot) * kD;
+  if (kBoundsChecks)
+    return bchk_range(*csrc, kD * 2, a.src, src_extent_bytes(a), a.err) &&
+           bchk_range(*cdst, kD * 2, a.win, ring_bytes(a.B, a.H, a.W), a.err);
+  return true;
+}
+
+// The ring writes of a warp's vectors v (lanes with in_range; see
+// ring_copy_of).  Lane l copies 16-byte chunk l % 16 of the rows of lanes
+// l / 16, l / 16 + 2, ...: all loads first, then all stores, so that the
+// loads' latencies overlap.  Called after the warp's rows have landed in
+// shared memory; not inlined, as only appends with a window take it.
+static __device__ __noinline__ void ring_copies(const QuantArgs& a, uint32_t v, bool in_range,
+                                                   int lane) {
+  const uint8_t* cs = nullptr;
+  uint16_t* cd = nullptr;
+  const bool want = in_range && ring_copy_of(a, v, &cs, &cd);
+  const uint32_t m = __ballot_sync(0xffffffffu, want);
+  if (m == 0u) return;
+  const int c = lane & 15, hf = lane >> 4;
+  uint4 buf[16];
+  uint4* dst[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const int r = 2 * k + hf;
+    const uint4* s = (const uint4*)__shfl_sync(0xffffffffu, (unsigned long long)cs, r);
+    dst[k] = (uint4*)__shfl_sync(0xffffffffu, (unsigned long long)cd, r);
+    buf[k] = (m >> r) & 1u ? __ldg(s + c) : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int k = 0; k < 16; ++k)
+    if ((m >> (2 * k + hf)) & 1u) dst[k][c] = buf[k];
+}
+
 __device__ __forceinline__ float2 lds64f(uint32_t addr) {
   float2 v;
   asm("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));

@@ -28,8 +28,10 @@ __host__ __device__ constexpr size_t quant_smem_bytes(bool f32, int cells, bool 
 
 // SGN: keys in Direct Sign mode also get the sign of every rotated residual
 // coordinate and the scale mean |r_i| ("TurboQuant KV 캐시 압축 for
-// llama.cpp", v1.1.0 "Direct Sign").
-template <int BITS, bool F32, bool CLAMP, bool SGN>
+// llama.cpp", v1.1.0 "Direct Sign").  RING: an append with a window (bf16
+// rows), which also writes the new tokens that stay into the ring (see
+// ring_copy_of); a variant of its own, so that the bulk path carries none of it.
+template <int BITS, bool F32, bool CLAMP, bool SGN, bool RING>
 __global__ void __launch_bounds__(kQRows, 3) quantize_kernel(const QuantArgs a) {
   constexpr int kPitch = RowCfg<F32>::kPitch;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -77,6 +79,8 @@ __global__ void __launch_bounds__(kQRows, 3) quantize_kernel(const QuantArgs a) 
     cp_async_commit();
     cp_async_wait<1>();                  // this lane's copies of `tile` have landed
     __syncwarp();                        // ... and every other lane's
+    // the ring slots whose tokens this tile has read take the new tokens
+    if constexpr (RING) ring_copies(a, tile * 32 + lane, tile * 32 + lane < total, lane);
     const uint8_t* rows = wrows + buf * 32 * kPitch;
     if (valid) {
       float2 p[64];
@@ -92,26 +96,6 @@ __global__ void __launch_bounds__(kQRows, 3) quantize_kernel(const QuantArgs a) 
     valid = nvalid;
   }
   cp_async_wait<0>();
-}
-
-// Window ring update of tq_append_kv: new token t >= T1 - W goes to slot t mod W.
-__global__ void window_scatter_kernel(const WindowScatterArgs a) {
-  const long long rows = (long long)a.B * a.H * a.n;
-  const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long r = gid >> 4;          // 16 threads per row of 128 bf16
-  const int part = (int)(gid & 15);
-  if (r >= rows) return;
-  const int j = (int)(r % a.n);
-  const long long bh = r / a.n;
-  const int h = (int)(bh % a.H);
-  const int b = (int)(bh / a.H);
-  const long long T0 = a.seq_before[b];
-  const long long t = T0 + j;
-  const long long T1 = T0 + a.n;
-  if (t < T1 - a.W) return;              // quantized directly, never enters the ring
-  const uint4* s = (const uint4*)((const uint8_t*)a.src + (b * a.sb + h * a.sh + (long long)j * a.st) * 2);
-  uint4* d = (uint4*)(a.win + (((long long)b * a.H + h) * a.W + t % a.W) * kD);
-  d[part] = s[part];
 }
 
 // ---- tq_append_kv with a few new tokens: one CTA per (sequence, kv-head).
@@ -371,9 +355,9 @@ int sm_count() {
   return n;
 }
 
-template <int BITS, bool F32, bool SGN>
+template <int BITS, bool F32, bool SGN, bool RING>
 static int launch_q(const QuantArgs& a, cudaStream_t s) {
-  auto k = quantize_kernel<BITS, F32, (BITS > 4), SGN>;
+  auto k = quantize_kernel<BITS, F32, (BITS > 4), SGN, RING>;
   const size_t smem = quant_smem_bytes(F32, a.grid_cells, SGN);
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return 1;
@@ -392,8 +376,13 @@ static int launch_q(const QuantArgs& a, cudaStream_t s) {
 template <int BITS>
 static int launch_q_bits(const QuantArgs& a, cudaStream_t s) {
   if (a.qjl) return launch_quantize_qjl(a, s);
-  if (a.dsign) return a.src_f32 ? launch_q<BITS, true, true>(a, s) : launch_q<BITS, false, true>(a, s);
-  return a.src_f32 ? launch_q<BITS, true, false>(a, s) : launch_q<BITS, false, false>(a, s);
+  if (a.append && a.W > 0) {               // the window ring holds bf16 rows
+    if (a.src_f32) return 1;
+    return a.dsign ? launch_q<BITS, false, true, true>(a, s) : launch_q<BITS, false, false, true>(a, s);
+  }
+  if (a.dsign)
+    return a.src_f32 ? launch_q<BITS, true, true, false>(a, s) : launch_q<BITS, false, true, false>(a, s);
+  return a.src_f32 ? launch_q<BITS, true, false, false>(a, s) : launch_q<BITS, false, false, false>(a, s);
 }
 
 int launch_quantize(const QuantArgs& a, void* stream) {
@@ -405,13 +394,6 @@ int launch_quantize(const QuantArgs& a, void* stream) {
     case 8: return launch_q_bits<8>(a, s);
   }
   return 1;
-}
-
-int launch_window_scatter(const WindowScatterArgs& a, void* stream) {
-  const long long threads = (long long)a.B * a.H * a.n * 16;
-  const int block = 256;
-  window_scatter_kernel<<<(unsigned)((threads + block - 1) / block), block, 0, (cudaStream_t)stream>>>(a);
-  return cudaGetLastError() != cudaSuccess;
 }
 
 int launch_append(const AppendArgs& a, void* stream) {
