@@ -736,9 +736,10 @@ extern "C" tq_status tq_append_kv(const tq_config* cfg, const void* tables, int 
     return launch_append(a, stream) != 0 ? TQ_ERR_CUDA : TQ_OK;
   }
   if ((long long)batch * n_kv_heads * n_new >= (1ll << 31)) return TQ_ERR_UNSUPPORTED;
+  QuantArgs qa[2] = {};
   for (int kind = 0; kind < 2; ++kind) {
     const tq_planes& p = kind == 0 ? k : v;
-    QuantArgs a{};
+    QuantArgs& a = qa[kind];
     a.src = kind == 0 ? k_new : v_new;
     a.src_f32 = src_dtype == TQ_F32;
     a.sb = src_strides[0];
@@ -758,8 +759,13 @@ extern "C" tq_status tq_append_kv(const tq_config* cfg, const void* tables, int 
     a.cap = p.capacity;
     fill_quant_codec(a, cfg, tables, layer, kind);
     if (a.grid_cells <= 0 || a.grid_cells > kMaxGridCells) return TQ_ERR_UNSUPPORTED;
-    if (launch_quantize(a, stream) != 0) return TQ_ERR_CUDA;
   }
+  // one launch for both kinds when they share the kernel variant's shape
+  if (!qa[0].src_f32 && !qa[0].qjl && !qa[1].qjl && !qa[1].dsign && qa[0].bits == qa[1].bits &&
+      qa[0].grid_cells == qa[1].grid_cells)
+    return launch_quantize_kv(qa[0], qa[1], stream) != 0 ? TQ_ERR_CUDA : TQ_OK;
+  for (int kind = 0; kind < 2; ++kind)
+    if (launch_quantize(qa[kind], stream) != 0) return TQ_ERR_CUDA;
   return TQ_OK;
 }
 

@@ -246,6 +246,9 @@ struct DecodeArgs {
 
 // ---- launchers (defined in the .cu files) -------------------------------------
 int launch_quantize(const QuantArgs& a, void* stream);
+// keys and values of an append in one launch: bf16 rows, neither kind in QJL
+// mode, the same bit width and search grid (tq_append_kv checks)
+int launch_quantize_kv(const QuantArgs& ak, const QuantArgs& av, void* stream);
 int launch_quantize_qjl(const QuantArgs& a, cudaStream_t stream);   // keys in MSE+QJL mode
 int sm_count();
 int launch_append(const AppendArgs& a, void* stream);

@@ -31,8 +31,9 @@ __host__ __device__ constexpr size_t quant_smem_bytes(bool f32, int cells, bool 
 // llama.cpp", v1.1.0 "Direct Sign").  RING: an append with a window (bf16
 // rows), which also writes the new tokens that stay into the ring (see
 // ring_copy_of); a variant of its own, so that the bulk path carries none of it.
+// (the tiles that CTA `cta` of the `ncta` working on `a` takes)
 template <int BITS, bool F32, bool CLAMP, bool SGN, bool RING>
-__global__ void __launch_bounds__(kQRows, 3) quantize_kernel(const QuantArgs a) {
+__device__ __forceinline__ void quantize_tiles(const QuantArgs& a, uint32_t cta, uint32_t ncta) {
   constexpr int kPitch = RowCfg<F32>::kPitch;
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -54,8 +55,8 @@ __global__ void __launch_bounds__(kQRows, 3) quantize_kernel(const QuantArgs a) 
   // every warp streams its own tiles of 32 vectors: no CTA barrier below
   const uint32_t total = (uint32_t)a.B * (uint32_t)a.H * (uint32_t)a.n;
   const uint32_t ntiles = (total + 31) / 32;
-  const uint32_t stride = gridDim.x * (kQRows / 32);
-  uint32_t tile = blockIdx.x * (kQRows / 32) + warp;
+  const uint32_t stride = ncta * (kQRows / 32);
+  uint32_t tile = cta * (kQRows / 32) + warp;
   const void* src = nullptr;
   long long drow = 0;
   bool valid = false;
@@ -96,6 +97,24 @@ __global__ void __launch_bounds__(kQRows, 3) quantize_kernel(const QuantArgs a) 
     valid = nvalid;
   }
   cp_async_wait<0>();
+}
+
+template <int BITS, bool F32, bool CLAMP, bool SGN, bool RING>
+__global__ void __launch_bounds__(kQRows, 3) quantize_kernel(const QuantArgs a) {
+  quantize_tiles<BITS, F32, CLAMP, SGN, RING>(a, blockIdx.x, gridDim.x);
+}
+
+// An append of both kinds in one launch (bf16 rows, keys and values of the
+// same bit width, so that one search grid size serves both): CTAs below nk
+// take the keys, the others the values.  For a streaming chunk of a few
+// thousand tokens per head each kind alone fills about half an SM wave.
+template <int BITS, bool SGN, bool RING>
+__global__ void __launch_bounds__(kQRows, 3)
+    quantize_kv_kernel(const QuantArgs ak, const QuantArgs av, uint32_t nk) {
+  if (blockIdx.x < nk)
+    quantize_tiles<BITS, false, (BITS > 4), SGN, RING>(ak, blockIdx.x, nk);
+  else
+    quantize_tiles<BITS, false, (BITS > 4), false, RING>(av, blockIdx.x - nk, gridDim.x - nk);
 }
 
 // ---- tq_append_kv with a few new tokens: one CTA per (sequence, kv-head).
@@ -383,6 +402,48 @@ static int launch_q_bits(const QuantArgs& a, cudaStream_t s) {
   if (a.dsign)
     return a.src_f32 ? launch_q<BITS, true, true, false>(a, s) : launch_q<BITS, false, true, false>(a, s);
   return a.src_f32 ? launch_q<BITS, true, false, false>(a, s) : launch_q<BITS, false, false, false>(a, s);
+}
+
+template <int BITS, bool SGN, bool RING>
+static int launch_qkv(const QuantArgs& ak, const QuantArgs& av, cudaStream_t s) {
+  auto k = quantize_kv_kernel<BITS, SGN, RING>;
+  const size_t smem = quant_smem_bytes(false, ak.grid_cells, SGN);
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return 1;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kQRows, smem) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  // CTAs in proportion to each kind's tiles of 128 vectors, at least one each
+  const long long tk = ((long long)ak.B * ak.H * ak.n + kQRows - 1) / kQRows;
+  const long long tv = ((long long)av.B * av.H * av.n + kQRows - 1) / kQRows;
+  long long grid = (long long)sm_count() * per_sm;
+  if (grid > tk + tv) grid = tk + tv;
+  if (grid < 2) grid = 2;
+  long long nk = (grid * tk + (tk + tv) / 2) / (tk + tv);
+  if (nk < 1) nk = 1;
+  if (nk > grid - 1) nk = grid - 1;
+  k<<<(unsigned)grid, kQRows, smem, s>>>(ak, av, (uint32_t)nk);
+  return cudaGetLastError() != cudaSuccess;
+}
+
+template <int BITS>
+static int launch_qkv_bits(const QuantArgs& ak, const QuantArgs& av, cudaStream_t s) {
+  const bool ring = ak.append && ak.W > 0;
+  if (ak.dsign)
+    return ring ? launch_qkv<BITS, true, true>(ak, av, s) : launch_qkv<BITS, true, false>(ak, av, s);
+  return ring ? launch_qkv<BITS, false, true>(ak, av, s) : launch_qkv<BITS, false, false>(ak, av, s);
+}
+
+int launch_quantize_kv(const QuantArgs& ak, const QuantArgs& av, void* stream) {
+  cudaStream_t s = (cudaStream_t)stream;
+  switch (ak.bits) {
+    case 2: return launch_qkv_bits<2>(ak, av, s);
+    case 3: return launch_qkv_bits<3>(ak, av, s);
+    case 4: return launch_qkv_bits<4>(ak, av, s);
+    case 8: return launch_qkv_bits<8>(ak, av, s);
+  }
+  return 1;
 }
 
 int launch_quantize(const QuantArgs& a, void* stream) {
