@@ -432,7 +432,6 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
   __shared__ uint32_t slut[4];                   // (+-1, +-1) fp16 pairs of two sign bits
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr bool QJL = RES == 1;        // QJL sketch of the key residual
-  constexpr bool SGN = RES == 2;        // Direct Sign key residual
   constexpr bool HAS_RES = RES != 0;
   // G <= 4 query heads leave half of the 8 MMA columns free: they carry the
   // query's lo part (see score_ktile)
@@ -467,6 +466,15 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
   const int Hkv = a.Hkv;
   const uint32_t limit = a.wait_limit ? a.wait_limit : kDefaultWaitLimit;
   const int mg = lane >> 2, tig = lane & 3;   // MMA group / thread-in-group
+
+  // A kernel launched after this one with programmatic dependent launch (the
+  // next decode) may start its CTAs as soon as SMs free up and build its
+  // tables while this grid's last CTAs merge; it still waits
+  // (griddepcontrol.wait) for this grid to complete before it reads anything
+  // this grid writes.  Only for one wave of one CTA per SM (a.pdl_trigger):
+  // with two CTAs per SM or several waves, the early CTAs slowed this grid's
+  // own (measured).
+  if (a.pdl_trigger) asm volatile("griddepcontrol.launch_dependents;");
 
   // ------------------------------------------------------------- prologue
   // The codec tables are loaded and the lookup tables built before the
@@ -543,7 +551,20 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
   }
   if (tid < 4) slut[tid] = ((tid & 2) ? 0x3C000000u : 0xBC000000u) | ((tid & 1) ? 0x3C00u : 0xBC00u);
 
-
+  // this pair's plane rows and this split's first token
+  const long long row0 = ((long long)b * Hkv + kvh);
+  const uint8_t* kc = a.kc + row0 * a.kcap * KROW;
+  const uint8_t* vc = a.vc + row0 * a.vcap * VROW;
+  const float* knp = a.kn + row0 * a.kcap;
+  const float* vnp = a.vn + row0 * a.vcap;
+  const uint8_t* ksp = HAS_RES ? a.ks + row0 * a.kcap * 16 : nullptr;
+  const float* krp = HAS_RES ? a.kr + row0 * a.kcap : nullptr;
+  const int t_begin = split * a.split_tokens;
+  // L2 prefetch of the codes of this warp's first chunks, before the wait: the
+  // rows the plan gives this split for the longest sequence (the real length
+  // is not known yet).  A prefetch only warms L2, so it is safe on rows the
+  // previous kernel may still be writing; it brings the first chunks' HBM
+  // latency forward, under the previous kernel's tail.
   // everything below may read what the previous kernel on the stream wrote
   // (sequence lengths, query, planes, window ring, workspace): wait for it
   // to finish.  In a decode step (a.step_new > 0) the previous kernel is the
@@ -560,17 +581,9 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
     T = 0;
   }
   const int nq = T - W > 0 ? T - W : 0;
-  // this split's token range and plane rows (quantized splits)
-  const int t_begin = split * a.split_tokens;
+  // this split's token range (quantized splits)
   int t_end = t_begin + a.split_tokens;
   if (t_end > nq) t_end = nq;
-  const long long row0 = ((long long)b * Hkv + kvh);
-  const uint8_t* kc = a.kc + row0 * a.kcap * KROW;
-  const uint8_t* vc = a.vc + row0 * a.vcap * VROW;
-  const float* knp = a.kn + row0 * a.kcap;
-  const float* vnp = a.vn + row0 * a.vcap;
-  const uint8_t* ksp = HAS_RES ? a.ks + row0 * a.kcap * 16 : nullptr;
-  const float* krp = HAS_RES ? a.kr + row0 * a.kcap : nullptr;
 
   // chunk c0 -> ring slot: codes by bulk copy; norms by bulk copy when the
   // 16-byte-rounded range stays inside the plane, else by plain loads

@@ -889,6 +889,10 @@ static tq_status decode_prepare(const tq_config* cfg, const void* tables, int la
   a.split_tokens = p.split_tokens;
   a.wsplit_tokens = p.wsplit_tokens;
   a.long_first = p.long_first;
+  {
+    const int res = a.qjl ? 1 : a.dsign ? 2 : 0;
+    a.pdl_trigger = !p.long_first && decode_ctas_per_sm(G, s.k_bits, s.v_bits, res) == 1;
+  }
   a.ck = (const float*)tbl_codebook(tables, s.k_bits);
   a.cv = (const float*)tbl_codebook(tables, s.v_bits);
   a.sk = tbl_signs(cfg, tables, layer, 0);

@@ -231,6 +231,8 @@ struct DecodeArgs {
   int wsplit_tokens;             // window tokens per window split
   int long_first;                // CTA order: all quantized splits before the window
                                  // splits (several waves), else split-major per pair
+  int pdl_trigger;               // one wave of one CTA per SM: let the next decode's
+                                 // CTAs start early (griddepcontrol.launch_dependents)
   // codec
   const float* ck; const float* cv;
   const float* sk; const float* sv;
