@@ -656,6 +656,9 @@ def run_single(args, w, rank, world, local):
             "traffic": (args.decode_traffic if args.decode_traffic is not None
                         else captured_traffic("decode_kernel", w.name)),
             "bytes_per_launch": dec_bytes, "launch_ms": dec_ms,
+            "note": "launch_ms = a CUDA graph of decode launches back to back, over cache replicas, "
+                    "divided by the launches; a one-wave grid lets the next launch's CTAs build "
+                    "their tables while its last CTAs merge",
         },
         "decode": {"ms": dec_ms, "gbs": dec_gbs, "frac_of_peak": dec_gbs / hbm_peak,
                    "tokens_per_s": tokens_per_step / (dec_ms * 1e-3), "bytes": dec_bytes},
