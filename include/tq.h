@@ -311,11 +311,17 @@ tq_status tq_decode_attention_multi(const tq_config* cfg, const void* tables, in
  * + 1 tokens of every sequence, with the same arguments and results as those
  * two calls ("[GitHub 탐방] TurboQuant 3-bit KV 캐시 압축 — 단일 GPU 재현 기록",
  * "실험 설계": the newest tokens stay in the bf16 window).  max_seq_len bounds
- * seq_lens_before[b] + 1.  Two launches: the decode starts while the append
- * runs and waits for it only before it reads what the append writes (the
- * window ring, the plane rows from max(seq_lens_before[b] - W, 0) on); with at
- * most 16 (sequence, kv-head) pairs and short splits the decode leaves the
- * append's CTA slots free.  The planes, ring and workspace must not be used by other work on the
+ * seq_lens_before[b] + 1.  With a window (W > 0) and keys in MSE or Direct
+ * Sign mode this is one launch: the quantized splits stop before the token
+ * leaving the window, and each pair's first window split quantizes that token
+ * from its ring slot into the planes (the same warp-per-vector quantizer, and
+ * so the same codes, as tq_append_kv), attends to its dequantized key and
+ * value, and writes the new token into the slot; the window splits read the
+ * new token from k_new / v_new, which must then be bf16.  Otherwise (QJL keys,
+ * or W = 0) two launches: the append kernel, and the decode, which starts
+ * while the append runs and waits for it only before it reads what the append
+ * writes (the window ring, the plane rows from max(seq_lens_before[b] - W, 0)
+ * on).  The planes, ring and workspace must not be used by other work on the
  * device meanwhile. */
 tq_status tq_decode_step(const tq_config* cfg, const void* tables, int layer, const void* q,
                          int q_dtype, float softmax_scale, int batch, int n_q_heads,

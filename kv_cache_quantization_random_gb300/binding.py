@@ -354,7 +354,8 @@ def tq_decode_step(cfg: Config, tables, layer: int, q, softmax_scale: float, k_n
                    k_win=None, v_win=None, stream=None):
     """tq_append_kv of one token per (sequence, kv-head) (k_new, v_new
     [B, Hkv, 1, d]) followed by tq_decode_attention over seq_lens_before + 1
-    tokens, as one call (the decode overlaps the append)."""
+    tokens, as one call (one launch with a window and keys in MSE or Direct
+    Sign mode)."""
     B, Hq, _ = q.shape
     H = k_new.shape[1]
     if v_new.shape != k_new.shape or v_new.stride() != k_new.stride() or k_new.shape[2] != 1:

@@ -39,6 +39,7 @@
 #include <stdint.h>
 
 #include "tq_device.cuh"
+#include "tq_quant_common.cuh"
 
 namespace tq {
 
@@ -420,6 +421,71 @@ __device__ __forceinline__ void qjl_scores(uint32_t sa, uint32_t sb, const uint3
   }
 }
 
+// Decode step in one launch (DecodeArgs::fused_step, W > 0): the token L =
+// T - 1 - W that leaves the window, handled by warp 0 of its pair's first
+// window split.  The warp reads L's bf16 rows from ring slot L mod W,
+// quantizes them into plane row L (codes, norm and, for Direct Sign keys, the
+// residual signs and scale: the same warp-per-vector quantizer as
+// tq_append_kv), writes the new token T - 1 into that slot, and returns L's
+// dequantized key and value (lane l: coordinates 4l..4l+3) for the window
+// split to attend to: the quantized splits of this launch stop before row L,
+// so no CTA waits for another.  The boundaries (2 KB) and 32 words of packing
+// scratch sit at byte scr of the dynamic shared memory.  Not inlined: it runs
+// once per pair, off the main loop.
+static __device__ __noinline__ void step_leaving_token(const DecodeArgs& a, long long pair, int L,
+                                                       int scr, const float* kcen,
+                                                       const float* vcen, float* kx, float* vx,
+                                                       int lane) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const float* bnd = (const float*)(smem + scr);
+  uint32_t* words = (uint32_t*)(smem + scr + 2048);
+  const long long ring = (pair * a.W + L % a.W) * kD2;
+  const long long kr = pair * a.kcap + L, vr = pair * a.vcap + L;
+  uint8_t* kc = (uint8_t*)a.kc + kr * 16 * a.kb;
+  uint8_t* vc = (uint8_t*)a.vc + vr * 16 * a.vb;
+  const size_t ring_bytes_ = (size_t)a.B * a.Hkv * a.W * kD2 * 2;
+  if (!bchk_range(kc, 16 * a.kb, a.kc, (size_t)a.B * a.Hkv * a.kcap * 16 * a.kb, a.err) ||
+      !bchk_range(vc, 16 * a.vb, a.vc, (size_t)a.B * a.Hkv * a.vcap * 16 * a.vb, a.err) ||
+      !bchk_range(a.kwin + ring, kD2 * 2, a.kwin, ring_bytes_, a.err)) {
+    for (int c = 0; c < 4; ++c) kx[c] = vx[c] = 0.f;
+    return;
+  }
+  // all four rows' loads first (the leaving token's key and value, the new
+  // token's key and value), so that their latencies overlap
+  const long long noff = (pair / a.Hkv) * a.nsb + (pair % a.Hkv) * a.nsh;
+  const uint2 kold = ((const uint2*)(a.kwin + ring))[lane];
+  const uint2 vold = ((const uint2*)(a.vwin + ring))[lane];
+  const uint2 knw = ((const uint2*)((const uint16_t*)a.knew + noff))[lane];
+  const uint2 vnw = ((const uint2*)((const uint16_t*)a.vnew + noff))[lane];
+  const float4 sk = __ldg((const float4*)a.sk + lane), sv = __ldg((const float4*)a.sv + lane);
+  const float sks[4] = {sk.x, sk.y, sk.z, sk.w}, svs_[4] = {sv.x, sv.y, sv.z, sv.w};
+  float r[4], yq[4], t[4];
+  // keys: quantize, then dequantize as a reader of the planes would (norm x
+  // centroid, plus the Direct Sign term; inverse rotation H / sqrt(d); signs)
+  float x[4] = {bf16lo(kold.x), bf16hi(kold.x), bf16lo(kold.y), bf16hi(kold.y)};
+  const float nk = warp_quantize_vals(x, sk, a.kb, bnd, kcen, kc, (float*)a.kn + kr, words, lane,
+                                      r, yq);
+  float sc = 0.f;
+  if (a.dsign) sc = warp_direct_sign(r, (uint8_t*)a.ks + kr * 16, (float*)a.kr + kr, lane);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) t[c] = nk * yq[c] + (a.dsign ? (r[c] >= 0.f ? sc : -sc) : 0.f);
+  warp_fwht4(t, lane);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) kx[c] = t[c] * 0.08838834764831845f * sks[c];
+  // values
+  x[0] = bf16lo(vold.x); x[1] = bf16hi(vold.x); x[2] = bf16lo(vold.y); x[3] = bf16hi(vold.y);
+  const float nv = warp_quantize_vals(x, sv, a.vb, bnd + 256, vcen, vc, (float*)a.vn + vr, words,
+                                      lane, r, yq);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) t[c] = nv * yq[c];
+  warp_fwht4(t, lane);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) vx[c] = t[c] * 0.08838834764831845f * svs_[c];
+  // the new token into the slot (each lane rewrites the 8 bytes it read)
+  ((uint2*)((uint16_t*)a.kwin + ring))[lane] = knw;
+  ((uint2*)((uint16_t*)a.vwin + ring))[lane] = vnw;
+}
+
 template <int G, int KB, int VB, int RES, bool SPARSE>
 __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
                                   decode_ctas_per_sm(G, KB, VB, RES))
@@ -483,6 +549,17 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
   // flight, and each warp's later chunks follow the CTA barrier of the query
   // scale, so that the first chunks of all warps are not queued behind them.
   __shared__ float cks[256], cvs[256];
+  // fused decode step: the codebooks' boundaries and 32 words of packing
+  // scratch after the dynamic shared memory (see step_leaving_token)
+  constexpr int kScr = (L.total + 127) & ~127;
+  if (a.fused_step) {
+    float* qbnd = (float*)(smem + kScr);           // [2][256]
+    for (int i = tid; i < 256; i += kDT) {
+      qbnd[i] = __ldg(a.ck + 256 + i);
+      qbnd[256 + i] = __ldg(a.cv + 256 + i);
+    }
+    if (tid < 32) ((uint32_t*)(smem + kScr + 2048))[tid] = 0u;
+  }
   const int W = a.W;
   const bool window_split = split >= a.n_qsplits;
   constexpr int GW = (G + kDWarps - 1) / kDWarps;   // query heads rotated per warp
@@ -572,7 +649,8 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
   // max(nq - step_new, 0) on: window splits wait here, quantized splits only
   // before the copy of a chunk that reaches row t_end - step_new of their
   // range (see issue; t_end <= nq, so that covers those rows).
-  if (a.step_new == 0 || window_split) asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (a.step_new == 0 || a.fused_step || window_split)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
   int T = *bchk(a.seq_lens + b, a.seq_lens, (size_t)a.B * 4, a.err) + a.step_new;
   // a length outside the plan's range would read past this pair's plane rows
   // or ring: flag it and decode the sequence as empty
@@ -581,9 +659,10 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
     T = 0;
   }
   const int nq = T - W > 0 ? T - W : 0;
-  // this split's token range (quantized splits)
+  // this split's token range (quantized splits); in a fused decode step the
+  // window split takes row nq - 1, the token leaving the window
   int t_end = t_begin + a.split_tokens;
-  if (t_end > nq) t_end = nq;
+  if (t_end > nq - a.fused_step) t_end = nq - a.fused_step;
 
   // chunk c0 -> ring slot: codes by bulk copy; norms by bulk copy when the
   // 16-byte-rounded range stays inside the plane, else by plain loads
@@ -591,7 +670,7 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
     const int nv = t_end - c0 < 32 ? t_end - c0 : 32;
     const int n4 = (nv + 3) & ~3;
     // warp-uniform: rows the step's append may still be writing
-    if (a.step_new > 0 && c0 + n4 > t_end - a.step_new)
+    if (a.step_new > 0 && !a.fused_step && c0 + n4 > t_end - a.step_new)
       asm volatile("griddepcontrol.wait;" ::: "memory");
     // bulk copies need 16-byte aligned sources: the norm rows of a (sequence,
     // head) start at row0 * capacity floats, aligned only if capacity % 4 == 0
@@ -1195,47 +1274,86 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
     const int kw0 = a.wsplit_tokens * (split - a.n_qsplits);   // this split's share
     const int kw1 = kw0 + a.wsplit_tokens < nw ? kw0 + a.wsplit_tokens : nw;
     const long long base = ((long long)b * Hkv + kvh) * W;
+    // one token's key and value (lane l: coordinates 4l..4l+3, original
+    // domain) into the warp's online softmax state
+    auto attend = [&](const float (&kx)[4], const float (&vx)[4], int tpos) {
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        // several query tokens per sequence: column g is query token g % n_q
+        // at position T - n_q + g % n_q, which sees tokens up to itself
+        // (branch-free, so the per-column state stays in registers)
+        const bool vis = tpos <= T - a.n_q + g % a.n_q;
+        float part = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          part = fmaf(*bchk(qo + (4 * lane + j) * G + g, qo, kD2 * G * 4, a.err), kx[j], part);
+        const float s = warp_sum(part);
+        const float mnew = vis ? fmaxf(m[g], s) : m[g];
+        const float al = vis ? ex2(m[g] - mnew) : 1.f;
+        const float p = vis ? ex2(s - mnew) : 0.f;
+        l[g] = fmaf(l[g], al, p);
+        m[g] = mnew;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) ow[g][j] = fmaf(p, vx[j], ow[g][j] * al);
+      }
+    };
+    // fused decode step: the new token T - 1 is read from the step's input (its
+    // ring slot is written in this launch).  The pair's first window split also
+    // takes the token leaving the window (row nq - 1, see step_leaving_token)
+    // or, when none leaves (T <= W), writes the new token into slot T - 1,
+    // which held none
+    const uint16_t* knrow = nullptr;
+    const uint16_t* vnrow = nullptr;
+    if (a.fused_step && T >= 1) {
+      const long long noff = (long long)b * a.nsb + (long long)kvh * a.nsh;
+      knrow = (const uint16_t*)a.knew + noff;
+      vnrow = (const uint16_t*)a.vnew + noff;
+      if (split == a.n_qsplits && warp == 0) {
+        if (nq > 0) {
+          float kx[4], vx[4];
+          step_leaving_token(a, (long long)b * Hkv + kvh, nq - 1, kScr, cks, cvs, kx, vx, lane);
+          attend(kx, vx, nq - 1);
+        } else {
+          uint2* dk = (uint2*)(a.kwin + (base + T - 1) * kD2) + lane;
+          uint2* dv = (uint2*)(a.vwin + (base + T - 1) * kD2) + lane;
+          const size_t rb = (size_t)a.B * Hkv * W * kD2 * 2;
+          if (bchk_range(dk, 8, a.kwin, rb, a.err) && bchk_range(dv, 8, a.vwin, rb, a.err)) {
+            *dk = ((const uint2*)knrow)[lane];
+            *dv = ((const uint2*)vnrow)[lane];
+          }
+        }
+      }
+    }
     // warp w takes window tokens w, w + warps, ...; 8 tokens' rows are loaded
-    // before any is used, so the loads overlap instead of paying one latency each
-    for (int k0 = kw0 + warp; k0 < kw1; k0 += 8 * kDWarps) {
+    // before any is used, so the loads overlap instead of paying one latency
+    // each.  Warp 0 of a split that took the leaving token takes none.
+    const bool took = a.fused_step && T >= 1 && nq > 0 && split == a.n_qsplits;
+    const int ww = took ? warp - 1 : warp, nww = took ? kDWarps - 1 : kDWarps;
+    for (int k0 = kw0 + ww; ww >= 0 && k0 < kw1; k0 += 8 * nww) {
       uint2 kw[8], vw[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int k = k0 + u * kDWarps;
+        const int k = k0 + u * nww;
         if (k < kw1) {
           const long long slotrow = (base + (tw0 + k) % W) * kD2;
-          // this pair's W ring rows
-          kw[u] = *bchk((const uint2*)(a.kwin + slotrow + 4 * lane), a.kwin + base * kD2,
-                        (size_t)W * kD2 * 2, a.err);
-          vw[u] = *bchk((const uint2*)(a.vwin + slotrow + 4 * lane), a.vwin + base * kD2,
-                        (size_t)W * kD2 * 2, a.err);
+          if (knrow != nullptr && tw0 + k == T - 1) {
+            kw[u] = ((const uint2*)knrow)[lane];
+            vw[u] = ((const uint2*)vnrow)[lane];
+          } else {
+            // this pair's W ring rows
+            kw[u] = *bchk((const uint2*)(a.kwin + slotrow + 4 * lane), a.kwin + base * kD2,
+                          (size_t)W * kD2 * 2, a.err);
+            vw[u] = *bchk((const uint2*)(a.vwin + slotrow + 4 * lane), a.vwin + base * kD2,
+                          (size_t)W * kD2 * 2, a.err);
+          }
         }
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        if (k0 + u * kDWarps >= kw1) break;
+        if (k0 + u * nww >= kw1) break;
         const float kx[4] = {bf16lo(kw[u].x), bf16hi(kw[u].x), bf16lo(kw[u].y), bf16hi(kw[u].y)};
         const float vx[4] = {bf16lo(vw[u].x), bf16hi(vw[u].x), bf16lo(vw[u].y), bf16hi(vw[u].y)};
-        const int tpos = tw0 + k0 + u * kDWarps;      // token position
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          // several query tokens per sequence: column g is query token g % n_q
-          // at position T - n_q + g % n_q, which sees tokens up to itself
-          // (branch-free, so the per-column state stays in registers)
-          const bool vis = tpos <= T - a.n_q + g % a.n_q;
-          float part = 0.f;
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            part = fmaf(*bchk(qo + (4 * lane + j) * G + g, qo, kD2 * G * 4, a.err), kx[j], part);
-          const float s = warp_sum(part);
-          const float mnew = vis ? fmaxf(m[g], s) : m[g];
-          const float al = vis ? ex2(m[g] - mnew) : 1.f;
-          const float p = vis ? ex2(s - mnew) : 0.f;
-          l[g] = fmaf(l[g], al, p);
-          m[g] = mnew;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) ow[g][j] = fmaf(p, vx[j], ow[g][j] * al);
-        }
+        attend(kx, vx, tw0 + k0 + u * nww);
       }
     }
     __syncthreads();
@@ -1440,8 +1558,10 @@ template <int G, int KB, int VB, int RES, bool SPARSE = false>
 int launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
   auto k = decode_kernel<G, KB, VB, RES, SPARSE>;
   constexpr int kWarps = decode_warps(G, KB, VB, RES);
-  const size_t smem = (size_t)DecodeSmem(G, RES, KB, VB, kWarps).total;
-  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+  const size_t base = (size_t)DecodeSmem(G, RES, KB, VB, kWarps).total;
+  const size_t smem = base + (a.fused_step ? kFusedScratchBytes : 0);
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)(base + kFusedScratchBytes)) != cudaSuccess)
     return 1;
   // programmatic dependent launch: the CTAs may start while the previous
   // kernel on the stream is still running; they read only the codec tables

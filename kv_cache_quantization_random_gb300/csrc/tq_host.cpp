@@ -967,16 +967,43 @@ extern "C" tq_status tq_decode_step(const tq_config* cfg, const void* tables, in
                                     void* stream) {
   if (batch == 0) return TQ_OK;
   if (max_seq_len < 1) return TQ_ERR_INVALID_ARG;
-  // the append's CTAs (one per sequence and kv-head) run beside the decode's
-  // first wave: with few of them and short splits, the decode leaves their
-  // slots free
+  tq_status st = check_gpu_common(cfg, tables, layer);
+  if (st != TQ_OK) return st;
+  if (spec_of(cfg, layer).k_mode != TQ_MODE_MSE_QJL && cfg->residual_window > 0) {
+    // one launch: the decode kernel appends the step's token itself (see
+    // DecodeArgs::fused_step); the inputs are checked as tq_append_kv checks them
+    if (!k_new || !v_new || !src_strides || !k_win || !v_win) return TQ_ERR_INVALID_ARG;
+    if (src_dtype != TQ_BF16 && src_dtype != TQ_F32) return TQ_ERR_INVALID_ARG;
+    if (src_dtype != TQ_BF16) return TQ_ERR_UNSUPPORTED;             // the ring is bf16
+    if (!aligned16(k_win) || !aligned16(v_win)) return TQ_ERR_ALIGNMENT;
+    if (!aligned16(k_new) || !aligned16(v_new)) return TQ_ERR_ALIGNMENT;
+    for (int i = 0; i < 2; ++i)
+      if (src_strides[i] < 0 || (src_strides[i] * 2) % 16 != 0) return TQ_ERR_ALIGNMENT;
+    DecodeArgs a{};
+    bool empty = false;
+    st = decode_prepare(cfg, tables, layer, q, q_dtype, softmax_scale, batch, n_q_heads, n_kv_heads,
+                        1, k, v, k_win, v_win, seq_lens_before, max_seq_len, out, workspace,
+                        workspace_bytes, 1, 0, &a, &empty);
+    if (st != TQ_OK) return st;
+    if (empty) return TQ_ERR_INVALID_ARG;            // unreachable with max_seq_len >= 1
+    a.fused_step = 1;
+    a.knew = k_new;
+    a.vnew = v_new;
+    a.new_f32 = 0;
+    a.nsb = src_strides[0];
+    a.nsh = src_strides[1];
+    return launch_decode(a, stream) == 0 ? TQ_OK : TQ_ERR_CUDA;
+  }
+  // keys in QJL mode, or no window: the append kernel, then the decode.  The
+  // append's CTAs (one per sequence and kv-head) run beside the decode's first
+  // wave: with few of them and short splits, the decode leaves their slots free
   const long long units = (long long)batch * n_kv_heads;
   const int reserve = units > 0 && units <= 16 ? (int)units : 0;
   DecodeArgs a{};
   bool empty = false;
-  tq_status st = decode_prepare(cfg, tables, layer, q, q_dtype, softmax_scale, batch, n_q_heads,
-                                n_kv_heads, 1, k, v, k_win, v_win, seq_lens_before, max_seq_len,
-                                out, workspace, workspace_bytes, 1, reserve, &a, &empty);
+  st = decode_prepare(cfg, tables, layer, q, q_dtype, softmax_scale, batch, n_q_heads, n_kv_heads,
+                      1, k, v, k_win, v_win, seq_lens_before, max_seq_len, out, workspace,
+                      workspace_bytes, 1, reserve, &a, &empty);
   if (st != TQ_OK) return st;
   if (empty) return TQ_ERR_INVALID_ARG;              // unreachable with max_seq_len >= 1
   st = tq_append_kv(cfg, tables, layer, k_new, v_new, src_dtype, src_strides, batch, n_kv_heads,

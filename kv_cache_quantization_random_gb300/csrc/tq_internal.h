@@ -68,8 +68,12 @@ struct DecodeSmem {
 };
 
 // dynamic shared memory a decode CTA may use (227 KB per CTA, less the
-// kernel's static tables)
+// kernel's static tables and a fused decode step's scratch)
 constexpr int kDecodeSmemBudget = 216 * 1024;
+// a fused decode step's scratch after the CTA's dynamic shared memory (see
+// step_leaving_token): 128-byte alignment slack, two codebooks' boundaries
+// and 32 words of packing scratch
+constexpr int kFusedScratchBytes = 128 + 2 * 256 * 4 + 32 * 4;
 
 // Warps of a decode CTA.  G <= 4 query columns with MSE keys (about 168
 // registers a thread): one CTA per SM of 12 warps, or 8 when 12 staging
@@ -233,6 +237,17 @@ struct DecodeArgs {
                                  // splits (several waves), else split-major per pair
   int pdl_trigger;               // one wave of one CTA per SM: let the next decode's
                                  // CTAs start early (griddepcontrol.launch_dependents)
+  // decode step in one launch (fused_step = 1, step_new = 1, W > 0): the
+  // kernel also appends the step's token.  The quantized splits stop before
+  // plane row T - 1 - W (the token leaving the window); the pair's first window
+  // split quantizes that token from its ring slot into the planes, attends to
+  // its dequantized key and value, and writes the new token into the slot;
+  // the window splits read the new token from knew / vnew.  Keys in MSE or
+  // Direct Sign mode.
+  int fused_step;
+  const void* knew; const void* vnew;   // [B][Hkv][.][d] bf16 rows
+  int new_f32;                   // unused (the ring, and so the fused step, is bf16)
+  int64_t nsb, nsh;              // element strides of knew / vnew (batch, head)
   // codec
   const float* ck; const float* cv;
   const float* sk; const float* sv;

@@ -366,6 +366,111 @@ __device__ __forceinline__ float quantize_row(const QuantArgs& a, const uint8_t*
   return nrm;
 }
 
+// Unnormalised Walsh-Hadamard transform (Sylvester order) of 128 values held
+// by a warp, lane l holding 4l..4l+3: stages 1 and 2 inside the lane, 4..64
+// across lanes.
+__device__ __forceinline__ void warp_fwht4(float (&x)[4], int lane) {
+  const float t0 = x[0] + x[1], t1 = x[0] - x[1], t2 = x[2] + x[3], t3 = x[2] - x[3];
+  x[0] = t0 + t2; x[2] = t0 - t2; x[1] = t1 + t3; x[3] = t1 - t3;
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const bool hi = (lane & m) != 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const float p = __shfl_xor_sync(0xffffffffu, x[c], m);
+      x[c] = hi ? p - x[c] : x[c] + p;
+    }
+  }
+}
+
+// One vector quantized by one warp: lane l holds coordinates 4l..4l+3 (x, in
+// place: flipped by the signs sg, then rotated), two butterfly stages in the
+// lane and five by shuffles.  Writes the codes
+// (16 * bits bytes, dense LSB-first) and the norm, returns the norm and leaves
+// the lane's centroids c[idx] in yq and rotated-domain residuals
+// ||x|| (y - c[idx]) in r.  bnd / cen: the codebook's boundaries and
+// centroids in shared memory; words: 32 words of shared scratch, zero on
+// entry and left zero.
+__device__ __forceinline__ float warp_quantize_vals(float (&x)[4], float4 sg, int bits,
+                                                    const float* bnd, const float* cen,
+                                                    uint8_t* codes_dst, float* norm_dst,
+                                                    uint32_t* words, int lane, float (&r)[4],
+                                                    float (&yq)[4]) {
+  x[0] *= sg.x; x[1] *= sg.y; x[2] *= sg.z; x[3] *= sg.w;
+  float ss = x[0] * x[0];
+  ss = fmaf(x[1], x[1], ss);
+  ss = fmaf(x[2], x[2], ss);
+  ss = fmaf(x[3], x[3], ss);
+  const float nrm = sqrtf(warp_sum(ss));
+  warp_fwht4(x, lane);
+  const float inv = nrm > 0.f ? 1.0f / (nrm * 11.313708498984761f) : 0.f;
+  uint32_t packed = 0;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const float y = x[c] * inv;
+    uint32_t idx = 0;
+    for (int step = 1 << (bits - 1); step >= 1; step >>= 1)
+      if (bnd[idx + step - 1] < y) idx += step;
+    packed |= idx << (c * bits);
+    yq[c] = cen[idx];
+    r[c] = nrm * (y - yq[c]);
+  }
+  // dense LSB-first stream: lane l's 4*bits bits start at bit 4*bits*l
+  const int pos = 4 * bits * lane;
+  const int wi = pos >> 5, sh = pos & 31;
+  atomicOr(&words[wi], packed << sh);
+  if (sh + 4 * bits > 32) atomicOr(&words[wi + 1], packed >> (32 - sh));
+  __syncwarp();
+  if (lane < bits)
+    ((uint4*)codes_dst)[lane] = make_uint4(words[4 * lane], words[4 * lane + 1],
+                                           words[4 * lane + 2], words[4 * lane + 3]);
+  if (lane == 0) *norm_dst = nrm;
+  __syncwarp();
+  if (lane < 4 * bits) words[lane] = 0u;
+  __syncwarp();
+  return nrm;
+}
+// the same from a row in memory (bf16, or fp32 when f32)
+__device__ __forceinline__ float warp_quantize_row(const void* src, int f32, float4 sg, int bits,
+                                                   const float* bnd, const float* cen,
+                                                   uint8_t* codes_dst, float* norm_dst,
+                                                   uint32_t* words, int lane, float (&r)[4],
+                                                   float (&yq)[4]) {
+  float x[4];
+  if (f32) {
+    const float4 v = ((const float4*)src)[lane];
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+  } else {
+    const uint2 v = ((const uint2*)src)[lane];
+    x[0] = bf16lo(v.x); x[1] = bf16hi(v.x); x[2] = bf16lo(v.y); x[3] = bf16hi(v.y);
+  }
+  return warp_quantize_vals(x, sg, bits, bnd, cen, codes_dst, norm_dst, words, lane, r, yq);
+}
+
+// Direct Sign of a residual held by a warp as in warp_quantize_row: bit i =
+// [r_i >= 0] (lane l: coordinates 4l..4l+3), scale = mean |r_i|
+// ("TurboQuant KV 캐시 압축 for llama.cpp", v1.1.0 "Direct Sign").  Returns
+// the scale (in every lane).
+__device__ __forceinline__ float warp_direct_sign(const float (&r)[4], uint8_t* signs_dst,
+                                                  float* scale_dst, int lane) {
+  uint32_t nib = 0u;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) nib |= (r[c] >= 0.f ? 1u : 0u) << c;
+  const float asum = warp_sum(fabsf(r[0]) + fabsf(r[1]) + fabsf(r[2]) + fabsf(r[3]));
+  // lanes 8w .. 8w+7 fill word w; gather with shuffles
+  uint32_t word = nib << (4 * (lane & 7));
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) word |= __shfl_xor_sync(0xffffffffu, word, o);
+  const uint32_t w0 = __shfl_sync(0xffffffffu, word, 0), w1 = __shfl_sync(0xffffffffu, word, 8);
+  const uint32_t w2 = __shfl_sync(0xffffffffu, word, 16), w3 = __shfl_sync(0xffffffffu, word, 24);
+  const float scale = asum * (1.0f / kD);
+  if (lane == 0) {
+    *(uint4*)signs_dst = make_uint4(w0, w1, w2, w3);
+    *scale_dst = scale;
+  }
+  return scale;
+}
+
 // Direct Sign sketch of a residual held as pairs p[j] = (r_j, r_{j+64}): bit
 // i of the 128-bit sign vector is [r_i >= 0]; the scale is mean |r_i|
 // ("TurboQuant KV 캐시 압축 for llama.cpp", v1.1.0 "Direct Sign").

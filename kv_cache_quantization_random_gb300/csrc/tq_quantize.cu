@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kQRows, 3)
 
 // ---- tq_append_kv with a few new tokens: one CTA per (sequence, kv-head).
 // Warp 0 quantizes the keys and warp 1 the values that leave the window (or
-// go straight to the planes); lane l owns coordinates 4l..4l+3, so the
+// go straight to the planes), see warp_quantize_row; lane l owns coordinates 4l..4l+3, so the
 // Walsh-Hadamard butterfly takes two in-register stages and five shuffle
 // stages.  After a CTA barrier (every ring slot that is about to be
 // overwritten has been read) all threads write the new tokens into the ring.
@@ -128,75 +128,11 @@ __device__ __forceinline__ void append_quantize_row(const AppendArgs& a, int kin
                                                     const float* cen, float4 sg, uint32_t* words,
                                                     float* rbuf, int lane) {
   constexpr int kDim = 128;
-  const int bits = a.bits[kind];
-  float x[4];
-  if (f32) {
-    const float4 v = ((const float4*)src)[lane];
-    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
-  } else {
-    const uint2 v = ((const uint2*)src)[lane];
-    x[0] = bf16lo(v.x); x[1] = bf16hi(v.x); x[2] = bf16lo(v.y); x[3] = bf16hi(v.y);
-  }
-  x[0] *= sg.x; x[1] *= sg.y; x[2] *= sg.z; x[3] *= sg.w;
-  float ss = x[0] * x[0];
-  ss = fmaf(x[1], x[1], ss);
-  ss = fmaf(x[2], x[2], ss);
-  ss = fmaf(x[3], x[3], ss);
-  const float nrm = sqrtf(warp_sum(ss));
-  // butterfly: stages 1 and 2 inside the lane, 4..64 across lanes
-  float t0 = x[0] + x[1], t1 = x[0] - x[1], t2 = x[2] + x[3], t3 = x[2] - x[3];
-  x[0] = t0 + t2; x[2] = t0 - t2; x[1] = t1 + t3; x[3] = t1 - t3;
-#pragma unroll
-  for (int m = 1; m < 32; m <<= 1) {
-    const bool hi = (lane & m) != 0;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const float p = __shfl_xor_sync(0xffffffffu, x[c], m);
-      x[c] = hi ? p - x[c] : x[c] + p;
-    }
-  }
-  const float inv = nrm > 0.f ? 1.0f / (nrm * 11.313708498984761f) : 0.f;
-  uint32_t packed = 0;
-  float r[4];
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const float y = x[c] * inv;
-    uint32_t idx = 0;
-    for (int step = 1 << (bits - 1); step >= 1; step >>= 1)
-      if (bnd[idx + step - 1] < y) idx += step;
-    packed |= idx << (c * bits);
-    r[c] = nrm * (y - cen[idx]);
-  }
-  // dense LSB-first stream: lane l's 4*bits bits start at bit 4*bits*l
-  const int pos = 4 * bits * lane;
-  const int wi = pos >> 5, sh = pos & 31;
-  atomicOr(&words[wi], packed << sh);
-  if (sh + 4 * bits > 32) atomicOr(&words[wi + 1], packed >> (32 - sh));
-  __syncwarp();
-  if (lane < bits) {
-    uint4* dc = (uint4*)(a.codes[kind] + drow * (16 * bits));
-    dc[lane] = make_uint4(words[4 * lane], words[4 * lane + 1], words[4 * lane + 2],
-                          words[4 * lane + 3]);
-  }
-  if (lane == 0) a.norms[kind][drow] = nrm;
-  if (kind == 0 && a.dsign) {
-    // Direct Sign: bit i = [r_i >= 0] (lane l holds coordinates 4l..4l+3),
-    // scale = mean |r_i|
-    uint32_t nib = 0u;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) nib |= (r[c] >= 0.f ? 1u : 0u) << c;
-    const float asum = warp_sum(fabsf(r[0]) + fabsf(r[1]) + fabsf(r[2]) + fabsf(r[3]));
-    // lanes 8w .. 8w+7 fill word w; gather with shuffles
-    uint32_t word = nib << (4 * (lane & 7));
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) word |= __shfl_xor_sync(0xffffffffu, word, o);
-    const uint32_t w0 = __shfl_sync(0xffffffffu, word, 0), w1 = __shfl_sync(0xffffffffu, word, 8);
-    const uint32_t w2 = __shfl_sync(0xffffffffu, word, 16), w3 = __shfl_sync(0xffffffffu, word, 24);
-    if (lane == 0) {
-      *(uint4*)(a.qjl_signs + drow * (kDim / 8)) = make_uint4(w0, w1, w2, w3);
-      a.qjl_rnorm[drow] = asum * (1.0f / kDim);
-    }
-  }
+  float r[4], yq[4];
+  warp_quantize_row(src, f32, sg, a.bits[kind], bnd, cen, a.codes[kind] + drow * (16 * a.bits[kind]),
+                    a.norms[kind] + drow, words, lane, r, yq);
+  if (kind == 0 && a.dsign)
+    warp_direct_sign(r, a.qjl_signs + drow * (kDim / 8), a.qjl_rnorm + drow, lane);
   if (kind == 0 && a.qjl) {
     float g = r[0] * r[0];
     g = fmaf(r[1], r[1], g);
@@ -230,10 +166,8 @@ __device__ __forceinline__ void append_quantize_row(const AppendArgs& a, int kin
       *(uint4*)(a.qjl_signs + drow * (kQjlM / 8)) = make_uint4(sb[0], sb[1], sb[2], sb[3]);
       a.qjl_rnorm[drow] = gamma;
     }
+    __syncwarp();      // rbuf is read by every lane before the next vector writes it
   }
-  __syncwarp();
-  if (lane < 4 * bits) words[lane] = 0u;
-  __syncwarp();
 }
 
 __global__ void __launch_bounds__(64) append_kernel(const AppendArgs a) {

@@ -391,17 +391,27 @@ def test_decode_multi_query_needs_the_hidden_tokens_in_the_window(B):
     assert e.value.status == 2
 
 
-@pytest.mark.parametrize("kb,vb,mode,W,rep", [(4, 2, "mse", 16, 1), (3, 3, "mse", 0, 1),
-                                             (2, 3, "qjl", 0, 1), (2, 3, "sign", 16, 1),
-                                             (8, 8, "mse", 8, 1), (4, 2, "mse", 128, 1),
-                                             (4, 2, "mse", 16, 2)])
-def test_decode_step_matches_append_then_decode(B, kb, vb, mode, W, rep):
-    """tq_decode_step (append of one token per sequence, then decode, in two
-    overlapping launches) writes the same planes and ring as tq_append_kv and
-    returns the output of tq_decode_attention after it.  The plane rows the
-    append writes are zeroed beforehand, so a decode that read them before the
-    append finished would differ.  rep = 2 gives 24 (sequence, kv-head) pairs:
-    the decode then keeps all CTA slots."""
+@pytest.mark.parametrize("kb,vb,mode,W,rep,f32", [(4, 2, "mse", 16, 1, False),
+                                                  (3, 3, "mse", 0, 1, False),
+                                                  (4, 2, "mse", 0, 1, True),
+                                                  (2, 3, "qjl", 0, 1, False),
+                                                  (2, 3, "qjl", 16, 1, False),
+                                                  (2, 3, "sign", 16, 1, False),
+                                                  (3, 2, "sign", 0, 1, True),
+                                                  (8, 8, "mse", 8, 1, False),
+                                                  (4, 2, "mse", 128, 1, False),
+                                                  (4, 2, "mse", 16, 2, False)])
+def test_decode_step_matches_append_then_decode(B, kb, vb, mode, W, rep, f32):
+    """tq_decode_step (append of one token per sequence and decode: one launch
+    with a window and keys in MSE or Direct Sign mode, else the append kernel
+    then an overlapping decode) writes the same planes and ring as
+    tq_append_kv and returns the output of tq_decode_attention after it.  The
+    plane rows the append writes are zeroed beforehand, so a decode that read
+    them before they were written would differ.  The lengths cover a token
+    leaving the window from its ring slot (as the first and as the last row of
+    the quantized part), a ring slot that held no token (T0 < W), and W = 0
+    (two launches; the new token goes straight to the planes, from bf16 or
+    fp32 rows).  rep = 2 gives 24 (sequence, kv-head) pairs."""
     import torch
     from kv_cache_quantization_random_gb300 import workloads as W_
     T0 = np.tile(np.array([699, max(W - 1, 0), W, 0, 37, 300], dtype=np.int64), rep)
@@ -436,6 +446,8 @@ def test_decode_step_matches_append_then_decode(B, kb, vb, mode, W, rep):
         caches.append((kp, vp, kw if W else None, vw if W else None))
     kn = torch.stack([K[b, :, int(T0[b]):int(T0[b]) + 1] for b in range(batch)]).cuda()
     vn = torch.stack([V[b, :, int(T0[b]):int(T0[b]) + 1] for b in range(batch)]).cuda()
+    if f32:
+        kn, vn = kn.float(), vn.float()
     before = torch.tensor(T0, dtype=torch.int32, device="cuda")
     after = before + 1
     ws = B.new_workspace(cfg, batch, hq, hkv, C)
@@ -459,4 +471,9 @@ def test_decode_step_matches_append_then_decode(B, kb, vb, mode, W, rep):
     if W:
         assert torch.equal(kwa.cpu(), kwb.cpu()) and torch.equal(vwa.cpu(), vwb.cpu())
     a, b = to64(outs[0]), to64(outs[1])
-    assert rel_l2_per_head(b, a).max() < 1e-5
+    # the one-launch step attends to the token leaving the window through its
+    # dequantized fp32 key and value, where the two-launch decode takes its
+    # fp16 MMA operands: the two agree within the decode tolerance; the
+    # two-launch step runs the same decode as tq_decode_attention
+    fused = mode != "qjl" and W > 0
+    assert rel_l2_per_head(b, a).max() < (2e-3 if fused else 1e-5)
