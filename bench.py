@@ -9,8 +9,9 @@ A step is one decode step of a serving loop over the workload's cache:
   decode   attention of every query head over the whole compressed context
            (query rotation, compressed-domain scoring, softmax, rotated V sum,
            split merge and inverse rotation).
-Single-layer workloads run one tq_decode_step call (append of one token and a
-decode that overlaps it).  The 36-layer serving workload runs, for every
+Single-layer workloads run one tq_decode_step call (append of one token and the
+decode: one launch with a window and keys in MSE or Direct Sign mode, else an
+append launch and a decode that overlaps it).  The 36-layer serving workload runs, for every
 layer, tq_append_kv of its 64 new tokens per sequence and tq_decode_attention.
 The headline value is context tokens attended per second (summed over layers).
 Bulk quantize of the whole context (K and V) is measured separately and
@@ -483,12 +484,14 @@ def run_single(args, w, rank, world, local):
                               k_win=kwr, v_win=vwr)
 
     def step(i):
-        # tq_decode_step: the append and the decode that overlaps it
         kr, vr, kwr, vwr = reps[i % R]
         B.tq_decode_step(cfg, tables, 0, q, w.softmax_scale, knew, vnew, seq_before, Tmax, kr, vr,
                          out, ws, k_win=kwr, v_win=vwr)
 
-    launches_per_step = 2          # one append launch + one decode launch
+    # tq_decode_step: one launch with a window and keys in MSE or Direct Sign
+    # mode (the decode kernel appends the token), else an append launch and a
+    # decode launch
+    launches_per_step = 1 if (w.window > 0 and not w.k_qjl) else 2
 
     # ---- warmup (direct launches), then graphs of S steps
     warm = max(args.warmup, 3)
@@ -662,7 +665,8 @@ def run_single(args, w, rank, world, local):
         },
         "decode": {"ms": dec_ms, "gbs": dec_gbs, "frac_of_peak": dec_gbs / hbm_peak,
                    "tokens_per_s": tokens_per_step / (dec_ms * 1e-3), "bytes": dec_bytes},
-        "append": {"ms": app_ms, "launches": launches_per_step - 1},
+        "append": {"ms": app_ms, "launches": 1,
+                   "what": "tq_append_kv of the step's token alone (append-only graph)"},
         "quantize": {"ms": q_ms, "gbs": q_gbs, "frac_of_peak": q_gbs / hbm_peak,
                      "vectors": 2 * n_vec, "bytes": q_bytes, "what": "bulk quantize of the "
                      "context's K and V (input dtype in, packed planes out)"},
