@@ -391,6 +391,61 @@ def test_decode_multi_query_needs_the_hidden_tokens_in_the_window(B):
     assert e.value.status == 2
 
 
+@pytest.mark.parametrize("mode,W", [("mse", 16), ("sign", 16), ("qjl", 0)])
+def test_decode_step_with_host_mapped_inputs_and_output(B, mode, W):
+    """The query, the new tokens and the output of tq_decode_step may be
+    pinned host memory, which the kernels read and write across the host link
+    (one launch with a window, two launches for QJL keys).  Planes, ring and
+    output must be bit-identical to the same step on device buffers."""
+    import torch
+    from kv_cache_quantization_random_gb300 import workloads as W_
+    T0 = np.array([299, 37, max(W - 1, 0)], dtype=np.int64)
+    batch, hkv, hq, C = len(T0), 2, 8, 300
+    w = W_.scaled(W_.get("llama8b_32k"), batch=batch, n_q_heads=hq, n_kv_heads=hkv, context=C,
+                  data_seed=23)
+    K, V = W_.make_kv(w)
+    q = W_.make_q(w)
+    km = {"mse": B.TQ_MODE_MSE, "sign": B.TQ_MODE_MSE_SIGN, "qjl": B.TQ_MODE_MSE_QJL}[mode]
+    cfg = B.Config(k_bits=4, v_bits=2, k_mode=km, residual_window=W, seed=8)
+    tables = B.device_tables(cfg)
+    Kd, Vd = K.cuda(), V.cuda()
+    caches = []
+    for _ in range(2):
+        kp, vp = B.Planes(cfg, 0, 0, batch, hkv, C), B.Planes(cfg, 0, 1, batch, hkv, C)
+        B.tq_quantize_kv(cfg, tables, 0, 0, Kd[:, :, :C - 1], kp)
+        B.tq_quantize_kv(cfg, tables, 0, 1, Vd[:, :, :C - 1], vp)
+        kw = torch.zeros(batch, hkv, max(W, 1), 128, dtype=torch.bfloat16, device="cuda")
+        vw = torch.zeros_like(kw)
+        for b in range(batch):
+            for t in range(max(int(T0[b]) - W, 0), int(T0[b])):
+                kw[b, :, t % W] = Kd[b, :, t]
+                vw[b, :, t % W] = Vd[b, :, t]
+        caches.append((kp, vp, kw if W else None, vw if W else None))
+    kn = torch.stack([K[b, :, int(T0[b]):int(T0[b]) + 1] for b in range(batch)])
+    vn = torch.stack([V[b, :, int(T0[b]):int(T0[b]) + 1] for b in range(batch)])
+    before = torch.tensor(T0, dtype=torch.int32, device="cuda")
+    ws = B.new_workspace(cfg, batch, hq, hkv, C)
+    out_d = torch.empty(batch, hq, 128, device="cuda")
+    out_h = torch.full((batch, hq, 128), float("nan")).pin_memory()
+    kp, vp, kw, vw = caches[0]
+    B.tq_decode_step(cfg, tables, 0, q.cuda(), w.softmax_scale, kn.cuda(), vn.cuda(), before, C,
+                     kp, vp, out_d, ws, k_win=kw, v_win=vw)
+    kp, vp, kw, vw = caches[1]
+    B.tq_decode_step(cfg, tables, 0, q.pin_memory(), w.softmax_scale, kn.pin_memory(),
+                     vn.pin_memory(), before, C, kp, vp, out_h, ws, k_win=kw, v_win=vw)
+    torch.cuda.synchronize()
+    assert B.tq_get_device_error() == B.TQ_OK
+    (ka, va, kwa, vwa), (kb_, vb_, kwb, vwb) = caches
+    for Pa, Pb in ((ka, kb_), (va, vb_)):
+        assert torch.equal(Pa.codes.cpu(), Pb.codes.cpu())
+        assert torch.equal(Pa.norms.cpu(), Pb.norms.cpu())
+        if Pa.qjl_signs is not None:
+            assert torch.equal(Pa.qjl_signs.cpu(), Pb.qjl_signs.cpu())
+    if W:
+        assert torch.equal(kwa.cpu(), kwb.cpu()) and torch.equal(vwa.cpu(), vwb.cpu())
+    assert torch.equal(out_h, out_d.cpu())
+
+
 @pytest.mark.parametrize("kb,vb,mode,W,rep,f32", [(4, 2, "mse", 16, 1, False),
                                                   (3, 3, "mse", 0, 1, False),
                                                   (4, 2, "mse", 0, 1, True),
