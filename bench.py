@@ -10,8 +10,8 @@ A step is one decode step of a serving loop over the workload's cache:
            (query rotation, compressed-domain scoring, softmax, rotated V sum,
            split merge and inverse rotation).
 Single-layer workloads run one tq_decode_step call (append of one token and the
-decode: one launch with a window and keys in MSE or Direct Sign mode, else an
-append launch and a decode that overlaps it).  The 36-layer serving workload runs, for every
+decode: one launch when its plan fits one wave of the GPU, else an append
+launch and a decode launch).  The 36-layer serving workload runs, for every
 layer, tq_append_kv of its 64 new tokens per sequence and tq_decode_attention.
 The headline value is context tokens attended per second (summed over layers).
 Bulk quantize of the whole context (K and V) is measured separately and
@@ -488,10 +488,10 @@ def run_single(args, w, rank, world, local):
         B.tq_decode_step(cfg, tables, 0, q, w.softmax_scale, knew, vnew, seq_before, Tmax, kr, vr,
                          out, ws, k_win=kwr, v_win=vwr)
 
-    # tq_decode_step: one launch with a window and keys in MSE or Direct Sign
-    # mode (the decode kernel appends the token), else an append launch and a
-    # decode launch
-    launches_per_step = 1 if (w.window > 0 and not w.k_qjl) else 2
+    # tq_decode_step: one launch (the decode kernel appends the token) when its
+    # plan fits one wave, else an append launch and a decode launch
+    launches_per_step = B.tq_decode_step_launches(cfg, 0, w.batch, w.n_q_heads, w.n_kv_heads,
+                                                  int(seq.max()))
 
     # ---- warmup (direct launches), then graphs of S steps
     warm = max(args.warmup, 3)

@@ -317,18 +317,21 @@ tq_status tq_decode_attention_multi(const tq_config* cfg, const void* tables, in
  * + 1 tokens of every sequence, with the same arguments and results as those
  * two calls ("[GitHub 탐방] TurboQuant 3-bit KV 캐시 압축 — 단일 GPU 재현 기록",
  * "실험 설계": the newest tokens stay in the bf16 window).  max_seq_len bounds
- * seq_lens_before[b] + 1.  With a window (W > 0) and keys in MSE or Direct
- * Sign mode this is one launch: the quantized splits stop before the token
- * leaving the window, and each pair's first window split quantizes that token
- * from its ring slot into the planes (the same warp-per-vector quantizer, and
- * so the same codes, as tq_append_kv), attends to its dequantized key and
- * value, and writes the new token into the slot; the window splits read the
- * new token from k_new / v_new, which must then be bf16.  Otherwise (QJL keys,
- * or W = 0) two launches: the append kernel, and the decode, which starts
- * while the append runs and waits for it only before it reads what the append
- * writes (the window ring, the plane rows from max(seq_lens_before[b] - W, 0)
- * on).  The planes, ring and workspace must not be used by other work on the
- * device meanwhile. */
+ * seq_lens_before[b] + 1.  One launch when the plan with the step's work
+ * fits one wave of the GPU (see tq_decode_step_launches): the quantized
+ * splits stop before the token that leaves the window (with W = 0 the new
+ * token itself), and each pair's first window split (with W = 0 a split of
+ * its own) quantizes that token into the planes with the same warp-per-vector
+ * quantizer as tq_append_kv (so the same codes, norms and residual terms),
+ * attends to its dequantized key and value, and with W > 0 writes the new
+ * token into the ring slot that token leaves; the window splits read the new
+ * token from k_new / v_new.  The output equals that of the two calls within
+ * the decode's rounding (that token enters the attention through fp32
+ * dequantized operands rather than fp16 MMA operands).  Otherwise the splits
+ * that append would run in a later wave, after the others: two launches, the
+ * append kernel and a decode that waits for it.  k_new / v_new are bf16, or
+ * fp32 when W = 0 (the ring is bf16).  The planes, ring and workspace must not
+ * be used by other work on the device meanwhile. */
 tq_status tq_decode_step(const tq_config* cfg, const void* tables, int layer, const void* q,
                          int q_dtype, float softmax_scale, int batch, int n_q_heads,
                          int n_kv_heads, const void* k_new, const void* v_new, int src_dtype,
@@ -336,6 +339,13 @@ tq_status tq_decode_step(const tq_config* cfg, const void* tables, int layer, co
                          int max_seq_len, uint16_t* k_win, uint16_t* v_win, tq_planes k,
                          tq_planes v, float* out, void* workspace, size_t workspace_bytes,
                          void* stream);
+
+/* Kernel launches tq_decode_step makes for these sizes: 1 (the decode kernel
+ * appends the token itself) or 2 (the append kernel, then the decode), or 0
+ * for invalid arguments.  The pages have no counterpart; this is an
+ * introspection helper for schedulers and benchmarks. */
+int tq_decode_step_launches(const tq_config* cfg, int layer, int batch, int n_q_heads,
+                            int n_kv_heads, int max_seq_len);
 
 /* Synchronize `stream`, then read and clear the device error words that the
  * kernels set instead of faulting: a bounded wait that ran out

@@ -38,7 +38,7 @@ EXPORTED = [
     "tq_workspace_bytes", "tq_workspace_init", "tq_quantize_kv", "tq_append_kv",
     "tq_dequantize", "tq_decode_attention", "tq_get_device_error", "tq_set_wait_limit",
     "tq_set_fault_injection", "tq_decode_attention_noalloc", "tq_decode_attention_multi",
-    "tq_decode_step",
+    "tq_decode_step", "tq_decode_step_launches",
 ]
 
 
@@ -115,6 +115,7 @@ def load(build_if_missing: bool = False):
                                           P, P, P, I, P, P, SZ, P]),
         "tq_decode_step": (I, [cfgp, P, I, P, I, F, I, I, I, P, P, I, C.POINTER(I64), P, I, P, P,
                                tq_planes, tq_planes, P, P, SZ, P]),
+        "tq_decode_step_launches": (I, [cfgp, I, I, I, I, I]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -354,8 +355,7 @@ def tq_decode_step(cfg: Config, tables, layer: int, q, softmax_scale: float, k_n
                    k_win=None, v_win=None, stream=None):
     """tq_append_kv of one token per (sequence, kv-head) (k_new, v_new
     [B, Hkv, 1, d]) followed by tq_decode_attention over seq_lens_before + 1
-    tokens, as one call (one launch with a window and keys in MSE or Direct
-    Sign mode)."""
+    tokens, as one call (one launch)."""
     B, Hq, _ = q.shape
     H = k_new.shape[1]
     if v_new.shape != k_new.shape or v_new.stride() != k_new.stride() or k_new.shape[2] != 1:
@@ -367,6 +367,13 @@ def tq_decode_step(cfg: Config, tables, layer: int, q, softmax_scale: float, k_n
         k.c(), v.c(), out.data_ptr(), workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _stream_ptr(stream))
     _check(st, "tq_decode_step")
+
+
+def tq_decode_step_launches(cfg: Config, layer: int, batch: int, n_q_heads: int, n_kv_heads: int,
+                            max_seq_len: int) -> int:
+    """Kernel launches of tq_decode_step for these sizes (1 or 2; 0: invalid)."""
+    return int(load().tq_decode_step_launches(C.byref(cfg.c()), layer, batch, n_q_heads,
+                                              n_kv_heads, max_seq_len))
 
 
 def tq_decode_attention_noalloc(cfg: Config, tables, layer: int, q, softmax_scale: float,

@@ -421,17 +421,18 @@ __device__ __forceinline__ void qjl_scores(uint32_t sa, uint32_t sb, const uint3
   }
 }
 
-// Decode step in one launch (DecodeArgs::fused_step, W > 0): the token L =
-// T - 1 - W that leaves the window, handled by warp 0 of its pair's first
-// window split.  The warp reads L's bf16 rows from ring slot L mod W,
-// quantizes them into plane row L (codes, norm and, for Direct Sign keys, the
-// residual signs and scale: the same warp-per-vector quantizer as
-// tq_append_kv), writes the new token T - 1 into that slot, and returns L's
-// dequantized key and value (lane l: coordinates 4l..4l+3) for the window
+// Decode step in one launch (DecodeArgs::fused_step): the token L = T - 1 - W
+// that leaves the window (with W = 0 the new token itself), handled by warp 0
+// of its pair's first window split.  The warp reads L's rows (ring slot
+// L mod W, bf16; with W = 0 the step's input), quantizes them into plane row L
+// with the warp-per-vector quantizer of tq_append_kv (codes, norm and the
+// key's residual term: Direct Sign bits and scale, or the QJL sketch and
+// gamma), writes the new token T - 1 into the ring slot (W > 0), and returns
+// L's dequantized key and value (lane l: coordinates 4l..4l+3) for the window
 // split to attend to: the quantized splits of this launch stop before row L,
-// so no CTA waits for another.  The boundaries (2 KB) and 32 words of packing
-// scratch sit at byte scr of the dynamic shared memory.  Not inlined: it runs
-// once per pair, off the main loop.
+// so no CTA waits for another.  The codebooks' boundaries (2 KB), 32 words of
+// packing scratch and 128 floats of residual scratch sit at byte scr of the
+// dynamic shared memory.  Not inlined: it runs once per pair, off the main loop.
 static __device__ __noinline__ void step_leaving_token(const DecodeArgs& a, long long pair, int L,
                                                        int scr, const float* kcen,
                                                        const float* vcen, float* kx, float* vx,
@@ -439,51 +440,87 @@ static __device__ __noinline__ void step_leaving_token(const DecodeArgs& a, long
   extern __shared__ __align__(128) uint8_t smem[];
   const float* bnd = (const float*)(smem + scr);
   uint32_t* words = (uint32_t*)(smem + scr + 2048);
-  const long long ring = (pair * a.W + L % a.W) * kD2;
+  float* rbuf = (float*)(smem + scr + 2048 + 128);
   const long long kr = pair * a.kcap + L, vr = pair * a.vcap + L;
   uint8_t* kc = (uint8_t*)a.kc + kr * 16 * a.kb;
   uint8_t* vc = (uint8_t*)a.vc + vr * 16 * a.vb;
+  const long long ring = a.W > 0 ? (pair * a.W + L % a.W) * kD2 : 0;
+  const long long noff = (pair / a.Hkv) * a.nsb + (pair % a.Hkv) * a.nsh;
   const size_t ring_bytes_ = (size_t)a.B * a.Hkv * a.W * kD2 * 2;
   if (!bchk_range(kc, 16 * a.kb, a.kc, (size_t)a.B * a.Hkv * a.kcap * 16 * a.kb, a.err) ||
       !bchk_range(vc, 16 * a.vb, a.vc, (size_t)a.B * a.Hkv * a.vcap * 16 * a.vb, a.err) ||
-      !bchk_range(a.kwin + ring, kD2 * 2, a.kwin, ring_bytes_, a.err)) {
+      (a.W > 0 && !bchk_range(a.kwin + ring, kD2 * 2, a.kwin, ring_bytes_, a.err))) {
     for (int c = 0; c < 4; ++c) kx[c] = vx[c] = 0.f;
     return;
   }
-  // all four rows' loads first (the leaving token's key and value, the new
-  // token's key and value), so that their latencies overlap
-  const long long noff = (pair / a.Hkv) * a.nsb + (pair % a.Hkv) * a.nsh;
-  const uint2 kold = ((const uint2*)(a.kwin + ring))[lane];
-  const uint2 vold = ((const uint2*)(a.vwin + ring))[lane];
-  const uint2 knw = ((const uint2*)((const uint16_t*)a.knew + noff))[lane];
-  const uint2 vnw = ((const uint2*)((const uint16_t*)a.vnew + noff))[lane];
+  // the rows' loads first (with a window: the leaving token's key and value
+  // and the new token's, for the ring), so that their latencies overlap
+  float xk[4], xv[4];
+  uint2 knw = make_uint2(0u, 0u), vnw = knw;
+  if (a.W > 0) {
+    const uint2 ko = ((const uint2*)(a.kwin + ring))[lane];
+    const uint2 vo = ((const uint2*)(a.vwin + ring))[lane];
+    knw = ((const uint2*)((const uint16_t*)a.knew + noff))[lane];
+    vnw = ((const uint2*)((const uint16_t*)a.vnew + noff))[lane];
+    xk[0] = bf16lo(ko.x); xk[1] = bf16hi(ko.x); xk[2] = bf16lo(ko.y); xk[3] = bf16hi(ko.y);
+    xv[0] = bf16lo(vo.x); xv[1] = bf16hi(vo.x); xv[2] = bf16lo(vo.y); xv[3] = bf16hi(vo.y);
+  } else if (a.new_f32) {
+    const float4 ko = ((const float4*)((const float*)a.knew + noff))[lane];
+    const float4 vo = ((const float4*)((const float*)a.vnew + noff))[lane];
+    xk[0] = ko.x; xk[1] = ko.y; xk[2] = ko.z; xk[3] = ko.w;
+    xv[0] = vo.x; xv[1] = vo.y; xv[2] = vo.z; xv[3] = vo.w;
+  } else {
+    const uint2 ko = ((const uint2*)((const uint16_t*)a.knew + noff))[lane];
+    const uint2 vo = ((const uint2*)((const uint16_t*)a.vnew + noff))[lane];
+    xk[0] = bf16lo(ko.x); xk[1] = bf16hi(ko.x); xk[2] = bf16lo(ko.y); xk[3] = bf16hi(ko.y);
+    xv[0] = bf16lo(vo.x); xv[1] = bf16hi(vo.x); xv[2] = bf16lo(vo.y); xv[3] = bf16hi(vo.y);
+  }
   const float4 sk = __ldg((const float4*)a.sk + lane), sv = __ldg((const float4*)a.sv + lane);
   const float sks[4] = {sk.x, sk.y, sk.z, sk.w}, svs_[4] = {sv.x, sv.y, sv.z, sv.w};
   float r[4], yq[4], t[4];
   // keys: quantize, then dequantize as a reader of the planes would (norm x
-  // centroid, plus the Direct Sign term; inverse rotation H / sqrt(d); signs)
-  float x[4] = {bf16lo(kold.x), bf16hi(kold.x), bf16lo(kold.y), bf16hi(kold.y)};
-  const float nk = warp_quantize_vals(x, sk, a.kb, bnd, kcen, kc, (float*)a.kn + kr, words, lane,
+  // centroid plus the residual term; inverse rotation H / sqrt(d); signs)
+  const float nk = warp_quantize_vals(xk, sk, a.kb, bnd, kcen, kc, (float*)a.kn + kr, words, lane,
                                       r, yq);
-  float sc = 0.f;
-  if (a.dsign) sc = warp_direct_sign(r, (uint8_t*)a.ks + kr * 16, (float*)a.kr + kr, lane);
 #pragma unroll
-  for (int c = 0; c < 4; ++c) t[c] = nk * yq[c] + (a.dsign ? (r[c] >= 0.f ? sc : -sc) : 0.f);
+  for (int c = 0; c < 4; ++c) t[c] = nk * yq[c];
+  if (a.dsign) {
+    const float sc = warp_direct_sign(r, (uint8_t*)a.ks + kr * 16, (float*)a.kr + kr, lane);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) t[c] += r[c] >= 0.f ? sc : -sc;
+  } else if (a.qjl) {
+    // residual estimate sqrt(pi/2) / m * gamma * S^T (2 bit - 1), coordinates 4l..4l+3
+    uint32_t sb[4];
+    const float gamma =
+        warp_qjl_sketch(r, a.S, rbuf, (uint8_t*)a.ks + kr * 16, (float*)a.kr + kr, lane, sb);
+    float e[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < kQjlM; ++j) {
+      const uint2 s4 = __ldg((const uint2*)(a.S + (size_t)j * kD2) + lane);
+      const float sg = (sb[j >> 5] >> (j & 31)) & 1u ? 1.f : -1.f;
+      e[0] = fmaf(sg, bf16lo(s4.x), e[0]);
+      e[1] = fmaf(sg, bf16hi(s4.x), e[1]);
+      e[2] = fmaf(sg, bf16lo(s4.y), e[2]);
+      e[3] = fmaf(sg, bf16hi(s4.y), e[3]);
+    }
+    const float coef = 1.2533141373155003f / (float)kQjlM * gamma;   // sqrt(pi/2) / m
+#pragma unroll
+    for (int c = 0; c < 4; ++c) t[c] = fmaf(coef, e[c], t[c]);
+  }
   warp_fwht4(t, lane);
 #pragma unroll
   for (int c = 0; c < 4; ++c) kx[c] = t[c] * 0.08838834764831845f * sks[c];
   // values
-  x[0] = bf16lo(vold.x); x[1] = bf16hi(vold.x); x[2] = bf16lo(vold.y); x[3] = bf16hi(vold.y);
-  const float nv = warp_quantize_vals(x, sv, a.vb, bnd + 256, vcen, vc, (float*)a.vn + vr, words,
+  const float nv = warp_quantize_vals(xv, sv, a.vb, bnd + 256, vcen, vc, (float*)a.vn + vr, words,
                                       lane, r, yq);
 #pragma unroll
   for (int c = 0; c < 4; ++c) t[c] = nv * yq[c];
   warp_fwht4(t, lane);
 #pragma unroll
   for (int c = 0; c < 4; ++c) vx[c] = t[c] * 0.08838834764831845f * svs_[c];
-  // the new token into the slot (each lane rewrites the 8 bytes it read)
-  ((uint2*)((uint16_t*)a.kwin + ring))[lane] = knw;
-  ((uint2*)((uint16_t*)a.vwin + ring))[lane] = vnw;
+  if (a.W > 0) {          // the new token into the slot (each lane rewrites the 8 bytes it read)
+    ((uint2*)((uint16_t*)a.kwin + ring))[lane] = knw;
+    ((uint2*)((uint16_t*)a.vwin + ring))[lane] = vnw;
+  }
 }
 
 template <int G, int KB, int VB, int RES, bool SPARSE>
@@ -637,20 +674,10 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
   const uint8_t* ksp = HAS_RES ? a.ks + row0 * a.kcap * 16 : nullptr;
   const float* krp = HAS_RES ? a.kr + row0 * a.kcap : nullptr;
   const int t_begin = split * a.split_tokens;
-  // L2 prefetch of the codes of this warp's first chunks, before the wait: the
-  // rows the plan gives this split for the longest sequence (the real length
-  // is not known yet).  A prefetch only warms L2, so it is safe on rows the
-  // previous kernel may still be writing; it brings the first chunks' HBM
-  // latency forward, under the previous kernel's tail.
   // everything below may read what the previous kernel on the stream wrote
   // (sequence lengths, query, planes, window ring, workspace): wait for it
-  // to finish.  In a decode step (a.step_new > 0) the previous kernel is the
-  // step's append, which writes only the window ring and the plane rows from
-  // max(nq - step_new, 0) on: window splits wait here, quantized splits only
-  // before the copy of a chunk that reaches row t_end - step_new of their
-  // range (see issue; t_end <= nq, so that covers those rows).
-  if (a.step_new == 0 || a.fused_step || window_split)
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+  // to finish
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   int T = *bchk(a.seq_lens + b, a.seq_lens, (size_t)a.B * 4, a.err) + a.step_new;
   // a length outside the plan's range would read past this pair's plane rows
   // or ring: flag it and decode the sequence as empty
@@ -669,9 +696,6 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
   auto issue = [&](int c0, int slot) {
     const int nv = t_end - c0 < 32 ? t_end - c0 : 32;
     const int n4 = (nv + 3) & ~3;
-    // warp-uniform: rows the step's append may still be writing
-    if (a.step_new > 0 && !a.fused_step && c0 + n4 > t_end - a.step_new)
-      asm volatile("griddepcontrol.wait;" ::: "memory");
     // bulk copies need 16-byte aligned sources: the norm rows of a (sequence,
     // head) start at row0 * capacity floats, aligned only if capacity % 4 == 0
     // (chunks start at multiples of 32 tokens, so this holds for all or none)
@@ -1565,8 +1589,7 @@ int launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
     return 1;
   // programmatic dependent launch: the CTAs may start while the previous
   // kernel on the stream is still running; they read only the codec tables
-  // before griddepcontrol.wait (in a decode step, also the data the step's
-  // append does not write)
+  // before griddepcontrol.wait
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((long long)a.n_splits * a.Hkv * a.B), 1, 1);
   cfg.blockDim = dim3(32 * kWarps, 1, 1);

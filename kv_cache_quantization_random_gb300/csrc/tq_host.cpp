@@ -468,11 +468,11 @@ struct DecodePlan {
 // kDecodeSms x decode_ctas_per_sm CTAs of decode_warps(...) warps.  The window is
 // cut into splits of at most 32 tokens per warp; the quantized tokens of each
 // (sequence, kv-head) are split evenly in multiples of 32 tokens over the rest.
-// reserve: CTA slots of the wave left to a kernel that runs beside the decode
-// (the append of a decode step)
-constexpr int kStepReserveMaxSplit = 4096;   // tokens per quantized split
+// step_split: a decode step in one launch with no window gets one split per
+// pair for the new token (see DecodeArgs::fused_step)
 static DecodePlan decode_plan(const tq_config* cfg, const tq_layer_spec& s, int batch,
-                              int n_q_heads, int n_kv_heads, int max_seq_len, int reserve = 0) {
+                              int n_q_heads, int n_kv_heads, int max_seq_len,
+                              bool step_split = false) {
   DecodePlan p;
   const int W = cfg->residual_window;
   long long max_nq = (long long)max_seq_len - W;
@@ -484,9 +484,8 @@ static DecodePlan decode_plan(const tq_config* cfg, const tq_layer_spec& s, int 
   int wst = (W + 31) / 32 * 32;
   if (wst > 32 * warps) wst = 32 * warps;
   p.wsplit_tokens = wst > 0 ? wst : 1;
-  const int n_wsplits = W > 0 ? (W + wst - 1) / wst : 0;
-  long long wave = (long long)kDecodeSms * decode_ctas_per_sm(p.G, s.k_bits, s.v_bits, res) - reserve;
-  if (wave < 1) wave = 1;
+  const int n_wsplits = W > 0 ? (W + wst - 1) / wst : step_split ? 1 : 0;
+  const long long wave = (long long)kDecodeSms * decode_ctas_per_sm(p.G, s.k_bits, s.v_bits, res);
   long long slots = wave - units * n_wsplits;
   if (slots < units) {
     // more than one wave: the quantized splits alone fill the wave (the short
@@ -512,11 +511,12 @@ extern "C" size_t tq_workspace_bytes(const tq_config* cfg, int batch, int n_q_he
   if (check_config(cfg) != TQ_OK || batch < 0 || n_kv_heads < 1 || n_q_heads < n_kv_heads ||
       max_seq_len < 0)
     return 0;
-  // the largest plan over the layers' formats
+  // the largest plan over the layers' formats (a decode step's, which with
+  // W = 0 has one split more per pair, covers a plain decode's)
   size_t total = 0;
   for (int layer = 0; layer < cfg->n_layers; ++layer) {
-    const size_t t =
-        decode_plan(cfg, spec_of(cfg, layer), batch, n_q_heads, n_kv_heads, max_seq_len).total;
+    const size_t t = decode_plan(cfg, spec_of(cfg, layer), batch, n_q_heads, n_kv_heads,
+                                 max_seq_len, true).total;
     if (t > total) total = t;
   }
   return total;
@@ -817,7 +817,7 @@ static tq_status decode_prepare(const tq_config* cfg, const void* tables, int la
                                 const uint16_t* k_win, const uint16_t* v_win,
                                 const int32_t* seq_lens, int max_seq_len, float* out,
                                 void* workspace, size_t workspace_bytes, int step_new,
-                                int reserve, DecodeArgs* args, bool* empty) {
+                                bool step_split, DecodeArgs* args, bool* empty) {
   *empty = false;
   tq_status st = check_gpu_common(cfg, tables, layer);
   if (st != TQ_OK) return st;
@@ -848,12 +848,7 @@ static tq_status decode_prepare(const tq_config* cfg, const void* tables, int la
   long long max_nq = (long long)max_seq_len - W;
   if (max_nq > k.capacity || max_nq > v.capacity) return TQ_ERR_INVALID_ARG;
   tq_layer_spec s = spec_of(cfg, layer);
-  DecodePlan p = decode_plan(cfg, s, batch, n_q_heads, n_kv_heads, max_seq_len);
-  // a decode step leaves the append's CTA slots free only when its splits are
-  // short: then the append's latency weighs more than the share of the
-  // decode's work that those slots would have taken
-  if (reserve > 0 && p.split_tokens <= kStepReserveMaxSplit)
-    p = decode_plan(cfg, s, batch, n_q_heads, n_kv_heads, max_seq_len, reserve);
+  const DecodePlan p = decode_plan(cfg, s, batch, n_q_heads, n_kv_heads, max_seq_len, step_split);
   if (workspace_bytes < p.total) return TQ_ERR_BUFFER_TOO_SMALL;
   if ((long long)p.n_splits * n_kv_heads * batch >= (1ll << 31)) return TQ_ERR_UNSUPPORTED;
   DecodeArgs a{};
@@ -921,7 +916,7 @@ static tq_status decode_common(const tq_config* cfg, const void* tables, int lay
   bool empty = false;
   tq_status st = decode_prepare(cfg, tables, layer, q, q_dtype, softmax_scale, batch, n_q_heads,
                                 n_kv_heads, n_queries, k, v, k_win, v_win, seq_lens, max_seq_len,
-                                out, workspace, workspace_bytes, 0, 0, &a, &empty);
+                                out, workspace, workspace_bytes, 0, false, &a, &empty);
   if (st != TQ_OK) return st;
   if (batch == 0) return TQ_OK;
   if (empty) {
@@ -969,47 +964,54 @@ extern "C" tq_status tq_decode_step(const tq_config* cfg, const void* tables, in
   if (max_seq_len < 1) return TQ_ERR_INVALID_ARG;
   tq_status st = check_gpu_common(cfg, tables, layer);
   if (st != TQ_OK) return st;
-  if (spec_of(cfg, layer).k_mode != TQ_MODE_MSE_QJL && cfg->residual_window > 0) {
-    // one launch: the decode kernel appends the step's token itself (see
-    // DecodeArgs::fused_step); the inputs are checked as tq_append_kv checks them
-    if (!k_new || !v_new || !src_strides || !k_win || !v_win) return TQ_ERR_INVALID_ARG;
-    if (src_dtype != TQ_BF16 && src_dtype != TQ_F32) return TQ_ERR_INVALID_ARG;
-    if (src_dtype != TQ_BF16) return TQ_ERR_UNSUPPORTED;             // the ring is bf16
-    if (!aligned16(k_win) || !aligned16(v_win)) return TQ_ERR_ALIGNMENT;
-    if (!aligned16(k_new) || !aligned16(v_new)) return TQ_ERR_ALIGNMENT;
-    for (int i = 0; i < 2; ++i)
-      if (src_strides[i] < 0 || (src_strides[i] * 2) % 16 != 0) return TQ_ERR_ALIGNMENT;
-    DecodeArgs a{};
-    bool empty = false;
-    st = decode_prepare(cfg, tables, layer, q, q_dtype, softmax_scale, batch, n_q_heads, n_kv_heads,
-                        1, k, v, k_win, v_win, seq_lens_before, max_seq_len, out, workspace,
-                        workspace_bytes, 1, 0, &a, &empty);
-    if (st != TQ_OK) return st;
-    if (empty) return TQ_ERR_INVALID_ARG;            // unreachable with max_seq_len >= 1
-    a.fused_step = 1;
-    a.knew = k_new;
-    a.vnew = v_new;
-    a.new_f32 = 0;
-    a.nsb = src_strides[0];
-    a.nsh = src_strides[1];
-    return launch_decode(a, stream) == 0 ? TQ_OK : TQ_ERR_CUDA;
-  }
-  // keys in QJL mode, or no window: the append kernel, then the decode.  The
-  // append's CTAs (one per sequence and kv-head) run beside the decode's first
-  // wave: with few of them and short splits, the decode leaves their slots free
-  const long long units = (long long)batch * n_kv_heads;
-  const int reserve = units > 0 && units <= 16 ? (int)units : 0;
+  // one launch: the decode kernel appends the step's token itself (see
+  // DecodeArgs::fused_step); the inputs are checked as tq_append_kv checks them
+  const int W = cfg->residual_window;
+  if (!k_new || !v_new || !src_strides) return TQ_ERR_INVALID_ARG;
+  if (src_dtype != TQ_BF16 && src_dtype != TQ_F32) return TQ_ERR_INVALID_ARG;
+  if (W > 0 && src_dtype != TQ_BF16) return TQ_ERR_UNSUPPORTED;    // the ring is bf16
+  const int esz = src_dtype == TQ_F32 ? 4 : 2;
+  if (!aligned16(k_new) || !aligned16(v_new)) return TQ_ERR_ALIGNMENT;
+  for (int i = 0; i < 2; ++i)
+    if (src_strides[i] < 0 || (src_strides[i] * esz) % 16 != 0) return TQ_ERR_ALIGNMENT;
   DecodeArgs a{};
   bool empty = false;
   st = decode_prepare(cfg, tables, layer, q, q_dtype, softmax_scale, batch, n_q_heads, n_kv_heads,
                       1, k, v, k_win, v_win, seq_lens_before, max_seq_len, out, workspace,
-                      workspace_bytes, 1, reserve, &a, &empty);
+                      workspace_bytes, 1, true, &a, &empty);
   if (st != TQ_OK) return st;
   if (empty) return TQ_ERR_INVALID_ARG;              // unreachable with max_seq_len >= 1
-  st = tq_append_kv(cfg, tables, layer, k_new, v_new, src_dtype, src_strides, batch, n_kv_heads,
-                    1, seq_lens_before, k_win, v_win, k, v, stream);
-  if (st != TQ_OK) return st;
+  if (a.long_first) {   // see tq_decode_step_launches
+    // the one-launch plan takes more than one wave, so the splits that append
+    // the token would run after the others: the append kernel, then a plain
+    // decode of the grown sequences (which waits for the append at its start)
+    st = decode_prepare(cfg, tables, layer, q, q_dtype, softmax_scale, batch, n_q_heads,
+                        n_kv_heads, 1, k, v, k_win, v_win, seq_lens_before, max_seq_len, out,
+                        workspace, workspace_bytes, 1, false, &a, &empty);
+    if (st != TQ_OK) return st;
+    st = tq_append_kv(cfg, tables, layer, k_new, v_new, src_dtype, src_strides, batch, n_kv_heads,
+                      1, seq_lens_before, k_win, v_win, k, v, stream);
+    if (st != TQ_OK) return st;
+    return launch_decode(a, stream) == 0 ? TQ_OK : TQ_ERR_CUDA;
+  }
+  a.fused_step = 1;
+  a.knew = k_new;
+  a.vnew = v_new;
+  a.new_f32 = src_dtype == TQ_F32;
+  a.nsb = src_strides[0];
+  a.nsh = src_strides[1];
   return launch_decode(a, stream) == 0 ? TQ_OK : TQ_ERR_CUDA;
+}
+
+extern "C" int tq_decode_step_launches(const tq_config* cfg, int layer, int batch, int n_q_heads,
+                                       int n_kv_heads, int max_seq_len) {
+  if (check_config(cfg) != TQ_OK || layer < 0 || layer >= cfg->n_layers || batch < 1 ||
+      n_kv_heads < 1 || n_q_heads < n_kv_heads || n_q_heads % n_kv_heads != 0 || max_seq_len < 1)
+    return 0;
+  // the one-launch plan (with the step's splits) must be one wave
+  const DecodePlan p = decode_plan(cfg, spec_of(cfg, layer), batch, n_q_heads, n_kv_heads,
+                                   max_seq_len, true);
+  return p.long_first ? 2 : 1;
 }
 
 extern "C" tq_status tq_get_device_error(void* stream) {

@@ -71,9 +71,9 @@ struct DecodeSmem {
 // kernel's static tables and a fused decode step's scratch)
 constexpr int kDecodeSmemBudget = 216 * 1024;
 // a fused decode step's scratch after the CTA's dynamic shared memory (see
-// step_leaving_token): 128-byte alignment slack, two codebooks' boundaries
-// and 32 words of packing scratch
-constexpr int kFusedScratchBytes = 128 + 2 * 256 * 4 + 32 * 4;
+// step_leaving_token): 128-byte alignment slack, two codebooks' boundaries,
+// 32 words of packing scratch and 128 floats of residual scratch
+constexpr int kFusedScratchBytes = 128 + 2 * 256 * 4 + 32 * 4 + 128 * 4;
 
 // Warps of a decode CTA.  G <= 4 query columns with MSE keys (about 168
 // registers a thread): one CTA per SM of 12 warps, or 8 when 12 staging
@@ -222,9 +222,8 @@ struct DecodeArgs {
   int dsign;                     // keys in Direct Sign mode
   float sparse_thr;              // skip a chunk's V sum below this weight (0: never)
   int n_q;                       // query tokens per sequence (columns g: token g % n_q)
-  int step_new;                  // > 0: decode step.  seq_lens are the lengths before
-                                 // step_new tokens that the kernel launched just before
-                                 // this one appends (tq_decode_step); T = seq_lens + step_new
+  int step_new;                  // decode step (1, with fused_step): seq_lens are the
+                                 // lengths before the step's token; T = seq_lens + step_new
   const uint16_t* kwin; const uint16_t* vwin; int W;
   const int32_t* seq_lens;
   int max_seq_len;               // host bound on every T: a T outside [0, max_seq_len]
@@ -237,16 +236,16 @@ struct DecodeArgs {
                                  // splits (several waves), else split-major per pair
   int pdl_trigger;               // one wave of one CTA per SM: let the next decode's
                                  // CTAs start early (griddepcontrol.launch_dependents)
-  // decode step in one launch (fused_step = 1, step_new = 1, W > 0): the
-  // kernel also appends the step's token.  The quantized splits stop before
-  // plane row T - 1 - W (the token leaving the window); the pair's first window
-  // split quantizes that token from its ring slot into the planes, attends to
-  // its dequantized key and value, and writes the new token into the slot;
-  // the window splits read the new token from knew / vnew.  Keys in MSE or
-  // Direct Sign mode.
+  // decode step in one launch (fused_step = 1, step_new = 1): the kernel also
+  // appends the step's token.  The quantized splits stop before plane row
+  // T - 1 - W (the token leaving the window; with W = 0 the new token itself);
+  // the pair's first window split (with W = 0 a split of its own) quantizes
+  // that token into the planes, attends to its dequantized key and value, and
+  // with W > 0 writes the new token into the ring slot it leaves; the window
+  // splits read the new token from knew / vnew.
   int fused_step;
-  const void* knew; const void* vnew;   // [B][Hkv][.][d] bf16 rows
-  int new_f32;                   // unused (the ring, and so the fused step, is bf16)
+  const void* knew; const void* vnew;   // [B][Hkv][.][d] rows
+  int new_f32;                   // knew / vnew are fp32 (W = 0 only: the ring is bf16)
   int64_t nsb, nsh;              // element strides of knew / vnew (batch, head)
   // codec
   const float* ck; const float* cv;

@@ -471,6 +471,50 @@ __device__ __forceinline__ float warp_direct_sign(const float (&r)[4], uint8_t* 
   return scale;
 }
 
+// QJL sketch of a residual held by a warp as in warp_quantize_vals (lane l:
+// coordinates 4l..4l+3): gamma = ||r|| and bit j = [(S r)_j >= 0] for the
+// kQjlM rows of S (bf16, [m][d]); lane l computes rows l, l + 32, l + 64,
+// l + 96 ("TurboQuant KV 캐시 압축 for llama.cpp", "QJL 보정 효과").  rbuf: 128
+// floats of shared scratch.  Writes the 16 sign bytes and gamma, leaves the
+// sign words (bit j of word j / 32) in sb in every lane and returns gamma.
+__device__ __forceinline__ float warp_qjl_sketch(const float (&r)[4], const uint16_t* S, float* rbuf,
+                                                 uint8_t* signs_dst, float* gamma_dst, int lane,
+                                                 uint32_t (&sb)[4]) {
+  float g = r[0] * r[0];
+  g = fmaf(r[1], r[1], g);
+  g = fmaf(r[2], r[2], g);
+  g = fmaf(r[3], r[3], g);
+  const float gamma = sqrtf(warp_sum(g));
+  *(float4*)(rbuf + 4 * lane) = make_float4(r[0], r[1], r[2], r[3]);
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint4* Sj = (const uint4*)(S + (size_t)(32 * k + lane) * kD);
+    float z0 = 0.f, z1 = 0.f;
+#pragma unroll 4
+    for (int e = 0; e < kD / 8; ++e) {
+      const uint4 s8 = __ldg(Sj + e);
+      const float4 ra = *(const float4*)(rbuf + 8 * e);
+      const float4 rb = *(const float4*)(rbuf + 8 * e + 4);
+      z0 = fmaf(bf16lo(s8.x), ra.x, z0);
+      z1 = fmaf(bf16hi(s8.x), ra.y, z1);
+      z0 = fmaf(bf16lo(s8.y), ra.z, z0);
+      z1 = fmaf(bf16hi(s8.y), ra.w, z1);
+      z0 = fmaf(bf16lo(s8.z), rb.x, z0);
+      z1 = fmaf(bf16hi(s8.z), rb.y, z1);
+      z0 = fmaf(bf16lo(s8.w), rb.z, z0);
+      z1 = fmaf(bf16hi(s8.w), rb.w, z1);
+    }
+    sb[k] = __ballot_sync(0xffffffffu, z0 + z1 >= 0.f);
+  }
+  if (lane == 0) {
+    *(uint4*)signs_dst = make_uint4(sb[0], sb[1], sb[2], sb[3]);
+    *gamma_dst = gamma;
+  }
+  __syncwarp();      // rbuf is read by every lane before it is written again
+  return gamma;
+}
+
 // Direct Sign sketch of a residual held as pairs p[j] = (r_j, r_{j+64}): bit
 // i of the 128-bit sign vector is [r_i >= 0]; the scale is mean |r_i|
 // ("TurboQuant KV 캐시 압축 for llama.cpp", v1.1.0 "Direct Sign").

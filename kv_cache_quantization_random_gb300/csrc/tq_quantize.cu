@@ -134,39 +134,8 @@ __device__ __forceinline__ void append_quantize_row(const AppendArgs& a, int kin
   if (kind == 0 && a.dsign)
     warp_direct_sign(r, a.qjl_signs + drow * (kDim / 8), a.qjl_rnorm + drow, lane);
   if (kind == 0 && a.qjl) {
-    float g = r[0] * r[0];
-    g = fmaf(r[1], r[1], g);
-    g = fmaf(r[2], r[2], g);
-    g = fmaf(r[3], r[3], g);
-    const float gamma = sqrtf(warp_sum(g));
-    *(float4*)(rbuf + 4 * lane) = make_float4(r[0], r[1], r[2], r[3]);
-    __syncwarp();
     uint32_t sb[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint4* Sj = (const uint4*)(a.S + (size_t)(32 * k + lane) * kDim);
-      float z0 = 0.f, z1 = 0.f;
-#pragma unroll 4
-      for (int e = 0; e < kDim / 8; ++e) {
-        const uint4 s8 = __ldg(Sj + e);
-        const float4 ra = *(const float4*)(rbuf + 8 * e);
-        const float4 rb = *(const float4*)(rbuf + 8 * e + 4);
-        z0 = fmaf(bf16lo(s8.x), ra.x, z0);
-        z1 = fmaf(bf16hi(s8.x), ra.y, z1);
-        z0 = fmaf(bf16lo(s8.y), ra.z, z0);
-        z1 = fmaf(bf16hi(s8.y), ra.w, z1);
-        z0 = fmaf(bf16lo(s8.z), rb.x, z0);
-        z1 = fmaf(bf16hi(s8.z), rb.y, z1);
-        z0 = fmaf(bf16lo(s8.w), rb.z, z0);
-        z1 = fmaf(bf16hi(s8.w), rb.w, z1);
-      }
-      sb[k] = __ballot_sync(0xffffffffu, z0 + z1 >= 0.f);
-    }
-    if (lane == 0) {
-      *(uint4*)(a.qjl_signs + drow * (kQjlM / 8)) = make_uint4(sb[0], sb[1], sb[2], sb[3]);
-      a.qjl_rnorm[drow] = gamma;
-    }
-    __syncwarp();      // rbuf is read by every lane before the next vector writes it
+    warp_qjl_sketch(r, a.S, rbuf, a.qjl_signs + drow * (kQjlM / 8), a.qjl_rnorm + drow, lane, sb);
   }
 }
 

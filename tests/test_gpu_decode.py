@@ -394,9 +394,9 @@ def test_decode_multi_query_needs_the_hidden_tokens_in_the_window(B):
 @pytest.mark.parametrize("mode,W", [("mse", 16), ("sign", 16), ("qjl", 0)])
 def test_decode_step_with_host_mapped_inputs_and_output(B, mode, W):
     """The query, the new tokens and the output of tq_decode_step may be
-    pinned host memory, which the kernels read and write across the host link
-    (one launch with a window, two launches for QJL keys).  Planes, ring and
-    output must be bit-identical to the same step on device buffers."""
+    pinned host memory, which the kernel reads and writes across the host
+    link.  Planes, ring and output must be bit-identical to the same step on
+    device buffers."""
     import torch
     from kv_cache_quantization_random_gb300 import workloads as W_
     T0 = np.array([299, 37, max(W - 1, 0)], dtype=np.int64)
@@ -455,18 +455,22 @@ def test_decode_step_with_host_mapped_inputs_and_output(B, mode, W):
                                                   (3, 2, "sign", 0, 1, True),
                                                   (8, 8, "mse", 8, 1, False),
                                                   (4, 2, "mse", 128, 1, False),
-                                                  (4, 2, "mse", 16, 2, False)])
+                                                  (4, 2, "mse", 16, 2, False),
+                                                  (4, 2, "mse", 16, 14, False),
+                                                  (2, 3, "qjl", 0, 14, False)])
 def test_decode_step_matches_append_then_decode(B, kb, vb, mode, W, rep, f32):
-    """tq_decode_step (append of one token per sequence and decode: one launch
-    with a window and keys in MSE or Direct Sign mode, else the append kernel
-    then an overlapping decode) writes the same planes and ring as
-    tq_append_kv and returns the output of tq_decode_attention after it.  The
-    plane rows the append writes are zeroed beforehand, so a decode that read
-    them before they were written would differ.  The lengths cover a token
-    leaving the window from its ring slot (as the first and as the last row of
-    the quantized part), a ring slot that held no token (T0 < W), and W = 0
-    (two launches; the new token goes straight to the planes, from bf16 or
-    fp32 rows).  rep = 2 gives 24 (sequence, kv-head) pairs."""
+    """tq_decode_step (append of one token per sequence and decode, in one
+    launch) writes the same planes and ring as tq_append_kv and returns the
+    output of tq_decode_attention after it, within the decode tolerance (the
+    token the step quantizes enters its attention through fp32 dequantized
+    operands, not fp16 MMA operands).  The plane rows the append writes are
+    zeroed beforehand, so a decode that read them before they were written
+    would differ.  The lengths cover a token leaving the window from its ring
+    slot (as the first and as the last row of the quantized part), a ring slot
+    that held no token (T0 < W), and W = 0 (the new token goes straight to the
+    planes, from bf16 or fp32 rows); keys in MSE, Direct Sign and QJL mode.
+    rep = 2 gives 24 (sequence, kv-head) pairs; rep = 14 gives 168, whose
+    one-launch plan would take two waves, so the step takes two launches."""
     import torch
     from kv_cache_quantization_random_gb300 import workloads as W_
     T0 = np.tile(np.array([699, max(W - 1, 0), W, 0, 37, 300], dtype=np.int64), rep)
@@ -506,6 +510,7 @@ def test_decode_step_matches_append_then_decode(B, kb, vb, mode, W, rep, f32):
     before = torch.tensor(T0, dtype=torch.int32, device="cuda")
     after = before + 1
     ws = B.new_workspace(cfg, batch, hq, hkv, C)
+    assert B.tq_decode_step_launches(cfg, 0, batch, hq, hkv, C) == (2 if rep > 2 else 1)
     outs = [torch.empty(batch, hq, 128, device="cuda") for _ in range(2)]
     kp, vp, kw, vw = caches[0]
     B.tq_append_kv(cfg, tables, 0, kn, vn, before, kw, vw, kp, vp)
@@ -526,9 +531,4 @@ def test_decode_step_matches_append_then_decode(B, kb, vb, mode, W, rep, f32):
     if W:
         assert torch.equal(kwa.cpu(), kwb.cpu()) and torch.equal(vwa.cpu(), vwb.cpu())
     a, b = to64(outs[0]), to64(outs[1])
-    # the one-launch step attends to the token leaving the window through its
-    # dequantized fp32 key and value, where the two-launch decode takes its
-    # fp16 MMA operands: the two agree within the decode tolerance; the
-    # two-launch step runs the same decode as tq_decode_attention
-    fused = mode != "qjl" and W > 0
-    assert rel_l2_per_head(b, a).max() < (2e-3 if fused else 1e-5)
+    assert rel_l2_per_head(b, a).max() < 2e-3
