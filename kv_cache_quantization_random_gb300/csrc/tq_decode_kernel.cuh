@@ -564,7 +564,7 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
       seq_head = (i - nq_total) / nws;
       split = a.n_qsplits + (i - nq_total - seq_head * nws);
     }
-  }  }
+  }
   const int kvh = seq_head % a.Hkv, b = seq_head / a.Hkv;
   const int Hkv = a.Hkv;
   const uint32_t limit = a.wait_limit ? a.wait_limit : kDefaultWaitLimit;
