@@ -786,17 +786,7 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
         *bchk(qo + (4 * lane + c) * G + g, qo, kD2 * G * 4, a.err) = v;
         x[c] = v * sgs[c];
       }
-      const float u0 = x[0] + x[1], u1 = x[0] - x[1], u2 = x[2] + x[3], u3 = x[2] - x[3];
-      x[0] = u0 + u2; x[2] = u0 - u2; x[1] = u1 + u3; x[3] = u1 - u3;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const bool upper = (lane & o) != 0;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const float other = __shfl_xor_sync(0xffffffffu, x[c], o);
-          x[c] = upper ? other - x[c] : x[c] + other;
-        }
-      }
+      warp_fwht4(x, lane);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const float v = x[c] * 0.08838834764831845f;   // 1/sqrt(128)
@@ -1504,19 +1494,7 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
     if constexpr (WH == 1) {
       // one warp per head: no combine step
       float x[4] = {rot.x, rot.y, rot.z, rot.w};
-      {
-        float u0 = x[0] + x[1], u1 = x[0] - x[1], u2 = x[2] + x[3], u3 = x[2] - x[3];
-        x[0] = u0 + u2; x[2] = u0 - u2; x[1] = u1 + u3; x[3] = u1 - u3;
-      }
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const bool upper = (lane & o) != 0;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float other = __shfl_xor_sync(0xffffffffu, x[j], o);
-          x[j] = upper ? other - x[j] : x[j] + other;
-        }
-      }
+      warp_fwht4(x, lane);
       const float4 sv4 = *(const float4*)(svs + 4 * lane);
       const float rr = 0.08838834764831845f;
       const float inv = Lsum > 0.f ? 1.0f / Lsum : 0.f;
@@ -1551,19 +1529,7 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
       }
       // butterfly over 128 values, 4 per lane (coordinates 4*lane .. 4*lane+3)
       float x[4] = {rot.x, rot.y, rot.z, rot.w};
-      {
-        float u0 = x[0] + x[1], u1 = x[0] - x[1], u2 = x[2] + x[3], u3 = x[2] - x[3];
-        x[0] = u0 + u2; x[2] = u0 - u2; x[1] = u1 + u3; x[3] = u1 - u3;
-      }
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const bool upper = (lane & o) != 0;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float other = __shfl_xor_sync(0xffffffffu, x[j], o);
-          x[j] = upper ? other - x[j] : x[j] + other;
-        }
-      }
+      warp_fwht4(x, lane);
       const float4 sv4 = *(const float4*)(svs + 4 * lane);
       const float rr = 0.08838834764831845f;
       const float inv = Lsum > 0.f ? 1.0f / Lsum : 0.f;
