@@ -1008,6 +1008,8 @@ extern "C" int tq_decode_step_launches(const tq_config* cfg, int layer, int batc
   if (check_config(cfg) != TQ_OK || layer < 0 || layer >= cfg->n_layers || batch < 1 ||
       n_kv_heads < 1 || n_q_heads < n_kv_heads || n_q_heads % n_kv_heads != 0 || max_seq_len < 1)
     return 0;
+  const int G = n_q_heads / n_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return 0;   // query groups the decode implements
   // the one-launch plan (with the step's splits) must be one wave
   const DecodePlan p = decode_plan(cfg, spec_of(cfg, layer), batch, n_q_heads, n_kv_heads,
                                    max_seq_len, true);

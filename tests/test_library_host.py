@@ -192,3 +192,22 @@ def test_decode_step_validates_both_calls_before_launch(B):
     assert lib.tq_decode_step(C.byref(cfg.c()), 4096, 0, 16384, 0, 1.0, 0, 8, 8, 20480, 24576, 0,
                               strides, 28672, 10, None, None, planes, planes, 32768, 65536,
                               1 << 20, None) == 0      # empty batch: nothing to do
+
+
+def test_decode_step_launches(B):
+    """tq_decode_step takes one launch when its plan, with the splits that
+    append the token, fits one wave of the GPU, else two (the append kernel,
+    then the decode); 0 flags invalid sizes.  Host logic only."""
+    llama = B.Config(k_bits=4, v_bits=2, residual_window=128)
+    assert B.tq_decode_step_launches(llama, 0, 1, 32, 8, 32768) == 1
+    long_ctx = B.Config(k_bits=3, v_bits=3, residual_window=256)
+    assert B.tq_decode_step_launches(long_ctx, 0, 1, 64, 8, 1 << 20) == 1
+    single = B.Config(k_bits=3, v_bits=3)
+    assert B.tq_decode_step_launches(single, 0, 1, 1, 1, 1024) == 1
+    for mode in (B.TQ_MODE_MSE_QJL, B.TQ_MODE_MSE_SIGN):   # 128 pairs, two CTAs per SM
+        cfg = B.Config(k_bits=2, v_bits=3, k_mode=mode)
+        assert B.tq_decode_step_launches(cfg, 0, 16, 32, 8, 8192) == 2
+    assert B.tq_decode_step_launches(llama, 0, 84, 8, 2, 700) == 2   # 168 pairs, one CTA per SM
+    assert B.tq_decode_step_launches(llama, 0, 1, 32, 8, 0) == 0
+    assert B.tq_decode_step_launches(llama, 1, 1, 32, 8, 100) == 0   # layer out of range
+    assert B.tq_decode_step_launches(llama, 0, 1, 24, 8, 100) == 0   # group size 3
