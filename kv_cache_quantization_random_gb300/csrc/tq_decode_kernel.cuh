@@ -421,6 +421,13 @@ __device__ __forceinline__ void qjl_scores(uint32_t sa, uint32_t sb, const uint3
   }
 }
 
+// Bytes spanned by a decode step's new-token rows knew / vnew ([B][Hkv][.][d],
+// element strides nsb, nsh), for the bounds-checked build.
+__device__ __forceinline__ size_t new_rows_bytes(const DecodeArgs& a) {
+  return (size_t)((long long)(a.B - 1) * a.nsb + (long long)(a.Hkv - 1) * a.nsh + kD2) *
+         (a.new_f32 ? 4 : 2);
+}
+
 // Decode step in one launch (DecodeArgs::fused_step): the token L = T - 1 - W
 // that leaves the window (with W = 0 the new token itself), handled by warp 0
 // of its pair's first window split.  The warp reads L's rows (ring slot
@@ -447,8 +454,13 @@ static __device__ __noinline__ void step_leaving_token(const DecodeArgs& a, long
   const long long ring = a.W > 0 ? (pair * a.W + L % a.W) * kD2 : 0;
   const long long noff = (pair / a.Hkv) * a.nsb + (pair % a.Hkv) * a.nsh;
   const size_t ring_bytes_ = (size_t)a.B * a.Hkv * a.W * kD2 * 2;
+  const size_t nrow = (size_t)kD2 * (a.new_f32 ? 4 : 2);
+  const uint8_t* kn_ = (const uint8_t*)a.knew + noff * (a.new_f32 ? 4 : 2);
+  const uint8_t* vn_ = (const uint8_t*)a.vnew + noff * (a.new_f32 ? 4 : 2);
   if (!bchk_range(kc, 16 * a.kb, a.kc, (size_t)a.B * a.Hkv * a.kcap * 16 * a.kb, a.err) ||
       !bchk_range(vc, 16 * a.vb, a.vc, (size_t)a.B * a.Hkv * a.vcap * 16 * a.vb, a.err) ||
+      !bchk_range(kn_, nrow, a.knew, new_rows_bytes(a), a.err) ||
+      !bchk_range(vn_, nrow, a.vnew, new_rows_bytes(a), a.err) ||
       (a.W > 0 && !bchk_range(a.kwin + ring, kD2 * 2, a.kwin, ring_bytes_, a.err))) {
     for (int c = 0; c < 4; ++c) kx[c] = vx[c] = 0.f;
     return;
@@ -1322,6 +1334,12 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
       const long long noff = (long long)b * a.nsb + (long long)kvh * a.nsh;
       knrow = (const uint16_t*)a.knew + noff;
       vnrow = (const uint16_t*)a.vnew + noff;
+      // bounds-checked build: rows outside the step's input read its first row
+      if (!bchk_range(knrow, kD2 * 2, a.knew, new_rows_bytes(a), a.err) ||
+          !bchk_range(vnrow, kD2 * 2, a.vnew, new_rows_bytes(a), a.err)) {
+        knrow = (const uint16_t*)a.knew;
+        vnrow = (const uint16_t*)a.vnew;
+      }
       if (split == a.n_qsplits && warp == 0) {
         if (nq > 0) {
           float kx[4], vx[4];
