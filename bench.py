@@ -837,6 +837,16 @@ def run_e2e(B, w, cfg, tables, reps, R, q, knew, vnew, seq_before, Tmax, out, ws
                                            "another"}}
 
 
+def append_launches(w, kb, vb, n_new):
+    """Kernel launches of one tq_append_kv (the library's dispatch): one for at
+    most 8 new tokens per sequence (the append kernel); above that one bulk
+    launch for keys and values of one bit width (bf16 rows, keys not in QJL
+    mode), else one per kind."""
+    if n_new <= 8:
+        return 1
+    return 1 if kb == vb and not w.k_qjl else 2
+
+
 # ------------------------------------------------------------ 36 layers
 def run_layered(args, w, rank, world, local):
     """The serving workload: every step appends new_tokens tokens per
@@ -950,18 +960,27 @@ def run_layered(args, w, rank, world, local):
         o += n
     outh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
 
+    # the query and every layer's new tokens become views of the device buffer
+    # that one host-to-device copy fills each step
+    dbuf.copy_(hbuf)
+    views, oo = [], 0
+    for t, n in zip(parts, nbytes):
+        views.append(dbuf[oo:oo + n].view(t.dtype).view(t.shape))
+        oo += n
+    kept = [q] + [(c["knew"], c["vnew"]) for c in layers]   # the graphs above hold their pointers
+    q = views[0]
+    for l, c in enumerate(layers):
+        c["knew"], c["vnew"] = views[1 + 2 * l], views[2 + 2 * l]
+
     def e2e_step(_):
         dbuf.copy_(hbuf, non_blocking=True)
-        oo = 0
-        for t, n in zip(parts, nbytes):
-            t.view(-1).view(torch.uint8).copy_(dbuf[oo:oo + n])
-            oo += n
         step(0)
         outh.copy_(out, non_blocking=True)
 
     e2e_step(0)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(graph_ms(graph_of(e2e_step, 1), 1, min_seconds=0.5), device)
+    del kept
 
     parity = None
     if not args.no_parity and rank == 0:
@@ -1000,7 +1019,7 @@ def run_layered(args, w, rank, world, local):
         "e2e": {"value": whole_job_rate(tokens_per_step, e2e_ms, world), "unit": "tokens/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": total_in,
                 "d2h_bytes_per_step": outh.numel() * outh.element_size(), "pipelined": False},
-        "gpu_launches": K_steps * 2 * L * n_reps,
+        "gpu_launches": K_steps * n_reps * sum(1 + append_launches(w, kb, vb, n_new) for kb, vb in fm),
         "clocks": clocks,
         "parity": parity,
     }
