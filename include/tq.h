@@ -44,11 +44,12 @@
  *
  * Memory and ownership: the caller allocates every buffer (device memory for
  * planes, tables, workspace, inputs and outputs); the library allocates
- * nothing at run time.  The query, the new tokens (k_new, v_new) and the
- * output of the decode calls may instead be pinned host memory that the
- * device can address (any page-locked allocation on a system with unified
- * addressing): the kernels then read and write them across the host link,
- * which for a decode step's few kilobytes costs less than separate copies.
+ * nothing at run time.  The query and the output of the decode calls, and
+ * the new tokens (k_new, v_new) of tq_decode_step, may instead be pinned host
+ * memory that the device can address (any page-locked allocation on a system
+ * with unified addressing): the kernels then read and write them across the
+ * host link, which for a decode step's few kilobytes costs less than separate
+ * copies.  The other calls take device memory.
  * Its device state is one error word per translation unit plus, on every GPU
  * that loads it, the fixed 8 MiB scratch array of tq_decode_attention_noalloc
  * (reserved at load time, held until exit).  Every device call is
