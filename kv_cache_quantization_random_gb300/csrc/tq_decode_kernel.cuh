@@ -13,7 +13,7 @@
 //
 // One CTA = (split, kv-head, sequence): with MSE keys one CTA per SM of 12
 // (or 8) warps for G <= 4 query columns and of 8 warps for G = 8; with a key
-// residual term two of 4 warps (decode_warps).  Prologue: the G query heads
+// residual term two or three of 4 warps (decode_warps, decode_ctas_per_sm).  Prologue: the G query heads
 // of the kv-head are scaled by softmax_scale*log2(e), rotated with the K sign
 // vector and split into fp16 hi + lo MMA operands held in registers; QJL keys
 // also get S q_rot as hi + lo operands.  Main loop, per warp and 32-token

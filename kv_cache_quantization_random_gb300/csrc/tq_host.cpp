@@ -492,7 +492,13 @@ static DecodePlan decode_plan(const tq_config* cfg, const tq_layer_spec& s, int 
     // window splits run after them, longest first), at least one per pair
     slots = (wave / units > 0 ? wave / units : 1) * units;
   }
-  long long per = units > 0 ? (units * max_nq + slots - 1) / slots : 0;
+  // the same number of quantized splits for every pair, as many as the slots
+  // allow: cutting the pairs' tokens into slots-many pieces instead leaves a
+  // ragged second wave (measured on 128 pairs of 8,192 tokens at two CTAs per
+  // SM: 89.2 us for 3 splits of 3,456 tokens in two waves, 80.1 us for 2
+  // splits of 4,096 in one)
+  const long long k = units > 0 ? slots / units : 1;
+  long long per = k > 0 ? (max_nq + k - 1) / k : max_nq;
   long long st = (per + 31) / 32 * 32;
   if (st < 256) st = 256;
   p.split_tokens = (int)st;
@@ -511,16 +517,35 @@ extern "C" size_t tq_workspace_bytes(const tq_config* cfg, int batch, int n_q_he
   if (check_config(cfg) != TQ_OK || batch < 0 || n_kv_heads < 1 || n_q_heads < n_kv_heads ||
       max_seq_len < 0)
     return 0;
-  // the largest plan over the layers' formats (a decode step's, which with
-  // W = 0 has one split more per pair, covers a plain decode's)
+  // the largest plan over the layers' formats, a plain decode's or a decode
+  // step's (which with W = 0 has one split more per pair)
   size_t total = 0;
   for (int layer = 0; layer < cfg->n_layers; ++layer) {
-    const size_t t = decode_plan(cfg, spec_of(cfg, layer), batch, n_q_heads, n_kv_heads,
-                                 max_seq_len, true).total;
-    if (t > total) total = t;
+    for (int step = 0; step < 2; ++step) {
+      const size_t t = decode_plan(cfg, spec_of(cfg, layer), batch, n_q_heads, n_kv_heads,
+                                   max_seq_len, step == 1).total;
+      if (t > total) total = t;
+    }
   }
   return total;
 }
+
+namespace tq {
+// A decode step runs in one launch when its plan (with the splits that append
+// the token) is one wave and gives the quantized splits no more tokens than a
+// plain decode's plan: with W = 0 the step's extra split per pair can cost the
+// pairs a quantized split (measured: on 128 pairs at three CTAs per SM, 3
+// splits of 2,752 tokens became 2 of 4,096 and the step took 111 us against
+// 90 us as an append and a decode).  Otherwise the append kernel runs first
+// and a plain decode after it.
+static bool step_one_launch(const tq_config* cfg, int layer, int batch, int n_q_heads,
+                            int n_kv_heads, int max_seq_len) {
+  const tq_layer_spec s = spec_of(cfg, layer);
+  const DecodePlan ps = decode_plan(cfg, s, batch, n_q_heads, n_kv_heads, max_seq_len, true);
+  const DecodePlan pd = decode_plan(cfg, s, batch, n_q_heads, n_kv_heads, max_seq_len, false);
+  return !ps.long_first && ps.split_tokens <= pd.split_tokens;
+}
+}  // namespace tq
 
 namespace tq {
 // Byte range [*off, *off + *bytes) of the split counters in the workspace of a
@@ -976,19 +1001,16 @@ extern "C" tq_status tq_decode_step(const tq_config* cfg, const void* tables, in
     if (src_strides[i] < 0 || (src_strides[i] * esz) % 16 != 0) return TQ_ERR_ALIGNMENT;
   DecodeArgs a{};
   bool empty = false;
+  const bool one = batch > 0 && n_kv_heads >= 1 && n_q_heads >= n_kv_heads &&
+                   step_one_launch(cfg, layer, batch, n_q_heads, n_kv_heads, max_seq_len);
   st = decode_prepare(cfg, tables, layer, q, q_dtype, softmax_scale, batch, n_q_heads, n_kv_heads,
                       1, k, v, k_win, v_win, seq_lens_before, max_seq_len, out, workspace,
-                      workspace_bytes, 1, true, &a, &empty);
+                      workspace_bytes, 1, one, &a, &empty);
   if (st != TQ_OK) return st;
   if (empty) return TQ_ERR_INVALID_ARG;              // unreachable with max_seq_len >= 1
-  if (a.long_first) {   // see tq_decode_step_launches
-    // the one-launch plan takes more than one wave, so the splits that append
-    // the token would run after the others: the append kernel, then a plain
-    // decode of the grown sequences (which waits for the append at its start)
-    st = decode_prepare(cfg, tables, layer, q, q_dtype, softmax_scale, batch, n_q_heads,
-                        n_kv_heads, 1, k, v, k_win, v_win, seq_lens_before, max_seq_len, out,
-                        workspace, workspace_bytes, 1, false, &a, &empty);
-    if (st != TQ_OK) return st;
+  if (!one) {   // see step_one_launch
+    // the append kernel, then a plain decode of the grown sequences (which
+    // waits for the append at its start)
     st = tq_append_kv(cfg, tables, layer, k_new, v_new, src_dtype, src_strides, batch, n_kv_heads,
                       1, seq_lens_before, k_win, v_win, k, v, stream);
     if (st != TQ_OK) return st;
@@ -1010,10 +1032,7 @@ extern "C" int tq_decode_step_launches(const tq_config* cfg, int layer, int batc
     return 0;
   const int G = n_q_heads / n_kv_heads;
   if (G != 1 && G != 2 && G != 4 && G != 8) return 0;   // query groups the decode implements
-  // the one-launch plan (with the step's splits) must be one wave
-  const DecodePlan p = decode_plan(cfg, spec_of(cfg, layer), batch, n_q_heads, n_kv_heads,
-                                   max_seq_len, true);
-  return p.long_first ? 2 : 1;
+  return step_one_launch(cfg, layer, batch, n_q_heads, n_kv_heads, max_seq_len) ? 1 : 2;
 }
 
 extern "C" tq_status tq_get_device_error(void* stream) {

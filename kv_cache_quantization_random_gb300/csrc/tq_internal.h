@@ -78,7 +78,7 @@ constexpr int kFusedScratchBytes = 128 + 2 * 256 * 4 + 32 * 4 + 128 * 4;
 // Warps of a decode CTA.  G <= 4 query columns with MSE keys (about 168
 // registers a thread): one CTA per SM of 12 warps, or 8 when 12 staging
 // rings do not fit.  G = 8 with MSE keys (about 240 registers): one CTA of 8
-// warps.  Keys with a residual term: two CTAs of 4 warps per SM, so that one
+// warps.  Keys with a residual term: two or three CTAs of 4 warps per SM, so that one
 // CTA's prologue runs beside the other's main loop (measured faster for these
 // formats).  Fewer, wider CTAs build the SM's lookup tables once and leave
 // half as many splits to merge.
@@ -89,13 +89,20 @@ __host__ __device__ constexpr int decode_warps(int G, int kb, int vb, int res) {
          : DecodeSmem(G, res, kb, vb, 8).total <= kDecodeSmemBudget  ? 8
                                                                        : 4;
 }
-// resident decode CTAs per SM: two CTAs of 4 warps when both fit in the SM's
-// shared memory (227 KB usable, less the kernel's 3 KB of static tables), else one
+// resident decode CTAs per SM: CTAs of 4 warps three (or two) to an SM when
+// they fit in its 228 KB of shared memory, each with its dynamic shared memory,
+// a decode step's scratch, up to 4.5 KB of static tables and 1 KB the system
+// reserves per CTA; else one.  Three CTAs (G <= 4 query heads) cap a thread
+// at 168 registers, which the 2-bit-key, 3-bit-value formats with a residual
+// term meet without spills (measured faster than two CTAs); with G = 8 the
+// register cap would spill.
 __host__ __device__ constexpr int decode_ctas_per_sm(int G, int kb, int vb, int res) {
-  return decode_warps(G, kb, vb, res) == 4 &&
-                 2 * (DecodeSmem(G, res, kb, vb, 4).total + 4 * 1024) <= 227 * 1024
-             ? 2
-             : 1;
+  return decode_warps(G, kb, vb, res) != 4 ? 1
+         : G <= 4 && 3 * (DecodeSmem(G, res, kb, vb, 4).total + kFusedScratchBytes + 5632) <=
+                         228 * 1024
+             ? 3
+         : 2 * (DecodeSmem(G, res, kb, vb, 4).total + 4 * 1024) <= 227 * 1024 ? 2
+                                                                             : 1;
 }
 
 // ---- device tables (built on the host by tq_build_tables) -------------------

@@ -457,7 +457,7 @@ def test_decode_step_with_host_mapped_inputs_and_output(B, mode, W):
                                                   (4, 2, "mse", 128, 1, False),
                                                   (4, 2, "mse", 16, 2, False),
                                                   (4, 2, "mse", 16, 14, False),
-                                                  (2, 3, "qjl", 0, 14, False)])
+                                                  (2, 3, "qjl", 0, 20, False)])
 def test_decode_step_matches_append_then_decode(B, kb, vb, mode, W, rep, f32):
     """tq_decode_step (append of one token per sequence and decode, in one
     launch) writes the same planes and ring as tq_append_kv and returns the
@@ -469,8 +469,10 @@ def test_decode_step_matches_append_then_decode(B, kb, vb, mode, W, rep, f32):
     slot (as the first and as the last row of the quantized part), a ring slot
     that held no token (T0 < W), and W = 0 (the new token goes straight to the
     planes, from bf16 or fp32 rows); keys in MSE, Direct Sign and QJL mode.
-    rep = 2 gives 24 (sequence, kv-head) pairs; rep = 14 gives 168, whose
-    one-launch plan would take two waves, so the step takes two launches."""
+    rep = 2 gives 24 (sequence, kv-head) pairs; rep = 14 gives 168 and rep =
+    20 gives 240, whose one-launch plans would take two waves (one CTA per SM
+    for these MSE keys, three for these QJL keys), so the step takes two
+    launches."""
     import torch
     from kv_cache_quantization_random_gb300 import workloads as W_
     T0 = np.tile(np.array([699, max(W - 1, 0), W, 0, 37, 300], dtype=np.int64), rep)

@@ -204,7 +204,9 @@ def test_decode_step_launches(B):
     assert B.tq_decode_step_launches(long_ctx, 0, 1, 64, 8, 1 << 20) == 1
     single = B.Config(k_bits=3, v_bits=3)
     assert B.tq_decode_step_launches(single, 0, 1, 1, 1, 1024) == 1
-    for mode in (B.TQ_MODE_MSE_QJL, B.TQ_MODE_MSE_SIGN):   # 128 pairs, two CTAs per SM
+    # 128 pairs at three CTAs per SM: a plain decode gives each pair 3 quantized
+    # splits, the step's plan (one split more per pair for the token) only 2
+    for mode in (B.TQ_MODE_MSE_QJL, B.TQ_MODE_MSE_SIGN):
         cfg = B.Config(k_bits=2, v_bits=3, k_mode=mode)
         assert B.tq_decode_step_launches(cfg, 0, 16, 32, 8, 8192) == 2
     assert B.tq_decode_step_launches(llama, 0, 84, 8, 2, 700) == 2   # 168 pairs, one CTA per SM
