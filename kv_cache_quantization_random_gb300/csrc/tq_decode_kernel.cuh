@@ -593,10 +593,11 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
 
   // ------------------------------------------------------------- prologue
   // The codec tables are loaded and the lookup tables built before the
-  // dependency wait; the sequence length and the bulk copy of each warp's
-  // first chunk come right after it, the query rotation overlaps the copies'
-  // flight, and each warp's later chunks follow the CTA barrier of the query
-  // scale, so that the first chunks of all warps are not queued behind them.
+  // dependency wait; right after it come the loads of the sequence length and
+  // the query, then the bulk copy of each warp's first chunk (before the
+  // length has arrived), the query rotation overlaps the copies' flight, and
+  // each warp's later chunks follow the CTA barrier of the query scale, so
+  // that the first chunks of all warps are not queued behind them.
   __shared__ float cks[256], cvs[256];
   // fused decode step: the codebooks' boundaries and 32 words of packing
   // scratch after the dynamic shared memory (see step_leaving_token)
@@ -691,22 +692,31 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
   // to finish
   asm volatile("griddepcontrol.wait;" ::: "memory");
   int T = *bchk(a.seq_lens + b, a.seq_lens, (size_t)a.B * 4, a.err) + a.step_new;
-  // a length outside the plan's range would read past this pair's plane rows
-  // or ring: flag it and decode the sequence as empty
-  if (T < 0 || T > a.max_seq_len) {
-    if (tid == 0) atomicOr(a.err, kErrBounds);
-    T = 0;
+  // the query's loads go out before any bulk copy, so that they are not
+  // queued behind the copies' burst
+  const long long qbase = ((long long)b * a.Hq + (long long)kvh * G) * kD2;
+  float qv[GW][4];
+#pragma unroll
+  for (int j = 0; j < GW; ++j) {
+    const int g = warp + kDWarps * j;
+    qv[j][0] = qv[j][1] = qv[j][2] = qv[j][3] = 0.f;
+    if (g < G) {
+      if (a.q_f32) {
+        const float4 v = __ldg(bchk((const float4*)((const float*)a.q + qbase + g * kD2) + lane,
+                                    a.q, (size_t)a.B * a.Hq * kD2 * 4, a.err));
+        qv[j][0] = v.x; qv[j][1] = v.y; qv[j][2] = v.z; qv[j][3] = v.w;
+      } else {
+        const uint2 v = __ldg(bchk((const uint2*)((const uint16_t*)a.q + qbase + g * kD2) + lane,
+                                   a.q, (size_t)a.B * a.Hq * kD2 * 2, a.err));
+        qv[j][0] = bf16lo(v.x); qv[j][1] = bf16hi(v.x); qv[j][2] = bf16lo(v.y); qv[j][3] = bf16hi(v.y);
+      }
+    }
   }
-  const int nq = T - W > 0 ? T - W : 0;
-  // this split's token range (quantized splits); in a fused decode step the
-  // window split takes row nq - 1, the token leaving the window
-  int t_end = t_begin + a.split_tokens;
-  if (t_end > nq - a.fused_step) t_end = nq - a.fused_step;
 
-  // chunk c0 -> ring slot: codes by bulk copy; norms by bulk copy when the
-  // 16-byte-rounded range stays inside the plane, else by plain loads
-  auto issue = [&](int c0, int slot) {
-    const int nv = t_end - c0 < 32 ? t_end - c0 : 32;
+  // rows c0 .. c0 + nv - 1 -> ring slot: codes by bulk copy; norms by bulk
+  // copy when the 16-byte-rounded range stays inside the plane, else by plain
+  // loads
+  auto issue = [&](int c0, int slot, int nv) {
     const int n4 = (nv + 3) & ~3;
     // bulk copies need 16-byte aligned sources: the norm rows of a (sequence,
     // head) start at row0 * capacity floats, aligned only if capacity % 4 == 0
@@ -760,28 +770,31 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
       }
     }
   };
-  const long long qbase = ((long long)b * a.Hq + (long long)kvh * G) * kD2;
-  float qv[GW][4];
-#pragma unroll
-  for (int j = 0; j < GW; ++j) {
-    const int g = warp + kDWarps * j;
-    qv[j][0] = qv[j][1] = qv[j][2] = qv[j][3] = 0.f;
-    if (g < G) {
-      if (a.q_f32) {
-        const float4 v = __ldg(bchk((const float4*)((const float*)a.q + qbase + g * kD2) + lane,
-                                    a.q, (size_t)a.B * a.Hq * kD2 * 4, a.err));
-        qv[j][0] = v.x; qv[j][1] = v.y; qv[j][2] = v.z; qv[j][3] = v.w;
-      } else {
-        const uint2 v = __ldg(bchk((const uint2*)((const uint16_t*)a.q + qbase + g * kD2) + lane,
-                                   a.q, (size_t)a.B * a.Hq * kD2 * 2, a.err));
-        qv[j][0] = bf16lo(v.x); qv[j][1] = bf16hi(v.x); qv[j][2] = bf16lo(v.y); qv[j][3] = bf16hi(v.y);
-      }
-    }
+  // Each warp's first chunk of a quantized split goes in flight while the
+  // sequence length is still on its way: 32 whole rows when they lie inside
+  // the planes (rows past the split's last token are staged but never used:
+  // their scores are masked and their value weights are zero).
+  const int c_first = t_begin + 32 * warp;
+  const bool spec0 =
+      !window_split && (long long)c_first + 32 <= a.kcap && (long long)c_first + 32 <= a.vcap;
+  if (spec0) issue(c_first, 0, 32);
+  // a length outside the plan's range would read past this pair's plane rows
+  // or ring: flag it and decode the sequence as empty
+  if (T < 0 || T > a.max_seq_len) {
+    if (tid == 0) atomicOr(a.err, kErrBounds);
+    T = 0;
   }
-  // every warp's first chunk (c = t_begin + 32 warp) goes in flight now; its
-  // next NS - 2 follow after the CTA barrier below, so that the first chunks
-  // of all warps are not queued behind the later ones
-  if (!window_split && t_begin + 32 * warp < t_end) issue(t_begin + 32 * warp, 0);
+  const int nq = T - W > 0 ? T - W : 0;
+  // this split's token range (quantized splits); in a fused decode step the
+  // window split takes row nq - 1, the token leaving the window
+  int t_end = t_begin + a.split_tokens;
+  if (t_end > nq - a.fused_step) t_end = nq - a.fused_step;
+  auto rows_of = [&](int c0) { return t_end - c0 < 32 ? t_end - c0 : 32; };
+  // a first chunk that reaches the planes' last rows goes in flight now, with
+  // the rows the split holds; every warp's next NS - 2 chunks follow after the
+  // CTA barrier below, so that the first chunks of all warps are not queued
+  // behind the later ones
+  if (!window_split && !spec0 && c_first < t_end) issue(c_first, 0, rows_of(c_first));
 
   // query rotation in registers: warp w rotates heads w (and w + 4), lane l
   // holds coordinates 4l .. 4l+3; two butterfly stages in the lane, five by shuffles
@@ -816,7 +829,7 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
 #pragma unroll
     for (int j = 1; j < NS - 1; ++j) {
       const int c = t_begin + 32 * warp + 32 * kDWarps * j;
-      if (c < t_end) issue(c, j);
+      if (c < t_end) issue(c, j, rows_of(c));
     }
   }
 #pragma unroll
@@ -948,7 +961,7 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
       // the chunk NS - 1 ahead goes into the slot released at the end of the
       // previous iteration
       const int c1 = c0 + 32 * kDWarps * (NS - 1);
-      if (c1 < t_end) issue(c1, (kq + NS - 1) % NS);
+      if (c1 < t_end) issue(c1, (kq + NS - 1) % NS, rows_of(c1));
       ok = __all_sync(0xffffffffu, mbar_wait(bar + slot, (kq / NS) & 1, limit, a.err));
       if (!ok) break;
       const int nv = t_end - c0 < 32 ? t_end - c0 : 32;
@@ -1241,6 +1254,15 @@ __global__ void __launch_bounds__(32 * decode_warps(G, KB, VB, RES),
         __syncwarp();
         for (uint32_t i = 0; i < limit && !mbar_try_wait(bar + kk % NS, (kk / NS) & 1); ++i) {
         }
+      }
+    }
+    if (spec0 && c_first >= t_end) {
+      // the first chunk went in flight before the length was known and holds
+      // no token of this split: let it land (bounded wait) before the ring's
+      // memory is reused
+      if (lane == 0 && a.extra_tx != 0) mbar_complete_tx(bar, a.extra_tx);
+      __syncwarp();
+      for (uint32_t i = 0; i < limit && !mbar_try_wait(bar, 0); ++i) {
       }
     }
     // per-head l: sum over the 8 lanes of each column group
