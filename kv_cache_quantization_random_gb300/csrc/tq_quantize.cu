@@ -121,41 +121,96 @@ __global__ void __launch_bounds__(kQRows, 3)
 // Warp 0 quantizes the keys and warp 1 the values that leave the window (or
 // go straight to the planes), see warp_quantize_row; lane l owns coordinates 4l..4l+3, so the
 // Walsh-Hadamard butterfly takes two in-register stages and five shuffle
-// stages.  After a CTA barrier (every ring slot that is about to be
-// overwritten has been read) all threads write the new tokens into the ring.
-__device__ __forceinline__ void append_quantize_row(const AppendArgs& a, int kind, const void* src,
-                                                    int f32, long long drow, const float* bnd,
-                                                    const float* cen, float4 sg, uint32_t* words,
-                                                    float* rbuf, int lane) {
-  constexpr int kDim = 128;
-  float r[4], yq[4];
-  warp_quantize_row(src, f32, sg, a.bits[kind], bnd, cen, a.codes[kind] + drow * (16 * a.bits[kind]),
-                    a.norms[kind] + drow, words, lane, r, yq);
-  if (kind == 0 && a.dsign)
-    warp_direct_sign(r, a.qjl_signs + drow * (kDim / 8), a.qjl_rnorm + drow, lane);
-  if (kind == 0 && a.qjl) {
-    uint32_t sb[4];
-    warp_qjl_sketch(r, a.S, rbuf, a.qjl_signs + drow * (kQjlM / 8), a.qjl_rnorm + drow, lane, sb);
+// stages.  QJL keys take three more warps (2-4): each of the four key warps
+// quantizes the key (only warp 0 stores codes and norm) and computes a quarter
+// of its sketch, so that the m = 128 projections run four at a time instead of
+// one after another.  After a CTA barrier (every ring slot that is about to
+// be overwritten has been read) all threads write the new tokens into the ring.
+constexpr int kAppendQjlWarps = 5;
+
+// Rows 32 s + lane of S r, for slice s of the QJL sketch of the key residual
+// r (lane l: coordinates 4l..4l+3; "TurboQuant KV 캐시 압축 for llama.cpp",
+// "QJL 보정 효과"): sign word s of the 16 sign bytes, and for s = 0 gamma =
+// ||r||.  The products are summed in the order of warp_qjl_sketch, so both
+// give the same bits.  rbuf: 128 floats of this warp's shared scratch.
+__device__ __forceinline__ void append_qjl_slice(const float (&r)[4], const uint16_t* S, float* rbuf,
+                                                 uint8_t* signs_dst, float* gamma_dst, int lane,
+                                                 int s) {
+  if (s == 0) {
+    float g = r[0] * r[0];
+    g = fmaf(r[1], r[1], g);
+    g = fmaf(r[2], r[2], g);
+    g = fmaf(r[3], r[3], g);
+    const float gamma = sqrtf(warp_sum(g));
+    if (lane == 0) *gamma_dst = gamma;
   }
+  *(float4*)(rbuf + 4 * lane) = make_float4(r[0], r[1], r[2], r[3]);
+  __syncwarp();
+  const uint4* Sj = (const uint4*)(S + (size_t)(32 * s + lane) * kD);
+  float z0 = 0.f, z1 = 0.f;
+#pragma unroll 4
+  for (int e = 0; e < kD / 8; ++e) {
+    const uint4 s8 = __ldg(Sj + e);
+    const float4 ra = *(const float4*)(rbuf + 8 * e);
+    const float4 rb = *(const float4*)(rbuf + 8 * e + 4);
+    z0 = fmaf(bf16lo(s8.x), ra.x, z0);
+    z1 = fmaf(bf16hi(s8.x), ra.y, z1);
+    z0 = fmaf(bf16lo(s8.y), ra.z, z0);
+    z1 = fmaf(bf16hi(s8.y), ra.w, z1);
+    z0 = fmaf(bf16lo(s8.z), rb.x, z0);
+    z1 = fmaf(bf16hi(s8.z), rb.y, z1);
+    z0 = fmaf(bf16lo(s8.w), rb.z, z0);
+    z1 = fmaf(bf16hi(s8.w), rb.w, z1);
+  }
+  const uint32_t w = __ballot_sync(0xffffffffu, z0 + z1 >= 0.f);
+  if (lane == 0) ((uint32_t*)signs_dst)[s] = w;
+  __syncwarp();      // rbuf is read by every lane before it is written again
 }
 
-__global__ void __launch_bounds__(64) append_kernel(const AppendArgs a) {
+// One row of kind `kind` by one warp.  slice: which quarter of a QJL key's
+// sketch this warp computes; the warp of slice 0 stores the codes and norm,
+// the others quantize into their scratch (16 * 8 bytes of codes, one norm).
+__device__ __forceinline__ void append_quantize_row(const AppendArgs& a, int kind, int slice,
+                                                    const void* src, int f32, long long drow,
+                                                    const float* bnd, const float* cen, float4 sg,
+                                                    uint32_t* words, float* rbuf, uint8_t* scratch,
+                                                    int lane) {
+  constexpr int kDim = 128;
+  float r[4], yq[4];
+  const bool own = slice == 0;
+  warp_quantize_row(src, f32, sg, a.bits[kind], bnd, cen,
+                    own ? a.codes[kind] + drow * (16 * a.bits[kind]) : scratch,
+                    own ? a.norms[kind] + drow : (float*)(scratch + 128), words, lane, r, yq);
+  if (kind == 0 && a.dsign)
+    warp_direct_sign(r, a.qjl_signs + drow * (kDim / 8), a.qjl_rnorm + drow, lane);
+  if (kind == 0 && a.qjl)
+    append_qjl_slice(r, a.S, rbuf, a.qjl_signs + drow * (kQjlM / 8), a.qjl_rnorm + drow, lane,
+                     slice);
+}
+
+__global__ void __launch_bounds__(32 * kAppendQjlWarps) append_kernel(const AppendArgs a) {
   __shared__ float bnd[2][256];
   __shared__ float cen[2][256];
-  __shared__ uint32_t words[2][32];
-  __shared__ __align__(16) float rbuf[kD];
+  __shared__ uint32_t words[kAppendQjlWarps][32];
+  __shared__ __align__(16) float rbuf[4][kD];
+  __shared__ __align__(16) uint8_t scratch[kAppendQjlWarps][16 * 8 + 16];
   // a decode launched after this kernel may start its prologue now (it reads
   // nothing this kernel writes before its griddepcontrol.wait)
   asm volatile("griddepcontrol.launch_dependents;");
-  const int tid = threadIdx.x, lane = tid & 31, kind = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // warp 1 takes the values; warps 0, 2, 3, 4 the keys (slices 0-3 of a QJL sketch)
+  const int kind = warp == 1 ? 1 : 0;
+  const int slice = warp < 2 ? 0 : warp - 1;
   const int h = blockIdx.x % a.H, b = blockIdx.x / a.H;
-  for (int i = lane; i < 256; i += 32) {
-    bnd[kind][i] = a.boundaries[kind][i];
-    cen[kind][i] = a.centroids[kind][i];
+  if (warp < 2) {
+    for (int i = lane; i < 256; i += 32) {
+      bnd[kind][i] = a.boundaries[kind][i];
+      cen[kind][i] = a.centroids[kind][i];
+    }
   }
-  words[kind][lane] = 0u;
+  words[warp][lane] = 0u;
   const float4 sg = ((const float4*)a.rot_signs[kind])[lane];
-  __syncwarp();
+  __syncthreads();                                    // the key warps share warp 0's tables
   const long long T0 = a.seq_before[b];
   const long long T1 = T0 + a.n;
   const long long q0 = T0 - a.W > 0 ? T0 - a.W : 0;
@@ -185,13 +240,14 @@ __global__ void __launch_bounds__(64) append_kernel(const AppendArgs a) {
         continue;
     }
     const long long drow = ((long long)b * a.H + h) * a.cap[kind] + pos;
-    append_quantize_row(a, kind, src, f32, drow, bnd[kind], cen[kind], sg, words[kind], rbuf, lane);
+    append_quantize_row(a, kind, slice, src, f32, drow, bnd[kind], cen[kind], sg, words[warp],
+                        rbuf[slice], scratch[warp], lane);
   }
   if (a.W == 0) return;
   __syncthreads();                                    // ring slots read before they are rewritten
   const long long first = T1 - a.W > T0 ? T1 - a.W : T0;   // first new token kept in the ring
   const int n_ring = (int)(T1 - first);
-  for (int e = tid; e < 2 * n_ring * 16; e += 64) {
+  for (int e = tid; e < 2 * n_ring * 16; e += (int)blockDim.x) {
     const int part = e & 15, row = e >> 4;
     const int k2 = row / n_ring;
     const long long t = first + row % n_ring;
@@ -363,7 +419,7 @@ int launch_quantize(const QuantArgs& a, void* stream) {
 int launch_append(const AppendArgs& a, void* stream) {
   const long long units = (long long)a.B * a.H;
   if (units <= 0) return 0;
-  append_kernel<<<(unsigned)units, 64, 0, (cudaStream_t)stream>>>(a);
+  append_kernel<<<(unsigned)units, a.qjl ? 32 * kAppendQjlWarps : 64, 0, (cudaStream_t)stream>>>(a);
   return cudaGetLastError() != cudaSuccess;
 }
 
