@@ -319,11 +319,11 @@ tq_status tq_decode_attention_multi(const tq_config* cfg, const void* tables, in
  * two calls ("[GitHub 탐방] TurboQuant 3-bit KV 캐시 압축 — 단일 GPU 재현 기록",
  * "실험 설계": the newest tokens stay in the bf16 window).  max_seq_len bounds
  * seq_lens_before[b] + 1.  One launch when the plan with the step's work
- * fits one wave of the GPU and gives the quantized splits no more tokens than
- * a plain decode's plan (see tq_decode_step_launches): the quantized
- * splits stop before the token that leaves the window (with W = 0 the new
- * token itself), and each pair's first window split (with W = 0 a split of
- * its own) quantizes that token into the planes with the same warp-per-vector
+ * fits one wave of the GPU and gives the warps of the quantized splits no more
+ * 32-token chunks than a plain decode's plan (see tq_decode_step_launches):
+ * the quantized splits stop before the token that leaves the window (with
+ * W = 0 the new token itself), and each pair's first window split (with
+ * W = 0 a split of its own) quantizes that token into the planes with the same warp-per-vector
  * quantizer as tq_append_kv (so the same codes, norms and residual terms),
  * attends to its dequantized key and value, and with W > 0 writes the new
  * token into the ring slot that token leaves; the window splits read the new
@@ -331,8 +331,8 @@ tq_status tq_decode_attention_multi(const tq_config* cfg, const void* tables, in
  * the decode's rounding (that token enters the attention through fp32
  * dequantized operands rather than fp16 MMA operands).  Otherwise (the splits
  * that append would run in a later wave, or with W = 0 their extra split per
- * pair would lengthen the quantized splits) two launches: the append kernel
- * and a decode that waits for it.  k_new / v_new are bf16, or
+ * pair would give the quantized splits' warps more chunks) two launches: the
+ * append kernel and a decode that waits for it.  k_new / v_new are bf16, or
  * fp32 when W = 0 (the ring is bf16).  The planes, ring and workspace must not
  * be used by other work on the device meanwhile. */
 tq_status tq_decode_step(const tq_config* cfg, const void* tables, int layer, const void* q,

@@ -532,18 +532,22 @@ extern "C" size_t tq_workspace_bytes(const tq_config* cfg, int batch, int n_q_he
 
 namespace tq {
 // A decode step runs in one launch when its plan (with the splits that append
-// the token) is one wave and gives the quantized splits no more tokens than a
-// plain decode's plan: with W = 0 the step's extra split per pair can cost the
-// pairs a quantized split (measured: on 128 pairs at three CTAs per SM, 3
-// splits of 2,752 tokens became 2 of 4,096 and the step took 111 us against
-// 90 us as an append and a decode).  Otherwise the append kernel runs first
-// and a plain decode after it.
+// the token) is one wave and gives the warps of the quantized splits no more
+// 32-token chunks than a plain decode's plan: with W = 0 the step's extra split
+// per pair can cost the pairs a quantized split (measured: on 128 pairs at
+// three CTAs per SM, 3 splits of 2,752 tokens, 22 chunks a warp, became 2 of
+// 4,096, 32 chunks a warp, and the step took 111 us against 90 us as an append
+// and a decode).  Otherwise the append kernel runs first and a plain decode
+// after it.
 static bool step_one_launch(const tq_config* cfg, int layer, int batch, int n_q_heads,
                             int n_kv_heads, int max_seq_len) {
   const tq_layer_spec s = spec_of(cfg, layer);
   const DecodePlan ps = decode_plan(cfg, s, batch, n_q_heads, n_kv_heads, max_seq_len, true);
   const DecodePlan pd = decode_plan(cfg, s, batch, n_q_heads, n_kv_heads, max_seq_len, false);
-  return !ps.long_first && ps.split_tokens <= pd.split_tokens;
+  const int res = s.k_mode == TQ_MODE_MSE_QJL ? 1 : s.k_mode == TQ_MODE_MSE_SIGN ? 2 : 0;
+  const long long warp_tokens = 32LL * decode_warps(ps.G, s.k_bits, s.v_bits, res);
+  auto chunks = [&](int st) { return (st + warp_tokens - 1) / warp_tokens; };
+  return !ps.long_first && chunks(ps.split_tokens) <= chunks(pd.split_tokens);
 }
 }  // namespace tq
 

@@ -200,6 +200,10 @@ def test_decode_step_launches(B):
     then the decode); 0 flags invalid sizes.  Host logic only."""
     llama = B.Config(k_bits=4, v_bits=2, residual_window=128)
     assert B.tq_decode_step_launches(llama, 0, 1, 32, 8, 32768) == 1
+    # no window: the step's split per pair leaves 18 quantized splits of 1,824
+    # tokens instead of 19 of 1,728, the same 5 chunks for the busiest warp
+    no_window = B.Config(k_bits=4, v_bits=2)
+    assert B.tq_decode_step_launches(no_window, 0, 1, 32, 8, 32768) == 1
     long_ctx = B.Config(k_bits=3, v_bits=3, residual_window=256)
     assert B.tq_decode_step_launches(long_ctx, 0, 1, 64, 8, 1 << 20) == 1
     single = B.Config(k_bits=3, v_bits=3)
