@@ -134,6 +134,25 @@ def test_workspace_bytes(B):
     assert B.tq_workspace_bytes(B.Config(), 1, 32, 8, 0) >= 0
 
 
+def test_workspace_bytes_follow_the_split_plan(B):
+    """The workspace holds (m, l, pad, pad, o[128]) fp32 per (pair, split,
+    query head) and one counter per pair, each region rounded up to 256
+    bytes.  The split counts pin the plan: every pair gets the same number of
+    whole quantized splits in one wave.  Host logic only."""
+    def expect(pairs, splits, G):
+        part = pairs * splits * G * 132 * 4
+        return -(-part // 256) * 256 + -(-pairs * 4 // 256) * 256
+    # Llama-shaped 32K cache, window 128: 152 CTAs = 8 pairs x (18 quantized + 1 window)
+    llama = B.Config(k_bits=4, v_bits=2, residual_window=128)
+    assert B.tq_workspace_bytes(llama, 1, 32, 8, 32768) == expect(8, 19, 4)
+    # 128 pairs with QJL keys (three CTAs per SM, 456 slots): 3 splits each for a
+    # plain decode, 2 + the step's own for a step
+    qjl = B.Config(k_bits=2, v_bits=3, k_mode=B.TQ_MODE_MSE_QJL)
+    assert B.tq_workspace_bytes(qjl, 16, 32, 8, 8192) == expect(128, 3, 4)
+    # more pairs than a wave: one quantized and one window split per pair (several waves)
+    assert B.tq_workspace_bytes(llama, 64, 32, 8, 16384) == expect(512, 2, 4)
+
+
 @pytest.mark.skipif(__import__("conftest").has_gpu(), reason="fake pointers are only used without a GPU")
 def test_argument_validation_rejects_before_launch(B):
     import ctypes as C
